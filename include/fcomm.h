@@ -1,0 +1,206 @@
+/*
+ * fcomm.h -- C ABI of libfcomm: the data-parallel compute of a quantized
+ * tensor-parallel All-Reduce followed by residual add and RMSNorm, on one
+ * GB300 (sm_103a).
+ *
+ * The method (pages, by title and section):
+ *  - "Flash Communication: Reducing Tensor Parallelization Bottleneck for
+ *    Fast Large Language Model Inference" (arXiv 2412.04964), summary,
+ *    "Main contributions" item 2 and "Core ideas": activations are quantized
+ *    to low bit-width in fine-grained groups before they are sent, and the
+ *    All-Reduce runs in two steps (reduce-scatter of quantized shards, then
+ *    all-gather of the requantized reduced shards).
+ *  - flash-comm, abstract: self-synchronizing transfers in which every data
+ *    block carries evidence of its readiness and the receiver validates the
+ *    blocks it needs directly; the reduction order is decoupled from the
+ *    transport order so every GPU gets the same result.
+ *  - "TokenWeave: Efficient Compute-Communication Overlap for Distributed LLM
+ *    Inference" (arXiv 2505.11329), abstract: the RMSNorm after each
+ *    All-Reduce is fused into it, and a batch's tokens are split into two
+ *    subsets whose work overlaps.
+ *
+ * On one GPU the P tensor-parallel ranks are P "slabs" (partial sums) in the
+ * same HBM.  Slab order is the reduction order.
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller owns all memory.  Tensor arguments are DEVICE
+ *    pointers; fc_qtensor / slab arrays themselves are HOST arrays of device
+ *    pointers.  The library never allocates device memory, never frees and
+ *    never synchronizes; every call is asynchronous on `stream` (NULL = the
+ *    legacy default stream).
+ *  - Layout: tensors are row-major [rows, hidden]; groups are `group`
+ *    consecutive elements of one row (hidden % group == 0).  INT8 codes are
+ *    int8[rows*hidden]; INT4 codes are uint8[rows*hidden/2] with element 2i
+ *    in the low nibble of byte i and 2i+1 in the high nibble.  Scales and
+ *    zero-points are fp32[rows*hidden/group], group-major.
+ *  - Alignment: bf16 and fp32 tensors 32 bytes, codes and tagged blocks 16
+ *    bytes, scales and zero-points 4 bytes.  Violations return
+ *    FC_ERR_INVALID.
+ *  - Errors: argument errors are returned before anything is launched
+ *    (FC_ERR_INVALID, FC_ERR_UNSUPPORTED); a failed launch returns
+ *    FC_ERR_CUDA.  fc_last_error() gives a message for the calling thread's
+ *    last failure.  Data-dependent errors (a stale tagged block) are only
+ *    reported through the optional device status words, so no call blocks.
+ *  - rows == 0 is valid and launches nothing.
+ */
+#ifndef FCOMM_H
+#define FCOMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st* fc_stream_t;
+
+typedef enum {
+  FC_OK = 0,
+  FC_ERR_INVALID = 1,     /* bad argument: null/misaligned pointer, bad size or format */
+  FC_ERR_CUDA = 2,        /* a CUDA call or kernel launch failed */
+  FC_ERR_STALE_BLOCK = 3, /* device status only: a tagged block carried a wrong epoch */
+  FC_ERR_UNSUPPORTED = 4  /* a valid request this build does not implement */
+} fc_status;
+
+typedef enum {
+  FC_FMT_BF16 = 0,        /* unquantized bf16 payload */
+  FC_FMT_INT8_SYM = 1,    /* INT8 symmetric: scale = absmax/127, codes in [-127, 127] */
+  FC_FMT_INT4_ASYM = 2,   /* INT4 asymmetric: scale = (max-min)/15, zero = min, codes in [0, 15] */
+  FC_FMT_BF16_TAGGED = 3, /* bf16 in epoch-tagged 16-byte blocks */
+  FC_FMT_F32 = 4          /* output dtype only (fc_requant_gather) */
+} fc_format;
+
+/* Quantization spec.  group: 16..512, a multiple of 16 (INT8 uses 128 and
+ * INT4 uses 32 in the reference workloads).  Ignored for BF16 and TAGGED. */
+typedef struct {
+  int32_t fmt;   /* fc_format */
+  int32_t group; /* elements per group */
+} fc_qspec;
+
+/* One quantized tensor: device pointers.  For FC_FMT_BF16 / FC_FMT_BF16_TAGGED
+ * slabs, `codes` is the bf16 data / the tagged blocks and scales/zeros are
+ * unused.  `zeros` is used by INT4 only. */
+typedef struct {
+  void* codes;
+  float* scales;
+  float* zeros;
+} fc_qtensor;
+
+/* ---------------------------------------------------------------- sizes -- */
+/* Bytes of codes for rows x hidden elements (INT8: n, INT4: n/2, BF16: 2n,
+ * TAGGED: fc_tagged_bytes).  0 for an invalid spec. */
+size_t fc_codes_bytes(fc_qspec spec, int64_t rows, int64_t hidden);
+/* Number of groups (= fp32 scales, = fp32 zero-points) for rows x hidden. */
+size_t fc_groups(fc_qspec spec, int64_t rows, int64_t hidden);
+/* Bytes of the tagged form of rows x hidden bf16: rows * ceil(hidden/6) * 16.
+ * Each row is cut into ceil(hidden/6) blocks of 16 bytes: block j carries row
+ * elements 6j..6j+5 as bf16 in 32-bit words 0..2 (element 6j+2k in the low
+ * half of word k, zero past the row end) and the 32-bit epoch in word 3.
+ * Blocks never straddle rows, so any row range is a contiguous block range. */
+size_t fc_tagged_bytes(int64_t rows, int64_t hidden);
+/* Group range [g0, g1) of shard `shard` when the groups are split into P
+ * contiguous shards of ceil(n_groups/P) groups (the reduce-scatter partition
+ * of the two-step All-Reduce).  Returns FC_ERR_INVALID on bad arguments. */
+fc_status fc_shard_range(fc_qspec spec, int64_t rows, int64_t hidden, int P, int shard,
+                         int64_t* g0, int64_t* g1);
+
+/* ------------------------------------------------------------- compute -- */
+
+/* Group-quantize one bf16 slab (the sender side of the quantized All-Reduce;
+ * Flash Communication, "Main contributions" 2).
+ *  x_bf16: [rows, hidden] bf16.  out: codes + scales (+ zeros for INT4), sized
+ *  by fc_codes_bytes / fc_groups.  spec.fmt: INT8_SYM or INT4_ASYM.
+ * Per group (fp32, IEEE division, round-to-nearest-even codes, no FMA):
+ *  INT8: s = max|x|/127; q = clamp(rne(x/s), -127, 127); s == 0 -> codes 0.
+ *  INT4: lo = min, hi = max (a zero extreme is +0); s = (hi-lo)/15; z = lo;
+ *        q = clamp(rne((x-lo)/s), 0, 15); s == 0 -> codes 0. */
+fc_status fc_group_quantize(const void* x_bf16, int64_t rows, int64_t hidden, fc_qspec spec,
+                            fc_qtensor out, fc_stream_t stream);
+
+/* Quantize P bf16 slabs in one launch; slab p reads x_bf16[p] and writes
+ * out[p] (host arrays of P entries, 1 <= P <= 8).  Same result as P calls of
+ * fc_group_quantize. */
+fc_status fc_group_quantize_multi(const void* const* x_bf16, int P, int64_t rows,
+                                  int64_t hidden, fc_qspec spec, const fc_qtensor* out,
+                                  fc_stream_t stream);
+
+/* Reduce-scatter stage math of the two-step All-Reduce (Flash Communication,
+ * "Main contributions" 2; flash-comm abstract for the fixed order):
+ *  out_f32[i] = ((0 + deq_0(i)) + deq_1(i)) + ... + deq_{P-1}(i), fp32,
+ *  slab order, where deq(i) = q*s (INT8) or q*s + z (INT4, two roundings).
+ *  slabs: host array of P (2..8) quantized slabs; out_f32: the whole
+ *  [rows, hidden] fp32 tensor.  shard = -1 writes every element; shard j in
+ *  [0, P) writes only shard j's groups (fc_shard_range). */
+fc_status fc_reduce_dequant_sum(const fc_qtensor* slabs, int P, int64_t rows, int64_t hidden,
+                                fc_qspec spec, int shard, float* out_f32, fc_stream_t stream);
+
+/* Requantize a reduced fp32 tensor (same quantizer as fc_group_quantize,
+ * applied to the fp32 values) into requant_out (the all-gather payload), and
+ * write its dequantization to `out` as out_dtype FC_FMT_BF16 (round to
+ * nearest even) or FC_FMT_F32.  requant_out.codes may be NULL (payload not
+ * stored); out may be NULL (no dequantized output). */
+fc_status fc_requant_gather(const float* reduced_f32, int64_t rows, int64_t hidden, fc_qspec spec,
+                            fc_qtensor requant_out, void* out, int32_t out_dtype,
+                            fc_stream_t stream);
+
+/* Producer side of the self-validating block format (flash-comm, abstract):
+ * pack [rows, hidden] bf16 into fc_tagged_bytes(rows, hidden) bytes of
+ * 16-byte blocks carrying `epoch`. */
+fc_status fc_pack_tagged(const void* x_bf16, int64_t rows, int64_t hidden, uint32_t epoch,
+                         void* blocks, fc_stream_t stream);
+
+/* The fused path: quantized All-Reduce + residual add + RMSNorm (Flash
+ * Communication two-step reduce; TokenWeave fused AllReduce-RMSNorm).
+ * For every row, in one kernel:
+ *   o   = two-step result: INT8/INT4: dequant(requant(sum_p deq_p)),
+ *         BF16/TAGGED: sum_p float(x_p) (fp32, slab order, from +0);
+ *   h   = bf16(o + float(residual_in))          -> residual_out
+ *   y_k = bf16((float(h_k) * inv) * float(gamma_k)),
+ *         inv = 1 / sqrt(sum_k h_k^2 / hidden + eps)  (fp32)
+ * slabs: host array of P (2..8) slabs in spec.fmt (INT8/INT4 quantized as by
+ *   fc_group_quantize; BF16 data; TAGGED blocks from fc_pack_tagged).
+ * residual_in, residual_out (may be the same pointer), y: [rows, hidden] bf16;
+ * gamma: [hidden] bf16.  requant_out: INT8/INT4 only, optional (codes == NULL:
+ * not written): the requantized reduced tensor, i.e. the all-gather payload.
+ * expected_epoch / d_status: TAGGED only.  Every block of every slab is
+ * checked against expected_epoch before it is summed; a block that fails is
+ * not summed.  d_status (optional, two int32 words of device memory) is set
+ * by this call to {FC_OK, 0x7F7F7F7F} and, if any block fails, to
+ * {FC_ERR_STALE_BLOCK, index of the first failing block of slab 0..P-1 in
+ * row-major block order within this call's rows}; rows with a failing block
+ * have unspecified outputs.  Nothing waits: on one GPU the producer has
+ * finished by stream order, so a wrong tag is an error, not a retry. */
+fc_status fc_allreduce_residual_rmsnorm(const fc_qtensor* slabs, int P, int64_t rows,
+                                        int64_t hidden, fc_qspec spec, const void* residual_in,
+                                        void* residual_out, const void* gamma, float eps,
+                                        fc_qtensor requant_out, void* y, uint32_t expected_epoch,
+                                        int32_t* d_status, fc_stream_t stream);
+
+/* Launch options for the fused path.  max_ctas > 0 caps the grid at that
+ * many CTAs (persistent CTAs loop over rows), so the fused kernel can run on
+ * a few SMs beside other work (TokenWeave, abstract: communication and
+ * RMSNorm on only 2-8 SMs).  0 = size the grid to the whole GPU. */
+typedef struct {
+  int32_t max_ctas;
+} fc_launch_opts;
+
+fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64_t rows,
+                                           int64_t hidden, fc_qspec spec,
+                                           const void* residual_in, void* residual_out,
+                                           const void* gamma, float eps, fc_qtensor requant_out,
+                                           void* y, uint32_t expected_epoch, int32_t* d_status,
+                                           const fc_launch_opts* opts, fc_stream_t stream);
+
+/* --------------------------------------------------------------- misc --- */
+const char* fc_status_string(fc_status s);
+/* Message describing the calling thread's last non-OK status ("" if none). */
+const char* fc_last_error(void);
+/* Library version, e.g. "libfcomm 0.1 sm_103a". */
+const char* fc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FCOMM_H */

@@ -1,0 +1,62 @@
+// internal.h -- launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fc {
+
+enum Fmt : int { kBF16 = 0, kINT8 = 1, kINT4 = 2, kTAGGED = 3, kF32 = 4 };
+
+// P slabs as device pointers (passed to kernels by value).
+struct Slabs {
+  const void* codes[8];
+  const float* scales[8];
+  const float* zeros[8];
+};
+
+// Group quantization of P tensors of n elements each (bf16 or fp32 input),
+// optionally writing the dequantized values (single tensor only).
+struct QuantJob {
+  const void* x[8];
+  void* codes[8];
+  float* scales[8];
+  float* zeros[8];
+  void* deq;  // NULL, bf16 or fp32 [n] (P == 1 only)
+  int64_t n;  // elements per tensor (multiple of G)
+  int P;
+  int G;
+};
+
+struct FusedArgs {
+  Slabs s;
+  const void* res_in;
+  void* res_out;
+  const void* gamma;
+  void* y;
+  void* rq_codes;  // NULL: the requantized payload is not stored
+  float* rq_scales;
+  float* rq_zeros;
+  int32_t* status;  // tagged only; NULL allowed
+  int64_t rows;
+  int H;
+  int G;
+  int P;
+  float eps;
+  uint32_t epoch;
+};
+
+int num_sms();
+
+// in_f32: input is fp32 (requantization) instead of bf16; deq_kind: 0 none,
+// kBF16 or kF32.
+cudaError_t launch_quantize(int fmt, bool in_f32, int deq_kind, const QuantJob& job,
+                            cudaStream_t st);
+// Sum of dequantized slabs over the 16-element chunks [c0, c1).
+cudaError_t launch_reduce(int fmt, const Slabs& s, int P, int G, int64_t c0, int64_t c1,
+                          float* out, cudaStream_t st);
+cudaError_t launch_pack_tagged(const void* x, int64_t rows, int H, uint32_t epoch, void* blocks,
+                               cudaStream_t st);
+cudaError_t launch_fused(int fmt, const FusedArgs& a, int max_ctas, cudaStream_t st);
+
+}  // namespace fc
