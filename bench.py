@@ -1,0 +1,394 @@
+#!/usr/bin/env python3
+"""Benchmark: achieved HBM GB/s (fraction of the GB300 roofline) and us/call of
+the quantized reduce + RMSNorm hot path.
+
+One step = one pass of the whole hot path over one batch of synthetic
+activations (inputs resident in HBM): sender-side group quantization of the
+P partial-sum slabs, then the fused two-step reduce (dequantize, fixed-order
+sum, requantize the all-gather payload, dequantize) + residual add + RMSNorm.
+Default workload: prefill, P=4 slabs of 8192 x 8192 bf16, INT4 asymmetric
+g32.  value = algorithmic bytes per step / device time per step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+  torchrun --nproc-per-node N bench.py --gpus N ...   # N independent replicas
+
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (% of GB300 roofline) and us/call for quantized reduce+RMSNorm"
+UNIT = "GB/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- clocks -----
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML (ctypes) while active."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, index: int, period_s: float = 0.005):
+        self.samples, self.reasons, self.ok = [], 0, False
+        self.period = period_s
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))  # 1 = SM
+            self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def _run(self):
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def report(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        names = [n for b, n in self.REASONS.items() if self.reasons & b and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "samples": len(self.samples), "reasons": names}
+
+
+# ------------------------------------------------------------- helpers ----
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def source_hash():
+    """Hash of the CUDA sources: ncu counters are only reported for this build."""
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "quantized_reduce_rmsnorm_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        h.update(f.encode())
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            tab = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = tab.get(f"{workload}/{kernel}")
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------- CPU arm ----
+def oracle_sample(w, inputs, target_s: float):
+    """Time the oracle on a bounded row sample of the workload's own inputs.
+
+    Returns (GB/s of algorithmic bytes, seconds, rows)."""
+    import oracle
+    from quantized_reduce_rmsnorm_gb300.pipeline import qs_bytes
+    from quantized_reduce_rmsnorm_gb300.synth import (FMT_BF16, FMT_BF16_TAGGED, FMT_INT4_ASYM,
+                                                      FMT_INT8_SYM, Workload)
+    orc = oracle.default()
+    fmt = FMT_BF16 if w.fmt == FMT_BF16_TAGGED else w.fmt
+
+    def run(rows):
+        sl = [s[:rows] for s in inputs["slabs"]]
+        t0 = time.perf_counter()
+        orc.allreduce_residual_rmsnorm(fmt, sl, inputs["residual"][:rows], inputs["gamma"],
+                                       rows, w.H, w.group, w.eps)
+        return time.perf_counter() - t0
+
+    probe = min(w.T, max(1, 8))
+    dt = run(probe)
+    rows = int(min(w.T, max(probe, probe * target_s / max(dt, 1e-6))))
+    dt = run(rows)
+    sub = Workload(**{**w.__dict__, "T": rows})
+    E = rows * w.H
+    if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
+        qs = qs_bytes(sub, E)
+        alg = (w.P * 2 * E + w.P * qs) + (w.P * qs + 2 * E + 2 * w.H + qs + 4 * E)
+    else:
+        alg = w.P * 2 * E + 2 * E + 2 * w.H + 4 * E
+    return alg / dt / 1e9, dt, rows
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from quantized_reduce_rmsnorm_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    # each step is a bounded sample of rows, sized so the whole run stays short
+    per_step = max(0.5, 120.0 / max(1, args.steps + args.warmup))
+    rows = min(w.T, max(1, int(64 * per_step)))
+    inputs = synth.make_inputs(w, seed=0, rows=np.arange(rows))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        gbs, dt, r = oracle_sample(w, inputs, per_step)
+        if i >= args.warmup:
+            vals.append((gbs, dt, r))
+    v = statistics.median(x[0] for x in vals)
+    ms = statistics.median(x[1] for x in vals) * 1e3
+    r = vals[-1][2]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w, note=f"oracle on {r} of {w.T} rows per step"),
+        "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{r} of {w.T} rows of the {w.name} workload per step"},
+        "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, note=None):
+    from quantized_reduce_rmsnorm_gb300.synth import FMT_NAMES
+    c = {"workload": f"{w.name}: P={w.P} slabs of {w.T}x{w.H} bf16, {FMT_NAMES[w.fmt]}"
+                     + (f", {w.splits} token subsets on {w.splits} streams" if w.splits > 1
+                        else ""),
+         "P": w.P, "tokens": w.T, "hidden": w.H, "format": FMT_NAMES[w.fmt], "group": w.group,
+         "dist": w.dist, "outlier_frac": w.outlier_frac, "outlier_scale": w.outlier_scale,
+         "eps": w.eps, "parallelism": "replicas"}
+    if note:
+        c["note"] = note
+    return c
+
+
+# ------------------------------------------------------------- GPU arm ----
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from quantized_reduce_rmsnorm_gb300 import fcomm, synth
+    from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
+    fcomm.load()
+    w = synth.WORKLOADS[args.workload]
+    inputs = synth.make_inputs(w, seed=rank)
+    pipe = Pipeline(w, inputs, device=dev)
+    alg = pipe.alg_bytes()
+    step_bytes = alg["sender"] + alg["fused"]
+    in_bytes = w.P * 2 * w.T * w.H  # bf16 slabs read by the first stage
+    flush = None
+    if in_bytes + 2 * w.T * w.H < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    st = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        pipe.step(st)
+    torch.cuda.synchronize(dev)
+
+    # timed region: per step, events around each stage on the launching stream
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index)
+    with sampler:
+        t_wall = time.perf_counter()
+        for i in range(n):
+            if flush is not None:
+                flush.add_(1.0)  # scrub L2 between timed steps (outside the events)
+            pipe.step_marked(st, ev[i])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    barrier(ws)
+    sender_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    fused_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = sum(a + b for a, b in zip(sender_ms, fused_ms)) / n
+    step_ms = allreduce_max(step_ms, ws, dev)
+
+    value = ws * step_bytes / (step_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    kern = [("sender", "k_quantize" if w.fmt in (1, 2) else "k_pack_tagged", alg["sender"],
+             statistics.mean(sender_ms)),
+            ("fused", "k_fused_tagged" if w.fmt == 3 else "k_fused", alg["fused"],
+             statistics.mean(fused_ms))]
+    dom = max(kern, key=lambda k: k[3])
+    achieved = dom[2] / (dom[3] * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": n, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "us_per_call": round(statistics.mean(fused_ms) * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {**workload_config(w),
+                   "l2": ("L2 scrubbed (256 MB write) before every timed step"
+                          if flush is not None else
+                          f"inputs larger than L2 ({in_bytes / 2**20:.0f} MB of bf16 slabs "
+                          f"read per step vs 129 MB L2)"),
+                   "alg_bytes_per_step": step_bytes},
+        "roofline": {"bound": "hbm", "kernel": dom[1], "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": measured_traffic(dom[1], w.name),
+                     "alg_bytes_per_launch": dom[2]},
+        "stages": {k[0]: {"kernel": k[1], "alg_bytes": k[2], "us": round(k[3] * 1e3, 2),
+                          "GB/s": round(k[2] / (k[3] * 1e-3) / 1e9, 1),
+                          "frac": round(k[2] / (k[3] * 1e-3) / 1e9 / peak, 4)} for k in kern},
+        "gpu_launches": n * pipe.launches_per_step,
+        "clocks": sampler.report(),
+        "timed_wall_s": round(t_wall, 4),
+    }
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(pipe, inputs, step_bytes, args, ws, dev)
+    if ws == 1 and rank == 0 and not args.no_cpu_baseline:
+        gbs, dt, rows = oracle_sample(w, inputs, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": 1,
+                               "kind": "oracle",
+                               "sample": f"first {rows} of {w.T} rows of the same inputs, "
+                                         f"{dt:.1f} s single-threaded"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(pipe, inputs, step_bytes, args, ws, dev):
+    """The same metric through the public API with host buffers: every step
+    copies the inputs from pinned host memory and reads y and residual_out
+    back, all inside the timed region."""
+    import torch
+    w = pipe.w
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+        torch.bfloat16).reshape(a.shape).pin_memory()
+    h_slabs = [pin(s) for s in inputs["slabs"]]
+    h_res, h_gam = pin(inputs["residual"]), pin(inputs["gamma"])
+    h_y = torch.empty(pipe.y.shape, dtype=torch.bfloat16).pin_memory()
+    h_h = torch.empty(pipe.y.shape, dtype=torch.bfloat16).pin_memory()
+    st = torch.cuda.current_stream(dev)
+    h2d = sum(t.numel() * 2 for t in h_slabs) + h_res.numel() * 2 + h_gam.numel() * 2
+    d2h = 2 * h_y.numel() * 2
+
+    def one():
+        for d, h in zip(pipe.x, h_slabs):
+            d.copy_(h, non_blocking=True)
+        pipe.residual.copy_(h_res, non_blocking=True)
+        pipe.gamma.copy_(h_gam, non_blocking=True)
+        pipe.step(st)
+        h_y.copy_(pipe.y, non_blocking=True)
+        h_h.copy_(pipe.residual_out, non_blocking=True)
+
+    steps = max(3, min(args.steps, 20))
+    for _ in range(min(3, args.warmup)):
+        one()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        one()
+    e1.record(st)
+    torch.cuda.synchronize(dev)
+    ms = allreduce_max(e0.elapsed_time(e1) / steps, ws, dev)
+    return {"value": round(ws * step_bytes / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "steps": steps, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(v, ws, dev):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -56,6 +56,7 @@ def _signatures():
     return {
         "or_bf16_to_f32_array": (None, [P, i64, P]),
         "or_f32_to_bf16": (ctypes.c_uint16, [f32]),
+        "or_f32_to_bf16_array": (None, [P, i64, P]),
         "or_f64_to_bf16": (ctypes.c_uint16, [ctypes.c_double]),
         "or_quant_i8s": (None, [P, i64, i32, P, P]),
         "or_dequant_i8s": (None, [P, P, i64, i32, P]),
@@ -106,6 +107,13 @@ class Oracle:
         x = _c(x, np.float32)
         fn = self.lib.or_f32_to_bf16
         return np.array([fn(float(v)) for v in x.ravel()], np.uint16).reshape(x.shape)
+
+    def f32_to_bf16_array(self, x):
+        """Same rounding as f32_to_bf16, one C loop over the whole array."""
+        x = _c(x, np.float32)
+        out = np.empty(x.shape, np.uint16)
+        self.lib.or_f32_to_bf16_array(_p(x), x.size, _p(out))
+        return out
 
     def f64_to_bf16(self, x):
         x = _c(x, np.float64)

@@ -59,6 +59,10 @@ void or_bf16_to_f32_array(const uint16_t* b, int64_t n, float* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = or_bf16_to_f32(b[i]);
 }
 
+void or_f32_to_bf16_array(const float* x, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = or_f32_to_bf16(x[i]);
+}
+
 /* ---------------------------------------------------------- quantizers -- */
 /* [FC] "Main contributions" 2: activations are quantized to low bit-width
  * in fine-grained groups before they are communicated.  Formats: INT8

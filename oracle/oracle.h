@@ -46,6 +46,7 @@ float or_bf16_to_f32(uint16_t b);
 uint16_t or_f32_to_bf16(float f);   /* round to nearest even */
 uint16_t or_f64_to_bf16(double d);  /* one rounding, to nearest even */
 void or_bf16_to_f32_array(const uint16_t* b, int64_t n, float* out);
+void or_f32_to_bf16_array(const float* x, int64_t n, uint16_t* out);
 
 /* Group quantizers over n elements in groups of G consecutive elements. */
 void or_quant_i8s(const float* x, int64_t n, int G, int8_t* q, float* s);

@@ -1,0 +1,297 @@
+// api.cu -- the libfcomm C ABI: argument validation and kernel dispatch.
+// Every entry point validates all arguments before it launches anything,
+// never allocates, frees or synchronizes, and launches on the caller's
+// stream.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/fcomm.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+fc_status fail(fc_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+fc_status ok() {
+  g_msg[0] = '\0';
+  return FC_OK;
+}
+
+fc_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(FC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool quantized(int fmt) { return fmt == FC_FMT_INT8_SYM || fmt == FC_FMT_INT4_ASYM; }
+
+// Common shape/spec checks.  needs_group: the format is quantized.
+fc_status check_shape(fc_qspec spec, int64_t rows, int64_t hidden, bool quant_only) {
+  if (rows < 0) return fail(FC_ERR_INVALID, "rows must be >= 0 (got %lld)", (long long)rows);
+  if (hidden <= 0 || hidden % 16 != 0)
+    return fail(FC_ERR_INVALID, "hidden must be a positive multiple of 16 (got %lld)",
+                (long long)hidden);
+  if (hidden > 65536) return fail(FC_ERR_UNSUPPORTED, "hidden > 65536 is not supported");
+  if (quant_only && !quantized(spec.fmt))
+    return fail(FC_ERR_INVALID, "format %d is not a quantized format", spec.fmt);
+  if (quantized(spec.fmt)) {
+    const int G = spec.group;
+    if (G < 16 || G > 512 || (G & (G - 1)) != 0)
+      return fail(FC_ERR_INVALID, "group must be a power of two in [16, 512] (got %d)", G);
+    if (hidden % G != 0)
+      return fail(FC_ERR_INVALID, "hidden (%lld) must be a multiple of group (%d)",
+                  (long long)hidden, G);
+  } else if (spec.fmt != FC_FMT_BF16 && spec.fmt != FC_FMT_BF16_TAGGED) {
+    return fail(FC_ERR_INVALID, "unknown format %d", spec.fmt);
+  }
+  return FC_OK;
+}
+
+fc_status check_ptr(const void* p, size_t align, const char* name) {
+  if (!p) return fail(FC_ERR_INVALID, "%s must not be NULL", name);
+  if (!aligned(p, align)) return fail(FC_ERR_INVALID, "%s must be %zu-byte aligned", name, align);
+  return FC_OK;
+}
+
+fc_status check_qtensor(const fc_qtensor& t, int fmt, const char* name) {
+  char buf[64];
+  snprintf(buf, sizeof buf, "%s.codes", name);
+  if (fc_status s = check_ptr(t.codes, 16, buf)) return s;
+  if (quantized(fmt)) {
+    snprintf(buf, sizeof buf, "%s.scales", name);
+    if (fc_status s = check_ptr(t.scales, 4, buf)) return s;
+    if (fmt == FC_FMT_INT4_ASYM) {
+      snprintf(buf, sizeof buf, "%s.zeros", name);
+      if (fc_status s = check_ptr(t.zeros, 4, buf)) return s;
+    }
+  } else if (fmt == FC_FMT_BF16 && !aligned(t.codes, 32)) {
+    return fail(FC_ERR_INVALID, "%s.codes (bf16 data) must be 32-byte aligned", name);
+  }
+  return FC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fc_status_string(fc_status s) {
+  switch (s) {
+    case FC_OK: return "FC_OK";
+    case FC_ERR_INVALID: return "FC_ERR_INVALID";
+    case FC_ERR_CUDA: return "FC_ERR_CUDA";
+    case FC_ERR_STALE_BLOCK: return "FC_ERR_STALE_BLOCK";
+    case FC_ERR_UNSUPPORTED: return "FC_ERR_UNSUPPORTED";
+  }
+  return "FC_ERR_UNKNOWN";
+}
+
+const char* fc_last_error(void) { return g_msg; }
+
+const char* fc_version(void) { return "libfcomm 0.1 sm_103a"; }
+
+size_t fc_tagged_bytes(int64_t rows, int64_t hidden) {
+  if (rows < 0 || hidden <= 0) return 0;
+  return static_cast<size_t>(rows) * static_cast<size_t>((hidden + 5) / 6) * 16u;
+}
+
+size_t fc_codes_bytes(fc_qspec spec, int64_t rows, int64_t hidden) {
+  if (rows < 0 || hidden <= 0) return 0;
+  const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(hidden);
+  switch (spec.fmt) {
+    case FC_FMT_BF16: return 2 * n;
+    case FC_FMT_INT8_SYM: return n;
+    case FC_FMT_INT4_ASYM: return n / 2;
+    case FC_FMT_BF16_TAGGED: return fc_tagged_bytes(rows, hidden);
+    default: return 0;
+  }
+}
+
+size_t fc_groups(fc_qspec spec, int64_t rows, int64_t hidden) {
+  if (!quantized(spec.fmt) || spec.group <= 0 || rows < 0 || hidden <= 0) return 0;
+  return static_cast<size_t>(rows) * static_cast<size_t>(hidden) / static_cast<size_t>(spec.group);
+}
+
+fc_status fc_shard_range(fc_qspec spec, int64_t rows, int64_t hidden, int P, int shard,
+                         int64_t* g0, int64_t* g1) {
+  if (fc_status s = check_shape(spec, rows, hidden, true)) return s;
+  if (P < 1 || shard < 0 || shard >= P || !g0 || !g1)
+    return fail(FC_ERR_INVALID, "need 0 <= shard < P and non-NULL outputs");
+  const int64_t ng = rows * hidden / spec.group;
+  const int64_t per = (ng + P - 1) / P;
+  int64_t a = per * shard, b = a + per;
+  if (a > ng) a = ng;
+  if (b > ng) b = ng;
+  *g0 = a;
+  *g1 = b;
+  return ok();
+}
+
+fc_status fc_group_quantize_multi(const void* const* x_bf16, int P, int64_t rows, int64_t hidden,
+                                  fc_qspec spec, const fc_qtensor* out, fc_stream_t stream) {
+  if (fc_status s = check_shape(spec, rows, hidden, true)) return s;
+  if (P < 1 || P > 8) return fail(FC_ERR_INVALID, "P must be in [1, 8] (got %d)", P);
+  if (rows == 0) return ok();
+  if (!x_bf16 || !out) return fail(FC_ERR_INVALID, "x_bf16 and out must not be NULL");
+  fc::QuantJob job{};
+  for (int p = 0; p < P; ++p) {
+    if (fc_status s = check_ptr(x_bf16[p], 32, "x_bf16[p]")) return s;
+    if (fc_status s = check_qtensor(out[p], spec.fmt, "out[p]")) return s;
+    job.x[p] = x_bf16[p];
+    job.codes[p] = out[p].codes;
+    job.scales[p] = out[p].scales;
+    job.zeros[p] = out[p].zeros;
+  }
+  job.n = rows * hidden;
+  job.P = P;
+  job.G = spec.group;
+  return cuda_status(fc::launch_quantize(spec.fmt, false, 0, job, (cudaStream_t)stream),
+                     "fc_group_quantize launch");
+}
+
+fc_status fc_group_quantize(const void* x_bf16, int64_t rows, int64_t hidden, fc_qspec spec,
+                            fc_qtensor out, fc_stream_t stream) {
+  return fc_group_quantize_multi(&x_bf16, 1, rows, hidden, spec, &out, stream);
+}
+
+fc_status fc_reduce_dequant_sum(const fc_qtensor* slabs, int P, int64_t rows, int64_t hidden,
+                                fc_qspec spec, int shard, float* out_f32, fc_stream_t stream) {
+  if (fc_status s = check_shape(spec, rows, hidden, true)) return s;
+  if (P < 2 || P > 8) return fail(FC_ERR_INVALID, "P must be in [2, 8] (got %d)", P);
+  if (shard < -1 || shard >= P)
+    return fail(FC_ERR_INVALID, "shard must be -1 or in [0, P) (got %d)", shard);
+  if (rows == 0) return ok();
+  if (!slabs) return fail(FC_ERR_INVALID, "slabs must not be NULL");
+  if (fc_status s = check_ptr(out_f32, 32, "out_f32")) return s;
+  fc::Slabs sl{};
+  for (int p = 0; p < P; ++p) {
+    if (fc_status s = check_qtensor(slabs[p], spec.fmt, "slabs[p]")) return s;
+    sl.codes[p] = slabs[p].codes;
+    sl.scales[p] = slabs[p].scales;
+    sl.zeros[p] = slabs[p].zeros;
+  }
+  const int64_t lpg = spec.group / 16;
+  int64_t c0 = 0, c1 = rows * hidden / 16;
+  if (shard >= 0) {
+    int64_t g0, g1;
+    fc_shard_range(spec, rows, hidden, P, shard, &g0, &g1);
+    c0 = g0 * lpg;
+    c1 = g1 * lpg;
+  }
+  return cuda_status(fc::launch_reduce(spec.fmt, sl, P, spec.group, c0, c1, out_f32,
+                                       (cudaStream_t)stream),
+                     "fc_reduce_dequant_sum launch");
+}
+
+fc_status fc_requant_gather(const float* reduced_f32, int64_t rows, int64_t hidden, fc_qspec spec,
+                            fc_qtensor requant_out, void* out, int32_t out_dtype,
+                            fc_stream_t stream) {
+  if (fc_status s = check_shape(spec, rows, hidden, true)) return s;
+  if (rows == 0) return ok();
+  if (fc_status s = check_ptr(reduced_f32, 32, "reduced_f32")) return s;
+  if (requant_out.codes)
+    if (fc_status s = check_qtensor(requant_out, spec.fmt, "requant_out")) return s;
+  int deq = 0;
+  if (out) {
+    if (out_dtype != FC_FMT_BF16 && out_dtype != FC_FMT_F32)
+      return fail(FC_ERR_INVALID, "out_dtype must be FC_FMT_BF16 or FC_FMT_F32");
+    if (fc_status s = check_ptr(out, 32, "out")) return s;
+    deq = out_dtype == FC_FMT_BF16 ? fc::kBF16 : fc::kF32;
+  }
+  fc::QuantJob job{};
+  job.x[0] = reduced_f32;
+  job.codes[0] = requant_out.codes;
+  job.scales[0] = requant_out.scales;
+  job.zeros[0] = requant_out.zeros;
+  job.deq = out;
+  job.n = rows * hidden;
+  job.P = 1;
+  job.G = spec.group;
+  return cuda_status(fc::launch_quantize(spec.fmt, true, deq, job, (cudaStream_t)stream),
+                     "fc_requant_gather launch");
+}
+
+fc_status fc_pack_tagged(const void* x_bf16, int64_t rows, int64_t hidden, uint32_t epoch,
+                         void* blocks, fc_stream_t stream) {
+  fc_qspec spec{FC_FMT_BF16_TAGGED, 0};
+  if (fc_status s = check_shape(spec, rows, hidden, false)) return s;
+  if (rows == 0) return ok();
+  if (fc_status s = check_ptr(x_bf16, 32, "x_bf16")) return s;
+  if (fc_status s = check_ptr(blocks, 16, "blocks")) return s;
+  return cuda_status(fc::launch_pack_tagged(x_bf16, rows, static_cast<int>(hidden), epoch, blocks,
+                                            (cudaStream_t)stream),
+                     "fc_pack_tagged launch");
+}
+
+fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64_t rows,
+                                           int64_t hidden, fc_qspec spec,
+                                           const void* residual_in, void* residual_out,
+                                           const void* gamma, float eps, fc_qtensor requant_out,
+                                           void* y, uint32_t expected_epoch, int32_t* d_status,
+                                           const fc_launch_opts* opts, fc_stream_t stream) {
+  if (fc_status s = check_shape(spec, rows, hidden, false)) return s;
+  if (P < 2 || P > 8) return fail(FC_ERR_INVALID, "P must be in [2, 8] (got %d)", P);
+  if (opts && opts->max_ctas < 0) return fail(FC_ERR_INVALID, "max_ctas must be >= 0");
+  if (rows == 0) return ok();
+  if (!slabs) return fail(FC_ERR_INVALID, "slabs must not be NULL");
+  if (!(eps >= 0.0f) || eps > 1.0f) return fail(FC_ERR_INVALID, "eps must be in [0, 1]");
+  if (fc_status s = check_ptr(residual_in, 32, "residual_in")) return s;
+  if (fc_status s = check_ptr(residual_out, 32, "residual_out")) return s;
+  if (fc_status s = check_ptr(gamma, 32, "gamma")) return s;
+  if (fc_status s = check_ptr(y, 32, "y")) return s;
+  if (opts && opts->max_ctas < 0) return fail(FC_ERR_INVALID, "max_ctas must be >= 0");
+  fc::FusedArgs a{};
+  for (int p = 0; p < P; ++p) {
+    if (fc_status s = check_qtensor(slabs[p], spec.fmt, "slabs[p]")) return s;
+    a.s.codes[p] = slabs[p].codes;
+    a.s.scales[p] = slabs[p].scales;
+    a.s.zeros[p] = slabs[p].zeros;
+  }
+  if (quantized(spec.fmt) && requant_out.codes) {
+    if (fc_status s = check_qtensor(requant_out, spec.fmt, "requant_out")) return s;
+    a.rq_codes = requant_out.codes;
+    a.rq_scales = requant_out.scales;
+    a.rq_zeros = requant_out.zeros;
+  }
+  if (d_status && !aligned(d_status, 4)) return fail(FC_ERR_INVALID, "d_status must be 4-byte aligned");
+  a.res_in = residual_in;
+  a.res_out = residual_out;
+  a.gamma = gamma;
+  a.y = y;
+  a.rows = rows;
+  a.H = static_cast<int>(hidden);
+  a.G = quantized(spec.fmt) ? spec.group : 16;
+  a.P = P;
+  a.eps = eps;
+  a.epoch = expected_epoch;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (spec.fmt == FC_FMT_BF16_TAGGED && d_status) {
+    a.status = d_status;
+    cudaError_t e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_status + 1, 0x7F, sizeof(int32_t), st);
+    if (e != cudaSuccess) return cuda_status(e, "d_status reset");
+  }
+  return cuda_status(fc::launch_fused(spec.fmt, a, opts ? opts->max_ctas : 0, st),
+                     "fc_allreduce_residual_rmsnorm launch");
+}
+
+fc_status fc_allreduce_residual_rmsnorm(const fc_qtensor* slabs, int P, int64_t rows,
+                                        int64_t hidden, fc_qspec spec, const void* residual_in,
+                                        void* residual_out, const void* gamma, float eps,
+                                        fc_qtensor requant_out, void* y, uint32_t expected_epoch,
+                                        int32_t* d_status, fc_stream_t stream) {
+  return fc_allreduce_residual_rmsnorm_ex(slabs, P, rows, hidden, spec, residual_in, residual_out,
+                                          gamma, eps, requant_out, y, expected_epoch, d_status,
+                                          nullptr, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,269 @@
+// quant.cu -- streaming kernels: group quantize / requantize, fixed-order
+// dequant-sum (reduce-scatter stage), tagged-block packing.
+//
+// Work unit: a "chunk" of 16 consecutive elements handled by one lane; a
+// group of G elements spans G/16 adjacent lanes, so every per-group
+// reduction is a few xor-shuffles.  A warp covers 32 consecutive chunks
+// (512 elements, 1 KB of bf16), so every load and store instruction of a
+// warp touches one contiguous span.  Grids are persistent: a multiple of the
+// SM count, each warp striding over warp tiles, with two tiles in flight per
+// iteration.
+#include "device.cuh"
+#include "internal.h"
+
+namespace fc {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 2;
+
+// ------------------------------------------------------- quantize kernel --
+template <int FMT, bool IN_F32, int DEQ>
+__global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chunks,
+                                                       int64_t tiles) {
+  const int lane = threadIdx.x & 31;
+  const int lpg = job.G >> 4;
+  const int64_t gwarp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  const int64_t total = tiles * job.P;
+
+  for (int64_t t0 = gwarp; t0 < total; t0 += nwarps * kUnroll) {
+    float v[kUnroll][16];
+    int pp[kUnroll];
+    int64_t cc[kUnroll];
+    bool act[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t t = t0 + u * nwarps;
+      const int p = t < total ? static_cast<int>(t / tiles) : 0;
+      const int64_t c = (t - p * tiles) * 32 + lane;
+      pp[u] = p;
+      cc[u] = c;
+      act[u] = t < total && c < chunks;
+      if (act[u]) {
+        if (IN_F32) {
+          const float* x = static_cast<const float*>(job.x[p]) + c * 16;
+          V8 a = ld256_stream(x), b = ld256_stream(x + 8);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            v[u][i] = __uint_as_float(a.w[i]);
+            v[u][8 + i] = __uint_as_float(b.w[i]);
+          }
+        } else {
+          unpack16(ld256_stream(static_cast<const uint16_t*>(job.x[p]) + c * 16), v[u]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[u][i] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int p = pp[u];
+      const int64_t c = cc[u];
+      float d[16];
+      if (FMT == kINT8) {
+        uint32_t q[4];
+        const float s = quant_i8_lane(v[u], lpg, q);
+        if (act[u]) {
+          if (job.codes[p]) st128(static_cast<int8_t*>(job.codes[p]) + c * 16, make_uint4(q[0], q[1], q[2], q[3]));
+          if (job.codes[p] && (lane & (lpg - 1)) == 0) stf(job.scales[p] + c / lpg, s);
+        }
+        if (DEQ) dequant_i8_lane(q, s, d);
+      } else {
+        uint32_t q[2];
+        float z;
+        const float s = quant_i4_lane(v[u], lpg, q, z);
+        if (act[u]) {
+          if (job.codes[p]) st64(static_cast<uint8_t*>(job.codes[p]) + c * 8, make_uint2(q[0], q[1]));
+          if (job.codes[p] && (lane & (lpg - 1)) == 0) {
+            stf(job.scales[p] + c / lpg, s);
+            stf(job.zeros[p] + c / lpg, z);
+          }
+        }
+        if (DEQ) dequant_i4_lane(q, s, z, d);
+      }
+      if (DEQ && act[u]) {
+        if (DEQ == kBF16) {
+          V8 o;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o.w[i] = pack_bf2(d[2 * i], d[2 * i + 1]);
+          st256(static_cast<uint16_t*>(job.deq) + c * 16, o);
+        } else {
+          V8 o0, o1;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            o0.w[i] = __float_as_uint(d[i]);
+            o1.w[i] = __float_as_uint(d[8 + i]);
+          }
+          float* out = static_cast<float*>(job.deq) + c * 16;
+          st256(out, o0);
+          st256(out + 8, o1);
+        }
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------- reduce kernel --
+// out[i] = ((0 + deq_0(i)) + deq_1(i)) + ... + deq_{P-1}(i)   (fp32, slab order)
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) k_reduce(Slabs s, int P, int G, int64_t c0,
+                                                     int64_t c1, float* out) {
+  const int lpg = G >> 4;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t c = c0 + static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; c < c1;
+       c += stride) {
+    const int64_t g = c / lpg;
+    uint32_t q[kMaxP][4];
+    float sc[kMaxP], zp[kMaxP];
+#pragma unroll
+    for (int p = 0; p < kMaxP; ++p) {
+      if (p < P) {
+        if (FMT == kINT8) {
+          uint4 w = ld128_stream(static_cast<const int8_t*>(s.codes[p]) + c * 16);
+          q[p][0] = w.x, q[p][1] = w.y, q[p][2] = w.z, q[p][3] = w.w;
+        } else {
+          uint2 w = ld64_stream(static_cast<const uint8_t*>(s.codes[p]) + c * 8);
+          q[p][0] = w.x, q[p][1] = w.y;
+          zp[p] = ldf_stream(s.zeros[p] + g);
+        }
+        sc[p] = ldf_stream(s.scales[p] + g);
+      }
+    }
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int p = 0; p < kMaxP; ++p) {
+      if (p < P) {
+        float d[16];
+        if (FMT == kINT8)
+          dequant_i8_lane(q[p], sc[p], d);
+        else
+          dequant_i4_lane(q[p], sc[p], zp[p], d);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], d[i]);
+      }
+    }
+    V8 o0, o1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      o0.w[i] = __float_as_uint(acc[i]);
+      o1.w[i] = __float_as_uint(acc[8 + i]);
+    }
+    st256(out + c * 16, o0);
+    st256(out + c * 16 + 8, o1);
+  }
+}
+
+// ---------------------------------------------------- tagged-block packing --
+// One thread packs a unit of 4 blocks (24 elements) of one row.
+__global__ void __launch_bounds__(kThreads) k_pack_tagged(const uint16_t* __restrict__ x,
+                                                          int64_t rows, int H, int nb,
+                                                          uint32_t epoch, uint4* blocks) {
+  const int units = (nb + 3) >> 2;
+  const int64_t total = rows * units;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; t < total;
+       t += stride) {
+    const int64_t row = t / units;
+    const int u = static_cast<int>(t - row * units);
+    const uint16_t* xr = x + row * H;
+    const int e0 = 24 * u;
+    uint32_t w[12];
+    if (e0 + 24 <= H) {
+      const uint4 a = ld128_stream(xr + e0), b = ld128_stream(xr + e0 + 8),
+                  c = ld128_stream(xr + e0 + 16);
+      w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w;
+      w[4] = b.x, w[5] = b.y, w[6] = b.z, w[7] = b.w;
+      w[8] = c.x, w[9] = c.y, w[10] = c.z, w[11] = c.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 12; ++i) {
+        const int e = e0 + 2 * i;
+        const uint32_t lo = e < H ? ld16(xr + e) : 0u;
+        const uint32_t hi = e + 1 < H ? ld16(xr + e + 1) : 0u;
+        w[i] = lo | (hi << 16);
+      }
+    }
+    uint4* br = blocks + row * nb;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int j = 4 * u + b;
+      if (j < nb) st128(br + j, make_uint4(w[3 * b], w[3 * b + 1], w[3 * b + 2], epoch));
+    }
+  }
+}
+
+// Persistent grid: enough blocks for the work, at most 8 x 256-thread
+// blocks (2048 threads, the per-SM maximum) per SM.
+int grid_for(int64_t work_items, int per_block) {
+  const int64_t need = (work_items + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  return static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+template <int FMT, bool IN_F32, int DEQ>
+cudaError_t launch_quantize_t(const QuantJob& job, cudaStream_t st) {
+  const int64_t chunks = job.n / 16;
+  const int64_t tiles = (chunks + 31) / 32;
+  const int64_t warps_needed = (tiles * job.P + kUnroll - 1) / kUnroll;
+  const int grid = grid_for(warps_needed * 32, kThreads);
+  k_quantize<FMT, IN_F32, DEQ><<<grid, kThreads, 0, st>>>(job, chunks, tiles);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int num_sms() {
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (sms[dev] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = v > 0 ? v : 1;
+  }
+  return sms[dev];
+}
+
+cudaError_t launch_quantize(int fmt, bool in_f32, int deq, const QuantJob& job, cudaStream_t st) {
+  if (job.n == 0) return cudaSuccess;
+  if (fmt == kINT8) {
+    if (!in_f32) return launch_quantize_t<kINT8, false, 0>(job, st);
+    if (deq == kBF16) return launch_quantize_t<kINT8, true, kBF16>(job, st);
+    if (deq == kF32) return launch_quantize_t<kINT8, true, kF32>(job, st);
+    return launch_quantize_t<kINT8, true, 0>(job, st);
+  }
+  if (!in_f32) return launch_quantize_t<kINT4, false, 0>(job, st);
+  if (deq == kBF16) return launch_quantize_t<kINT4, true, kBF16>(job, st);
+  if (deq == kF32) return launch_quantize_t<kINT4, true, kF32>(job, st);
+  return launch_quantize_t<kINT4, true, 0>(job, st);
+}
+
+cudaError_t launch_reduce(int fmt, const Slabs& s, int P, int G, int64_t c0, int64_t c1,
+                          float* out, cudaStream_t st) {
+  if (c1 <= c0) return cudaSuccess;
+  const int grid = grid_for(c1 - c0, kThreads);
+  if (fmt == kINT8)
+    k_reduce<kINT8><<<grid, kThreads, 0, st>>>(s, P, G, c0, c1, out);
+  else
+    k_reduce<kINT4><<<grid, kThreads, 0, st>>>(s, P, G, c0, c1, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_tagged(const void* x, int64_t rows, int H, uint32_t epoch, void* blocks,
+                               cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  const int nb = (H + 5) / 6;
+  const int64_t total = rows * ((nb + 3) / 4);
+  const int grid = grid_for(total, kThreads);
+  k_pack_tagged<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t*>(x), rows, H, nb, epoch,
+                                           static_cast<uint4*>(blocks));
+  return cudaGetLastError();
+}
+
+}  // namespace fc

@@ -1,0 +1,228 @@
+"""Thin Python binding of libfcomm (ctypes): argument marshalling only.
+
+Every step of the path runs in libfcomm's CUDA kernels; this module only
+turns torch tensors into device pointers and the current torch stream into a
+cudaStream_t, calls the C entry point of the same name, and raises FcommError
+on a non-OK status.  There is no CPU fallback: if the library cannot be
+built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+FMT_BF16, FMT_INT8_SYM, FMT_INT4_ASYM, FMT_BF16_TAGGED, FMT_F32 = 0, 1, 2, 3, 4
+FC_OK, FC_ERR_INVALID, FC_ERR_CUDA, FC_ERR_STALE_BLOCK, FC_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
+STATUS_NO_INDEX = 0x7F7F7F7F
+
+# Names exported by the C ABI (include/fcomm.h)
+EXPORTS = (
+    "fc_codes_bytes", "fc_groups", "fc_tagged_bytes", "fc_shard_range", "fc_group_quantize",
+    "fc_group_quantize_multi", "fc_reduce_dequant_sum", "fc_requant_gather", "fc_pack_tagged",
+    "fc_allreduce_residual_rmsnorm", "fc_allreduce_residual_rmsnorm_ex", "fc_status_string",
+    "fc_last_error", "fc_version",
+)
+
+
+class FcommError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+_STATUS_NAMES = {0: "FC_OK", 1: "FC_ERR_INVALID", 2: "FC_ERR_CUDA", 3: "FC_ERR_STALE_BLOCK",
+                 4: "FC_ERR_UNSUPPORTED"}
+
+
+class QSpec(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("group", ctypes.c_int32)]
+
+    def __repr__(self):
+        return f"QSpec(fmt={self.fmt}, group={self.group})"
+
+
+class QTensor(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("zeros", ctypes.c_void_p)]
+
+
+class LaunchOpts(ctypes.Structure):
+    _fields_ = [("max_ctas", ctypes.c_int32)]
+
+
+INT8_G128 = QSpec(FMT_INT8_SYM, 128)
+INT4_G32 = QSpec(FMT_INT4_ASYM, 32)
+BF16 = QSpec(FMT_BF16, 0)
+BF16_TAGGED = QSpec(FMT_BF16_TAGGED, 0)
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: Optional[str] = None):
+    """Load libfcomm.so (building it with nvcc if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or _build.build()
+    lib = ctypes.CDLL(p)
+    P, i64, i32, u32, f32 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32,
+                             ctypes.c_float)
+    QS, QT = QSpec, QTensor
+    sigs = {
+        "fc_codes_bytes": (ctypes.c_size_t, [QS, i64, i64]),
+        "fc_groups": (ctypes.c_size_t, [QS, i64, i64]),
+        "fc_tagged_bytes": (ctypes.c_size_t, [i64, i64]),
+        "fc_shard_range": (i32, [QS, i64, i64, i32, i32, ctypes.POINTER(i64),
+                                 ctypes.POINTER(i64)]),
+        "fc_group_quantize": (i32, [P, i64, i64, QS, QT, P]),
+        "fc_group_quantize_multi": (i32, [P, i32, i64, i64, QS, P, P]),
+        "fc_reduce_dequant_sum": (i32, [P, i32, i64, i64, QS, i32, P, P]),
+        "fc_requant_gather": (i32, [P, i64, i64, QS, QT, P, i32, P]),
+        "fc_pack_tagged": (i32, [P, i64, i64, u32, P, P]),
+        "fc_allreduce_residual_rmsnorm": (
+            i32, [P, i32, i64, i64, QS, P, P, P, f32, QT, P, u32, P, P]),
+        "fc_allreduce_residual_rmsnorm_ex": (
+            i32, [P, i32, i64, i64, QS, P, P, P, f32, QT, P, u32, P, P, P]),
+        "fc_status_string": (ctypes.c_char_p, [i32]),
+        "fc_last_error": (ctypes.c_char_p, []),
+        "fc_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != FC_OK:
+        raise FcommError(status, _lib.fc_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libfcomm takes CUDA tensors (device memory)")
+    if not t.is_contiguous():
+        raise ValueError("libfcomm takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _qt(q) -> QTensor:
+    """(codes, scales, zeros) tuple of tensors (or None entries) -> QTensor."""
+    if q is None:
+        return QTensor(None, None, None)
+    codes, scales, zeros = (tuple(q) + (None, None, None))[:3]
+    return QTensor(_ptr(codes), _ptr(scales), _ptr(zeros))
+
+
+def _rows_hidden(x: torch.Tensor):
+    if x.dim() != 2:
+        raise ValueError("expected a [rows, hidden] tensor")
+    return x.shape[0], x.shape[1]
+
+
+# ----------------------------------------------------------------- sizes ---
+def codes_bytes(spec: QSpec, rows: int, hidden: int) -> int:
+    return load().fc_codes_bytes(spec, rows, hidden)
+
+
+def groups(spec: QSpec, rows: int, hidden: int) -> int:
+    return load().fc_groups(spec, rows, hidden)
+
+
+def tagged_bytes(rows: int, hidden: int) -> int:
+    return load().fc_tagged_bytes(rows, hidden)
+
+
+def shard_range(spec: QSpec, rows: int, hidden: int, P: int, shard: int):
+    g0, g1 = ctypes.c_int64(), ctypes.c_int64()
+    _check(load().fc_shard_range(spec, rows, hidden, P, shard, ctypes.byref(g0), ctypes.byref(g1)))
+    return g0.value, g1.value
+
+
+def alloc_qtensor(spec: QSpec, rows: int, hidden: int, device="cuda"):
+    """Caller-owned (codes, scales, zeros) torch tensors for a quantized tensor."""
+    nb = codes_bytes(spec, rows, hidden)
+    ng = groups(spec, rows, hidden)
+    codes = torch.empty(nb, dtype=torch.uint8, device=device)
+    scales = torch.empty(ng, dtype=torch.float32, device=device)
+    zeros = torch.empty(ng, dtype=torch.float32, device=device) if spec.fmt == FMT_INT4_ASYM \
+        else None
+    return codes, scales, zeros
+
+
+# --------------------------------------------------------------- compute ---
+def group_quantize(x: torch.Tensor, spec: QSpec, out, stream=None):
+    """Quantize one [rows, hidden] bf16 slab into out = (codes, scales[, zeros])."""
+    rows, hidden = _rows_hidden(x)
+    _check(load().fc_group_quantize(_ptr(x), rows, hidden, spec, _qt(out), _stream(stream)))
+
+
+def group_quantize_multi(xs: Sequence[torch.Tensor], spec: QSpec, outs, stream=None):
+    rows, hidden = _rows_hidden(xs[0])
+    xp = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+    qo = (QTensor * len(outs))(*[_qt(o) for o in outs])
+    _check(load().fc_group_quantize_multi(xp, len(xs), rows, hidden, spec, qo, _stream(stream)))
+
+
+def reduce_dequant_sum(slabs, spec: QSpec, rows: int, hidden: int, out: torch.Tensor,
+                       shard: int = -1, stream=None):
+    """out[rows, hidden] fp32 = fixed-order sum of the dequantized slabs (or one shard)."""
+    qs = (QTensor * len(slabs))(*[_qt(s) for s in slabs])
+    _check(load().fc_reduce_dequant_sum(qs, len(slabs), rows, hidden, spec, shard, _ptr(out),
+                                        _stream(stream)))
+
+
+def requant_gather(reduced: torch.Tensor, spec: QSpec, requant_out=None,
+                   out: Optional[torch.Tensor] = None, out_dtype: int = FMT_BF16, stream=None):
+    rows, hidden = _rows_hidden(reduced)
+    _check(load().fc_requant_gather(_ptr(reduced), rows, hidden, spec, _qt(requant_out),
+                                    _ptr(out), out_dtype, _stream(stream)))
+
+
+def pack_tagged(x: torch.Tensor, epoch: int, blocks: torch.Tensor, stream=None):
+    rows, hidden = _rows_hidden(x)
+    _check(load().fc_pack_tagged(_ptr(x), rows, hidden, epoch, _ptr(blocks), _stream(stream)))
+
+
+def allreduce_residual_rmsnorm(slabs, spec: QSpec, rows: int, hidden: int,
+                               residual_in: torch.Tensor, residual_out: torch.Tensor,
+                               gamma: torch.Tensor, eps: float, y: torch.Tensor,
+                               requant_out=None, expected_epoch: int = 0,
+                               d_status: Optional[torch.Tensor] = None, max_ctas: int = 0,
+                               stream=None):
+    """The fused quantized All-Reduce + residual add + RMSNorm.
+
+    slabs: list of P (codes, scales, zeros) tuples (INT8/INT4), or of bf16
+    tensors / tagged-block tensors (BF16 / BF16_TAGGED)."""
+    qs = (QTensor * len(slabs))(*[_qt(s if isinstance(s, (tuple, list)) else (s,))
+                                  for s in slabs])
+    opts = LaunchOpts(max_ctas)
+    _check(load().fc_allreduce_residual_rmsnorm_ex(
+        qs, len(slabs), rows, hidden, spec, _ptr(residual_in), _ptr(residual_out), _ptr(gamma),
+        eps, _qt(requant_out), _ptr(y), expected_epoch, _ptr(d_status), ctypes.byref(opts),
+        _stream(stream)))
+
+
+def version() -> str:
+    return load().fc_version().decode()

@@ -1,0 +1,163 @@
+"""One step of the whole hot path on device-resident buffers.
+
+A step is what one tensor-parallel layer boundary does, with the P ranks
+standing in as P slabs in one GPU's HBM:
+
+* quantized formats (INT8 / INT4): sender-side group quantization of all P
+  slabs (one launch), then the fused two-step reduce + residual add +
+  RMSNorm (one launch) that also writes the requantized all-gather payload;
+* BF16: the fused reduce + residual add + RMSNorm on the bf16 slabs;
+* BF16_TAGGED: the producers pack every slab into epoch-tagged blocks with a
+  fresh epoch (one launch per slab), then the consumer validates and reduces
+  them; with ``splits`` > 1 the token rows are split into that many subsets
+  that run on their own streams (TokenWeave's token splitting).
+
+All device memory is allocated here by torch at construction; ``step()``
+only launches libfcomm kernels.  ``alg_bytes()`` gives the bytes the method
+must move per step (intermediates kept on chip are not counted).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import fcomm as fc
+from .synth import FMT_BF16, FMT_BF16_TAGGED, FMT_INT4_ASYM, FMT_INT8_SYM, Workload
+
+
+def _bf16_dev(bits: np.ndarray, device) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits, np.uint16).view(np.int16))
+    return t.view(torch.bfloat16).to(device)
+
+
+def qs_bytes(w: Workload, E: int) -> int:
+    """Bytes of one quantized slab of E elements: codes + scales (+ zeros)."""
+    ng = E // w.group
+    if w.fmt == FMT_INT8_SYM:
+        return E + 4 * ng
+    if w.fmt == FMT_INT4_ASYM:
+        return E // 2 + 8 * ng
+    raise ValueError(w.fmt)
+
+
+class Pipeline:
+    def __init__(self, w: Workload, inputs: dict, device="cuda", with_payload=True):
+        self.w = w
+        self.device = device
+        self.spec = fc.QSpec(w.fmt, w.group)
+        T, H = w.T, w.H
+        self.x = [_bf16_dev(s, device) for s in inputs["slabs"]]
+        self.residual = _bf16_dev(inputs["residual"], device)
+        self.gamma = _bf16_dev(inputs["gamma"], device)
+        self.residual_out = torch.empty_like(self.residual)
+        self.y = torch.empty_like(self.residual)
+        self.epoch = 0
+        self.status = None
+        self.payload = None
+        if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
+            self.codes = [fc.alloc_qtensor(self.spec, T, H, device) for _ in range(w.P)]
+            if with_payload:
+                self.payload = fc.alloc_qtensor(self.spec, T, H, device)
+        elif w.fmt == FMT_BF16_TAGGED:
+            self.blocks = [torch.empty(fc.tagged_bytes(T, H), dtype=torch.uint8, device=device)
+                           for _ in range(w.P)]
+            self.status = torch.zeros(max(1, w.splits), 2, dtype=torch.int32, device=device)
+            self.streams = [torch.cuda.Stream(device=device) for _ in range(max(1, w.splits))]
+        self.launches_per_step = self._launches()
+
+    # ------------------------------------------------------------------
+    def _launches(self) -> int:
+        w = self.w
+        if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
+            return 2
+        if w.fmt == FMT_BF16:
+            return 1
+        return w.P + max(1, w.splits)
+
+    def step(self, stream=None):
+        """Launch one pass of the hot path on `stream` (default: current)."""
+        st = stream or torch.cuda.current_stream(self.device)
+        self.sender(st)
+        self.consumer(st)
+
+    def step_marked(self, stream, marks):
+        """step() with CUDA events marks[0], marks[1], marks[2] recorded before
+        the sender stage, between the stages and after the fused stage."""
+        marks[0].record(stream)
+        self.sender(stream)
+        marks[1].record(stream)
+        self.consumer(stream)
+        marks[2].record(stream)
+
+    def sender(self, st):
+        """Sender side: group-quantize (INT8/INT4) or pack with a fresh epoch (tagged)."""
+        w = self.w
+        if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
+            fc.group_quantize_multi(self.x, self.spec, self.codes, stream=st)
+        elif w.fmt == FMT_BF16_TAGGED:
+            self.epoch = (self.epoch + 1) & 0xFFFFFFFF
+            for p in range(w.P):
+                fc.pack_tagged(self.x[p], self.epoch, self.blocks[p], stream=st)
+
+    def consumer(self, st):
+        """Receiver side: the fused reduce + residual add + RMSNorm."""
+        w = self.w
+        if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
+            fc.allreduce_residual_rmsnorm(self.codes, self.spec, w.T, w.H, self.residual,
+                                          self.residual_out, self.gamma, w.eps, self.y,
+                                          requant_out=self.payload, stream=st)
+        elif w.fmt == FMT_BF16:
+            fc.allreduce_residual_rmsnorm(self.x, self.spec, w.T, w.H, self.residual,
+                                          self.residual_out, self.gamma, w.eps, self.y,
+                                          stream=st)
+        else:
+            self._split_consume(st)
+
+    def _split_consume(self, st):
+        w = self.w
+        n = max(1, w.splits)
+        bpr = fc.tagged_bytes(1, w.H)
+        bounds = [w.T * i // n for i in range(n + 1)]
+        fork = torch.cuda.Event()
+        fork.record(st)
+        joins = []
+        for i, s in enumerate(self.streams):
+            r0, r1 = bounds[i], bounds[i + 1]
+            s.wait_event(fork)
+            fc.allreduce_residual_rmsnorm(
+                [b[r0 * bpr:r1 * bpr] for b in self.blocks], self.spec, r1 - r0, w.H,
+                self.residual[r0:r1], self.residual_out[r0:r1], self.gamma, w.eps,
+                self.y[r0:r1], expected_epoch=self.epoch, d_status=self.status[i], stream=s)
+            ev = torch.cuda.Event()
+            ev.record(s)
+            joins.append(ev)
+        for ev in joins:
+            st.wait_event(ev)
+
+    # ------------------------------------------------------------------
+    def alg_bytes(self) -> dict:
+        """Algorithmic bytes per step, by stage: {'sender': .., 'fused': ..}."""
+        w = self.w
+        E, H, P = w.T * w.H, w.H, w.P
+        if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
+            qs = qs_bytes(w, E)
+            return {"sender": P * 2 * E + P * qs,
+                    "fused": P * qs + 2 * E + 2 * H + (qs if self.payload is not None else 0)
+                    + 4 * E}
+        if w.fmt == FMT_BF16:
+            return {"sender": 0, "fused": P * 2 * E + 2 * E + 2 * H + 4 * E}
+        tb = fc.tagged_bytes(w.T, w.H)
+        return {"sender": P * 2 * E + P * tb,
+                "fused": P * tb + 2 * E + max(1, w.splits) * 2 * H + 4 * E}
+
+    def outputs(self) -> dict:
+        """Host copies (uint16 bf16 bits etc.) of the step's outputs."""
+        torch.cuda.synchronize(self.device)
+        out = dict(h=self.residual_out.view(torch.int16).cpu().numpy().view(np.uint16),
+                   y=self.y.view(torch.int16).cpu().numpy().view(np.uint16))
+        if self.payload is not None:
+            out.update(codes=self.payload[0].cpu().numpy(), scales=self.payload[1].cpu().numpy(),
+                       zeros=None if self.payload[2] is None else self.payload[2].cpu().numpy())
+        if self.status is not None:
+            out["status"] = self.status.cpu().numpy()
+        return out

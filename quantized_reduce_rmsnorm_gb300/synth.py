@@ -28,7 +28,9 @@ Every workload: residual N(0,1), gamma N(1, 0.1), eps 1e-5.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
+import os
 
 import numpy as np
 import torch
@@ -121,7 +123,8 @@ def _rows_tensor(w: Workload, seed: int, stream: int, rows: np.ndarray, dist: st
     """bf16 bits [len(rows), H] of the given rows of one [T, H] stream."""
     out = np.empty((len(rows), w.H), np.uint16)
     rows = np.asarray(rows, np.int64)
-    for c in np.unique(rows // ROW_CHUNK):
+
+    def fill(c):
         r0 = int(c) * ROW_CHUNK
         nr = min(ROW_CHUNK, w.T - r0)
         x = _draw(_rng(seed, stream, int(c)), nr * w.H, dist).reshape(nr, w.H)
@@ -129,6 +132,16 @@ def _rows_tensor(w: Workload, seed: int, stream: int, rows: np.ndarray, dist: st
             x[:, outliers] *= np.float32(w.outlier_scale)
         sel = np.nonzero(rows // ROW_CHUNK == c)[0]
         out[sel] = _to_bf16_bits(x[rows[sel] - r0])
+
+    chunks = np.unique(rows // ROW_CHUNK)
+    if len(chunks) > 4:
+        # each chunk has its own counter-based stream, so the result does not
+        # depend on how chunks are scheduled over threads
+        with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, chunks))
+    else:
+        for c in chunks:
+            fill(c)
     return out
 
 

@@ -96,6 +96,7 @@ def check_bf16_rne(orc):
                      1 + 2 ** -8 + 2 ** -20, 0.0, -0.0], np.float32)
     x = np.concatenate([x, ties])
     assert np.array_equal(orc.f32_to_bf16(x), torch_bf16_bits(x))
+    assert np.array_equal(orc.f32_to_bf16_array(x), torch_bf16_bits(x))
     assert list(orc.f32_to_bf16(ties[:2])) == [0x3F80, 0x3F82]
 
 

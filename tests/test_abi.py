@@ -1,0 +1,129 @@
+"""CPU checks of the C ABI: the library loads, exports every symbol the
+header declares, sizes and shard ranges are right, and bad arguments are
+rejected before anything touches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_reduce_rmsnorm_gb300 as fc
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "fcomm.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fc_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = fc.fcomm.load()
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in fcomm.h but not exported"
+    assert set(names) == set(fc.fcomm.EXPORTS)
+
+
+def test_version_and_status_strings():
+    lib = fc.fcomm.load()
+    assert "sm_103a" in fc.version()
+    assert lib.fc_status_string(3) == b"FC_ERR_STALE_BLOCK"
+
+
+def test_sizes():
+    assert fc.codes_bytes(fc.INT8_G128, 64, 8192) == 64 * 8192
+    assert fc.codes_bytes(fc.INT4_G32, 8192, 8192) == 8192 * 8192 // 2
+    assert fc.codes_bytes(fc.BF16, 3, 16) == 96
+    assert fc.groups(fc.INT4_G32, 8192, 8192) == 8192 * 8192 // 32
+    assert fc.groups(fc.BF16, 8192, 8192) == 0
+    assert fc.tagged_bytes(2048, 5120) == 2048 * 854 * 16
+    assert fc.tagged_bytes(1, 6) == 16 and fc.tagged_bytes(1, 7) == 32
+
+
+@pytest.mark.parametrize("P", [2, 3, 4, 8])
+def test_shard_ranges_partition_the_groups(P):
+    ng = fc.groups(fc.INT8_G128, 7, 1152)
+    ranges = [fc.shard_range(fc.INT8_G128, 7, 1152, P, j) for j in range(P)]
+    per = -(-ng // P)
+    assert ranges[0][0] == 0 and ranges[-1][1] == ng
+    for (a0, a1), (b0, b1) in zip(ranges, ranges[1:]):
+        assert a1 == b0
+    assert all(0 <= b - a <= per for a, b in ranges)
+
+
+def _status(call):
+    lib = fc.fcomm.load()
+    return call(lib), lib.fc_last_error().decode()
+
+
+@pytest.mark.parametrize("hidden,group,fmt", [
+    (100, 128, 1),     # hidden not a multiple of 16
+    (4096, 96, 1),     # group not a power of two
+    (4096, 8, 2),      # group below 16
+    (4000, 128, 1),    # hidden not a multiple of group
+    (4096, 128, 9),    # unknown format
+    (4096, 128, 0),    # bf16 is not a quantized format
+])
+def test_quantize_rejects_bad_specs(hidden, group, fmt):
+    st, msg = _status(lambda L: L.fc_group_quantize(None, 4, hidden, fc.QSpec(fmt, group),
+                                                    fc.QTensor(), None))
+    assert st == fc.FC_ERR_INVALID and msg
+
+
+def test_pointer_checks_precede_any_launch():
+    q = fc.QTensor(64, 128, None)
+    st, msg = _status(lambda L: L.fc_group_quantize(None, 4, 4096, fc.INT8_G128, q, None))
+    assert st == fc.FC_ERR_INVALID and "NULL" in msg
+    st, msg = _status(lambda L: L.fc_group_quantize(48, 4, 4096, fc.INT8_G128, q, None))
+    assert st == fc.FC_ERR_INVALID and "aligned" in msg
+    bad = fc.QTensor(64, 130, None)   # scales not 4-byte aligned
+    st, msg = _status(lambda L: L.fc_group_quantize(64, 4, 4096, fc.INT8_G128, bad, None))
+    assert st == fc.FC_ERR_INVALID and "scales" in msg
+    nozeros = fc.QTensor(64, 128, None)
+    st, msg = _status(lambda L: L.fc_group_quantize(64, 4, 4096, fc.INT4_G32, nozeros, None))
+    assert st == fc.FC_ERR_INVALID and "zeros" in msg
+
+
+def test_fused_rejects_bad_p_eps_and_opts():
+    slabs = (fc.QTensor * 9)(*[fc.QTensor(64, 128, 256)] * 9)
+    q = fc.QTensor()
+    lib = fc.fcomm.load()
+    for P in (0, 1, 9):
+        st = lib.fc_allreduce_residual_rmsnorm(slabs, P, 4, 4096, fc.INT8_G128, 64, 64, 64,
+                                               1e-5, q, 64, 0, None, None)
+        assert st == fc.FC_ERR_INVALID
+    st = lib.fc_allreduce_residual_rmsnorm(slabs, 2, 4, 4096, fc.INT8_G128, 64, 64, 64,
+                                           -1.0, q, 64, 0, None, None)
+    assert st == fc.FC_ERR_INVALID
+    opts = fc.LaunchOpts(-1)
+    st = lib.fc_allreduce_residual_rmsnorm_ex(slabs, 2, 4, 4096, fc.INT8_G128, 64, 64, 64,
+                                              1e-5, q, 64, 0, None, ctypes.byref(opts), None)
+    assert st == fc.FC_ERR_INVALID
+
+
+def test_reduce_rejects_bad_shard():
+    slabs = (fc.QTensor * 2)(*[fc.QTensor(64, 128, 256)] * 2)
+    lib = fc.fcomm.load()
+    for shard in (-2, 2):
+        st = lib.fc_reduce_dequant_sum(slabs, 2, 4, 4096, fc.INT8_G128, shard, 64, None)
+        assert st == fc.FC_ERR_INVALID
+
+
+def test_rows_zero_is_a_no_op():
+    lib = fc.fcomm.load()
+    st = lib.fc_group_quantize(None, 0, 4096, fc.INT8_G128, fc.QTensor(), None)
+    assert st == fc.FC_OK
+
+
+def test_product_package_never_imports_the_oracle():
+    pkg = os.path.dirname(fc.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(root, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle", txt, re.M), f
+                assert "liboracle" not in txt and "oracle.h" not in txt, f

@@ -1,0 +1,433 @@
+"""GPU parity: libfcomm (through its C ABI) against the CPU oracle, element by
+element, on the same seeded inputs.
+
+Bar: codes, scales, zero-points, fp32 sums and residual_out bit-exact; y
+(RMSNorm output, bf16) within one bf16 ulp of the oracle (|dy| <= 2^-7 |y|).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import quantized_reduce_rmsnorm_gb300 as fc
+from quantized_reduce_rmsnorm_gb300 import synth
+from gpu_util import (assert_bits_equal, assert_y_close, bf16_float, dev, dev_bf16, host,
+                      host_bits)
+
+pytestmark = pytest.mark.gpu
+
+I8, I4, BF, TG = synth.FMT_INT8_SYM, synth.FMT_INT4_ASYM, synth.FMT_BF16, synth.FMT_BF16_TAGGED
+
+
+def spec_of(fmt, G):
+    return fc.QSpec(fmt, G)
+
+
+def small(name, **kw):
+    """A workload of the given shape family (sizes the oracle finishes quickly)."""
+    base = synth.WORKLOADS.get(name)
+    if base is None:
+        base = synth.Workload(name, P=2, T=1, H=4096, fmt=I8, group=128)
+    return synth.Workload(**{**base.__dict__, "name": name, **kw})
+
+
+def quantize_on_gpu(w, inp):
+    spec = spec_of(w.fmt, w.group)
+    xs = [dev_bf16(s) for s in inp["slabs"]]
+    outs = [fc.alloc_qtensor(spec, w.T, w.H) for _ in range(w.P)]
+    fc.group_quantize_multi(xs, spec, outs)
+    return outs
+
+
+def oracle_quant(orc, w, slab_bits):
+    return orc.quantize(w.fmt, bf16_float(slab_bits).ravel(), w.group)
+
+
+# ------------------------------------------------------------- quantize ---
+QUANT_CASES = [
+    ("decode-tiny", {}),
+    ("decode", {}),
+    ("prefill", {"T": 48}),
+    ("i8-g32-ragged", {"P": 3, "T": 7, "H": 1184, "fmt": I8, "group": 32}),
+    ("i4-g64", {"P": 2, "T": 5, "H": 4160, "fmt": I4, "group": 64, "outlier_frac": 0.01,
+                "outlier_scale": 100.0}),
+    ("i8-g512", {"P": 2, "T": 3, "H": 2048, "fmt": I8, "group": 512}),
+    ("i4-g16", {"P": 2, "T": 3, "H": 1040, "fmt": I4, "group": 16}),
+]
+
+
+@pytest.mark.parametrize("name,kw", QUANT_CASES, ids=[c[0] for c in QUANT_CASES])
+def test_group_quantize_bit_exact(orc, name, kw):
+    w = small(name, **kw)
+    inp = synth.make_inputs(w, seed=1)
+    outs = quantize_on_gpu(w, inp)
+    torch.cuda.synchronize()
+    for p in range(w.P):
+        q, s, z = oracle_quant(orc, w, inp["slabs"][p])
+        assert_bits_equal(host(outs[p][0]), q, f"codes slab {p}")
+        assert_bits_equal(host(outs[p][1]), s, f"scales slab {p}")
+        if w.fmt == I4:
+            assert_bits_equal(host(outs[p][2]), z, f"zeros slab {p}")
+
+
+def test_group_quantize_single_matches_multi():
+    w = small("decode", T=8)
+    inp = synth.make_inputs(w, seed=2)
+    spec = spec_of(w.fmt, w.group)
+    multi = quantize_on_gpu(w, inp)
+    for p in range(w.P):
+        one = fc.alloc_qtensor(spec, w.T, w.H)
+        fc.group_quantize(dev_bf16(inp["slabs"][p]), spec, one)
+        torch.cuda.synchronize()
+        assert torch.equal(one[0], multi[p][0]) and torch.equal(one[1], multi[p][1])
+
+
+@pytest.mark.parametrize("fmt,G", [(I8, 128), (I4, 32)])
+def test_quantize_degenerate_groups(orc, fmt, G):
+    """All-zero groups, constant groups, signed zeros, one huge outlier, ties."""
+    H = 512
+    x = np.zeros((4, H), np.float32)
+    x[1, :] = 2.5                                  # constant row
+    x[2, :G] = -0.0
+    x[2, G:2 * G:2] = -0.0
+    x[2, G + 1:2 * G:2] = 0.0                      # mixed signed zeros
+    x[2, 2 * G:] = np.arange(H - 2 * G) * 0.5      # exact ties after scaling
+    x[3, :] = np.linspace(-3, 3, H)
+    x[3, 7] = 3.0e30                               # one huge outlier
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    spec = spec_of(fmt, G)
+    out = fc.alloc_qtensor(spec, 4, H)
+    fc.group_quantize(dev_bf16(bits), spec, out)
+    torch.cuda.synchronize()
+    q, s, z = orc.quantize(fmt, bf16_float(bits).ravel(), G)
+    assert_bits_equal(host(out[0]), q, "codes")
+    assert_bits_equal(host(out[1]), s, "scales")
+    if fmt == I4:
+        assert_bits_equal(host(out[2]), z, "zeros")
+
+
+# --------------------------------------------------------------- reduce ---
+REDUCE_CASES = [(I8, 128, 2), (I8, 128, 3), (I8, 128, 8), (I4, 32, 2), (I4, 32, 4),
+                (I4, 32, 8), (I8, 64, 5)]
+
+
+@pytest.mark.parametrize("fmt,G,P", REDUCE_CASES)
+def test_reduce_dequant_sum_bit_exact(orc, fmt, G, P):
+    w = synth.Workload("reduce", P=P, T=9, H=2048, fmt=fmt, group=G, outlier_frac=0.01,
+                       outlier_scale=30.0)
+    inp = synth.make_inputs(w, seed=3)
+    outs = quantize_on_gpu(w, inp)
+    red = torch.empty(w.T, w.H, dtype=torch.float32, device="cuda")
+    fc.reduce_dequant_sum(outs, spec_of(fmt, G), w.T, w.H, red)
+    torch.cuda.synchronize()
+    slabs = [oracle_quant(orc, w, s) for s in inp["slabs"]]
+    want = orc.two_step(fmt, slabs, G)
+    assert_bits_equal(host(red), want["reduced"], "reduced fp32")
+
+
+@pytest.mark.parametrize("fmt,G,P", [(I8, 128, 3), (I4, 32, 8)])
+def test_reduce_shards_write_only_their_range(orc, fmt, G, P):
+    w = synth.Workload("shards", P=P, T=5, H=1024, fmt=fmt, group=G)
+    inp = synth.make_inputs(w, seed=4)
+    outs = quantize_on_gpu(w, inp)
+    spec = spec_of(fmt, G)
+    slabs = [oracle_quant(orc, w, s) for s in inp["slabs"]]
+    want = orc.two_step(fmt, slabs, G)["reduced"]
+    full = torch.full((w.T, w.H), float("nan"), device="cuda")
+    for j in range(P):
+        part = torch.full((w.T, w.H), float("nan"), device="cuda")
+        fc.reduce_dequant_sum(outs, spec, w.T, w.H, part, shard=j)
+        fc.reduce_dequant_sum(outs, spec, w.T, w.H, full, shard=j)
+        g0, g1 = fc.shard_range(spec, w.T, w.H, P, j)
+        torch.cuda.synchronize()
+        got = host(part).ravel()
+        assert np.all(np.isnan(got[:g0 * G])) and np.all(np.isnan(got[g1 * G:]))
+        assert_bits_equal(got[g0 * G:g1 * G], want[g0 * G:g1 * G], f"shard {j}")
+    assert_bits_equal(host(full), want, "all shards")
+
+
+# ---------------------------------------------------------- requant/gather --
+@pytest.mark.parametrize("fmt,G", [(I8, 128), (I4, 32), (I8, 32), (I4, 128)])
+@pytest.mark.parametrize("out_dtype", [fc.FMT_BF16, fc.FMT_F32])
+def test_requant_gather_bit_exact(orc, fmt, G, out_dtype):
+    rng = np.random.default_rng(5)
+    T, H = 6, 2048
+    red = (rng.standard_normal((T, H)) * np.exp(rng.uniform(-5, 5, (T, 1)))).astype(np.float32)
+    red[2, :G] = 0.0
+    red[3, G:2 * G] = 1.25
+    spec = spec_of(fmt, G)
+    rq = fc.alloc_qtensor(spec, T, H)
+    out = torch.empty(T, H, dtype=torch.bfloat16 if out_dtype == fc.FMT_BF16 else torch.float32,
+                      device="cuda")
+    fc.requant_gather(dev(red), spec, rq, out, out_dtype)
+    torch.cuda.synchronize()
+    q, s, z = orc.quantize(fmt, red.ravel(), G)
+    d = orc.dequantize(fmt, q, s, z, G)
+    assert_bits_equal(host(rq[0]), q, "codes")
+    assert_bits_equal(host(rq[1]), s, "scales")
+    if fmt == I4:
+        assert_bits_equal(host(rq[2]), z, "zeros")
+    if out_dtype == fc.FMT_F32:
+        assert_bits_equal(host(out), d, "gathered fp32")
+    else:
+        assert_bits_equal(host_bits(out), orc.f32_to_bf16_array(d), "gathered bf16")
+
+
+@pytest.mark.parametrize("fmt,G,P", [(I8, 128, 8), (I4, 32, 4), (I4, 32, 3)])
+def test_two_step_chain_equals_oracle(orc, fmt, G, P):
+    """quantize -> reduce-scatter math per shard -> requant -> gather on the
+    GPU equals the oracle's two-step result (which equals the direct one)."""
+    w = synth.Workload("chain", P=P, T=16, H=4096, fmt=fmt, group=G, dist="student_t3")
+    inp = synth.make_inputs(w, seed=6)
+    spec = spec_of(fmt, G)
+    outs = quantize_on_gpu(w, inp)
+    red = torch.empty(w.T, w.H, device="cuda")
+    for j in range(P):
+        fc.reduce_dequant_sum(outs, spec, w.T, w.H, red, shard=j)
+    rq = fc.alloc_qtensor(spec, w.T, w.H)
+    gath = torch.empty(w.T, w.H, device="cuda")
+    fc.requant_gather(red, spec, rq, gath, fc.FMT_F32)
+    torch.cuda.synchronize()
+    want = orc.two_step(fmt, [oracle_quant(orc, w, s) for s in inp["slabs"]], G, shards=P)
+    assert_bits_equal(host(rq[0]), want["codes"], "payload codes")
+    assert_bits_equal(host(rq[1]), want["scales"], "payload scales")
+    assert_bits_equal(host(gath), want["gathered"], "gathered")
+
+
+# ------------------------------------------------------------------ fused --
+def run_fused(w, inp, seed_payload=True, max_ctas=0, alias=False, epoch=7):
+    """Quantize (or pack) the slabs on the GPU, run the fused call; returns host arrays."""
+    spec = spec_of(w.fmt, w.group)
+    if w.fmt in (I8, I4):
+        slabs = quantize_on_gpu(w, inp)
+    elif w.fmt == BF:
+        slabs = [dev_bf16(s) for s in inp["slabs"]]
+    else:
+        slabs = []
+        for s in inp["slabs"]:
+            blk = torch.empty(fc.tagged_bytes(w.T, w.H), dtype=torch.uint8, device="cuda")
+            fc.pack_tagged(dev_bf16(s), epoch, blk)
+            slabs.append(blk)
+    r_in = dev_bf16(inp["residual"])
+    r_out = r_in if alias else torch.empty_like(r_in)
+    gam = dev_bf16(inp["gamma"])
+    y = torch.empty_like(r_in)
+    rq = fc.alloc_qtensor(spec, w.T, w.H) if (w.fmt in (I8, I4) and seed_payload) else None
+    st = torch.zeros(2, dtype=torch.int32, device="cuda") if w.fmt == TG else None
+    fc.allreduce_residual_rmsnorm(slabs, spec, w.T, w.H, r_in, r_out, gam, w.eps, y,
+                                  requant_out=rq, expected_epoch=epoch, d_status=st,
+                                  max_ctas=max_ctas)
+    torch.cuda.synchronize()
+    res = dict(h=host_bits(r_out), y=host_bits(y))
+    if rq is not None:
+        res.update(codes=host(rq[0]), scales=host(rq[1]),
+                   zeros=host(rq[2]) if rq[2] is not None else None)
+    if st is not None:
+        res["status"] = host(st)
+    return res
+
+
+def oracle_fused(orc, w, inp):
+    fmt = BF if w.fmt == TG else w.fmt
+    return orc.allreduce_residual_rmsnorm(fmt, inp["slabs"], inp["residual"], inp["gamma"],
+                                          w.T, w.H, w.group, w.eps)
+
+
+def check_fused(orc, w, got, want):
+    assert_bits_equal(got["h"], want["h"], "residual_out")
+    exact = assert_y_close(got["y"], want["y"])
+    assert exact > 0.99, f"only {exact:.4f} of y bit-exact"
+    if "codes" in got:
+        assert_bits_equal(got["codes"], want["codes"], "payload codes")
+        assert_bits_equal(got["scales"], want["scales"], "payload scales")
+        if w.fmt == I4:
+            assert_bits_equal(got["zeros"], want["zeros"], "payload zeros")
+
+
+FUSED_CASES = [
+    ("decode-tiny", {}),
+    ("decode", {}),
+    ("prefill", {"T": 24}),
+    ("token-split", {"T": 40}),
+    ("bf16-p3", {"P": 3, "T": 5, "H": 4096, "fmt": BF, "group": 0}),
+    ("i8-ragged-h", {"P": 3, "T": 11, "H": 1152, "fmt": I8, "group": 128}),
+    ("i4-ragged-h", {"P": 5, "T": 9, "H": 4128, "fmt": I4, "group": 32}),
+    ("i4-wide-h", {"P": 2, "T": 3, "H": 16384, "fmt": I4, "group": 32}),
+    ("i8-wide-h", {"P": 2, "T": 2, "H": 32768, "fmt": I8, "group": 128}),
+    ("tagged-ragged-h", {"P": 2, "T": 6, "H": 1040, "fmt": TG, "group": 0}),
+    ("tagged-h16", {"P": 4, "T": 3, "H": 16, "fmt": TG, "group": 0}),
+    ("i8-h16", {"P": 2, "T": 5, "H": 16, "fmt": I8, "group": 16}),
+]
+
+
+@pytest.mark.parametrize("name,kw", FUSED_CASES, ids=[c[0] for c in FUSED_CASES])
+def test_fused_matches_oracle(orc, name, kw):
+    w = small(name, **kw)
+    inp = synth.make_inputs(w, seed=8)
+    got = run_fused(w, inp)
+    check_fused(orc, w, got, oracle_fused(orc, w, inp))
+    if w.fmt == TG:
+        assert list(got["status"]) == [fc.FC_OK, fc.STATUS_NO_INDEX]
+
+
+def test_fused_in_place_residual_and_capped_grid(orc):
+    w = small("prefill", T=20)
+    inp = synth.make_inputs(w, seed=9)
+    want = oracle_fused(orc, w, inp)
+    check_fused(orc, w, run_fused(w, inp, alias=True), want)
+    for cap in (1, 2, 8):
+        check_fused(orc, w, run_fused(w, inp, max_ctas=cap), want)
+
+
+def test_fused_without_payload(orc):
+    w = small("decode", T=4)
+    inp = synth.make_inputs(w, seed=10)
+    got = run_fused(w, inp, seed_payload=False)
+    want = oracle_fused(orc, w, inp)
+    assert_bits_equal(got["h"], want["h"], "residual_out")
+    assert_y_close(got["y"], want["y"])
+
+
+def test_fused_degenerate_rows(orc):
+    """All-zero slabs and residual (y = 0), constant rows, zero gamma."""
+    w = synth.Workload("degenerate", P=2, T=3, H=1024, fmt=I8, group=128)
+    inp = synth.make_inputs(w, seed=11)
+    inp["slabs"] = [s.copy() for s in inp["slabs"]]
+    for s in inp["slabs"]:
+        s[0] = 0
+        s[1] = 0x3FC0  # 1.5
+    inp["residual"] = inp["residual"].copy()
+    inp["residual"][0] = 0
+    inp["residual"][1] = 0
+    inp["gamma"] = inp["gamma"].copy()
+    inp["gamma"][:8] = 0
+    got = run_fused(w, inp)
+    want = oracle_fused(orc, w, inp)
+    check_fused(orc, w, got, want)
+    assert not got["y"][0].any()
+
+
+def test_tagged_pack_bit_exact(orc):
+    for T, H in ((3, 5120), (4, 1040), (2, 16), (5, 4096)):
+        rng = np.random.default_rng(T * H)
+        x = rng.integers(0, 1 << 16, (T, H)).astype(np.uint16)
+        blk = torch.empty(fc.tagged_bytes(T, H), dtype=torch.uint8, device="cuda")
+        fc.pack_tagged(dev_bf16(x), 0xABCD1234, blk)
+        torch.cuda.synchronize()
+        assert_bits_equal(host(blk).view(np.uint32), orc.pack_tagged(x, T, H, 0xABCD1234),
+                          f"tagged blocks {T}x{H}")
+
+
+def test_tagged_stale_block_is_reported(orc):
+    """Blocks built on the host by the oracle; one or two tags corrupted
+    before upload: the call reports FC_ERR_STALE_BLOCK and the first index,
+    and never hangs.  Clean blocks give FC_OK and oracle-equal outputs."""
+    w = synth.Workload("stale", P=4, T=6, H=1000 // 16 * 16, fmt=TG, group=0)
+    inp = synth.make_inputs(w, seed=12)
+    ep = 41
+    blocks = [orc.pack_tagged(s, w.T, w.H, ep) for s in inp["slabs"]]
+    nb = orc.tagged_blocks_per_row(w.H)
+    spec = spec_of(TG, 0)
+    r_in, gam = dev_bf16(inp["residual"]), dev_bf16(inp["gamma"])
+    r_out, y = torch.empty_like(r_in), torch.empty_like(r_in)
+    st = torch.full((2,), -5, dtype=torch.int32, device="cuda")
+
+    def call(bl, epoch=ep):
+        fc.allreduce_residual_rmsnorm([dev(b.view(np.int32)) for b in bl], spec, w.T, w.H, r_in, r_out, gam,
+                                      w.eps, y, expected_epoch=epoch, d_status=st)
+        torch.cuda.synchronize()
+        return list(host(st))
+
+    assert call(blocks) == [fc.FC_OK, fc.STATUS_NO_INDEX]
+    want = oracle_fused(orc, w, inp)
+    assert_bits_equal(host_bits(r_out), want["h"], "residual_out")
+    assert_y_close(host_bits(y), want["y"])
+
+    bad = [b.copy() for b in blocks]
+    bad[2][4 * (3 * nb + 17) + 3] = ep - 1          # slab 2, row 3, block 17
+    bad[3][4 * 5 + 3] = ep + 1                      # slab 3, row 0, block 5
+    first = (2 * w.T + 3) * nb + 17
+    assert call(bad) == [fc.FC_ERR_STALE_BLOCK, first]
+    bad[1][4 * (5 * nb + nb - 1) + 3] = 0           # slab 1, last block of the last row
+    assert call(bad) == [fc.FC_ERR_STALE_BLOCK, (1 * w.T + 5) * nb + nb - 1]
+    assert call(blocks, epoch=ep + 1) == [fc.FC_ERR_STALE_BLOCK, 0]
+    assert call(blocks) == [fc.FC_OK, fc.STATUS_NO_INDEX]
+
+
+def test_token_split_two_streams_equals_one_call(orc):
+    """Two subsets of rows on two streams give the same bits as one call."""
+    w = small("token-split", T=64)
+    inp = synth.make_inputs(w, seed=13)
+    spec = spec_of(TG, 0)
+    blocks = []
+    for s in inp["slabs"]:
+        b = torch.empty(fc.tagged_bytes(w.T, w.H), dtype=torch.uint8, device="cuda")
+        fc.pack_tagged(dev_bf16(s), 3, b)
+        blocks.append(b)
+    r_in, gam = dev_bf16(inp["residual"]), dev_bf16(inp["gamma"])
+    r_out, y = torch.empty_like(r_in), torch.empty_like(r_in)
+    half = w.T // 2
+    bpr = fc.tagged_bytes(1, w.H)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    st = torch.zeros(2, 2, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    for i, s in enumerate(streams):
+        r0, r1 = i * half, (i + 1) * half
+        fc.allreduce_residual_rmsnorm([b[r0 * bpr:r1 * bpr] for b in blocks], spec, half, w.H,
+                                      r_in[r0:r1], r_out[r0:r1], gam, w.eps, y[r0:r1],
+                                      expected_epoch=3, d_status=st[i], stream=s)
+    torch.cuda.synchronize()
+    assert host(st).tolist() == [[0, fc.STATUS_NO_INDEX]] * 2
+    want = oracle_fused(orc, w, inp)
+    assert_bits_equal(host_bits(r_out), want["h"], "residual_out")
+    assert_y_close(host_bits(y), want["y"])
+
+
+# --------------------------------------------------- full-size, sampled rows --
+@pytest.mark.parametrize("name", ["prefill", "token-split", "decode"])
+def test_full_size_sampled_rows(orc, name):
+    """The full-size workloads through the same Pipeline.step() the
+    benchmark times (token-split: two subsets on two streams); the oracle
+    checks a sample of rows (first, last, random)."""
+    from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
+    w = synth.WORKLOADS[name]
+    pipe = Pipeline(w, synth.make_inputs(w, seed=0))
+    pipe.step()
+    pipe.step()  # a second step: new epoch for tagged blocks, same outputs
+    got = pipe.outputs()
+    rows = np.unique(np.concatenate([[0, 1, w.T - 1],
+                                     np.random.default_rng(0).integers(0, w.T, 13)]))
+    sub = synth.Workload(**{**w.__dict__, "T": len(rows)})
+    want = oracle_fused(orc, sub, synth.make_inputs(w, seed=0, rows=rows))
+    assert_bits_equal(got["h"][rows], want["h"], "residual_out")
+    assert_y_close(got["y"][rows], want["y"])
+    if w.fmt in (I8, I4):
+        codes = got["codes"].reshape(w.T, -1)[rows]
+        assert_bits_equal(codes, want["codes"], "payload codes")
+        assert_bits_equal(got["scales"].reshape(w.T, -1)[rows], want["scales"], "payload scales")
+        if w.fmt == I4:
+            assert_bits_equal(got["zeros"].reshape(w.T, -1)[rows], want["zeros"], "payload zeros")
+    if w.fmt == TG:
+        assert got["status"].tolist() == [[fc.FC_OK, fc.STATUS_NO_INDEX]] * w.splits
+
+
+def test_rows_zero_launches_nothing():
+    spec = fc.INT8_G128
+    t = torch.empty(0, 4096, dtype=torch.bfloat16, device="cuda")
+    fc.group_quantize(t, spec, fc.alloc_qtensor(spec, 0, 4096))
+    torch.cuda.synchronize()
+
+
+def test_invalid_arguments_rejected_before_launch():
+    spec = fc.INT8_G128
+    x = torch.zeros(2, 4096, dtype=torch.bfloat16, device="cuda")
+    out = fc.alloc_qtensor(spec, 2, 4096)
+    bad = torch.zeros(2 * 4096 + 8, dtype=torch.bfloat16, device="cuda")[8:].view(2, 4096)
+    with pytest.raises(fc.FcommError) as e:
+        fc.group_quantize(bad, spec, out)            # 16-byte but not 32-byte aligned
+    assert e.value.status == fc.FC_ERR_INVALID
+    with pytest.raises(fc.FcommError):
+        fc.group_quantize(x, fc.QSpec(fc.FMT_INT8_SYM, 96), out)   # group not a power of 2
+    with pytest.raises(fc.FcommError):
+        fc.allreduce_residual_rmsnorm([out], spec, 2, 4096, x, x, x[0], 1e-5, x)  # P = 1
