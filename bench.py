@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="override the workload's token count (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -169,9 +171,10 @@ def oracle_sample(w, inputs, target_s: float):
                                        rows, w.H, w.group, w.eps)
         return time.perf_counter() - t0
 
-    probe = min(w.T, max(1, 8))
+    avail = int(inputs["residual"].shape[0])  # rows actually present in `inputs`
+    probe = min(avail, 8)
     dt = run(probe)
-    rows = int(min(w.T, max(probe, probe * target_s / max(dt, 1e-6))))
+    rows = int(min(avail, max(probe, probe * target_s / max(dt, 1e-6))))
     dt = run(rows)
     sub = Workload(**{**w.__dict__, "T": rows})
     E = rows * w.H
@@ -188,10 +191,11 @@ def run_reference(args):
     if rank != 0:
         return
     from quantized_reduce_rmsnorm_gb300 import synth
-    w = synth.WORKLOADS[args.workload]
-    # each step is a bounded sample of rows, sized so the whole run stays short
-    per_step = max(0.5, 120.0 / max(1, args.steps + args.warmup))
-    rows = min(w.T, max(1, int(64 * per_step)))
+    w = get_workload(args)
+    # each step is a bounded sample of rows, sized so the whole run stays
+    # within about two minutes of CPU time
+    per_step = min(10.0, max(0.2, 120.0 / max(1, args.steps + args.warmup)))
+    rows = min(w.T, 4096)
     inputs = synth.make_inputs(w, seed=0, rows=np.arange(rows))
     vals = []
     for i in range(args.warmup + args.steps):
@@ -213,6 +217,14 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def get_workload(args):
+    from quantized_reduce_rmsnorm_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.rows:
+        w = synth.Workload(**{**w.__dict__, "T": args.rows})
+    return w
 
 
 def workload_config(w, note=None):
@@ -242,7 +254,7 @@ def run_ours(args):
     from quantized_reduce_rmsnorm_gb300 import fcomm, synth
     from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
     fcomm.load()
-    w = synth.WORKLOADS[args.workload]
+    w = get_workload(args)
     inputs = synth.make_inputs(w, seed=rank)
     pipe = Pipeline(w, inputs, device=dev)
     alg = pipe.alg_bytes()

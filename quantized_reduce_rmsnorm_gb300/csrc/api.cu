@@ -154,7 +154,7 @@ fc_status fc_group_quantize_multi(const void* const* x_bf16, int P, int64_t rows
   job.n = rows * hidden;
   job.P = P;
   job.G = spec.group;
-  return cuda_status(fc::launch_quantize(spec.fmt, false, 0, job, (cudaStream_t)stream),
+  return cuda_status(fc::launch_quantize(spec.fmt, false, fc::kDeqNone, job, (cudaStream_t)stream),
                      "fc_group_quantize launch");
 }
 
@@ -200,12 +200,12 @@ fc_status fc_requant_gather(const float* reduced_f32, int64_t rows, int64_t hidd
   if (fc_status s = check_ptr(reduced_f32, 32, "reduced_f32")) return s;
   if (requant_out.codes)
     if (fc_status s = check_qtensor(requant_out, spec.fmt, "requant_out")) return s;
-  int deq = 0;
+  int deq = fc::kDeqNone;
   if (out) {
     if (out_dtype != FC_FMT_BF16 && out_dtype != FC_FMT_F32)
       return fail(FC_ERR_INVALID, "out_dtype must be FC_FMT_BF16 or FC_FMT_F32");
     if (fc_status s = check_ptr(out, 32, "out")) return s;
-    deq = out_dtype == FC_FMT_BF16 ? fc::kBF16 : fc::kF32;
+    deq = out_dtype == FC_FMT_BF16 ? fc::kDeqBF16 : fc::kDeqF32;
   }
   fc::QuantJob job{};
   job.x[0] = reduced_f32;

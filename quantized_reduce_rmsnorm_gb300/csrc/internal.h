@@ -8,6 +8,9 @@ namespace fc {
 
 enum Fmt : int { kBF16 = 0, kINT8 = 1, kINT4 = 2, kTAGGED = 3, kF32 = 4 };
 
+// Dequantized output of a requantization: none, bf16 or fp32.
+enum DeqOut : int { kDeqNone = 0, kDeqBF16 = 1, kDeqF32 = 2 };
+
 // P slabs as device pointers (passed to kernels by value).
 struct Slabs {
   const void* codes[8];
@@ -48,8 +51,7 @@ struct FusedArgs {
 
 int num_sms();
 
-// in_f32: input is fp32 (requantization) instead of bf16; deq_kind: 0 none,
-// kBF16 or kF32.
+// in_f32: input is fp32 (requantization) instead of bf16; deq_kind: a DeqOut.
 cudaError_t launch_quantize(int fmt, bool in_f32, int deq_kind, const QuantJob& job,
                             cudaStream_t st);
 // Sum of dequantized slabs over the 16-element chunks [c0, c1).

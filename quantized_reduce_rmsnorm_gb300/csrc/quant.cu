@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
           if (job.codes[p]) st128(static_cast<int8_t*>(job.codes[p]) + c * 16, make_uint4(q[0], q[1], q[2], q[3]));
           if (job.codes[p] && (lane & (lpg - 1)) == 0) stf(job.scales[p] + c / lpg, s);
         }
-        if (DEQ) dequant_i8_lane(q, s, d);
+        if (DEQ != kDeqNone) dequant_i8_lane(q, s, d);
       } else {
         uint32_t q[2];
         float z;
@@ -82,10 +82,10 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
             stf(job.zeros[p] + c / lpg, z);
           }
         }
-        if (DEQ) dequant_i4_lane(q, s, z, d);
+        if (DEQ != kDeqNone) dequant_i4_lane(q, s, z, d);
       }
-      if (DEQ && act[u]) {
-        if (DEQ == kBF16) {
+      if (DEQ != kDeqNone && act[u]) {
+        if (DEQ == kDeqBF16) {
           V8 o;
 #pragma unroll
           for (int i = 0; i < 8; ++i) o.w[i] = pack_bf2(d[2 * i], d[2 * i + 1]);
@@ -233,15 +233,15 @@ int num_sms() {
 cudaError_t launch_quantize(int fmt, bool in_f32, int deq, const QuantJob& job, cudaStream_t st) {
   if (job.n == 0) return cudaSuccess;
   if (fmt == kINT8) {
-    if (!in_f32) return launch_quantize_t<kINT8, false, 0>(job, st);
-    if (deq == kBF16) return launch_quantize_t<kINT8, true, kBF16>(job, st);
-    if (deq == kF32) return launch_quantize_t<kINT8, true, kF32>(job, st);
-    return launch_quantize_t<kINT8, true, 0>(job, st);
+    if (!in_f32) return launch_quantize_t<kINT8, false, kDeqNone>(job, st);
+    if (deq == kDeqBF16) return launch_quantize_t<kINT8, true, kDeqBF16>(job, st);
+    if (deq == kDeqF32) return launch_quantize_t<kINT8, true, kDeqF32>(job, st);
+    return launch_quantize_t<kINT8, true, kDeqNone>(job, st);
   }
-  if (!in_f32) return launch_quantize_t<kINT4, false, 0>(job, st);
-  if (deq == kBF16) return launch_quantize_t<kINT4, true, kBF16>(job, st);
-  if (deq == kF32) return launch_quantize_t<kINT4, true, kF32>(job, st);
-  return launch_quantize_t<kINT4, true, 0>(job, st);
+  if (!in_f32) return launch_quantize_t<kINT4, false, kDeqNone>(job, st);
+  if (deq == kDeqBF16) return launch_quantize_t<kINT4, true, kDeqBF16>(job, st);
+  if (deq == kDeqF32) return launch_quantize_t<kINT4, true, kDeqF32>(job, st);
+  return launch_quantize_t<kINT4, true, kDeqNone>(job, st);
 }
 
 cudaError_t launch_reduce(int fmt, const Slabs& s, int P, int G, int64_t c0, int64_t c1,
