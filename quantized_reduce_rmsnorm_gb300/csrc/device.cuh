@@ -108,16 +108,82 @@ __device__ __forceinline__ void unpack16(const V8& v, float f[16]) {
   }
 }
 
+// -------------------------------------------------- packed fp32 pairs --
+// Blackwell executes two binary32 operations per instruction on a register
+// pair (add/mul/fma .f32x2).  Each half is an ordinary IEEE round-to-nearest
+// operation on its own operands, denormals kept: bit-identical to two scalar
+// __fadd_rn / __fmul_rn calls.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+__device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
+
 // ------------------------------------------------------- code unpacking --
-// INT8 code k of a 32-bit word, as float (exact).
-__device__ __forceinline__ float i8_at(uint32_t w, int k) {
-  return __int2float_rn(static_cast<int>(static_cast<int8_t>((w >> (8 * k)) & 0xFFu)));
+// Codes become floats without an int->float conversion: the code is placed
+// in the low mantissa bits of 2^23 with a byte permute and 2^23 (+128 for the
+// sign-flipped INT8 bytes) is subtracted; both steps are exact.
+constexpr float kTwo23 = 8388608.0f;            // 2^23, bits 0x4B000000
+constexpr float kTwo23p128 = 8388736.0f;        // 2^23 + 128
+constexpr uint32_t kTwo23Bits = 0x4B000000u;
+
+// byte k of w as the low byte of 2^23's bit pattern
+__device__ __forceinline__ float byte_in_two23(uint32_t w, int k) {
+  return __uint_as_float(__byte_perm(w, kTwo23Bits, 0x7540u | static_cast<uint32_t>(k)));
 }
 
-// INT4 code k (0..7) of a 32-bit word, as float (exact): the code is placed
-// in the mantissa of 2^23 and 2^23 is subtracted.
-__device__ __forceinline__ float u4_at(uint32_t w, int k) {
-  return __uint_as_float(0x4B000000u | ((w >> (4 * k)) & 0xFu)) - 8388608.0f;
+// acc[i] += q_i * s for the 16 INT8 codes in w[4] (code i = byte i%4 of w[i/4]).
+__device__ __forceinline__ void dequant_i8_acc(const uint32_t w[4], float s, float acc[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t x = w[j] ^ 0x80808080u;  // int8 -> q + 128
+#pragma unroll
+    for (int k = 0; k < 4; k += 2) {
+      float2 q = add2(make_float2(byte_in_two23(x, k), byte_in_two23(x, k + 1)), dup2(-kTwo23p128));
+      float2 d = mul2(q, dup2(s));
+      float2 a = add2(make_float2(acc[4 * j + k], acc[4 * j + k + 1]), d);
+      acc[4 * j + k] = a.x;
+      acc[4 * j + k + 1] = a.y;
+    }
+  }
+}
+
+// acc[i] += (q_i * s) + z for the 16 INT4 codes in w[2] (code i = nibble i%8 of w[i/8]).
+__device__ __forceinline__ void dequant_i4_acc(const uint32_t w[2], float s, float z,
+                                               float acc[16]) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t ev = w[j] & 0x0F0F0F0Fu;         // codes 8j + 2k
+    const uint32_t od = (w[j] >> 4) & 0x0F0F0F0Fu;  // codes 8j + 2k + 1
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float2 q = add2(make_float2(byte_in_two23(ev, k), byte_in_two23(od, k)), dup2(-kTwo23));
+      float2 d = add2(mul2(q, dup2(s)), dup2(z));
+      float2 a = add2(make_float2(acc[8 * j + 2 * k], acc[8 * j + 2 * k + 1]), d);
+      acc[8 * j + 2 * k] = a.x;
+      acc[8 * j + 2 * k + 1] = a.y;
+    }
+  }
 }
 
 // ------------------------------------------------------- group reductions --
@@ -139,37 +205,82 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ------------------------------------------------------------ quantizers --
-// INT8 symmetric on this lane's 16 values of a group spread over lpg lanes.
-// Writes the 16 codes packed in q[4] and returns the group's scale.
+// Codes are rne(fl(x / s)) (INT8) and rne(fl(fl(x - lo) / s)) (INT4), i.e. an
+// IEEE division per element.  Fast path: one IEEE reciprocal r = fl(1/s) per
+// group and t = fl(x * r).  t differs from the exact quotient by at most
+// 2^-22 |t| + 2^-149 <= 2^-15 (|t| <= 128), and fl(x / s) differs from it by
+// at most 2^-17, so when t is at least 2^-13 away from every half-integer
+// both round to the same integer.  The rounding itself is an exact add of
+// 1.5 * 2^23 (INT8) or 2^23 (INT4), which leaves the integer in the low
+// mantissa bits; t - rint(t) is exact (Sterbenz), so the distance test is
+// exact too.  A per-group bound on the largest t (which is fl(max * r))
+// keeps every code inside its range without clamping.  Lanes where any test
+// fails recompute their 16 codes with the IEEE division.
+constexpr float kMagicI8 = 12582912.0f;         // 1.5 * 2^23, bits 0x4B400000
+constexpr float kTieGuard = 0.5f - 1.0f / 8192;  // a half-integer is > 2^-13 away
+
+__device__ __forceinline__ uint32_t low_bytes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
+}
+
+// INT8 symmetric on this lane's 16 values of a group spread over lpg lanes:
 //   s = max|x| / 127;  q = clamp(rne(x / s), -127, 127);  s == 0 -> q = 0.
-__device__ __forceinline__ float quant_i8_lane(const float v[16], int lpg, uint32_t q[4]) {
+// Writes the codes packed in q[4]; with DEQ also d[i] = q_i * s.  Returns s.
+template <bool DEQ>
+__device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q[4],
+                                          float d[16]) {
   float a = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(v[i]));
   a = group_max(a, lpg);
   const float s = __fdiv_rn(a, 127.0f);
+  uint32_t ub[16];  // low byte: the code
+  float qf[16];     // the code as a float
+  if (s == 0.0f) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t w = 0;
+    for (int i = 0; i < 16; ++i) ub[i] = 0u, qf[i] = 0.0f;
+  } else {
+    const float r = __fdiv_rn(1.0f, s);
+    bool slow = !(__fmul_rn(a, r) <= 127.25f);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      int c = 0;
-      if (s != 0.0f) {
-        c = __float2int_rn(__fdiv_rn(v[4 * j + k], s));
-        c = max(-127, min(127, c));
-      }
-      w |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * k);
+    for (int i = 0; i < 16; i += 2) {
+      const float2 t = mul2(make_float2(v[i], v[i + 1]), dup2(r));
+      const float2 u = add2(t, dup2(kMagicI8));
+      const float2 c = add2(u, dup2(-kMagicI8));
+      const float2 e = add2(t, make_float2(-c.x, -c.y));
+      slow |= fabsf(e.x) >= kTieGuard;
+      slow |= fabsf(e.y) >= kTieGuard;
+      ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
+      qf[i] = c.x, qf[i + 1] = c.y;
     }
-    q[j] = w;
+    if (slow) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c = max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], s))));
+        ub[i] = static_cast<uint32_t>(c);
+        qf[i] = static_cast<float>(c);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) q[j] = low_bytes4(ub[4 * j], ub[4 * j + 1], ub[4 * j + 2], ub[4 * j + 3]);
+  if (DEQ) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const float2 m = mul2(make_float2(qf[i], qf[i + 1]), dup2(s));
+      d[i] = m.x, d[i + 1] = m.y;
+    }
   }
   return s;
 }
 
 // INT4 asymmetric: lo = min, hi = max (a zero extreme taken as +0),
 // s = (hi - lo) / 15, z = lo, q = clamp(rne((x - lo) / s), 0, 15).
-// Element 2i in the low nibble of byte i.  Returns s, writes z.
-__device__ __forceinline__ float quant_i4_lane(const float v[16], int lpg, uint32_t q[2],
-                                               float& z) {
+// Element 2i in the low nibble of byte i.  Returns s, writes z; with DEQ also
+// d[i] = (q_i * s) + z.
+template <bool DEQ>
+__device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q[2], float& z,
+                                          float d[16]) {
   float lo = v[0], hi = v[0];
 #pragma unroll
   for (int i = 1; i < 16; ++i) {
@@ -180,34 +291,51 @@ __device__ __forceinline__ float quant_i4_lane(const float v[16], int lpg, uint3
   hi = group_max(hi, lpg);
   if (lo == 0.0f) lo = 0.0f;  // -0 -> +0
   if (hi == 0.0f) hi = 0.0f;
-  const float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+  const float span = __fsub_rn(hi, lo);
+  const float s = __fdiv_rn(span, 15.0f);
   z = lo;
+  uint32_t ub[16];
+  float qf[16];
+  if (s == 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ub[i] = 0u, qf[i] = 0.0f;
+  } else {
+    const float r = __fdiv_rn(1.0f, s);
+    bool slow = !(__fmul_rn(span, r) <= 15.25f);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const float2 t = mul2(add2(make_float2(v[i], v[i + 1]), dup2(-lo)), dup2(r));
+      const float2 u = add2(t, dup2(kTwo23));
+      const float2 c = add2(u, dup2(-kTwo23));
+      const float2 e = add2(t, make_float2(-c.x, -c.y));
+      slow |= fabsf(e.x) >= kTieGuard;
+      slow |= fabsf(e.y) >= kTieGuard;
+      ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
+      qf[i] = c.x, qf[i + 1] = c.y;
+    }
+    if (slow) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c = max(0, min(15, __float2int_rn(__fdiv_rn(__fsub_rn(v[i], lo), s))));
+        ub[i] = static_cast<uint32_t>(c);
+        qf[i] = static_cast<float>(c);
+      }
+    }
+  }
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    uint32_t w = 0;
+    const uint32_t ev = low_bytes4(ub[8 * j], ub[8 * j + 2], ub[8 * j + 4], ub[8 * j + 6]);
+    const uint32_t od = low_bytes4(ub[8 * j + 1], ub[8 * j + 3], ub[8 * j + 5], ub[8 * j + 7]);
+    q[j] = ev | (od << 4);
+  }
+  if (DEQ) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      int c = 0;
-      if (s != 0.0f) {
-        c = __float2int_rn(__fdiv_rn(__fsub_rn(v[8 * j + k], lo), s));
-        c = max(0, min(15, c));
-      }
-      w |= static_cast<uint32_t>(c) << (4 * k);
+    for (int i = 0; i < 16; i += 2) {
+      const float2 m = add2(mul2(make_float2(qf[i], qf[i + 1]), dup2(s)), dup2(z));
+      d[i] = m.x, d[i + 1] = m.y;
     }
-    q[j] = w;
   }
   return s;
-}
-
-// Dequantizers: d = q * s (INT8), d = q * s + z (INT4; multiply, then add).
-__device__ __forceinline__ void dequant_i8_lane(const uint32_t q[4], float s, float d[16]) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) d[i] = __fmul_rn(i8_at(q[i >> 2], i & 3), s);
-}
-__device__ __forceinline__ void dequant_i4_lane(const uint32_t q[2], float s, float z,
-                                                float d[16]) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) d[i] = __fadd_rn(__fmul_rn(u4_at(q[i >> 3], i & 7), s), z);
 }
 
 }  // namespace fc

@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
 
   for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, parity ^= 1) {
     uint32_t hb[NCH][8];
-    float ss = 0.0f;
+    float2 ss2 = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
       const int c = k * nthr + tid;
@@ -75,8 +75,9 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
           if (p < P && act) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              acc[2 * i] = __fadd_rn(acc[2 * i], bf_lo(xv[p].w[i]));
-              acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], bf_hi(xv[p].w[i]));
+              const float2 t = add2(make_float2(acc[2 * i], acc[2 * i + 1]),
+                                    make_float2(bf_lo(xv[p].w[i]), bf_hi(xv[p].w[i])));
+              acc[2 * i] = t.x, acc[2 * i + 1] = t.y;
             }
           }
         }
@@ -102,28 +103,25 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
 #pragma unroll
         for (int p = 0; p < kMaxP; ++p) {
           if (p < P && act) {
-            float d[16];
             if (FMT == kINT8)
-              dequant_i8_lane(qv[p], sc[p], d);
+              dequant_i8_acc(qv[p], sc[p], acc);
             else
-              dequant_i4_lane(qv[p], sc[p], zp[p], d);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], d[i]);
+              dequant_i4_acc(qv[p], sc[p], zp[p], acc);
           }
         }
-        // ---- requantize the reduced group (all-gather payload), dequantize
+        // ---- requantize the reduced group (all-gather payload) and
+        //      dequantize it in place (every lane joins the group shuffles)
         if (FMT == kINT8) {
           uint32_t q[4];
-          const float s = quant_i8_lane(acc, lpg, q);
+          const float s = quant_i8<true>(acc, lpg, q, acc);
           if (act && a.rq_codes) {
             st128(static_cast<int8_t*>(a.rq_codes) + gc * 16, make_uint4(q[0], q[1], q[2], q[3]));
             if ((lane & (lpg - 1)) == 0) stf(a.rq_scales + g, s);
           }
-          dequant_i8_lane(q, s, acc);
         } else {
           uint32_t q[2];
           float z;
-          const float s = quant_i4_lane(acc, lpg, q, z);
+          const float s = quant_i4<true>(acc, lpg, q, z, acc);
           if (act && a.rq_codes) {
             st64(static_cast<uint8_t*>(a.rq_codes) + gc * 8, make_uint2(q[0], q[1]));
             if ((lane & (lpg - 1)) == 0) {
@@ -131,29 +129,28 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
               stf(a.rq_zeros + g, z);
             }
           }
-          dequant_i4_lane(q, s, z, acc);
         }
       }
 
       // ---- residual add, bf16 rounding, sum of squares
       if (act) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          hb[k][i] = pack_bf2(__fadd_rn(acc[2 * i], bf_lo(rv.w[i])),
-                              __fadd_rn(acc[2 * i + 1], bf_hi(rv.w[i])));
         V8 hv;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) hv.w[i] = hb[k][i];
+        for (int i = 0; i < 8; ++i) {
+          const float2 h = add2(make_float2(acc[2 * i], acc[2 * i + 1]),
+                                make_float2(bf_lo(rv.w[i]), bf_hi(rv.w[i])));
+          hb[k][i] = hv.w[i] = pack_bf2(h.x, h.y);
+        }
         st256(static_cast<uint16_t*>(a.res_out) + gc * 16, hv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float h0 = bf_lo(hb[k][i]), h1 = bf_hi(hb[k][i]);
-          ss = __fmaf_rn(h0, h0, ss);
-          ss = __fmaf_rn(h1, h1, ss);
+          const float2 h = make_float2(bf_lo(hb[k][i]), bf_hi(hb[k][i]));
+          ss2 = fma2(h, h, ss2);
         }
       }
     }
 
+    const float ss = __fadd_rn(ss2.x, ss2.y);
     const float inv = inv_rms(block_sum(ss, red, parity), a.H, a.eps);
 
     // ---- y = bf16((h * inv) * gamma)
@@ -164,9 +161,11 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
         const V8 gv = ld256_keep(static_cast<const uint16_t*>(a.gamma) + c * 16);
         V8 yv;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          yv.w[i] = pack_bf2(__fmul_rn(__fmul_rn(bf_lo(hb[k][i]), inv), bf_lo(gv.w[i])),
-                             __fmul_rn(__fmul_rn(bf_hi(hb[k][i]), inv), bf_hi(gv.w[i])));
+        for (int i = 0; i < 8; ++i) {
+          const float2 y = mul2(mul2(make_float2(bf_lo(hb[k][i]), bf_hi(hb[k][i])), dup2(inv)),
+                                make_float2(bf_lo(gv.w[i]), bf_hi(gv.w[i])));
+          yv.w[i] = pack_bf2(y.x, y.y);
+        }
         st256(static_cast<uint16_t*>(a.y) + (row * cpr + c) * 16, yv);
       }
     }

@@ -65,24 +65,22 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
       float d[16];
       if (FMT == kINT8) {
         uint32_t q[4];
-        const float s = quant_i8_lane(v[u], lpg, q);
-        if (act[u]) {
-          if (job.codes[p]) st128(static_cast<int8_t*>(job.codes[p]) + c * 16, make_uint4(q[0], q[1], q[2], q[3]));
-          if (job.codes[p] && (lane & (lpg - 1)) == 0) stf(job.scales[p] + c / lpg, s);
+        const float s = quant_i8<DEQ != kDeqNone>(v[u], lpg, q, d);
+        if (act[u] && job.codes[p]) {
+          st128(static_cast<int8_t*>(job.codes[p]) + c * 16, make_uint4(q[0], q[1], q[2], q[3]));
+          if ((lane & (lpg - 1)) == 0) stf(job.scales[p] + c / lpg, s);
         }
-        if (DEQ != kDeqNone) dequant_i8_lane(q, s, d);
       } else {
         uint32_t q[2];
         float z;
-        const float s = quant_i4_lane(v[u], lpg, q, z);
-        if (act[u]) {
-          if (job.codes[p]) st64(static_cast<uint8_t*>(job.codes[p]) + c * 8, make_uint2(q[0], q[1]));
-          if (job.codes[p] && (lane & (lpg - 1)) == 0) {
+        const float s = quant_i4<DEQ != kDeqNone>(v[u], lpg, q, z, d);
+        if (act[u] && job.codes[p]) {
+          st64(static_cast<uint8_t*>(job.codes[p]) + c * 8, make_uint2(q[0], q[1]));
+          if ((lane & (lpg - 1)) == 0) {
             stf(job.scales[p] + c / lpg, s);
             stf(job.zeros[p] + c / lpg, z);
           }
         }
-        if (DEQ != kDeqNone) dequant_i4_lane(q, s, z, d);
       }
       if (DEQ != kDeqNone && act[u]) {
         if (DEQ == kDeqBF16) {
@@ -138,13 +136,10 @@ __global__ void __launch_bounds__(kThreads) k_reduce(Slabs s, int P, int G, int6
 #pragma unroll
     for (int p = 0; p < kMaxP; ++p) {
       if (p < P) {
-        float d[16];
         if (FMT == kINT8)
-          dequant_i8_lane(q[p], sc[p], d);
+          dequant_i8_acc(q[p], sc[p], acc);
         else
-          dequant_i4_lane(q[p], sc[p], zp[p], d);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], d[i]);
+          dequant_i4_acc(q[p], sc[p], zp[p], acc);
       }
     }
     V8 o0, o1;

@@ -174,6 +174,46 @@ def test_requant_gather_bit_exact(orc, fmt, G, out_dtype):
         assert_bits_equal(host_bits(out), orc.f32_to_bf16_array(d), "gathered bf16")
 
 
+def _near_ties(fmt, G, rng):
+    """fp32 groups whose quotients x/s sit exactly on, or a few ulps around,
+    half-integers: the cases where rounding x*(1/s) could disagree with
+    rounding fl(x/s), so the kernels must take their exact division path."""
+    groups = []
+    for s0 in (3.0, 0.5, float(np.float32(1.0) / np.float32(127.0)), 1.0e-3, 7.0e4):
+        s0 = np.float32(s0)
+        if fmt == I8:
+            k = rng.integers(-127, 127, G).astype(np.float32)
+            x = ((k + np.float32(0.5)) * s0).astype(np.float32)
+            x[0] = np.float32(127) * s0          # absmax fixes s = fl(127 s0 / 127)
+        else:
+            k = rng.integers(0, 15, G).astype(np.float32)
+            x = ((k + np.float32(0.5)) * s0).astype(np.float32)
+            x[0], x[1] = np.float32(0), np.float32(15) * s0   # lo = 0, hi = 15 s0
+        nud = rng.integers(-3, 4, G)
+        for i in range(2, G):
+            for _ in range(abs(nud[i])):
+                x[i] = np.nextafter(x[i], np.float32(np.inf) if nud[i] > 0 else np.float32(-np.inf))
+        groups.append(x)
+    return np.concatenate(groups)
+
+
+@pytest.mark.parametrize("fmt,G", [(I8, 128), (I4, 32), (I8, 16), (I4, 64)])
+def test_quantizer_near_half_integer_quotients(orc, fmt, G):
+    rng = np.random.default_rng(21)
+    red = np.concatenate([_near_ties(fmt, G, rng) for _ in range(8)])
+    T = red.size // (4 * G)
+    red = red[:T * 4 * G].reshape(T, 4 * G)
+    spec = spec_of(fmt, G)
+    rq = fc.alloc_qtensor(spec, T, 4 * G)
+    out = torch.empty(T, 4 * G, dtype=torch.float32, device="cuda")
+    fc.requant_gather(dev(red), spec, rq, out, fc.FMT_F32)
+    torch.cuda.synchronize()
+    q, s, z = orc.quantize(fmt, red.ravel(), G)
+    assert_bits_equal(host(rq[0]), q, "codes")
+    assert_bits_equal(host(rq[1]), s, "scales")
+    assert_bits_equal(host(out), orc.dequantize(fmt, q, s, z, G), "dequantized")
+
+
 @pytest.mark.parametrize("fmt,G,P", [(I8, 128, 8), (I4, 32, 4), (I4, 32, 3)])
 def test_two_step_chain_equals_oracle(orc, fmt, G, P):
     """quantize -> reduce-scatter math per shard -> requant -> gather on the
