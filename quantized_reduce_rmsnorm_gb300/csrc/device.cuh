@@ -109,10 +109,10 @@ __device__ __forceinline__ void unpack16(const V8& v, float f[16]) {
 }
 
 // -------------------------------------------------- packed fp32 pairs --
-// Blackwell executes two binary32 operations per instruction on a register
-// pair (add/mul/fma .f32x2).  Each half is an ordinary IEEE round-to-nearest
-// operation on its own operands, denormals kept: bit-identical to two scalar
-// __fadd_rn / __fmul_rn calls.
+// Pairs of binary32 operations.  With FC_F32X2 the pairs issue as one
+// Blackwell .f32x2 instruction; otherwise as two scalar round-to-nearest
+// intrinsics, which the compiler never contracts into a fused multiply-add.
+#ifdef FC_F32X2
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   float2 r;
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
@@ -137,6 +137,17 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return r;
 }
+#else
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  return make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y));
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  return make_float2(__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y));
+}
+#endif
 __device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
 
 // ------------------------------------------------------- code unpacking --
