@@ -270,6 +270,8 @@ fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64
   a.rows = rows;
   a.H = static_cast<int>(hidden);
   a.G = quantized(spec.fmt) ? spec.group : 16;
+  a.lpg_shift = 0;
+  while ((16 << a.lpg_shift) < a.G) ++a.lpg_shift;
   a.P = P;
   a.eps = eps;
   a.epoch = expected_epoch;

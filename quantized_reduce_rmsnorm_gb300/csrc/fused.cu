@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
       const int c = k * nthr + tid;
       const bool act = c < cpr;
       const int64_t gc = row * cpr + c;  // global chunk index
-      const int64_t g = gc / (lpg > 0 ? lpg : 1);
+      const int64_t g = gc >> a.lpg_shift;
       float acc[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) acc[i] = 0.0f;

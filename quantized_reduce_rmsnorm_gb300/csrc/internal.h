@@ -44,6 +44,7 @@ struct FusedArgs {
   int64_t rows;
   int H;
   int G;
+  int lpg_shift;  // log2(G / 16)
   int P;
   float eps;
   uint32_t epoch;

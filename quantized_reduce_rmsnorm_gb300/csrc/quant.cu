@@ -21,26 +21,24 @@ constexpr int kUnroll = 2;
 // ------------------------------------------------------- quantize kernel --
 template <int FMT, bool IN_F32, int DEQ>
 __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chunks,
-                                                       int64_t tiles) {
+                                                       int lpg_shift) {
   const int lane = threadIdx.x & 31;
-  const int lpg = job.G >> 4;
+  const int lpg = 1 << lpg_shift;
+  const int64_t tiles = (chunks + 31) >> 5;
   const int64_t gwarp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-  const int64_t total = tiles * job.P;
 
-  for (int64_t t0 = gwarp; t0 < total; t0 += nwarps * kUnroll) {
+  for (int p = 0; p < job.P; ++p)
+  for (int64_t t0 = gwarp; t0 < tiles; t0 += nwarps * kUnroll) {
     float v[kUnroll][16];
-    int pp[kUnroll];
     int64_t cc[kUnroll];
     bool act[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t t = t0 + u * nwarps;
-      const int p = t < total ? static_cast<int>(t / tiles) : 0;
-      const int64_t c = (t - p * tiles) * 32 + lane;
-      pp[u] = p;
+      const int64_t c = t * 32 + lane;
       cc[u] = c;
-      act[u] = t < total && c < chunks;
+      act[u] = t < tiles && c < chunks;
       if (act[u]) {
         if (IN_F32) {
           const float* x = static_cast<const float*>(job.x[p]) + c * 16;
@@ -60,7 +58,6 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int p = pp[u];
       const int64_t c = cc[u];
       float d[16];
       if (FMT == kINT8) {
@@ -68,7 +65,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
         const float s = quant_i8<DEQ != kDeqNone>(v[u], lpg, q, d);
         if (act[u] && job.codes[p]) {
           st128(static_cast<int8_t*>(job.codes[p]) + c * 16, make_uint4(q[0], q[1], q[2], q[3]));
-          if ((lane & (lpg - 1)) == 0) stf(job.scales[p] + c / lpg, s);
+          if ((lane & (lpg - 1)) == 0) stf(job.scales[p] + (c >> lpg_shift), s);
         }
       } else {
         uint32_t q[2];
@@ -77,8 +74,8 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
         if (act[u] && job.codes[p]) {
           st64(static_cast<uint8_t*>(job.codes[p]) + c * 8, make_uint2(q[0], q[1]));
           if ((lane & (lpg - 1)) == 0) {
-            stf(job.scales[p] + c / lpg, s);
-            stf(job.zeros[p] + c / lpg, z);
+            stf(job.scales[p] + (c >> lpg_shift), s);
+            stf(job.zeros[p] + (c >> lpg_shift), z);
           }
         }
       }
@@ -107,13 +104,12 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
 // --------------------------------------------------------- reduce kernel --
 // out[i] = ((0 + deq_0(i)) + deq_1(i)) + ... + deq_{P-1}(i)   (fp32, slab order)
 template <int FMT>
-__global__ void __launch_bounds__(kThreads) k_reduce(Slabs s, int P, int G, int64_t c0,
+__global__ void __launch_bounds__(kThreads) k_reduce(Slabs s, int P, int lpg_shift, int64_t c0,
                                                      int64_t c1, float* out) {
-  const int lpg = G >> 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   for (int64_t c = c0 + static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; c < c1;
        c += stride) {
-    const int64_t g = c / lpg;
+    const int64_t g = c >> lpg_shift;
     uint32_t q[kMaxP][4];
     float sc[kMaxP], zp[kMaxP];
 #pragma unroll
@@ -192,6 +188,13 @@ __global__ void __launch_bounds__(kThreads) k_pack_tagged(const uint16_t* __rest
   }
 }
 
+// log2 of the lanes per group (G / 16; G is a power of two in [16, 512])
+int log2_lanes(int G) {
+  int sh = 0;
+  while ((16 << sh) < G) ++sh;
+  return sh;
+}
+
 // Persistent grid: enough blocks for the work, at most 8 x 256-thread
 // blocks (2048 threads, the per-SM maximum) per SM.
 int grid_for(int64_t work_items, int per_block) {
@@ -206,7 +209,7 @@ cudaError_t launch_quantize_t(const QuantJob& job, cudaStream_t st) {
   const int64_t tiles = (chunks + 31) / 32;
   const int64_t warps_needed = (tiles * job.P + kUnroll - 1) / kUnroll;
   const int grid = grid_for(warps_needed * 32, kThreads);
-  k_quantize<FMT, IN_F32, DEQ><<<grid, kThreads, 0, st>>>(job, chunks, tiles);
+  k_quantize<FMT, IN_F32, DEQ><<<grid, kThreads, 0, st>>>(job, chunks, log2_lanes(job.G));
   return cudaGetLastError();
 }
 
@@ -244,9 +247,9 @@ cudaError_t launch_reduce(int fmt, const Slabs& s, int P, int G, int64_t c0, int
   if (c1 <= c0) return cudaSuccess;
   const int grid = grid_for(c1 - c0, kThreads);
   if (fmt == kINT8)
-    k_reduce<kINT8><<<grid, kThreads, 0, st>>>(s, P, G, c0, c1, out);
+    k_reduce<kINT8><<<grid, kThreads, 0, st>>>(s, P, log2_lanes(G), c0, c1, out);
   else
-    k_reduce<kINT4><<<grid, kThreads, 0, st>>>(s, P, G, c0, c1, out);
+    k_reduce<kINT4><<<grid, kThreads, 0, st>>>(s, P, log2_lanes(G), c0, c1, out);
   return cudaGetLastError();
 }
 
