@@ -164,14 +164,17 @@ fc_status fc_pack_tagged(const void* x_bf16, int64_t rows, int64_t hidden, uint3
  * residual_in, residual_out (may be the same pointer), y: [rows, hidden] bf16;
  * gamma: [hidden] bf16.  requant_out: INT8/INT4 only, optional (codes == NULL:
  * not written): the requantized reduced tensor, i.e. the all-gather payload.
- * expected_epoch / d_status: TAGGED only.  Every block of every slab is
- * checked against expected_epoch before it is summed; a block that fails is
- * not summed.  d_status (optional, two int32 words of device memory) is set
- * by this call to {FC_OK, 0x7F7F7F7F} and, if any block fails, to
- * {FC_ERR_STALE_BLOCK, index of the first failing block of slab 0..P-1 in
- * row-major block order within this call's rows}; rows with a failing block
- * have unspecified outputs.  Nothing waits: on one GPU the producer has
- * finished by stream order, so a wrong tag is an error, not a retry. */
+ * expected_epoch: TAGGED only.  Every block of every slab is checked against
+ * expected_epoch before it is summed; a block that fails is not summed.
+ * d_status (optional, two int32 words of device memory) is set by this call
+ * to {FC_OK, 0x7F7F7F7F}; if any tagged block fails it becomes
+ * {FC_ERR_STALE_BLOCK, index of the first failing block, counting blocks
+ * row-major over slab 0, then slab 1, ..., within this call's rows}; rows
+ * with a failing block have unspecified outputs.  Nothing waits for data: on
+ * one GPU the producer has finished by stream order, so a wrong tag is an
+ * error, not a retry.  If a shared-memory staging copy of the TMA-staged
+ * kernel fails to complete within its bounded wait (about a second), word 0
+ * becomes FC_ERR_CUDA and the outputs are unspecified. */
 fc_status fc_allreduce_residual_rmsnorm(const fc_qtensor* slabs, int P, int64_t rows,
                                         int64_t hidden, fc_qspec spec, const void* residual_in,
                                         void* residual_out, const void* gamma, float eps,
@@ -184,6 +187,11 @@ fc_status fc_allreduce_residual_rmsnorm(const fc_qtensor* slabs, int P, int64_t 
  * RMSNorm on only 2-8 SMs).  0 = size the grid to the whole GPU. */
 typedef struct {
   int32_t max_ctas;
+  /* 0: automatic; 1: the register-streaming kernel; 2: the TMA-staged kernel
+   * (rows staged in shared memory by bulk copies; needs every per-row piece
+   * to be a multiple of 16 bytes and 16-byte aligned tensors, else the call
+   * returns FC_ERR_UNSUPPORTED).  All give bit-identical results. */
+  int32_t kernel;
 } fc_launch_opts;
 
 fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64_t rows,

@@ -241,6 +241,8 @@ fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64
   if (fc_status s = check_shape(spec, rows, hidden, false)) return s;
   if (P < 2 || P > 8) return fail(FC_ERR_INVALID, "P must be in [2, 8] (got %d)", P);
   if (opts && opts->max_ctas < 0) return fail(FC_ERR_INVALID, "max_ctas must be >= 0");
+  if (opts && (opts->kernel < 0 || opts->kernel > 2))
+    return fail(FC_ERR_INVALID, "kernel must be 0 (auto), 1 (streaming) or 2 (TMA-staged)");
   if (rows == 0) return ok();
   if (!slabs) return fail(FC_ERR_INVALID, "slabs must not be NULL");
   if (!(eps >= 0.0f) || eps > 1.0f) return fail(FC_ERR_INVALID, "eps must be in [0, 1]");
@@ -276,14 +278,17 @@ fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64
   a.eps = eps;
   a.epoch = expected_epoch;
   cudaStream_t st = (cudaStream_t)stream;
-  if (spec.fmt == FC_FMT_BF16_TAGGED && d_status) {
+  if (d_status) {
     a.status = d_status;
     cudaError_t e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(d_status + 1, 0x7F, sizeof(int32_t), st);
     if (e != cudaSuccess) return cuda_status(e, "d_status reset");
   }
-  return cuda_status(fc::launch_fused(spec.fmt, a, opts ? opts->max_ctas : 0, st),
-                     "fc_allreduce_residual_rmsnorm launch");
+  const int path = opts ? opts->kernel : 0;
+  const cudaError_t e = fc::launch_fused(spec.fmt, a, opts ? opts->max_ctas : 0, path, st);
+  if (e == cudaErrorNotSupported)
+    return fail(FC_ERR_UNSUPPORTED, "the TMA-staged kernel does not support this shape/alignment");
+  return cuda_status(e, "fc_allreduce_residual_rmsnorm launch");
 }
 
 fc_status fc_allreduce_residual_rmsnorm(const fc_qtensor* slabs, int P, int64_t rows,

@@ -381,8 +381,10 @@ cudaError_t launch_tagged(const FusedArgs& a, int max_ctas, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_fused(int fmt, const FusedArgs& a, int max_ctas, cudaStream_t st) {
+cudaError_t launch_fused(int fmt, const FusedArgs& a, int max_ctas, int path, cudaStream_t st) {
   if (a.rows == 0) return cudaSuccess;
+  if (path != kPathStream && fused_tma_eligible(fmt, a)) return launch_fused_tma(fmt, a, max_ctas, st);
+  if (path == kPathTma) return cudaErrorNotSupported;
   switch (fmt) {
     case kBF16: return launch_fmt<kBF16>(a, max_ctas, st);
     case kINT8: return launch_fmt<kINT8>(a, max_ctas, st);

@@ -1,0 +1,299 @@
+// fused_tma.cu -- the fused reduce + requant + residual add + RMSNorm with
+// TMA-staged rows.
+//
+// Same arithmetic as k_fused (fused.cu), different data movement: one CTA
+// owns one token row at a time, and one elected thread streams the CTA's
+// NEXT row -- every slab's codes, scales and zero-points (or bf16 data) and
+// the residual -- into a ring of NSTAGE shared-memory stages with 1-D bulk
+// copies (cp.async.bulk) that complete on an mbarrier.  While those bytes
+// are in flight, all threads work on the current row out of shared memory.
+// The bf16 row h (residual + reduced value) is written back over the
+// residual in shared memory, so nothing row-sized is held in registers and
+// occupancy is set by shared memory alone.  gamma is staged once per CTA.
+//
+// Stage layout (every piece a multiple of 16 bytes, 16-byte aligned):
+//   [codes of slab 0..P-1][scales 0..P-1][zeros 0..P-1 (INT4)][residual]
+#include <climits>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace fc {
+
+namespace {
+
+constexpr int kTmaThreads = 256;
+
+struct TmaGeom {
+  int cb;           // code (or bf16 data) bytes of one slab row
+  int sb;           // scale bytes of one slab row (0 for bf16)
+  int zb;           // zero-point bytes of one slab row (INT4 only)
+  int stage_bytes;  // P * (cb + sb + zb) + 2H
+  int gamma_off;    // byte offset of gamma in dynamic smem
+  int stage_off;    // byte offset of stage 0
+};
+
+__device__ __forceinline__ float block_sum_tma(float v, float (*red)[32], int parity) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  if (lane == 0) red[parity][wid] = v;
+  __syncthreads();
+  float t = 0.0f;
+  for (int w = 0; w < nw; ++w) t += red[parity][w];
+  return t;
+}
+
+template <int FMT>
+__device__ __forceinline__ void issue_row(const FusedArgs& a, const TmaGeom& g, uint8_t* st,
+                                          uint64_t* bar, int64_t row) {
+  mbar_expect_tx(bar, static_cast<uint32_t>(g.stage_bytes));
+  const int P = a.P;
+  for (int p = 0; p < P; ++p) {
+    bulk_load(st + p * g.cb, static_cast<const uint8_t*>(a.s.codes[p]) + row * g.cb, g.cb, bar);
+    if (FMT != kBF16)
+      bulk_load(st + P * g.cb + p * g.sb,
+                reinterpret_cast<const uint8_t*>(a.s.scales[p]) + row * g.sb, g.sb, bar);
+    if (FMT == kINT4)
+      bulk_load(st + P * (g.cb + g.sb) + p * g.zb,
+                reinterpret_cast<const uint8_t*>(a.s.zeros[p]) + row * g.zb, g.zb, bar);
+  }
+  bulk_load(st + P * (g.cb + g.sb + g.zb), static_cast<const uint8_t*>(a.res_in) + row * 2 * a.H,
+            2 * a.H, bar);
+}
+
+template <int FMT, int NSTAGE>
+__global__ void __launch_bounds__(kTmaThreads) k_fused_tma(FusedArgs a, TmaGeom g) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float red[2][32];
+  __shared__ uint64_t bar[NSTAGE + 1];  // [NSTAGE] = gamma
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int nthr = blockDim.x;
+  const int H = a.H, cpr = H >> 4, P = a.P;
+  const int lpg = a.G >> 4, sh = a.lpg_shift;
+  uint16_t* gam = reinterpret_cast<uint16_t*>(smem + g.gamma_off);
+  uint8_t* stage0 = smem + g.stage_off;
+  const int64_t row0 = blockIdx.x, rstride = gridDim.x;
+  if (row0 >= a.rows) return;
+
+  if (tid == 0) {
+    for (int s = 0; s <= NSTAGE; ++s) mbar_init(&bar[s], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_expect_tx(&bar[NSTAGE], static_cast<uint32_t>(2 * H));
+    bulk_load(gam, a.gamma, 2 * H, &bar[NSTAGE]);
+    for (int s = 0; s < NSTAGE - 1; ++s)
+      if (row0 + s * rstride < a.rows)
+        issue_row<FMT>(a, g, stage0 + s * g.stage_bytes, &bar[s], row0 + s * rstride);
+  }
+  // every wait ends in a block-wide vote, so all threads leave together
+  bool ok = __syncthreads_and(mbar_wait_bounded(&bar[NSTAGE], 0));
+
+  int i = 0;
+  for (int64_t row = row0; row < a.rows && ok; row += rstride, ++i) {
+    const int s = i % NSTAGE;
+    uint8_t* st = stage0 + s * g.stage_bytes;
+    if (tid == 0) {
+      // refill the stage that row i-1 used (every thread passed its end-of-row
+      // barrier) with row i + NSTAGE - 1
+      const int64_t nrow = row + (NSTAGE - 1) * rstride;
+      if (nrow < a.rows) {
+        fence_proxy_async_smem();
+        const int ns = (i + NSTAGE - 1) % NSTAGE;
+        issue_row<FMT>(a, g, stage0 + ns * g.stage_bytes, &bar[ns], nrow);
+      }
+    }
+    if (!__syncthreads_and(mbar_wait_bounded(&bar[s], (i / NSTAGE) & 1))) {
+      ok = false;
+      break;
+    }
+    const uint8_t* codes = st;
+    const float* scales = reinterpret_cast<const float*>(st + P * g.cb);
+    const float* zeros = reinterpret_cast<const float*>(st + P * (g.cb + g.sb));
+    uint16_t* hrow = reinterpret_cast<uint16_t*>(st + P * (g.cb + g.sb + g.zb));
+
+    // ---- pass 1: reduce, requantize, dequantize, residual add (h -> smem).
+    // Every thread runs the same number of iterations so whole warps join
+    // the group shuffles; lanes past the row end feed zeros (their groups
+    // hold no real element) and touch no memory.
+    float ss = 0.0f;
+    for (int cbase = 0; cbase < cpr; cbase += nthr) {
+      const int c = cbase + tid;
+      const bool act = c < cpr;
+      float acc[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+#pragma unroll
+      for (int p = 0; p < kMaxP; ++p) {
+        if (p < P && act) {
+          if (FMT == kBF16) {
+            const uint4* x = reinterpret_cast<const uint4*>(codes + p * g.cb) + 2 * c;
+            const uint4 x0 = x[0], x1 = x[1];
+            const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              acc[2 * k] = __fadd_rn(acc[2 * k], bf_lo(w[k]));
+              acc[2 * k + 1] = __fadd_rn(acc[2 * k + 1], bf_hi(w[k]));
+            }
+          } else if (FMT == kINT8) {
+            const uint4 q = reinterpret_cast<const uint4*>(codes + p * g.cb)[c];
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+            dequant_i8_acc(w, scales[p * (g.sb >> 2) + (c >> sh)], acc);
+          } else {
+            const uint2 q = reinterpret_cast<const uint2*>(codes + p * g.cb)[c];
+            const uint32_t w[2] = {q.x, q.y};
+            const int gi = p * (g.sb >> 2) + (c >> sh);
+            dequant_i4_acc(w, scales[gi], zeros[gi], acc);
+          }
+        }
+      }
+      const int64_t gc = row * cpr + c;
+      const int64_t gg = gc >> sh;
+      if (FMT == kINT8) {
+        uint32_t q[4];
+        const float s8 = quant_i8<true>(acc, lpg, q, acc);
+        if (act && a.rq_codes) {
+          st128(static_cast<int8_t*>(a.rq_codes) + gc * 16, make_uint4(q[0], q[1], q[2], q[3]));
+          if ((lane & (lpg - 1)) == 0) stf(a.rq_scales + gg, s8);
+        }
+      } else if (FMT == kINT4) {
+        uint32_t q[2];
+        float z;
+        const float s4 = quant_i4<true>(acc, lpg, q, z, acc);
+        if (act && a.rq_codes) {
+          st64(static_cast<uint8_t*>(a.rq_codes) + gc * 8, make_uint2(q[0], q[1]));
+          if ((lane & (lpg - 1)) == 0) {
+            stf(a.rq_scales + gg, s4);
+            stf(a.rq_zeros + gg, z);
+          }
+        }
+      }
+      if (act) {
+        uint4* hp = reinterpret_cast<uint4*>(hrow) + 2 * c;
+        const uint4 r0 = hp[0], r1 = hp[1];
+        const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        V8 hv;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          hv.w[k] = pack_bf2(__fadd_rn(acc[2 * k], bf_lo(rw[k])),
+                             __fadd_rn(acc[2 * k + 1], bf_hi(rw[k])));
+        hp[0] = make_uint4(hv.w[0], hv.w[1], hv.w[2], hv.w[3]);
+        hp[1] = make_uint4(hv.w[4], hv.w[5], hv.w[6], hv.w[7]);
+        st256(static_cast<uint16_t*>(a.res_out) + gc * 16, hv);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float h0 = bf_lo(hv.w[k]), h1 = bf_hi(hv.w[k]);
+          ss = __fmaf_rn(h0, h0, ss);
+          ss = __fmaf_rn(h1, h1, ss);
+        }
+      }
+    }
+    const float tot = block_sum_tma(ss, red, i & 1);  // also orders the h writes
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, static_cast<float>(H)), a.eps)));
+
+    // ---- pass 2: y = bf16((h * inv) * gamma)
+    for (int c = tid; c < cpr; c += nthr) {
+      const uint4* hp = reinterpret_cast<const uint4*>(hrow) + 2 * c;
+      const uint4* gp = reinterpret_cast<const uint4*>(gam) + 2 * c;
+      const uint4 h0 = hp[0], h1 = hp[1], g0 = gp[0], g1 = gp[1];
+      const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+      const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      V8 yv;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float2 y = mul2(mul2(make_float2(bf_lo(hw[k]), bf_hi(hw[k])), dup2(inv)),
+                              make_float2(bf_lo(gw[k]), bf_hi(gw[k])));
+        yv.w[k] = pack_bf2(y.x, y.y);
+      }
+      st256(static_cast<uint16_t*>(a.y) + (row * cpr + c) * 16, yv);
+    }
+    __syncthreads();  // the stage is free for the next refill
+  }
+  if (!ok && tid == 0) {
+    // a staged copy did not land within the bound: report it and give the
+    // copies still in flight one more bounded wait before the CTA exits
+    if (a.status) atomicExch(a.status, 2 /* FC_ERR_CUDA */);
+    for (int s = 0; s <= NSTAGE; ++s) {
+      mbar_wait_bounded(&bar[s], 0);
+      mbar_wait_bounded(&bar[s], 1);
+    }
+  }
+}
+
+int geometry(int fmt, const FusedArgs& a, TmaGeom& g) {
+  const int H = a.H, P = a.P;
+  if (fmt == kBF16) {
+    g.cb = 2 * H, g.sb = 0, g.zb = 0;
+  } else {
+    g.cb = fmt == kINT8 ? H : H / 2;
+    g.sb = (H / a.G) * 4;
+    g.zb = fmt == kINT4 ? g.sb : 0;
+  }
+  if (g.cb % 16 || g.sb % 16 || g.zb % 16) return 0;
+  g.stage_bytes = P * (g.cb + g.sb + g.zb) + 2 * H;
+  g.gamma_off = 0;
+  g.stage_off = (2 * H + 127) & ~127;
+  return 1;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <int FMT, int NSTAGE>
+cudaError_t launch_tma_t(const FusedArgs& a, const TmaGeom& g, int smem, int max_ctas,
+                         cudaStream_t st) {
+  auto kern = k_fused_tma<FMT, NSTAGE>;
+  static int configured_smem[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  dev = dev < 64 ? dev : 63;
+  if (configured_smem[dev] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured_smem[dev] = smem;
+  }
+  const int cpr = a.H >> 4;
+  int threads = cpr < kTmaThreads ? ((cpr + 31) & ~31) : kTmaThreads;
+  int occ = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+  if (occ < 1) return cudaErrorInvalidConfiguration;
+  int64_t grid = static_cast<int64_t>(num_sms()) * occ;
+  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+  if (grid > a.rows) grid = a.rows;
+  kern<<<static_cast<int>(grid), threads, smem, st>>>(a, g);
+  return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t launch_tma_fmt(const FusedArgs& a, const TmaGeom& g, int max_ctas, cudaStream_t st) {
+  const int two = g.stage_off + 2 * g.stage_bytes, one = g.stage_off + g.stage_bytes;
+  if (two <= kTmaSmemLimit) return launch_tma_t<FMT, 2>(a, g, two, max_ctas, st);
+  return launch_tma_t<FMT, 1>(a, g, one, max_ctas, st);
+}
+
+}  // namespace
+
+bool fused_tma_eligible(int fmt, const FusedArgs& a) {
+  if (fmt != kBF16 && fmt != kINT8 && fmt != kINT4) return false;
+  TmaGeom g;
+  if (!geometry(fmt, a, g)) return false;
+  if (g.stage_off + g.stage_bytes > kTmaSmemLimit) return false;
+  for (int p = 0; p < a.P; ++p) {
+    if (!aligned16(a.s.codes[p])) return false;
+    if (fmt != kBF16 && !aligned16(a.s.scales[p])) return false;
+    if (fmt == kINT4 && !aligned16(a.s.zeros[p])) return false;
+  }
+  return aligned16(a.res_in) && aligned16(a.gamma);
+}
+
+cudaError_t launch_fused_tma(int fmt, const FusedArgs& a, int max_ctas, cudaStream_t st) {
+  TmaGeom g;
+  geometry(fmt, a, g);
+  switch (fmt) {
+    case kBF16: return launch_tma_fmt<kBF16>(a, g, max_ctas, st);
+    case kINT8: return launch_tma_fmt<kINT8>(a, g, max_ctas, st);
+    default: return launch_tma_fmt<kINT4>(a, g, max_ctas, st);
+  }
+}
+
+}  // namespace fc

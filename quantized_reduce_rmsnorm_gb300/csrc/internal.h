@@ -52,6 +52,15 @@ struct FusedArgs {
 
 int num_sms();
 
+// Dynamic shared memory a TMA-staged fused CTA may use (GB300: 227 KB per CTA).
+constexpr int kTmaSmemLimit = 224 * 1024;
+
+// Fused-kernel choice: automatic, the register-streaming kernel, or the
+// TMA-staged kernel.
+enum FusedPath : int { kPathAuto = 0, kPathStream = 1, kPathTma = 2 };
+bool fused_tma_eligible(int fmt, const FusedArgs& a);
+cudaError_t launch_fused_tma(int fmt, const FusedArgs& a, int max_ctas, cudaStream_t st);
+
 // in_f32: input is fp32 (requantization) instead of bf16; deq_kind: a DeqOut.
 cudaError_t launch_quantize(int fmt, bool in_f32, int deq_kind, const QuantJob& job,
                             cudaStream_t st);
@@ -60,6 +69,6 @@ cudaError_t launch_reduce(int fmt, const Slabs& s, int P, int G, int64_t c0, int
                           float* out, cudaStream_t st);
 cudaError_t launch_pack_tagged(const void* x, int64_t rows, int H, uint32_t epoch, void* blocks,
                                cudaStream_t st);
-cudaError_t launch_fused(int fmt, const FusedArgs& a, int max_ctas, cudaStream_t st);
+cudaError_t launch_fused(int fmt, const FusedArgs& a, int max_ctas, int path, cudaStream_t st);
 
 }  // namespace fc

@@ -28,17 +28,22 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
   const int64_t gwarp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
 
-  for (int p = 0; p < job.P; ++p)
-  for (int64_t t0 = gwarp; t0 < tiles; t0 += nwarps * kUnroll) {
+  const int64_t total = tiles * job.P;
+  for (int64_t t0 = gwarp; t0 < total; t0 += nwarps * kUnroll) {
     float v[kUnroll][16];
     int64_t cc[kUnroll];
+    int pp[kUnroll];
     bool act[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t t = t0 + u * nwarps;
+      // tile t of the flattened (slab, tile) space; slab found by subtraction (P <= 8)
+      int64_t t = t0 + u * nwarps;
+      int p = 0;
+      while (p < job.P - 1 && t >= tiles) t -= tiles, ++p;
       const int64_t c = t * 32 + lane;
       cc[u] = c;
-      act[u] = t < tiles && c < chunks;
+      pp[u] = p;
+      act[u] = t0 + u * nwarps < total && c < chunks;
       if (act[u]) {
         if (IN_F32) {
           const float* x = static_cast<const float*>(job.x[p]) + c * 16;
@@ -59,6 +64,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t c = cc[u];
+      const int p = pp[u];
       float d[16];
       if (FMT == kINT8) {
         uint32_t q[4];

@@ -52,7 +52,10 @@ class QTensor(ctypes.Structure):
 
 
 class LaunchOpts(ctypes.Structure):
-    _fields_ = [("max_ctas", ctypes.c_int32)]
+    _fields_ = [("max_ctas", ctypes.c_int32), ("kernel", ctypes.c_int32)]
+
+
+KERNEL_AUTO, KERNEL_STREAM, KERNEL_TMA = 0, 1, 2
 
 
 INT8_G128 = QSpec(FMT_INT8_SYM, 128)
@@ -210,14 +213,14 @@ def allreduce_residual_rmsnorm(slabs, spec: QSpec, rows: int, hidden: int,
                                gamma: torch.Tensor, eps: float, y: torch.Tensor,
                                requant_out=None, expected_epoch: int = 0,
                                d_status: Optional[torch.Tensor] = None, max_ctas: int = 0,
-                               stream=None):
+                               kernel: int = KERNEL_AUTO, stream=None):
     """The fused quantized All-Reduce + residual add + RMSNorm.
 
     slabs: list of P (codes, scales, zeros) tuples (INT8/INT4), or of bf16
     tensors / tagged-block tensors (BF16 / BF16_TAGGED)."""
     qs = (QTensor * len(slabs))(*[_qt(s if isinstance(s, (tuple, list)) else (s,))
                                   for s in slabs])
-    opts = LaunchOpts(max_ctas)
+    opts = LaunchOpts(max_ctas, kernel)
     _check(load().fc_allreduce_residual_rmsnorm_ex(
         qs, len(slabs), rows, hidden, spec, _ptr(residual_in), _ptr(residual_out), _ptr(gamma),
         eps, _qt(requant_out), _ptr(y), expected_epoch, _ptr(d_status), ctypes.byref(opts),

@@ -236,7 +236,7 @@ def test_two_step_chain_equals_oracle(orc, fmt, G, P):
 
 
 # ------------------------------------------------------------------ fused --
-def run_fused(w, inp, seed_payload=True, max_ctas=0, alias=False, epoch=7):
+def run_fused(w, inp, seed_payload=True, max_ctas=0, alias=False, epoch=7, kernel=0):
     """Quantize (or pack) the slabs on the GPU, run the fused call; returns host arrays."""
     spec = spec_of(w.fmt, w.group)
     if w.fmt in (I8, I4):
@@ -257,7 +257,7 @@ def run_fused(w, inp, seed_payload=True, max_ctas=0, alias=False, epoch=7):
     st = torch.zeros(2, dtype=torch.int32, device="cuda") if w.fmt == TG else None
     fc.allreduce_residual_rmsnorm(slabs, spec, w.T, w.H, r_in, r_out, gam, w.eps, y,
                                   requant_out=rq, expected_epoch=epoch, d_status=st,
-                                  max_ctas=max_ctas)
+                                  max_ctas=max_ctas, kernel=kernel)
     torch.cuda.synchronize()
     res = dict(h=host_bits(r_out), y=host_bits(y))
     if rq is not None:
@@ -301,23 +301,56 @@ FUSED_CASES = [
 ]
 
 
+@pytest.mark.parametrize("kernel", [fc.KERNEL_STREAM, fc.KERNEL_AUTO], ids=["stream", "auto"])
 @pytest.mark.parametrize("name,kw", FUSED_CASES, ids=[c[0] for c in FUSED_CASES])
-def test_fused_matches_oracle(orc, name, kw):
+def test_fused_matches_oracle(orc, name, kw, kernel):
     w = small(name, **kw)
     inp = synth.make_inputs(w, seed=8)
-    got = run_fused(w, inp)
+    got = run_fused(w, inp, kernel=kernel)
     check_fused(orc, w, got, oracle_fused(orc, w, inp))
     if w.fmt == TG:
         assert list(got["status"]) == [fc.FC_OK, fc.STATUS_NO_INDEX]
+
+
+TMA_CASES = [
+    ("prefill", {"T": 40}),
+    ("decode", {"T": 16}),
+    ("decode-tiny", {}),
+    ("bf16-p8", {"P": 8, "T": 9, "H": 5120, "fmt": BF, "group": 0}),
+    ("i4-ragged-h", {"P": 3, "T": 13, "H": 4224, "fmt": I4, "group": 32}),  # 132 groups/row
+    ("i8-cpr-not-warp-multiple", {"P": 2, "T": 7, "H": 1152, "fmt": I8, "group": 64}),
+    ("i4-wide-h", {"P": 2, "T": 5, "H": 16384, "fmt": I4, "group": 32}),
+]
+
+
+@pytest.mark.parametrize("name,kw", TMA_CASES, ids=[c[0] for c in TMA_CASES])
+def test_fused_tma_kernel_matches_oracle(orc, name, kw):
+    """The TMA-staged kernel, forced, on shapes it supports (incl. rows whose
+    chunk count is not a multiple of the warp size, and 1- and 2-stage rings)."""
+    w = small(name, **kw)
+    inp = synth.make_inputs(w, seed=18)
+    want = oracle_fused(orc, w, inp)
+    check_fused(orc, w, run_fused(w, inp, kernel=fc.KERNEL_TMA), want)
+    for cap in (1, 3):
+        check_fused(orc, w, run_fused(w, inp, kernel=fc.KERNEL_TMA, max_ctas=cap), want)
+
+
+def test_fused_tma_kernel_rejects_unsupported_shape():
+    w = small("i8-h16", P=2, T=5, H=16, fmt=I8, group=16)   # 4-byte scale rows
+    inp = synth.make_inputs(w, seed=19)
+    with pytest.raises(fc.FcommError) as e:
+        run_fused(w, inp, kernel=fc.KERNEL_TMA)
+    assert e.value.status == fc.FC_ERR_UNSUPPORTED
 
 
 def test_fused_in_place_residual_and_capped_grid(orc):
     w = small("prefill", T=20)
     inp = synth.make_inputs(w, seed=9)
     want = oracle_fused(orc, w, inp)
-    check_fused(orc, w, run_fused(w, inp, alias=True), want)
-    for cap in (1, 2, 8):
-        check_fused(orc, w, run_fused(w, inp, max_ctas=cap), want)
+    for kernel in (fc.KERNEL_STREAM, fc.KERNEL_TMA):
+        check_fused(orc, w, run_fused(w, inp, alias=True, kernel=kernel), want)
+        for cap in (1, 2, 8):
+            check_fused(orc, w, run_fused(w, inp, max_ctas=cap, kernel=kernel), want)
 
 
 def test_fused_without_payload(orc):
