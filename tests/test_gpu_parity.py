@@ -318,7 +318,7 @@ TMA_CASES = [
     ("decode-tiny", {}),
     ("bf16-p8", {"P": 8, "T": 9, "H": 5120, "fmt": BF, "group": 0}),
     ("i4-ragged-h", {"P": 3, "T": 13, "H": 4224, "fmt": I4, "group": 32}),  # 132 groups/row
-    ("i8-cpr-not-warp-multiple", {"P": 2, "T": 7, "H": 1152, "fmt": I8, "group": 64}),
+    ("i8-cpr-not-warp-multiple", {"P": 2, "T": 7, "H": 1152, "fmt": I8, "group": 32}),
     ("i4-wide-h", {"P": 2, "T": 5, "H": 16384, "fmt": I4, "group": 32}),
 ]
 
