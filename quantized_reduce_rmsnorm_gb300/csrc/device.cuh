@@ -161,11 +161,16 @@ __device__ __forceinline__ void unpack16(const V8& v, float f[16]) {
 }
 
 // -------------------------------------------------- packed fp32 pairs --
-// Pairs of binary32 operations.  With FC_F32X2 the pairs issue as one
-// Blackwell .f32x2 instruction; otherwise as two scalar round-to-nearest
-// intrinsics, which the compiler never contracts into a fused multiply-add.
-#ifdef FC_F32X2
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+// Blackwell issues two binary32 operations per instruction on a register
+// pair (.f32x2); each half is an IEEE round-to-nearest operation.  The
+// compiler may fuse a packed multiply whose product has one use with a
+// following packed add into one fused multiply-add, so packed pairs are
+// used only where that cannot change a result: additions of loaded values,
+// the rounding fast path of the quantizers (its exactness test covers either
+// form), and the tolerance-checked RMSNorm output.  Multiply-then-add chains
+// that must round twice (dequantization, the residual add after it) use the
+// scalar __fmul_rn / __fadd_rn intrinsics, which are never contracted.
+__device__ __forceinline__ float2 padd(float2 a, float2 b) {
   float2 r;
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
       " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
@@ -173,7 +178,7 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return r;
 }
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+__device__ __forceinline__ float2 pmul(float2 a, float2 b) {
   float2 r;
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
       " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
@@ -181,7 +186,7 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return r;
 }
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+__device__ __forceinline__ float2 pfma(float2 a, float2 b, float2 c) {
   float2 r;
   asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
       " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
@@ -189,17 +194,6 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return r;
 }
-#else
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  return make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y));
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  return make_float2(__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y));
-}
-#endif
 __device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
 
 // ------------------------------------------------------- code unpacking --
@@ -221,12 +215,9 @@ __device__ __forceinline__ void dequant_i8_acc(const uint32_t w[4], float s, flo
   for (int j = 0; j < 4; ++j) {
     const uint32_t x = w[j] ^ 0x80808080u;  // int8 -> q + 128
 #pragma unroll
-    for (int k = 0; k < 4; k += 2) {
-      float2 q = add2(make_float2(byte_in_two23(x, k), byte_in_two23(x, k + 1)), dup2(-kTwo23p128));
-      float2 d = mul2(q, dup2(s));
-      float2 a = add2(make_float2(acc[4 * j + k], acc[4 * j + k + 1]), d);
-      acc[4 * j + k] = a.x;
-      acc[4 * j + k + 1] = a.y;
+    for (int k = 0; k < 4; ++k) {
+      const float q = __fadd_rn(byte_in_two23(x, k), -kTwo23p128);
+      acc[4 * j + k] = __fadd_rn(acc[4 * j + k], __fmul_rn(q, s));
     }
   }
 }
@@ -240,11 +231,10 @@ __device__ __forceinline__ void dequant_i4_acc(const uint32_t w[2], float s, flo
     const uint32_t od = (w[j] >> 4) & 0x0F0F0F0Fu;  // codes 8j + 2k + 1
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      float2 q = add2(make_float2(byte_in_two23(ev, k), byte_in_two23(od, k)), dup2(-kTwo23));
-      float2 d = add2(mul2(q, dup2(s)), dup2(z));
-      float2 a = add2(make_float2(acc[8 * j + 2 * k], acc[8 * j + 2 * k + 1]), d);
-      acc[8 * j + 2 * k] = a.x;
-      acc[8 * j + 2 * k + 1] = a.y;
+      const float q0 = __fadd_rn(byte_in_two23(ev, k), -kTwo23);
+      const float q1 = __fadd_rn(byte_in_two23(od, k), -kTwo23);
+      acc[8 * j + 2 * k] = __fadd_rn(acc[8 * j + 2 * k], __fadd_rn(__fmul_rn(q0, s), z));
+      acc[8 * j + 2 * k + 1] = __fadd_rn(acc[8 * j + 2 * k + 1], __fadd_rn(__fmul_rn(q1, s), z));
     }
   }
 }
@@ -286,15 +276,40 @@ __device__ __forceinline__ uint32_t low_bytes4(uint32_t a, uint32_t b, uint32_t 
   return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
 }
 
+// Lane-local group statistics on the 16 bf16 inputs packed in w[8] with
+// bf16x2 min/max (exact: selections of input values).
+__device__ __forceinline__ float bf16_absmax16(const uint32_t w[8]) {
+  __nv_bfloat162 m = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[0]));
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[i])));
+  return fmaxf(__low2float(m), __high2float(m));
+}
+__device__ __forceinline__ void bf16_minmax16(const uint32_t w[8], float& lo, float& hi) {
+  __nv_bfloat162 mn = *reinterpret_cast<const __nv_bfloat162*>(&w[0]), mx = mn;
+#pragma unroll
+  for (int i = 1; i < 8; ++i) {
+    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    mn = __hmin2(mn, v);
+    mx = __hmax2(mx, v);
+  }
+  lo = fminf(__low2float(mn), __high2float(mn));
+  hi = fmaxf(__low2float(mx), __high2float(mx));
+}
+
 // INT8 symmetric on this lane's 16 values of a group spread over lpg lanes:
 //   s = max|x| / 127;  q = clamp(rne(x / s), -127, 127);  s == 0 -> q = 0.
 // Writes the codes packed in q[4]; with DEQ also d[i] = q_i * s.  Returns s.
-template <bool DEQ>
-__device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q[4],
-                                          float d[16]) {
+// With BFW, the lane's max|x| is taken from the packed bf16 inputs bw[8].
+template <bool DEQ, bool BFW = false>
+__device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q[4], float d[16],
+                                          const uint32_t* bw = nullptr) {
   float a = 0.0f;
+  if (BFW) {
+    a = bf16_absmax16(bw);
+  } else {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(v[i]));
+    for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(v[i]));
+  }
   a = group_max(a, lpg);
   const float s = __fdiv_rn(a, 127.0f);
   uint32_t ub[16];  // low byte: the code
@@ -304,19 +319,18 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
     for (int i = 0; i < 16; ++i) ub[i] = 0u, qf[i] = 0.0f;
   } else {
     const float r = __fdiv_rn(1.0f, s);
-    bool slow = !(__fmul_rn(a, r) <= 127.25f);
+    float emax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
-      const float2 t = mul2(make_float2(v[i], v[i + 1]), dup2(r));
-      const float2 u = add2(t, dup2(kMagicI8));
-      const float2 c = add2(u, dup2(-kMagicI8));
-      const float2 e = add2(t, make_float2(-c.x, -c.y));
-      slow |= fabsf(e.x) >= kTieGuard;
-      slow |= fabsf(e.y) >= kTieGuard;
+      const float2 t = pmul(make_float2(v[i], v[i + 1]), dup2(r));
+      const float2 u = padd(t, dup2(kMagicI8));
+      const float2 c = padd(u, dup2(-kMagicI8));
+      const float2 e = padd(t, make_float2(-c.x, -c.y));
+      emax = fmaxf(emax, fmaxf(fabsf(e.x), fabsf(e.y)));
       ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
       qf[i] = c.x, qf[i + 1] = c.y;
     }
-    if (slow) {
+    if (!(emax < kTieGuard) || !(__fmul_rn(a, r) <= 127.25f)) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int c = max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], s))));
@@ -329,10 +343,7 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
   for (int j = 0; j < 4; ++j) q[j] = low_bytes4(ub[4 * j], ub[4 * j + 1], ub[4 * j + 2], ub[4 * j + 3]);
   if (DEQ) {
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      const float2 m = mul2(make_float2(qf[i], qf[i + 1]), dup2(s));
-      d[i] = m.x, d[i + 1] = m.y;
-    }
+    for (int i = 0; i < 16; ++i) d[i] = __fmul_rn(qf[i], s);
   }
   return s;
 }
@@ -340,15 +351,21 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
 // INT4 asymmetric: lo = min, hi = max (a zero extreme taken as +0),
 // s = (hi - lo) / 15, z = lo, q = clamp(rne((x - lo) / s), 0, 15).
 // Element 2i in the low nibble of byte i.  Returns s, writes z; with DEQ also
-// d[i] = (q_i * s) + z.
-template <bool DEQ>
+// d[i] = (q_i * s) + z.  With BFW, the lane's min and max come from the
+// packed bf16 inputs bw[8].
+template <bool DEQ, bool BFW = false>
 __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q[2], float& z,
-                                          float d[16]) {
-  float lo = v[0], hi = v[0];
+                                          float d[16], const uint32_t* bw = nullptr) {
+  float lo, hi;
+  if (BFW) {
+    bf16_minmax16(bw, lo, hi);
+  } else {
+    lo = v[0], hi = v[0];
 #pragma unroll
-  for (int i = 1; i < 16; ++i) {
-    lo = fminf(lo, v[i]);
-    hi = fmaxf(hi, v[i]);
+    for (int i = 1; i < 16; ++i) {
+      lo = fminf(lo, v[i]);
+      hi = fmaxf(hi, v[i]);
+    }
   }
   lo = group_min(lo, lpg);
   hi = group_max(hi, lpg);
@@ -364,19 +381,18 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
     for (int i = 0; i < 16; ++i) ub[i] = 0u, qf[i] = 0.0f;
   } else {
     const float r = __fdiv_rn(1.0f, s);
-    bool slow = !(__fmul_rn(span, r) <= 15.25f);
+    float emax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
-      const float2 t = mul2(add2(make_float2(v[i], v[i + 1]), dup2(-lo)), dup2(r));
-      const float2 u = add2(t, dup2(kTwo23));
-      const float2 c = add2(u, dup2(-kTwo23));
-      const float2 e = add2(t, make_float2(-c.x, -c.y));
-      slow |= fabsf(e.x) >= kTieGuard;
-      slow |= fabsf(e.y) >= kTieGuard;
+      const float2 t = pmul(padd(make_float2(v[i], v[i + 1]), dup2(-lo)), dup2(r));
+      const float2 u = padd(t, dup2(kTwo23));
+      const float2 c = padd(u, dup2(-kTwo23));
+      const float2 e = padd(t, make_float2(-c.x, -c.y));
+      emax = fmaxf(emax, fmaxf(fabsf(e.x), fabsf(e.y)));
       ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
       qf[i] = c.x, qf[i + 1] = c.y;
     }
-    if (slow) {
+    if (!(emax < kTieGuard) || !(__fmul_rn(span, r) <= 15.25f)) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int c = max(0, min(15, __float2int_rn(__fdiv_rn(__fsub_rn(v[i], lo), s))));
@@ -393,10 +409,7 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
   }
   if (DEQ) {
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      const float2 m = add2(mul2(make_float2(qf[i], qf[i + 1]), dup2(s)), dup2(z));
-      d[i] = m.x, d[i + 1] = m.y;
-    }
+    for (int i = 0; i < 16; ++i) d[i] = __fadd_rn(__fmul_rn(qf[i], s), z);
   }
   return s;
 }

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
           if (p < P && act) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float2 t = add2(make_float2(acc[2 * i], acc[2 * i + 1]),
+              const float2 t = padd(make_float2(acc[2 * i], acc[2 * i + 1]),
                                     make_float2(bf_lo(xv[p].w[i]), bf_hi(xv[p].w[i])));
               acc[2 * i] = t.x, acc[2 * i + 1] = t.y;
             }
@@ -137,15 +137,14 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
         V8 hv;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float2 h = add2(make_float2(acc[2 * i], acc[2 * i + 1]),
-                                make_float2(bf_lo(rv.w[i]), bf_hi(rv.w[i])));
-          hb[k][i] = hv.w[i] = pack_bf2(h.x, h.y);
+          hb[k][i] = hv.w[i] = pack_bf2(__fadd_rn(acc[2 * i], bf_lo(rv.w[i])),
+                                        __fadd_rn(acc[2 * i + 1], bf_hi(rv.w[i])));
         }
         st256(static_cast<uint16_t*>(a.res_out) + gc * 16, hv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float2 h = make_float2(bf_lo(hb[k][i]), bf_hi(hb[k][i]));
-          ss2 = fma2(h, h, ss2);
+          ss2 = pfma(h, h, ss2);
         }
       }
     }
@@ -162,7 +161,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
         V8 yv;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float2 y = mul2(mul2(make_float2(bf_lo(hb[k][i]), bf_hi(hb[k][i])), dup2(inv)),
+          const float2 y = pmul(pmul(make_float2(bf_lo(hb[k][i]), bf_hi(hb[k][i])), dup2(inv)),
                                 make_float2(bf_lo(gv.w[i]), bf_hi(gv.w[i])));
           yv.w[i] = pack_bf2(y.x, y.y);
         }

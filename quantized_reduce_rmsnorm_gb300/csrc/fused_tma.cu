@@ -61,7 +61,7 @@ __device__ __forceinline__ void issue_row(const FusedArgs& a, const TmaGeom& g, 
             2 * a.H, bar);
 }
 
-template <int FMT, int NSTAGE>
+template <int FMT, int NSTAGE, int PMAX>
 __global__ void __launch_bounds__(kTmaThreads) k_fused_tma(FusedArgs a, TmaGeom g) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float red[2][32];
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kTmaThreads) k_fused_tma(FusedArgs a, TmaGeom 
     // Every thread runs the same number of iterations so whole warps join
     // the group shuffles; lanes past the row end feed zeros (their groups
     // hold no real element) and touch no memory.
-    float ss = 0.0f;
+    float2 ss2 = make_float2(0.0f, 0.0f);
     for (int cbase = 0; cbase < cpr; cbase += nthr) {
       const int c = cbase + tid;
       const bool act = c < cpr;
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kTmaThreads) k_fused_tma(FusedArgs a, TmaGeom 
 #pragma unroll
       for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
 #pragma unroll
-      for (int p = 0; p < kMaxP; ++p) {
+      for (int p = 0; p < PMAX; ++p) {
         if (p < P && act) {
           if (FMT == kBF16) {
             const uint4* x = reinterpret_cast<const uint4*>(codes + p * g.cb) + 2 * c;
@@ -133,8 +133,9 @@ __global__ void __launch_bounds__(kTmaThreads) k_fused_tma(FusedArgs a, TmaGeom 
             const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              acc[2 * k] = __fadd_rn(acc[2 * k], bf_lo(w[k]));
-              acc[2 * k + 1] = __fadd_rn(acc[2 * k + 1], bf_hi(w[k]));
+              const float2 t = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
+                                    make_float2(bf_lo(w[k]), bf_hi(w[k])));
+              acc[2 * k] = t.x, acc[2 * k + 1] = t.y;
             }
           } else if (FMT == kINT8) {
             const uint4 q = reinterpret_cast<const uint4*>(codes + p * g.cb)[c];
@@ -183,13 +184,12 @@ __global__ void __launch_bounds__(kTmaThreads) k_fused_tma(FusedArgs a, TmaGeom 
         st256(static_cast<uint16_t*>(a.res_out) + gc * 16, hv);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float h0 = bf_lo(hv.w[k]), h1 = bf_hi(hv.w[k]);
-          ss = __fmaf_rn(h0, h0, ss);
-          ss = __fmaf_rn(h1, h1, ss);
+          const float2 h = make_float2(bf_lo(hv.w[k]), bf_hi(hv.w[k]));
+          ss2 = pfma(h, h, ss2);
         }
       }
     }
-    const float tot = block_sum_tma(ss, red, i & 1);  // also orders the h writes
+    const float tot = block_sum_tma(__fadd_rn(ss2.x, ss2.y), red, i & 1);  // also orders the h writes
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, static_cast<float>(H)), a.eps)));
 
     // ---- pass 2: y = bf16((h * inv) * gamma)
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kTmaThreads) k_fused_tma(FusedArgs a, TmaGeom 
       V8 yv;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const float2 y = mul2(mul2(make_float2(bf_lo(hw[k]), bf_hi(hw[k])), dup2(inv)),
+        const float2 y = pmul(pmul(make_float2(bf_lo(hw[k]), bf_hi(hw[k])), dup2(inv)),
                               make_float2(bf_lo(gw[k]), bf_hi(gw[k])));
         yv.w[k] = pack_bf2(y.x, y.y);
       }
@@ -239,10 +239,10 @@ int geometry(int fmt, const FusedArgs& a, TmaGeom& g) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int FMT, int NSTAGE>
+template <int FMT, int NSTAGE, int PMAX>
 cudaError_t launch_tma_t(const FusedArgs& a, const TmaGeom& g, int smem, int max_ctas,
                          cudaStream_t st) {
-  auto kern = k_fused_tma<FMT, NSTAGE>;
+  auto kern = k_fused_tma<FMT, NSTAGE, PMAX>;
   static int configured_smem[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -264,11 +264,20 @@ cudaError_t launch_tma_t(const FusedArgs& a, const TmaGeom& g, int smem, int max
   return cudaGetLastError();
 }
 
+template <int FMT, int PMAX>
+cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cudaStream_t st) {
+  const int two = g.stage_off + 2 * g.stage_bytes, one = g.stage_off + g.stage_bytes;
+  if (two <= kTmaSmemLimit) return launch_tma_t<FMT, 2, PMAX>(a, g, two, max_ctas, st);
+  return launch_tma_t<FMT, 1, PMAX>(a, g, one, max_ctas, st);
+}
+
+// The slab loop is unrolled to PMAX (2, 4 or 8) slots, so no instruction is
+// spent on slots beyond P when P is 2, 4 or 8.
 template <int FMT>
 cudaError_t launch_tma_fmt(const FusedArgs& a, const TmaGeom& g, int max_ctas, cudaStream_t st) {
-  const int two = g.stage_off + 2 * g.stage_bytes, one = g.stage_off + g.stage_bytes;
-  if (two <= kTmaSmemLimit) return launch_tma_t<FMT, 2>(a, g, two, max_ctas, st);
-  return launch_tma_t<FMT, 1>(a, g, one, max_ctas, st);
+  if (a.P <= 2) return launch_tma_p<FMT, 2>(a, g, max_ctas, st);
+  if (a.P <= 4) return launch_tma_p<FMT, 4>(a, g, max_ctas, st);
+  return launch_tma_p<FMT, 8>(a, g, max_ctas, st);
 }
 
 }  // namespace

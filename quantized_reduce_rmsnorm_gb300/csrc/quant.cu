@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
   const int64_t total = tiles * job.P;
   for (int64_t t0 = gwarp; t0 < total; t0 += nwarps * kUnroll) {
     float v[kUnroll][16];
+    uint32_t bw[kUnroll][8];  // the bf16 inputs, packed
     int64_t cc[kUnroll];
     int pp[kUnroll];
     bool act[kUnroll];
@@ -54,11 +55,16 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
             v[u][8 + i] = __uint_as_float(b.w[i]);
           }
         } else {
-          unpack16(ld256_stream(static_cast<const uint16_t*>(job.x[p]) + c * 16), v[u]);
+          const V8 x = ld256_stream(static_cast<const uint16_t*>(job.x[p]) + c * 16);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) bw[u][i] = x.w[i];
+          unpack16(x, v[u]);
         }
       } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[u][i] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) bw[u][i] = 0u;
       }
     }
 #pragma unroll
@@ -68,7 +74,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
       float d[16];
       if (FMT == kINT8) {
         uint32_t q[4];
-        const float s = quant_i8<DEQ != kDeqNone>(v[u], lpg, q, d);
+        const float s = quant_i8<DEQ != kDeqNone, !IN_F32>(v[u], lpg, q, d, bw[u]);
         if (act[u] && job.codes[p]) {
           st128(static_cast<int8_t*>(job.codes[p]) + c * 16, make_uint4(q[0], q[1], q[2], q[3]));
           if ((lane & (lpg - 1)) == 0) stf(job.scales[p] + (c >> lpg_shift), s);
@@ -76,7 +82,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
       } else {
         uint32_t q[2];
         float z;
-        const float s = quant_i4<DEQ != kDeqNone>(v[u], lpg, q, z, d);
+        const float s = quant_i4<DEQ != kDeqNone, !IN_F32>(v[u], lpg, q, z, d, bw[u]);
         if (act[u] && job.codes[p]) {
           st64(static_cast<uint8_t*>(job.codes[p]) + c * 8, make_uint2(q[0], q[1]));
           if ((lane & (lpg - 1)) == 0) {
