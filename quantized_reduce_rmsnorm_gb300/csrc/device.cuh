@@ -258,22 +258,97 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ------------------------------------------------------------ quantizers --
-// Codes are rne(fl(x / s)) (INT8) and rne(fl(fl(x - lo) / s)) (INT4), i.e. an
-// IEEE division per element.  Fast path: one IEEE reciprocal r = fl(1/s) per
-// group and t = fl(x * r).  t differs from the exact quotient by at most
-// 2^-22 |t| + 2^-149 <= 2^-15 (|t| <= 128), and fl(x / s) differs from it by
-// at most 2^-17, so when t is at least 2^-13 away from every half-integer
-// both round to the same integer.  The rounding itself is an exact add of
-// 1.5 * 2^23 (INT8) or 2^23 (INT4), which leaves the integer in the low
-// mantissa bits; t - rint(t) is exact (Sterbenz), so the distance test is
-// exact too.  A per-group bound on the largest t (which is fl(max * r))
-// keeps every code inside its range without clamping.  Lanes where any test
-// fails recompute their 16 codes with the IEEE division.
+// Codes are rne(fl(v / s)), v = x (INT8) or v = fl(x - lo) (INT4): an IEEE
+// division per element by definition.  Computed without one:
+//  1. r ~ 1/s from the hardware reciprocal (relative error <= 2^-23) and
+//     t = v * r; |t| <= 128, so |t - v/s| <= 2^-15.4 and fl(v/s) is within
+//     2^-17 of v/s.  t is rounded by adding 1.5*2^23 (INT8) or 2^23 (INT4),
+//     which leaves rint(t) in the low mantissa bits; e = t - rint(t).
+//  2. If |e| < 1/2 - 2^-13, t is farther than 2^-14 from every half-integer
+//     and rne(fl(v/s)) = rint(t).  (Whether the compiler fuses t into the
+//     following add or not, this holds: the errors above cover both forms.)
+//  3. Otherwise v/s lies within 2^-12 of the half-integer m next to t.  Then
+//     D = v - m*s is an integer multiple of 2^(e_s - 25) smaller than
+//     2^(e_s - 11), so it fits in 24 bits and fma(-m, s, v) gives it exactly
+//     (for s >= 2^-100).  fl(v/s) == m exactly when D lies in m's half-ulp
+//     band [-hd, +hu] (hu = 2^(E-24) s for m = +-2^E...; hd = hu/2 only for
+//     |m| = 1/2), ties at the band edges going to m (its significand is
+//     even).  So the code is the even neighbour of m inside the band, and the
+//     neighbour on D's side outside it.
+//  4. Groups where the bound t <= 127.25 (INT8) / 15.25 (INT4) fails or
+//     s < 2^-100 take the IEEE division for every element (never seen on
+//     finite activations; it keeps denormal scales exact).
 constexpr float kMagicI8 = 12582912.0f;         // 1.5 * 2^23, bits 0x4B400000
-constexpr float kTieGuard = 0.5f - 1.0f / 8192;  // a half-integer is > 2^-13 away
+constexpr float kTieGuard = 0.5f - 1.0f / 8192;  // |e| below this: not near a half-integer
+constexpr float kTwoM24 = 5.9604644775390625e-08f;  // 2^-24
+constexpr float kTwoM100 = 7.888609052210118e-31f;  // 2^-100
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 
 __device__ __forceinline__ uint32_t low_bytes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
+}
+
+// Exact code for an element whose fast-path value sits next to a half-integer
+// (step 3 above).  c: the fast-path integer, e = t - c, v the numerator.
+__device__ __forceinline__ float resolve_near_half(float v, float s, float c, float e) {
+  const float m = __fadd_rn(c, copysignf(0.5f, e));   // the half-integer next to t (exact)
+  const float am = fabsf(m);
+  const float d = __fmaf_rn(-m, s, v);                // v - m*s, exact
+  const float hu = __fmul_rn(__fmul_rn(__uint_as_float(__float_as_uint(am) & 0x7F800000u), kTwoM24), s);
+  const float hd = am == 0.5f ? __fmul_rn(hu, 0.5f) : hu;
+  const float dp = m > 0.0f ? d : -d;                 // > 0: |v/s| beyond |m|
+  const float away = __fadd_rn(m, copysignf(0.5f, m));
+  const float toward = __fadd_rn(m, -copysignf(0.5f, m));
+  if (dp > hu) return away;
+  if (dp < -hd) return toward;
+  // fl(v/s) == m: ties to the even integer
+  return (__float2int_rz(away) & 1) ? toward : away;
+}
+
+// Rounds the 16 quotients v[i] / s; ub[i] gets the code in its low byte (or
+// low nibble), qf[i] the code as a float.  group_ok: fl(vmax * r) is within
+// the code range and s >= 2^-100 (else every element takes the division).
+template <bool SIGNED>
+__device__ __forceinline__ void round_codes(const float v[16], float s, float r, bool group_ok,
+                                            uint32_t ub[16], float qf[16]) {
+  const float magic = SIGNED ? kMagicI8 : 8388608.0f;
+  if (group_ok) {
+    float e[16];
+    float emax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const float2 t = pmul(make_float2(v[i], v[i + 1]), dup2(r));
+      const float2 u = padd(t, dup2(magic));
+      const float2 c = padd(u, dup2(-magic));
+      const float2 d = padd(t, make_float2(-c.x, -c.y));
+      e[i] = d.x, e[i + 1] = d.y;
+      emax = fmaxf(emax, fmaxf(fabsf(d.x), fabsf(d.y)));
+      ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
+      qf[i] = c.x, qf[i + 1] = c.y;
+    }
+    if (!(emax < kTieGuard)) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (!(fabsf(e[i]) < kTieGuard)) {
+          qf[i] = resolve_near_half(v[i], s, qf[i], e[i]);
+          ub[i] = __float_as_uint(__fadd_rn(qf[i], magic));
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = SIGNED ? max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], s))))
+                           : max(0, min(15, __float2int_rn(__fdiv_rn(v[i], s))));
+      ub[i] = static_cast<uint32_t>(c);
+      qf[i] = static_cast<float>(c);
+    }
+  }
 }
 
 // Lane-local group statistics on the 16 bf16 inputs packed in w[8] with
@@ -318,26 +393,8 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
 #pragma unroll
     for (int i = 0; i < 16; ++i) ub[i] = 0u, qf[i] = 0.0f;
   } else {
-    const float r = __fdiv_rn(1.0f, s);
-    float emax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      const float2 t = pmul(make_float2(v[i], v[i + 1]), dup2(r));
-      const float2 u = padd(t, dup2(kMagicI8));
-      const float2 c = padd(u, dup2(-kMagicI8));
-      const float2 e = padd(t, make_float2(-c.x, -c.y));
-      emax = fmaxf(emax, fmaxf(fabsf(e.x), fabsf(e.y)));
-      ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
-      qf[i] = c.x, qf[i + 1] = c.y;
-    }
-    if (!(emax < kTieGuard) || !(__fmul_rn(a, r) <= 127.25f)) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int c = max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], s))));
-        ub[i] = static_cast<uint32_t>(c);
-        qf[i] = static_cast<float>(c);
-      }
-    }
+    const float r = rcp_approx(s);
+    round_codes<true>(v, s, r, __fmul_rn(a, r) <= 127.25f && s >= kTwoM100, ub, qf);
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) q[j] = low_bytes4(ub[4 * j], ub[4 * j + 1], ub[4 * j + 2], ub[4 * j + 3]);
@@ -380,26 +437,14 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
 #pragma unroll
     for (int i = 0; i < 16; ++i) ub[i] = 0u, qf[i] = 0.0f;
   } else {
-    const float r = __fdiv_rn(1.0f, s);
-    float emax = 0.0f;
+    float num[16];
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
-      const float2 t = pmul(padd(make_float2(v[i], v[i + 1]), dup2(-lo)), dup2(r));
-      const float2 u = padd(t, dup2(kTwo23));
-      const float2 c = padd(u, dup2(-kTwo23));
-      const float2 e = padd(t, make_float2(-c.x, -c.y));
-      emax = fmaxf(emax, fmaxf(fabsf(e.x), fabsf(e.y)));
-      ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
-      qf[i] = c.x, qf[i + 1] = c.y;
+      const float2 n = padd(make_float2(v[i], v[i + 1]), dup2(-lo));
+      num[i] = n.x, num[i + 1] = n.y;
     }
-    if (!(emax < kTieGuard) || !(__fmul_rn(span, r) <= 15.25f)) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int c = max(0, min(15, __float2int_rn(__fdiv_rn(__fsub_rn(v[i], lo), s))));
-        ub[i] = static_cast<uint32_t>(c);
-        qf[i] = static_cast<float>(c);
-      }
-    }
+    const float r = rcp_approx(s);
+    round_codes<false>(num, s, r, __fmul_rn(span, r) <= 15.25f && s >= kTwoM100, ub, qf);
   }
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
