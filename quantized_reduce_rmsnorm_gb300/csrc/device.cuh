@@ -318,7 +318,6 @@ __device__ __forceinline__ void round_codes(const float v[16], float s, float r,
                                             uint32_t ub[16], float qf[16]) {
   const float magic = SIGNED ? kMagicI8 : 8388608.0f;
   if (group_ok) {
-    float e[16];
     float emax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
@@ -326,16 +325,17 @@ __device__ __forceinline__ void round_codes(const float v[16], float s, float r,
       const float2 u = padd(t, dup2(magic));
       const float2 c = padd(u, dup2(-magic));
       const float2 d = padd(t, make_float2(-c.x, -c.y));
-      e[i] = d.x, e[i + 1] = d.y;
       emax = fmaxf(emax, fmaxf(fabsf(d.x), fabsf(d.y)));
       ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
       qf[i] = c.x, qf[i + 1] = c.y;
     }
     if (!(emax < kTieGuard)) {
+      // rare: recompute each residual and settle the ones next to a half-integer
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        if (!(fabsf(e[i]) < kTieGuard)) {
-          qf[i] = resolve_near_half(v[i], s, qf[i], e[i]);
+        const float e = __fadd_rn(__fmul_rn(v[i], r), -qf[i]);
+        if (!(fabsf(e) < kTieGuard)) {
+          qf[i] = resolve_near_half(v[i], s, qf[i], e);
           ub[i] = __float_as_uint(__fadd_rn(qf[i], magic));
         }
       }

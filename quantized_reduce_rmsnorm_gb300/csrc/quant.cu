@@ -113,6 +113,111 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
   }
 }
 
+// --------------------------------------------- TMA-streamed quantize kernel --
+// Sender-side quantization of bf16 slabs with the input streamed by the TMA
+// engine: the flattened (slab, tile) space is cut into tiles of kTile
+// elements; each persistent CTA keeps NSTAGE-1 tiles in flight in a ring of
+// shared-memory stages (one elected thread issues cp.async.bulk copies that
+// complete on the stage's mbarrier) while its threads quantize the current
+// tile out of shared memory and store codes and scales directly.
+constexpr int kTile = 8192;              // elements per tile (16 KB of bf16)
+constexpr int kQStages = 4;
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) k_quantize_tma(QuantJob job, int lpg_shift,
+                                                           int64_t tiles_per_slab) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t bar[kQStages];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int lpg = 1 << lpg_shift;
+  const int64_t total = tiles_per_slab * job.P;
+  const int64_t t0 = blockIdx.x, tstride = gridDim.x;
+  if (t0 >= total) return;
+
+  // tile -> (slab, first element, elements)
+  auto locate = [&](int64_t t, int& p, int64_t& e0, int& ne) {
+    p = 0;
+    while (p < job.P - 1 && t >= tiles_per_slab) t -= tiles_per_slab, ++p;
+    e0 = t * kTile;
+    const int64_t rem = job.n - e0;
+    ne = static_cast<int>(rem < kTile ? rem : kTile);
+  };
+  auto issue = [&](int64_t t, int st) {
+    int p, ne;
+    int64_t e0;
+    locate(t, p, e0, ne);
+    mbar_expect_tx(&bar[st], static_cast<uint32_t>(ne * 2));
+    bulk_load(smem + st * (kTile * 2), static_cast<const uint16_t*>(job.x[p]) + e0, ne * 2, &bar[st]);
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < kQStages; ++s) mbar_init(&bar[s], 1);
+    mbar_init_fence();
+    for (int s = 0; s < kQStages - 1; ++s)
+      if (t0 + s * tstride < total) issue(t0 + s * tstride, s);
+  }
+  __syncthreads();
+
+  int k = 0;
+  bool ok = true;
+  for (int64_t t = t0; t < total; t += tstride, ++k) {
+    const int st = k % kQStages;
+    if (tid == 0) {
+      const int64_t nt = t + (kQStages - 1) * tstride;
+      if (nt < total) issue(nt, (k + kQStages - 1) % kQStages);  // that stage was freed last iteration
+    }
+    if (!__syncthreads_and(mbar_wait_bounded(&bar[st], (k / kQStages) & 1))) {
+      ok = false;  // a tile never landed (about a second): stop, outputs incomplete
+      break;
+    }
+    int p, ne;
+    int64_t e0;
+    locate(t, p, e0, ne);
+    const uint4* tile = reinterpret_cast<const uint4*>(smem + st * (kTile * 2));
+    const int nch = ne >> 4;
+#pragma unroll 1
+    for (int cl = tid; cl < kTile / 16; cl += kThreads) {  // uniform trip count: whole warps
+      const bool act = cl < nch;
+      uint32_t bw[8];
+      if (act) {
+        const uint4 a = tile[2 * cl], b = tile[2 * cl + 1];
+        bw[0] = a.x, bw[1] = a.y, bw[2] = a.z, bw[3] = a.w;
+        bw[4] = b.x, bw[5] = b.y, bw[6] = b.z, bw[7] = b.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) bw[i] = 0u;
+      }
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[2 * i] = bf_lo(bw[i]), v[2 * i + 1] = bf_hi(bw[i]);
+      const int64_t c = (e0 >> 4) + cl;  // global chunk of slab p
+      float d[16];
+      if (FMT == kINT8) {
+        uint32_t q[4];
+        const float s = quant_i8<false, true>(v, lpg, q, d, bw);
+        if (act) {
+          st128(static_cast<int8_t*>(job.codes[p]) + c * 16, make_uint4(q[0], q[1], q[2], q[3]));
+          if ((lane & (lpg - 1)) == 0) stf(job.scales[p] + (c >> lpg_shift), s);
+        }
+      } else {
+        uint32_t q[2];
+        float z;
+        const float s = quant_i4<false, true>(v, lpg, q, z, d, bw);
+        if (act) {
+          st64(static_cast<uint8_t*>(job.codes[p]) + c * 8, make_uint2(q[0], q[1]));
+          if ((lane & (lpg - 1)) == 0) {
+            stf(job.scales[p] + (c >> lpg_shift), s);
+            stf(job.zeros[p] + (c >> lpg_shift), z);
+          }
+        }
+      }
+    }
+    __syncthreads();  // the stage may be refilled
+  }
+  if (!ok && tid == 0)  // give copies still in flight a bounded wait before exiting
+    for (int s = 0; s < kQStages; ++s) mbar_wait_bounded(&bar[s], 0), mbar_wait_bounded(&bar[s], 1);
+}
+
 // --------------------------------------------------------- reduce kernel --
 // out[i] = ((0 + deq_0(i)) + deq_1(i)) + ... + deq_{P-1}(i)   (fp32, slab order)
 template <int FMT>
@@ -240,8 +345,39 @@ int num_sms() {
   return sms[dev];
 }
 
+template <int FMT>
+cudaError_t launch_quantize_tma(const QuantJob& job, cudaStream_t st) {
+  const int smem = kQStages * kTile * 2;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  dev = dev < 64 ? dev : 63;
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_quantize_tma<FMT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  int occ = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_quantize_tma<FMT>, kThreads, smem);
+  if (occ < 1) return cudaErrorInvalidConfiguration;
+  const int64_t tps = (job.n + kTile - 1) / kTile;
+  int64_t grid = static_cast<int64_t>(num_sms()) * occ;
+  if (grid > tps * job.P) grid = tps * job.P;
+  k_quantize_tma<FMT><<<static_cast<int>(grid), kThreads, smem, st>>>(job, log2_lanes(job.G), tps);
+  return cudaGetLastError();
+}
+
+bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
 cudaError_t launch_quantize(int fmt, bool in_f32, int deq, const QuantJob& job, cudaStream_t st) {
   if (job.n == 0) return cudaSuccess;
+  if (!in_f32) {
+    // bf16 slabs: TMA-streamed input (16-byte aligned slabs, which the ABI guarantees)
+    bool ok = true;
+    for (int p = 0; p < job.P; ++p) ok = ok && aligned_to(job.x[p], 16) && job.codes[p];
+    if (ok) return fmt == kINT8 ? launch_quantize_tma<kINT8>(job, st) : launch_quantize_tma<kINT4>(job, st);
+  }
   if (fmt == kINT8) {
     if (!in_f32) return launch_quantize_t<kINT8, false, kDeqNone>(job, st);
     if (deq == kDeqBF16) return launch_quantize_t<kINT8, true, kDeqBF16>(job, st);
