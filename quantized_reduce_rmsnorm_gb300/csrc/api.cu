@@ -6,7 +6,7 @@
 #include <cstdio>
 #include <cstring>
 
-#include "../../include/fcomm.h"
+#include "fcomm.h"
 #include "internal.h"
 
 namespace {

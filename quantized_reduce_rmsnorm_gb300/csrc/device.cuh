@@ -223,20 +223,34 @@ __device__ __forceinline__ void dequant_i8_acc(const uint32_t w[4], float s, flo
 }
 
 // acc[i] += (q_i * s) + z for the 16 INT4 codes in w[2] (code i = nibble i%8 of w[i/8]).
-__device__ __forceinline__ void dequant_i4_acc(const uint32_t w[2], float s, float z,
-                                               float acc[16]) {
+// With U = 2^23 + q (the code in the low bits of 2^23) and nms = -2^23 * s
+// (exact while 2^23 * s does not overflow, i.e. s < 2^100 here),
+// fma(U, s, nms) rounds the exact value q*s once: it equals the separately
+// rounded product fl(q*s).  Larger scales take the plain product.
+template <bool FUSED>
+__device__ __forceinline__ void dequant_i4_acc_t(const uint32_t w[2], float s, float z,
+                                                 float acc[16]) {
+  const float nms = __fmul_rn(-kTwo23, s);
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const uint32_t ev = w[j] & 0x0F0F0F0Fu;         // codes 8j + 2k
     const uint32_t od = (w[j] >> 4) & 0x0F0F0F0Fu;  // codes 8j + 2k + 1
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float q0 = __fadd_rn(byte_in_two23(ev, k), -kTwo23);
-      const float q1 = __fadd_rn(byte_in_two23(od, k), -kTwo23);
-      acc[8 * j + 2 * k] = __fadd_rn(acc[8 * j + 2 * k], __fadd_rn(__fmul_rn(q0, s), z));
-      acc[8 * j + 2 * k + 1] = __fadd_rn(acc[8 * j + 2 * k + 1], __fadd_rn(__fmul_rn(q1, s), z));
+      const float u0 = byte_in_two23(ev, k), u1 = byte_in_two23(od, k);
+      const float p0 = FUSED ? __fmaf_rn(u0, s, nms) : __fmul_rn(__fadd_rn(u0, -kTwo23), s);
+      const float p1 = FUSED ? __fmaf_rn(u1, s, nms) : __fmul_rn(__fadd_rn(u1, -kTwo23), s);
+      acc[8 * j + 2 * k] = __fadd_rn(acc[8 * j + 2 * k], __fadd_rn(p0, z));
+      acc[8 * j + 2 * k + 1] = __fadd_rn(acc[8 * j + 2 * k + 1], __fadd_rn(p1, z));
     }
   }
+}
+__device__ __forceinline__ void dequant_i4_acc(const uint32_t w[2], float s, float z,
+                                               float acc[16]) {
+  if (s < 1.2676506e30f)  // 2^100: 2^23 * s stays finite
+    dequant_i4_acc_t<true>(w, s, z, acc);
+  else
+    dequant_i4_acc_t<false>(w, s, z, acc);
 }
 
 // ------------------------------------------------------- group reductions --

@@ -7,9 +7,9 @@
 // the residual -- into a ring of NSTAGE shared-memory stages with 1-D bulk
 // copies (cp.async.bulk) that complete on an mbarrier.  While those bytes
 // are in flight, all threads work on the current row out of shared memory.
-// The bf16 row h (residual + reduced value) is written back over the
-// residual in shared memory, so nothing row-sized is held in registers and
-// occupancy is set by shared memory alone.  gamma is staged once per CTA.
+// The bf16 row h (residual + reduced value) goes to a shared-memory row
+// buffer, so nothing row-sized is held in registers and
+// occupancy is set by shared memory alone.
 //
 // Stage layout (every piece a multiple of 16 bytes, 16-byte aligned):
 //   [codes of slab 0..P-1][scales 0..P-1][zeros 0..P-1 (INT4)][residual]
@@ -29,19 +29,9 @@ struct TmaGeom {
   int sb;           // scale bytes of one slab row (0 for bf16)
   int zb;           // zero-point bytes of one slab row (INT4 only)
   int stage_bytes;  // P * (cb + sb + zb) + 2H
-  int gamma_off;    // byte offset of gamma in dynamic smem
+  int gamma_off;    // byte offset of the h row buffer in dynamic smem
   int stage_off;    // byte offset of stage 0
 };
-
-__device__ __forceinline__ float block_sum_tma(float v, float (*red)[32], int parity) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  v = warp_sum(v);
-  if (lane == 0) red[parity][wid] = v;
-  __syncthreads();
-  float t = 0.0f;
-  for (int w = 0; w < nw; ++w) t += red[parity][w];
-  return t;
-}
 
 template <int FMT>
 __device__ __forceinline__ void issue_row(const FusedArgs& a, const TmaGeom& g, uint8_t* st,
@@ -65,55 +55,39 @@ template <int FMT, int NSTAGE, int PMAX>
 __global__ void __launch_bounds__(kTmaThreads) k_fused_tma(FusedArgs a, TmaGeom g) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float red[2][32];
-  __shared__ uint64_t bar[NSTAGE + 1];  // [NSTAGE] = gamma
-  const int tid = threadIdx.x, lane = tid & 31;
+  __shared__ uint64_t bar[NSTAGE];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
   const int nthr = blockDim.x;
   const int H = a.H, cpr = H >> 4, P = a.P;
   const int lpg = a.G >> 4, sh = a.lpg_shift;
-  uint16_t* gam = reinterpret_cast<uint16_t*>(smem + g.gamma_off);
+  // h (the bf16 row) lives in its own buffer: each thread reads back only the
+  // chunks it wrote, so it needs no barrier and frees the stage early.
+  uint16_t* hbuf = reinterpret_cast<uint16_t*>(smem + g.gamma_off);
   uint8_t* stage0 = smem + g.stage_off;
   const int64_t row0 = blockIdx.x, rstride = gridDim.x;
   if (row0 >= a.rows) return;
 
   if (tid == 0) {
-    for (int s = 0; s <= NSTAGE; ++s) mbar_init(&bar[s], 1);
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(&bar[s], 1);
     mbar_init_fence();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    mbar_expect_tx(&bar[NSTAGE], static_cast<uint32_t>(2 * H));
-    bulk_load(gam, a.gamma, 2 * H, &bar[NSTAGE]);
-    for (int s = 0; s < NSTAGE - 1; ++s)
+    for (int s = 0; s < NSTAGE; ++s)
       if (row0 + s * rstride < a.rows)
         issue_row<FMT>(a, g, stage0 + s * g.stage_bytes, &bar[s], row0 + s * rstride);
   }
-  // every wait ends in a block-wide vote, so all threads leave together
-  bool ok = __syncthreads_and(mbar_wait_bounded(&bar[NSTAGE], 0));
+  __syncthreads();
 
+  bool all_ok = true;
   int i = 0;
-  for (int64_t row = row0; row < a.rows && ok; row += rstride, ++i) {
+  for (int64_t row = row0; row < a.rows; row += rstride, ++i) {
     const int s = i % NSTAGE;
-    uint8_t* st = stage0 + s * g.stage_bytes;
-    if (tid == 0) {
-      // refill the stage that row i-1 used (every thread passed its end-of-row
-      // barrier) with row i + NSTAGE - 1
-      const int64_t nrow = row + (NSTAGE - 1) * rstride;
-      if (nrow < a.rows) {
-        fence_proxy_async_smem();
-        const int ns = (i + NSTAGE - 1) % NSTAGE;
-        issue_row<FMT>(a, g, stage0 + ns * g.stage_bytes, &bar[ns], nrow);
-      }
-    }
-    if (!__syncthreads_and(mbar_wait_bounded(&bar[s], (i / NSTAGE) & 1))) {
-      ok = false;
-      break;
-    }
+    const uint8_t* st = stage0 + s * g.stage_bytes;
+    const bool ok = mbar_wait_bounded(&bar[s], (i / NSTAGE) & 1);
     const uint8_t* codes = st;
     const float* scales = reinterpret_cast<const float*>(st + P * g.cb);
     const float* zeros = reinterpret_cast<const float*>(st + P * (g.cb + g.sb));
-    uint16_t* hrow = reinterpret_cast<uint16_t*>(st + P * (g.cb + g.sb + g.zb));
+    const uint4* rrow = reinterpret_cast<const uint4*>(st + P * (g.cb + g.sb + g.zb));
 
-    // ---- pass 1: reduce, requantize, dequantize, residual add (h -> smem).
+    // ---- pass 1: reduce, requantize, dequantize, residual add (h -> hbuf).
     // Every thread runs the same number of iterations so whole warps join
     // the group shuffles; lanes past the row end feed zeros (their groups
     // hold no real element) and touch no memory.
@@ -171,14 +145,14 @@ __global__ void __launch_bounds__(kTmaThreads) k_fused_tma(FusedArgs a, TmaGeom 
         }
       }
       if (act) {
-        uint4* hp = reinterpret_cast<uint4*>(hrow) + 2 * c;
-        const uint4 r0 = hp[0], r1 = hp[1];
+        const uint4 r0 = rrow[2 * c], r1 = rrow[2 * c + 1];
         const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
         V8 hv;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           hv.w[k] = pack_bf2(__fadd_rn(acc[2 * k], bf_lo(rw[k])),
                              __fadd_rn(acc[2 * k + 1], bf_hi(rw[k])));
+        uint4* hp = reinterpret_cast<uint4*>(hbuf) + 2 * c;
         hp[0] = make_uint4(hv.w[0], hv.w[1], hv.w[2], hv.w[3]);
         hp[1] = make_uint4(hv.w[4], hv.w[5], hv.w[6], hv.w[7]);
         st256(static_cast<uint16_t*>(a.res_out) + gc * 16, hv);
@@ -189,32 +163,46 @@ __global__ void __launch_bounds__(kTmaThreads) k_fused_tma(FusedArgs a, TmaGeom 
         }
       }
     }
-    const float tot = block_sum_tma(__fadd_rn(ss2.x, ss2.y), red, i & 1);  // also orders the h writes
+
+    // ---- the row's only barrier: sum of squares + vote on the staged copy
+    float v = warp_sum(__fadd_rn(ss2.x, ss2.y));
+    if (lane == 0) red[i & 1][wid] = v;
+    all_ok = __syncthreads_and(ok) != 0;
+    if (!all_ok) break;
+    float tot = 0.0f;
+    for (int w = 0; w < nw; ++w) tot += red[i & 1][w];
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, static_cast<float>(H)), a.eps)));
+
+    // every thread is past its reads of stage s: refill it NSTAGE rows ahead
+    if (tid == 0) {
+      const int64_t nrow = row + NSTAGE * rstride;
+      if (nrow < a.rows) {
+        fence_proxy_async_smem();
+        issue_row<FMT>(a, g, stage0 + s * g.stage_bytes, &bar[s], nrow);
+      }
+    }
 
     // ---- pass 2: y = bf16((h * inv) * gamma)
     for (int c = tid; c < cpr; c += nthr) {
-      const uint4* hp = reinterpret_cast<const uint4*>(hrow) + 2 * c;
-      const uint4* gp = reinterpret_cast<const uint4*>(gam) + 2 * c;
-      const uint4 h0 = hp[0], h1 = hp[1], g0 = gp[0], g1 = gp[1];
+      const uint4* hp = reinterpret_cast<const uint4*>(hbuf) + 2 * c;
+      const uint4 h0 = hp[0], h1 = hp[1];
+      const V8 gv = ld256_keep(static_cast<const uint16_t*>(a.gamma) + c * 16);
       const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-      const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
       V8 yv;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const float2 y = pmul(pmul(make_float2(bf_lo(hw[k]), bf_hi(hw[k])), dup2(inv)),
-                              make_float2(bf_lo(gw[k]), bf_hi(gw[k])));
+                              make_float2(bf_lo(gv.w[k]), bf_hi(gv.w[k])));
         yv.w[k] = pack_bf2(y.x, y.y);
       }
       st256(static_cast<uint16_t*>(a.y) + (row * cpr + c) * 16, yv);
     }
-    __syncthreads();  // the stage is free for the next refill
   }
-  if (!ok && tid == 0) {
+  if (!all_ok && tid == 0) {
     // a staged copy did not land within the bound: report it and give the
     // copies still in flight one more bounded wait before the CTA exits
     if (a.status) atomicExch(a.status, 2 /* FC_ERR_CUDA */);
-    for (int s = 0; s <= NSTAGE; ++s) {
+    for (int s = 0; s < NSTAGE; ++s) {
       mbar_wait_bounded(&bar[s], 0);
       mbar_wait_bounded(&bar[s], 1);
     }

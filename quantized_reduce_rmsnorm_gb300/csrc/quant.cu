@@ -115,68 +115,79 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
 
 // --------------------------------------------- TMA-streamed quantize kernel --
 // Sender-side quantization of bf16 slabs with the input streamed by the TMA
-// engine: the flattened (slab, tile) space is cut into tiles of kTile
-// elements; each persistent CTA keeps NSTAGE-1 tiles in flight in a ring of
-// shared-memory stages (one elected thread issues cp.async.bulk copies that
-// complete on the stage's mbarrier) while its threads quantize the current
-// tile out of shared memory and store codes and scales directly.
-constexpr int kTile = 8192;              // elements per tile (16 KB of bf16)
-constexpr int kQStages = 4;
+// engine.  Every warp is autonomous: it owns a private ring of kWStages
+// shared-memory tiles of kWTile elements, its lane 0 issues the bulk copies
+// (cp.async.bulk, completing on the tile's mbarrier) kWStages-1 tiles ahead,
+// and its 32 lanes quantize the current tile out of shared memory and store
+// codes and scales directly.  Warps never wait for each other: no CTA-wide
+// barrier is used.  Tiles cover the flattened (slab, tile) space.
+constexpr int kWTile = 1024;  // elements per warp tile (2 KB of bf16, 2 chunks per lane)
+constexpr int kWStages = 4;
+constexpr int kQWarps = kThreads / 32;
 
 template <int FMT>
 __global__ void __launch_bounds__(kThreads) k_quantize_tma(QuantJob job, int lpg_shift,
                                                            int64_t tiles_per_slab) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint64_t bar[kQStages];
-  const int tid = threadIdx.x, lane = tid & 31;
+  __shared__ uint64_t bars[kQWarps][kWStages];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int lpg = 1 << lpg_shift;
   const int64_t total = tiles_per_slab * job.P;
-  const int64_t t0 = blockIdx.x, tstride = gridDim.x;
-  if (t0 >= total) return;
+  const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kQWarps + wid;
+  const int64_t wstride = static_cast<int64_t>(gridDim.x) * kQWarps;
+  if (w0 >= total) return;  // whole warp
+  uint8_t* ring = smem + wid * (kWStages * kWTile * 2);
+  uint64_t* bar = bars[wid];
 
   // tile -> (slab, first element, elements)
   auto locate = [&](int64_t t, int& p, int64_t& e0, int& ne) {
     p = 0;
     while (p < job.P - 1 && t >= tiles_per_slab) t -= tiles_per_slab, ++p;
-    e0 = t * kTile;
+    e0 = t * kWTile;
     const int64_t rem = job.n - e0;
-    ne = static_cast<int>(rem < kTile ? rem : kTile);
+    ne = static_cast<int>(rem < kWTile ? rem : kWTile);
   };
   auto issue = [&](int64_t t, int st) {
     int p, ne;
     int64_t e0;
     locate(t, p, e0, ne);
     mbar_expect_tx(&bar[st], static_cast<uint32_t>(ne * 2));
-    bulk_load(smem + st * (kTile * 2), static_cast<const uint16_t*>(job.x[p]) + e0, ne * 2, &bar[st]);
+    bulk_load(ring + st * (kWTile * 2), static_cast<const uint16_t*>(job.x[p]) + e0, ne * 2,
+              &bar[st]);
   };
 
-  if (tid == 0) {
-    for (int s = 0; s < kQStages; ++s) mbar_init(&bar[s], 1);
+  if (lane == 0) {
+    for (int s = 0; s < kWStages; ++s) mbar_init(&bar[s], 1);
     mbar_init_fence();
-    for (int s = 0; s < kQStages - 1; ++s)
-      if (t0 + s * tstride < total) issue(t0 + s * tstride, s);
+    for (int s = 0; s < kWStages - 1; ++s)
+      if (w0 + s * wstride < total) issue(w0 + s * wstride, s);
   }
-  __syncthreads();
+  __syncwarp();
 
   int k = 0;
   bool ok = true;
-  for (int64_t t = t0; t < total; t += tstride, ++k) {
-    const int st = k % kQStages;
-    if (tid == 0) {
-      const int64_t nt = t + (kQStages - 1) * tstride;
-      if (nt < total) issue(nt, (k + kQStages - 1) % kQStages);  // that stage was freed last iteration
+  for (int64_t t = w0; t < total; t += wstride, ++k) {
+    const int st = k % kWStages;
+    if (lane == 0) {
+      // refill the stage the warp finished with last iteration (after __syncwarp)
+      const int64_t nt = t + (kWStages - 1) * wstride;
+      if (nt < total) {
+        fence_proxy_async_smem();
+        issue(nt, (k + kWStages - 1) % kWStages);
+      }
     }
-    if (!__syncthreads_and(mbar_wait_bounded(&bar[st], (k / kQStages) & 1))) {
+    if (!__all_sync(kFull, mbar_wait_bounded(&bar[st], (k / kWStages) & 1))) {
       ok = false;  // a tile never landed (about a second): stop, outputs incomplete
       break;
     }
     int p, ne;
     int64_t e0;
     locate(t, p, e0, ne);
-    const uint4* tile = reinterpret_cast<const uint4*>(smem + st * (kTile * 2));
+    const uint4* tile = reinterpret_cast<const uint4*>(ring + st * (kWTile * 2));
     const int nch = ne >> 4;
-#pragma unroll 1
-    for (int cl = tid; cl < kTile / 16; cl += kThreads) {  // uniform trip count: whole warps
+#pragma unroll
+    for (int j = 0; j < kWTile / 16 / 32; ++j) {
+      const int cl = j * 32 + lane;
       const bool act = cl < nch;
       uint32_t bw[8];
       if (act) {
@@ -212,10 +223,10 @@ __global__ void __launch_bounds__(kThreads) k_quantize_tma(QuantJob job, int lpg
         }
       }
     }
-    __syncthreads();  // the stage may be refilled
+    __syncwarp();  // every lane is done with stage st before lane 0 refills it
   }
-  if (!ok && tid == 0)  // give copies still in flight a bounded wait before exiting
-    for (int s = 0; s < kQStages; ++s) mbar_wait_bounded(&bar[s], 0), mbar_wait_bounded(&bar[s], 1);
+  if (!ok && lane == 0)  // give copies still in flight a bounded wait before exiting
+    for (int s = 0; s < kWStages; ++s) mbar_wait_bounded(&bar[s], 0), mbar_wait_bounded(&bar[s], 1);
 }
 
 // --------------------------------------------------------- reduce kernel --
@@ -347,7 +358,7 @@ int num_sms() {
 
 template <int FMT>
 cudaError_t launch_quantize_tma(const QuantJob& job, cudaStream_t st) {
-  const int smem = kQStages * kTile * 2;
+  const int smem = kQWarps * kWStages * kWTile * 2;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -361,9 +372,10 @@ cudaError_t launch_quantize_tma(const QuantJob& job, cudaStream_t st) {
   int occ = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_quantize_tma<FMT>, kThreads, smem);
   if (occ < 1) return cudaErrorInvalidConfiguration;
-  const int64_t tps = (job.n + kTile - 1) / kTile;
+  const int64_t tps = (job.n + kWTile - 1) / kWTile;
   int64_t grid = static_cast<int64_t>(num_sms()) * occ;
-  if (grid > tps * job.P) grid = tps * job.P;
+  const int64_t need = (tps * job.P + kQWarps - 1) / kQWarps;
+  if (grid > need) grid = need;
   k_quantize_tma<FMT><<<static_cast<int>(grid), kThreads, smem, st>>>(job, log2_lanes(job.G), tps);
   return cudaGetLastError();
 }

@@ -126,6 +126,22 @@ def test_reduce_dequant_sum_bit_exact(orc, fmt, G, P):
     assert_bits_equal(host(red), want["reduced"], "reduced fp32")
 
 
+@pytest.mark.parametrize("fmt,G", [(I4, 32), (I8, 128)])
+def test_reduce_huge_scales(orc, fmt, G):
+    """Groups whose scale exceeds 2^100 (outliers near 1e34) take the plain
+    dequantization product; the rest the fused one.  Both bit-exact."""
+    w = synth.Workload("huge", P=3, T=4, H=1024, fmt=fmt, group=G, outlier_frac=0.05,
+                       outlier_scale=1.0e34)
+    inp = synth.make_inputs(w, seed=23)
+    outs = quantize_on_gpu(w, inp)
+    red = torch.empty(w.T, w.H, device="cuda")
+    fc.reduce_dequant_sum(outs, spec_of(fmt, G), w.T, w.H, red)
+    torch.cuda.synchronize()
+    slabs = [oracle_quant(orc, w, s) for s in inp["slabs"]]
+    assert max(float(np.max(sl[1])) for sl in slabs) > 2.0 ** 100
+    assert_bits_equal(host(red), orc.two_step(fmt, slabs, G)["reduced"], "reduced fp32")
+
+
 @pytest.mark.parametrize("fmt,G,P", [(I8, 128, 3), (I4, 32, 8)])
 def test_reduce_shards_write_only_their_range(orc, fmt, G, P):
     w = synth.Workload("shards", P=P, T=5, H=1024, fmt=fmt, group=G)
