@@ -326,35 +326,40 @@ __device__ __forceinline__ float resolve_near_half(float v, float s, float c, fl
 
 // Rounds the 16 quotients v[i] / s; ub[i] gets the code in its low byte (or
 // low nibble), qf[i] the code as a float.  group_ok: fl(vmax * r) is within
-// the code range and s >= 2^-100 (else every element takes the division).
+// the code range and s >= 2^-100 (else every element takes the division);
+// s == 0 is passed as r == 0 with group_ok set, which yields codes 0.
+// Every lane of the warp must call this: the near-half-integer pass is
+// entered by warp vote and runs converged, one vote per element index.
 template <bool SIGNED>
 __device__ __forceinline__ void round_codes(const float v[16], float s, float r, bool group_ok,
                                             uint32_t ub[16], float qf[16]) {
   const float magic = SIGNED ? kMagicI8 : 8388608.0f;
-  if (group_ok) {
-    float emax = 0.0f;
+  float emax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      const float2 t = pmul(make_float2(v[i], v[i + 1]), dup2(r));
-      const float2 u = padd(t, dup2(magic));
-      const float2 c = padd(u, dup2(-magic));
-      const float2 d = padd(t, make_float2(-c.x, -c.y));
-      emax = fmaxf(emax, fmaxf(fabsf(d.x), fabsf(d.y)));
-      ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
-      qf[i] = c.x, qf[i + 1] = c.y;
-    }
-    if (!(emax < kTieGuard)) {
-      // rare: recompute each residual and settle the ones next to a half-integer
+  for (int i = 0; i < 16; i += 2) {
+    const float2 t = pmul(make_float2(v[i], v[i + 1]), dup2(r));
+    const float2 u = padd(t, dup2(magic));
+    const float2 c = padd(u, dup2(-magic));
+    const float2 d = padd(t, make_float2(-c.x, -c.y));
+    emax = fmaxf(emax, fmaxf(fabsf(d.x), fabsf(d.y)));
+    ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
+    qf[i] = c.x, qf[i + 1] = c.y;
+  }
+  if (__any_sync(kFull, group_ok && !(emax < kTieGuard))) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float e = __fadd_rn(__fmul_rn(v[i], r), -qf[i]);
-        if (!(fabsf(e) < kTieGuard)) {
-          qf[i] = resolve_near_half(v[i], s, qf[i], e);
-          ub[i] = __float_as_uint(__fadd_rn(qf[i], magic));
+    for (int i = 0; i < 16; ++i) {
+      const float e = __fadd_rn(__fmul_rn(v[i], r), -qf[i]);
+      const bool near = group_ok && !(fabsf(e) < kTieGuard);
+      if (__any_sync(kFull, near)) {
+        const float res = resolve_near_half(v[i], s, qf[i], e);
+        if (near) {
+          qf[i] = res;
+          ub[i] = __float_as_uint(__fadd_rn(res, magic));
         }
       }
     }
-  } else {
+  }
+  if (!group_ok) {  // per lane; never taken on finite activations
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int c = SIGNED ? max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], s))))
@@ -403,13 +408,8 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
   const float s = __fdiv_rn(a, 127.0f);
   uint32_t ub[16];  // low byte: the code
   float qf[16];     // the code as a float
-  if (s == 0.0f) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) ub[i] = 0u, qf[i] = 0.0f;
-  } else {
-    const float r = rcp_approx(s);
-    round_codes<true>(v, s, r, __fmul_rn(a, r) <= 127.25f && s >= kTwoM100, ub, qf);
-  }
+  const float r = s == 0.0f ? 0.0f : rcp_approx(s);
+  round_codes<true>(v, s, r, s == 0.0f || (__fmul_rn(a, r) <= 127.25f && s >= kTwoM100), ub, qf);
 #pragma unroll
   for (int j = 0; j < 4; ++j) q[j] = low_bytes4(ub[4 * j], ub[4 * j + 1], ub[4 * j + 2], ub[4 * j + 3]);
   if (DEQ) {
@@ -447,19 +447,14 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
   z = lo;
   uint32_t ub[16];
   float qf[16];
-  if (s == 0.0f) {
+  float num[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) ub[i] = 0u, qf[i] = 0.0f;
-  } else {
-    float num[16];
-#pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      const float2 n = padd(make_float2(v[i], v[i + 1]), dup2(-lo));
-      num[i] = n.x, num[i + 1] = n.y;
-    }
-    const float r = rcp_approx(s);
-    round_codes<false>(num, s, r, __fmul_rn(span, r) <= 15.25f && s >= kTwoM100, ub, qf);
+  for (int i = 0; i < 16; i += 2) {
+    const float2 n = padd(make_float2(v[i], v[i + 1]), dup2(-lo));
+    num[i] = n.x, num[i + 1] = n.y;
   }
+  const float r = s == 0.0f ? 0.0f : rcp_approx(s);
+  round_codes<false>(num, s, r, s == 0.0f || (__fmul_rn(span, r) <= 15.25f && s >= kTwoM100), ub, qf);
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const uint32_t ev = low_bytes4(ub[8 * j], ub[8 * j + 2], ub[8 * j + 4], ub[8 * j + 6]);
