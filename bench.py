@@ -289,7 +289,7 @@ def run_ours(args):
     step_ms = sum(a + b for a, b in zip(sender_ms, fused_ms)) / n
     step_ms = allreduce_max(step_ms, ws, dev)
 
-    value = ws * step_bytes / (step_ms * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, ws, step_ms)
     peak, peak_kind = peaks()
     kern = [("sender", "k_quantize" if w.fmt in (1, 2) else "k_pack_tagged", alg["sender"],
              statistics.mean(sender_ms)),
@@ -373,9 +373,15 @@ def run_e2e(pipe, inputs, step_bytes, args, ws, dev):
     e1.record(st)
     torch.cuda.synchronize(dev)
     ms = allreduce_max(e0.elapsed_time(e1) / steps, ws, dev)
-    return {"value": round(ws * step_bytes / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+    return {"value": round(whole_job_gbs(step_bytes, ws, ms), 2), "unit": UNIT,
             "ms_per_step": round(ms, 4), "steps": steps, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
+
+
+def whole_job_gbs(bytes_per_rank_step: int, ws: int, max_step_ms: float) -> float:
+    """Weak scaling: every rank moves bytes_per_rank_step per step; the job's
+    throughput is all ranks' bytes over the slowest rank's step time."""
+    return ws * bytes_per_rank_step / (max_step_ms * 1e-3) / 1e9
 
 
 def barrier(ws):
