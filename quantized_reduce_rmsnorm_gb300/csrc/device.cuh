@@ -335,12 +335,14 @@ __device__ __forceinline__ void round_codes(const float v[16], float s, float r,
                                             uint32_t ub[16], float qf[16]) {
   const float magic = SIGNED ? kMagicI8 : 8388608.0f;
   float emax = 0.0f;
+  float e[16];  // t - rint(t), kept for the near-half-integer pass
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
     const float2 t = pmul(make_float2(v[i], v[i + 1]), dup2(r));
     const float2 u = padd(t, dup2(magic));
     const float2 c = padd(u, dup2(-magic));
     const float2 d = padd(t, make_float2(-c.x, -c.y));
+    e[i] = d.x, e[i + 1] = d.y;
     emax = fmaxf(emax, fmaxf(fabsf(d.x), fabsf(d.y)));
     ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
     qf[i] = c.x, qf[i + 1] = c.y;
@@ -348,10 +350,9 @@ __device__ __forceinline__ void round_codes(const float v[16], float s, float r,
   if (__any_sync(kFull, group_ok && !(emax < kTieGuard))) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float e = __fadd_rn(__fmul_rn(v[i], r), -qf[i]);
-      const bool near = group_ok && !(fabsf(e) < kTieGuard);
+      const bool near = group_ok && !(fabsf(e[i]) < kTieGuard);
       if (__any_sync(kFull, near)) {
-        const float res = resolve_near_half(v[i], s, qf[i], e);
+        const float res = resolve_near_half(v[i], s, qf[i], e[i]);
         if (near) {
           qf[i] = res;
           ub[i] = __float_as_uint(__fadd_rn(res, magic));

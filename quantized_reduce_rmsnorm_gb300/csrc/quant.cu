@@ -126,7 +126,7 @@ constexpr int kWStages = 4;
 constexpr int kQWarps = kThreads / 32;
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads) k_quantize_tma(QuantJob job, int lpg_shift,
+__global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int lpg_shift,
                                                            int64_t tiles_per_slab) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t bars[kQWarps][kWStages];
@@ -139,50 +139,59 @@ __global__ void __launch_bounds__(kThreads) k_quantize_tma(QuantJob job, int lpg
   uint8_t* ring = smem + wid * (kWStages * kWTile * 2);
   uint64_t* bar = bars[wid];
 
-  // tile -> (slab, first element, elements)
-  auto locate = [&](int64_t t, int& p, int64_t& e0, int& ne) {
-    p = 0;
-    while (p < job.P - 1 && t >= tiles_per_slab) t -= tiles_per_slab, ++p;
-    e0 = t * kWTile;
-    const int64_t rem = job.n - e0;
-    ne = static_cast<int>(rem < kWTile ? rem : kWTile);
+  // A cursor over the flattened (slab, tile) space that only moves forward by
+  // wstride tiles: (slab p, tile tt of that slab).
+  struct Cursor {
+    int p;
+    int64_t tt;
   };
-  auto issue = [&](int64_t t, int st) {
-    int p, ne;
-    int64_t e0;
-    locate(t, p, e0, ne);
+  auto advance = [&](Cursor cur, int64_t by) {
+    cur.tt += by;
+    while (cur.tt >= tiles_per_slab && cur.p < job.P - 1) cur.tt -= tiles_per_slab, ++cur.p;
+    return cur;
+  };
+  auto issue = [&](Cursor cur, int st) {
+    const int64_t e0 = cur.tt * kWTile;
+    const int64_t rem = job.n - e0;
+    const int ne = static_cast<int>(rem < kWTile ? rem : kWTile);
     mbar_expect_tx(&bar[st], static_cast<uint32_t>(ne * 2));
-    bulk_load(ring + st * (kWTile * 2), static_cast<const uint16_t*>(job.x[p]) + e0, ne * 2,
+    bulk_load(ring + st * (kWTile * 2), static_cast<const uint16_t*>(job.x[cur.p]) + e0, ne * 2,
               &bar[st]);
   };
 
+  const Cursor first = advance(Cursor{0, 0}, w0);
+  Cursor ahead = first;  // lane 0's issue cursor, kWStages - 1 tiles ahead
   if (lane == 0) {
     for (int s = 0; s < kWStages; ++s) mbar_init(&bar[s], 1);
     mbar_init_fence();
-    for (int s = 0; s < kWStages - 1; ++s)
-      if (w0 + s * wstride < total) issue(w0 + s * wstride, s);
+    for (int s = 0; s < kWStages - 1; ++s) {
+      if (w0 + s * wstride < total) issue(ahead, s);
+      ahead = advance(ahead, wstride);
+    }
   }
   __syncwarp();
 
   int k = 0;
   bool ok = true;
-  for (int64_t t = w0; t < total; t += wstride, ++k) {
+  Cursor cur = first;
+  for (int64_t t = w0; t < total; t += wstride, ++k, cur = advance(cur, wstride)) {
     const int st = k % kWStages;
     if (lane == 0) {
       // refill the stage the warp finished with last iteration (after __syncwarp)
-      const int64_t nt = t + (kWStages - 1) * wstride;
-      if (nt < total) {
+      if (t + (kWStages - 1) * wstride < total) {
         fence_proxy_async_smem();
-        issue(nt, (k + kWStages - 1) % kWStages);
+        issue(ahead, (k + kWStages - 1) % kWStages);
       }
+      ahead = advance(ahead, wstride);
     }
     if (!__all_sync(kFull, mbar_wait_bounded(&bar[st], (k / kWStages) & 1))) {
       ok = false;  // a tile never landed (about a second): stop, outputs incomplete
       break;
     }
-    int p, ne;
-    int64_t e0;
-    locate(t, p, e0, ne);
+    const int p = cur.p;
+    const int64_t e0 = cur.tt * kWTile;
+    const int64_t rem = job.n - e0;
+    const int ne = static_cast<int>(rem < kWTile ? rem : kWTile);
     const uint4* tile = reinterpret_cast<const uint4*>(ring + st * (kWTile * 2));
     const int nch = ne >> 4;
 #pragma unroll
