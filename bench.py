@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--sweep", choices=["quick", "full"], default=None,
+                    help="message-size sweep (16 KB..256 MB x P x format): one JSON line per point")
     return ap.parse_args()
 
 
@@ -400,8 +402,89 @@ def allreduce_max(v, ws, dev):
     return float(t.item())
 
 
+def run_sweep(args):
+    """Message-size sweep of the fused kernel (and the sender quantizer).
+
+    Inputs are seeded N(0,1) bf16 generated on the device (a measurement,
+    not a parity case); each point is timed with CUDA events, median of
+    repetitions, with a 256 MB L2 scrub before every repetition when the
+    point's inputs fit in L2."""
+    import torch
+    from quantized_reduce_rmsnorm_gb300 import fcomm, synth
+    from quantized_reduce_rmsnorm_gb300.pipeline import qs_bytes
+    fcomm.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, _ = peaks()
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    pts = synth.sweep_points()
+    if args.sweep == "quick":
+        pts = [p for p in pts if p[0] in (16 << 10, 1 << 20, 16 << 20, 64 << 20, 256 << 20)]
+    gen = torch.Generator(device=dev)
+    for msg, H, T, P, fmt, G in pts:
+        if T == 0:
+            continue
+        gen.manual_seed(msg ^ (H << 8) ^ (P << 4) ^ fmt)
+        w = synth.sweep_workload(H, T, P, fmt, G)
+        spec = fcomm.QSpec(fmt, G)
+        xs = [torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16) for _ in range(P)]
+        res = torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16)
+        gam = (1 + 0.1 * torch.randn(H, generator=gen, device=dev)).to(torch.bfloat16)
+        r_out, y = torch.empty_like(res), torch.empty_like(res)
+        E = T * H
+        if fmt in (synth.FMT_INT8_SYM, synth.FMT_INT4_ASYM):
+            codes = [fcomm.alloc_qtensor(spec, T, H, dev) for _ in range(P)]
+            payload = fcomm.alloc_qtensor(spec, T, H, dev)
+            qs = qs_bytes(w, E)
+            sender_bytes = P * 2 * E + P * qs
+            fused_bytes = P * qs + 2 * E + 2 * H + qs + 4 * E
+            send = lambda: fcomm.group_quantize_multi(xs, spec, codes)
+            fuse = lambda: fcomm.allreduce_residual_rmsnorm(codes, spec, T, H, res, r_out, gam,
+                                                            1e-5, y, requant_out=payload)
+        else:
+            sender_bytes = 0
+            fused_bytes = P * 2 * E + 2 * E + 2 * H + 4 * E
+            send = None
+            fuse = lambda: fcomm.allreduce_residual_rmsnorm(xs, spec, T, H, res, r_out, gam,
+                                                            1e-5, y)
+        small = (P * 2 + 6) * E < 2 * L2_BYTES
+        reps = 15 if E * P * 2 < (64 << 20) else 7
+
+        def timed(fn):
+            out = []
+            for i in range(reps + 2):
+                if small:
+                    flush.add_(1.0)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                b.synchronize()
+                if i >= 2:
+                    out.append(a.elapsed_time(b) * 1e3)
+            return statistics.median(out)
+
+        su = timed(send) if send else None
+        fu = timed(fuse)
+        line = {"sweep": True, "message_bytes": msg, "hidden": H, "tokens": T, "P": P,
+                "format": synth.FMT_NAMES[fmt], "fused_us": round(fu, 2),
+                "fused_GBps": round(fused_bytes / fu / 1e3, 1),
+                "fused_frac": round(fused_bytes / fu / 1e3 / peak, 4),
+                "sender_us": None if su is None else round(su, 2),
+                "sender_GBps": None if su is None else round(sender_bytes / su / 1e3, 1),
+                "l2_scrubbed": small}
+        print(json.dumps(line), flush=True)
+        del xs, res, gam, r_out, y
+        if send:
+            del codes, payload
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -324,6 +324,54 @@ __device__ __forceinline__ float resolve_near_half(float v, float s, float c, fl
   return (__float2int_rz(away) & 1) ? toward : away;
 }
 
+// Lane-local group statistics on the 16 bf16 inputs packed in w[8] with
+// bf16x2 min/max (exact: selections of input values), as pairwise trees so
+// the dependency chains stay short.
+__device__ __forceinline__ __nv_bfloat162 bf2(uint32_t w) {
+  return *reinterpret_cast<const __nv_bfloat162*>(&w);
+}
+__device__ __forceinline__ float bf16_absmax16(const uint32_t w[8]) {
+  __nv_bfloat162 m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = __hmax2(__habs2(bf2(w[2 * i])), __habs2(bf2(w[2 * i + 1])));
+  const __nv_bfloat162 r = __hmax2(__hmax2(m[0], m[1]), __hmax2(m[2], m[3]));
+  return fmaxf(__low2float(r), __high2float(r));
+}
+__device__ __forceinline__ void bf16_minmax16(const uint32_t w[8], float& lo, float& hi) {
+  __nv_bfloat162 mn[4], mx[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    mn[i] = __hmin2(bf2(w[2 * i]), bf2(w[2 * i + 1]));
+    mx[i] = __hmax2(bf2(w[2 * i]), bf2(w[2 * i + 1]));
+  }
+  const __nv_bfloat162 a = __hmin2(__hmin2(mn[0], mn[1]), __hmin2(mn[2], mn[3]));
+  const __nv_bfloat162 b = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
+  lo = fminf(__low2float(a), __high2float(a));
+  hi = fmaxf(__low2float(b), __high2float(b));
+}
+
+// Tree reductions over 16 floats (max of |v|, min and max).
+__device__ __forceinline__ float absmax16(const float v[16]) {
+  float m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m[i] = fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
+#pragma unroll
+  for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  return m[0];
+}
+__device__ __forceinline__ void minmax16(const float v[16], float& lo, float& hi) {
+  float a[8], b[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = fminf(v[2 * i], v[2 * i + 1]), b[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) a[i] = fminf(a[i], a[i + w]), b[i] = fmaxf(b[i], b[i + w]);
+  lo = a[0], hi = b[0];
+}
+
 // Rounds the 16 quotients v[i] / s; ub[i] gets the code in its low byte (or
 // low nibble), qf[i] the code as a float.  group_ok: fl(vmax * r) is within
 // the code range and s >= 2^-100 (else every element takes the division);
@@ -334,7 +382,6 @@ template <bool SIGNED>
 __device__ __forceinline__ void round_codes(const float v[16], float s, float r, bool group_ok,
                                             uint32_t ub[16], float qf[16]) {
   const float magic = SIGNED ? kMagicI8 : 8388608.0f;
-  float emax = 0.0f;
   float e[16];  // t - rint(t), kept for the near-half-integer pass
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
@@ -343,10 +390,10 @@ __device__ __forceinline__ void round_codes(const float v[16], float s, float r,
     const float2 c = padd(u, dup2(-magic));
     const float2 d = padd(t, make_float2(-c.x, -c.y));
     e[i] = d.x, e[i + 1] = d.y;
-    emax = fmaxf(emax, fmaxf(fabsf(d.x), fabsf(d.y)));
     ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
     qf[i] = c.x, qf[i + 1] = c.y;
   }
+  const float emax = absmax16(e);
   if (__any_sync(kFull, group_ok && !(emax < kTieGuard))) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -371,26 +418,6 @@ __device__ __forceinline__ void round_codes(const float v[16], float s, float r,
   }
 }
 
-// Lane-local group statistics on the 16 bf16 inputs packed in w[8] with
-// bf16x2 min/max (exact: selections of input values).
-__device__ __forceinline__ float bf16_absmax16(const uint32_t w[8]) {
-  __nv_bfloat162 m = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[0]));
-#pragma unroll
-  for (int i = 1; i < 8; ++i) m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[i])));
-  return fmaxf(__low2float(m), __high2float(m));
-}
-__device__ __forceinline__ void bf16_minmax16(const uint32_t w[8], float& lo, float& hi) {
-  __nv_bfloat162 mn = *reinterpret_cast<const __nv_bfloat162*>(&w[0]), mx = mn;
-#pragma unroll
-  for (int i = 1; i < 8; ++i) {
-    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-    mn = __hmin2(mn, v);
-    mx = __hmax2(mx, v);
-  }
-  lo = fminf(__low2float(mn), __high2float(mn));
-  hi = fmaxf(__low2float(mx), __high2float(mx));
-}
-
 // INT8 symmetric on this lane's 16 values of a group spread over lpg lanes:
 //   s = max|x| / 127;  q = clamp(rne(x / s), -127, 127);  s == 0 -> q = 0.
 // Writes the codes packed in q[4]; with DEQ also d[i] = q_i * s.  Returns s.
@@ -398,13 +425,7 @@ __device__ __forceinline__ void bf16_minmax16(const uint32_t w[8], float& lo, fl
 template <bool DEQ, bool BFW = false>
 __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q[4], float d[16],
                                           const uint32_t* bw = nullptr) {
-  float a = 0.0f;
-  if (BFW) {
-    a = bf16_absmax16(bw);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(v[i]));
-  }
+  float a = BFW ? bf16_absmax16(bw) : absmax16(v);
   a = group_max(a, lpg);
   const float s = __fdiv_rn(a, 127.0f);
   uint32_t ub[16];  // low byte: the code
@@ -429,16 +450,10 @@ template <bool DEQ, bool BFW = false>
 __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q[2], float& z,
                                           float d[16], const uint32_t* bw = nullptr) {
   float lo, hi;
-  if (BFW) {
+  if (BFW)
     bf16_minmax16(bw, lo, hi);
-  } else {
-    lo = v[0], hi = v[0];
-#pragma unroll
-    for (int i = 1; i < 16; ++i) {
-      lo = fminf(lo, v[i]);
-      hi = fmaxf(hi, v[i]);
-    }
-  }
+  else
+    minmax16(v, lo, hi);
   lo = group_min(lo, lpg);
   hi = group_max(hi, lpg);
   if (lo == 0.0f) lo = 0.0f;  // -0 -> +0
