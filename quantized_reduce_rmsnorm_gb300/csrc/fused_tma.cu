@@ -22,7 +22,8 @@ namespace fc {
 
 namespace {
 
-constexpr int kTmaThreads = 256;
+constexpr int kTmaThreads = 256;     // per CTA when two or more CTAs fit an SM
+constexpr int kTmaThreadsMax = 512;  // when only one does
 
 struct TmaGeom {
   int cb;           // code (or bf16 data) bytes of one slab row
@@ -52,7 +53,7 @@ __device__ __forceinline__ void issue_row(const FusedArgs& a, const TmaGeom& g, 
 }
 
 template <int FMT, int NSTAGE, int PMAX>
-__global__ void __launch_bounds__(kTmaThreads) k_fused_tma(FusedArgs a, TmaGeom g) {
+__global__ void __launch_bounds__(kTmaThreadsMax) k_fused_tma(FusedArgs a, TmaGeom g) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float red[2][32];
   __shared__ uint64_t bar[NSTAGE];
@@ -244,6 +245,11 @@ cudaError_t launch_tma_t(const FusedArgs& a, const TmaGeom& g, int smem, int max
   int threads = cpr < kTmaThreads ? ((cpr + 31) & ~31) : kTmaThreads;
   int occ = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+  if (occ == 1 && cpr >= kTmaThreadsMax) {
+    // shared memory admits a single CTA per SM: give it more warps instead
+    threads = kTmaThreadsMax;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+  }
   if (occ < 1) return cudaErrorInvalidConfiguration;
   int64_t grid = static_cast<int64_t>(num_sms()) * occ;
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
