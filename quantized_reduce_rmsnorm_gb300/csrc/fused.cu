@@ -172,142 +172,139 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
 }
 
 // ------------------------------------------------------ tagged bf16 path --
-// A unit is 4 blocks = 24 elements of one row (48 bytes of residual / gamma /
-// outputs, 16-byte aligned).  Each block's tag is checked in the same
-// 16-byte load that brings its payload; a failing block is not summed.
-template <int NU>
-__global__ void __launch_bounds__(kMaxThreads) k_fused_tagged(FusedArgs a) {
-  __shared__ float red[2][32];
-  const int tid = threadIdx.x;
-  const int nthr = blockDim.x;
+// One warp per token row, one lane per 16-byte block.  Per group of 32
+// blocks: each slab's block arrives in one 16-byte load (a warp reads 512
+// contiguous bytes per slab) and its tag is checked in that same load; a
+// block that fails is not summed.  The residual and the outputs move as
+// three 4-byte words per lane (6 bf16 at a 12-byte stride).  The row's sum
+// of squares is a warp reduction, so warps never wait for each other; pass 2
+// reads h back from residual_out, which this lane has just written (the row
+// is still in L2).
+__device__ __forceinline__ uint32_t ld32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.u32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
+  return r;
+}
+__device__ __forceinline__ uint32_t ld32_nc(const void* p) {
+  uint32_t r;
+  asm("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st32(void* p, uint32_t v) {
+  asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// 6 bf16 (3 words) of row element e0.. of a row of length H; full: e0 + 6 <= H.
+template <bool NC>
+__device__ __forceinline__ void load6(const uint16_t* row, int e0, int H, bool full, uint32_t w[3]) {
+  if (full) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) w[k] = NC ? ld32_nc(row + e0 + 2 * k) : ld32(row + e0 + 2 * k);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int e = e0 + 2 * k;
+      const uint32_t lo = e < H ? ld16(row + e) : 0u;
+      const uint32_t hi = e + 1 < H ? ld16(row + e + 1) : 0u;
+      w[k] = lo | (hi << 16);
+    }
+  }
+}
+__device__ __forceinline__ void store6(uint16_t* row, int e0, int H, bool full, const uint32_t w[3]) {
+  if (full) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) st32(row + e0 + 2 * k, w[k]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 6; ++k)
+      if (e0 + k < H) row[e0 + k] = static_cast<uint16_t>(w[k >> 1] >> (16 * (k & 1)));
+  }
+}
+
+template <int PMAX>
+__global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int H = a.H;
   const int nb = (H + 5) / 6;
-  const int units = (nb + 3) >> 2;
+  const int gpr = (nb + 31) >> 5;
   const int P = a.P;
   const uint32_t epoch = a.epoch;
-  int parity = 0;
 
-  for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, parity ^= 1) {
-    uint32_t hb[NU][12];
+  for (int64_t row = w0; row < a.rows; row += nw) {
+    const uint16_t* rr = static_cast<const uint16_t*>(a.res_in) + row * H;
+    uint16_t* ro = static_cast<uint16_t*>(a.res_out) + row * H;
     float ss = 0.0f;
+    int64_t first_bad = LLONG_MAX;
+    for (int gi = 0; gi < gpr; ++gi) {
+      const int j = gi * 32 + lane;
+      if (j >= nb) continue;
+      uint4 b[PMAX];
 #pragma unroll
-    for (int k = 0; k < NU; ++k) {
-      const int u = k * nthr + tid;
-      const bool act = u < units;
-      const bool full = act && 24 * u + 24 <= H;
-      float acc[24];
+      for (int p = 0; p < PMAX; ++p)
+        if (p < P) b[p] = ld128_stream(static_cast<const uint4*>(a.s.codes[p]) + row * nb + j);
+      const int e0 = 6 * j;
+      const bool full = e0 + 6 <= H;
+      uint32_t rw[3];
+      load6<true>(rr, e0, H, full, rw);
+      float acc[6] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int i = 0; i < 24; ++i) acc[i] = 0.0f;
-      int64_t first_bad = LLONG_MAX;
+      for (int p = 0; p < PMAX; ++p) {
+        if (p < P) {
+          if (b[p].w == epoch) {
+            const uint32_t w[3] = {b[p].x, b[p].y, b[p].z};
 #pragma unroll
-      for (int p = 0; p < kMaxP; ++p) {
-        if (p < P && act) {
-          const uint4* bl = static_cast<const uint4*>(a.s.codes[p]) + row * nb + 4 * u;
-          uint4 b[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            b[j] = (4 * u + j < nb) ? ld128_stream(bl + j) : make_uint4(0, 0, 0, epoch);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (b[j].w == epoch) {
-              acc[6 * j + 0] = __fadd_rn(acc[6 * j + 0], bf_lo(b[j].x));
-              acc[6 * j + 1] = __fadd_rn(acc[6 * j + 1], bf_hi(b[j].x));
-              acc[6 * j + 2] = __fadd_rn(acc[6 * j + 2], bf_lo(b[j].y));
-              acc[6 * j + 3] = __fadd_rn(acc[6 * j + 3], bf_hi(b[j].y));
-              acc[6 * j + 4] = __fadd_rn(acc[6 * j + 4], bf_lo(b[j].z));
-              acc[6 * j + 5] = __fadd_rn(acc[6 * j + 5], bf_hi(b[j].z));
-            } else {
-              const int64_t idx = (static_cast<int64_t>(p) * a.rows + row) * nb + 4 * u + j;
-              first_bad = idx < first_bad ? idx : first_bad;
+            for (int k = 0; k < 3; ++k) {
+              const float2 t = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
+                                    make_float2(bf_lo(w[k]), bf_hi(w[k])));
+              acc[2 * k] = t.x, acc[2 * k + 1] = t.y;
             }
+          } else {
+            const int64_t idx = (static_cast<int64_t>(p) * a.rows + row) * nb + j;
+            first_bad = idx < first_bad ? idx : first_bad;
           }
         }
       }
-      if (first_bad != LLONG_MAX && a.status) {
-        atomicCAS(a.status, 0, 3 /* FC_ERR_STALE_BLOCK */);
-        atomicMin(a.status + 1, first_bad < INT_MAX ? static_cast<int>(first_bad) : INT_MAX - 1);
-      }
-      // residual
-      const uint16_t* rr = static_cast<const uint16_t*>(a.res_in) + row * H + 24 * u;
-      uint32_t rw[12];
-      if (full) {
-        const uint4 r0 = ld128_stream(rr), r1 = ld128_stream(rr + 8), r2 = ld128_stream(rr + 16);
-        rw[0] = r0.x, rw[1] = r0.y, rw[2] = r0.z, rw[3] = r0.w;
-        rw[4] = r1.x, rw[5] = r1.y, rw[6] = r1.z, rw[7] = r1.w;
-        rw[8] = r2.x, rw[9] = r2.y, rw[10] = r2.z, rw[11] = r2.w;
-      } else {
+      uint32_t hw[3];
 #pragma unroll
-        for (int i = 0; i < 12; ++i) {
-          const int e = 24 * u + 2 * i;
-          const uint32_t lo = (act && e < H) ? ld16(rr + 2 * i) : 0u;
-          const uint32_t hi = (act && e + 1 < H) ? ld16(rr + 2 * i + 1) : 0u;
-          rw[i] = lo | (hi << 16);
-        }
+      for (int k = 0; k < 3; ++k) {
+        const float2 h = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
+                              make_float2(bf_lo(rw[k]), bf_hi(rw[k])));
+        hw[k] = pack_bf2(h.x, h.y);
+        const float h0 = bf_lo(hw[k]), h1 = bf_hi(hw[k]);
+        ss = __fmaf_rn(h0, h0, ss);
+        ss = __fmaf_rn(h1, h1, ss);
       }
-#pragma unroll
-      for (int i = 0; i < 12; ++i)
-        hb[k][i] = pack_bf2(__fadd_rn(acc[2 * i], bf_lo(rw[i])),
-                            __fadd_rn(acc[2 * i + 1], bf_hi(rw[i])));
-      uint16_t* ro = static_cast<uint16_t*>(a.res_out) + row * H + 24 * u;
-      if (full) {
-        st128(ro, make_uint4(hb[k][0], hb[k][1], hb[k][2], hb[k][3]));
-        st128(ro + 8, make_uint4(hb[k][4], hb[k][5], hb[k][6], hb[k][7]));
-        st128(ro + 16, make_uint4(hb[k][8], hb[k][9], hb[k][10], hb[k][11]));
-      } else if (act) {
-#pragma unroll
-        for (int i = 0; i < 24; ++i)
-          if (24 * u + i < H) ro[i] = static_cast<uint16_t>(hb[k][i >> 1] >> (16 * (i & 1)));
-      }
-      if (act) {
-#pragma unroll
-        for (int i = 0; i < 12; ++i) {
-          const float h0 = bf_lo(hb[k][i]), h1 = bf_hi(hb[k][i]);
-          ss = __fmaf_rn(h0, h0, ss);
-          ss = __fmaf_rn(h1, h1, ss);
-        }
-      }
+      store6(ro, e0, H, full, hw);
     }
-
-    const float inv = inv_rms(block_sum(ss, red, parity), H, a.eps);
-
+    ss = warp_sum(ss);
+    // first failing block of the row (lanes agree via a min-reduction)
 #pragma unroll
-    for (int k = 0; k < NU; ++k) {
-      const int u = k * nthr + tid;
-      if (u >= units) continue;
-      const bool full = 24 * u + 24 <= H;
-      const uint16_t* gp = static_cast<const uint16_t*>(a.gamma) + 24 * u;
-      uint32_t gw[12];
-      if (full) {
-        const uint4 g0 = *reinterpret_cast<const uint4*>(gp),
-                    g1 = *reinterpret_cast<const uint4*>(gp + 8),
-                    g2 = *reinterpret_cast<const uint4*>(gp + 16);
-        gw[0] = g0.x, gw[1] = g0.y, gw[2] = g0.z, gw[3] = g0.w;
-        gw[4] = g1.x, gw[5] = g1.y, gw[6] = g1.z, gw[7] = g1.w;
-        gw[8] = g2.x, gw[9] = g2.y, gw[10] = g2.z, gw[11] = g2.w;
-      } else {
+    for (int m = 16; m >= 1; m >>= 1) {
+      const int64_t o = __shfl_xor_sync(kFull, first_bad, m);
+      first_bad = o < first_bad ? o : first_bad;
+    }
+    if (lane == 0 && first_bad != LLONG_MAX && a.status) {
+      atomicCAS(a.status, 0, 3 /* FC_ERR_STALE_BLOCK */);
+      atomicMin(a.status + 1, first_bad < INT_MAX ? static_cast<int>(first_bad) : INT_MAX - 1);
+    }
+    const float inv = inv_rms(ss, H, a.eps);
+    for (int gi = 0; gi < gpr; ++gi) {
+      const int j = gi * 32 + lane;
+      if (j >= nb) continue;
+      const int e0 = 6 * j;
+      const bool full = e0 + 6 <= H;
+      uint32_t hw[3], gw[3], yw[3];
+      load6<false>(ro, e0, H, full, hw);  // this lane's own h, written above
+      load6<true>(static_cast<const uint16_t*>(a.gamma), e0, H, full, gw);
 #pragma unroll
-        for (int i = 0; i < 12; ++i) {
-          const int e = 24 * u + 2 * i;
-          const uint32_t lo = e < H ? ld16(gp + 2 * i) : 0u;
-          const uint32_t hi = e + 1 < H ? ld16(gp + 2 * i + 1) : 0u;
-          gw[i] = lo | (hi << 16);
-        }
+      for (int k = 0; k < 3; ++k) {
+        const float2 y = pmul(pmul(make_float2(bf_lo(hw[k]), bf_hi(hw[k])), dup2(inv)),
+                              make_float2(bf_lo(gw[k]), bf_hi(gw[k])));
+        yw[k] = pack_bf2(y.x, y.y);
       }
-      uint32_t yw[12];
-#pragma unroll
-      for (int i = 0; i < 12; ++i)
-        yw[i] = pack_bf2(__fmul_rn(__fmul_rn(bf_lo(hb[k][i]), inv), bf_lo(gw[i])),
-                         __fmul_rn(__fmul_rn(bf_hi(hb[k][i]), inv), bf_hi(gw[i])));
-      uint16_t* yo = static_cast<uint16_t*>(a.y) + row * H + 24 * u;
-      if (full) {
-        st128(yo, make_uint4(yw[0], yw[1], yw[2], yw[3]));
-        st128(yo + 8, make_uint4(yw[4], yw[5], yw[6], yw[7]));
-        st128(yo + 16, make_uint4(yw[8], yw[9], yw[10], yw[11]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < 24; ++i)
-          if (24 * u + i < H) yo[i] = static_cast<uint16_t>(yw[i >> 1] >> (16 * (i & 1)));
-      }
+      store6(static_cast<uint16_t*>(a.y) + row * H, e0, H, full, yw);
     }
   }
 }
@@ -363,19 +360,23 @@ cudaError_t launch_fmt(const FusedArgs& a, int max_ctas, cudaStream_t st) {
   }
 }
 
+// One warp per row: the grid covers the rows with 8-warp CTAs (capped by
+// max_ctas and by the resident limit).
+template <typename K>
+cudaError_t launch_warp_rows(K kernel, const FusedArgs& a, int max_ctas, cudaStream_t st) {
+  const int threads = 256;
+  int64_t grid = static_cast<int64_t>(num_sms()) * occupancy(reinterpret_cast<const void*>(kernel), threads);
+  const int64_t need = (a.rows + 7) / 8;
+  if (grid > need) grid = need;
+  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+  kernel<<<static_cast<int>(grid), threads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_tagged(const FusedArgs& a, int max_ctas, cudaStream_t st) {
-  const int nb = (a.H + 5) / 6;
-  const int units = (nb + 3) / 4;
-  int nu = 1;
-  while (nu < 8 && (units + nu - 1) / nu > 256) nu <<= 1;
-  const int threads = round_warp((units + nu - 1) / nu);
-  if (threads > kMaxThreads) return cudaErrorInvalidConfiguration;
-  switch (nu) {
-    case 1: return launch_rows(k_fused_tagged<1>, threads, a, max_ctas, st);
-    case 2: return launch_rows(k_fused_tagged<2>, threads, a, max_ctas, st);
-    case 4: return launch_rows(k_fused_tagged<4>, threads, a, max_ctas, st);
-    default: return launch_rows(k_fused_tagged<8>, threads, a, max_ctas, st);
-  }
+  if (a.P <= 2) return launch_warp_rows(k_fused_tagged<2>, a, max_ctas, st);
+  if (a.P <= 4) return launch_warp_rows(k_fused_tagged<4>, a, max_ctas, st);
+  return launch_warp_rows(k_fused_tagged<8>, a, max_ctas, st);
 }
 
 }  // namespace

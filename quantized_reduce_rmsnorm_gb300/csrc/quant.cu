@@ -287,41 +287,71 @@ __global__ void __launch_bounds__(kThreads) k_reduce(Slabs s, int P, int lpg_shi
 }
 
 // ---------------------------------------------------- tagged-block packing --
-// One thread packs a unit of 4 blocks (24 elements) of one row.
+// One lane per 16-byte block, one warp per 32 consecutive blocks of a row:
+// the warp reads 384 contiguous input bytes (three 4-byte loads per lane)
+// and writes 512 contiguous output bytes (one 16-byte store per lane), two
+// block groups in flight per iteration.
+constexpr int kPackUnroll = 2;
+
+__device__ __forceinline__ uint32_t ld32_stream(const void* p) {
+  uint32_t r;
+  asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
 __global__ void __launch_bounds__(kThreads) k_pack_tagged(const uint16_t* __restrict__ x,
                                                           int64_t rows, int H, int nb,
                                                           uint32_t epoch, uint4* blocks) {
-  const int units = (nb + 3) >> 2;
-  const int64_t total = rows * units;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; t < total;
-       t += stride) {
-    const int64_t row = t / units;
-    const int u = static_cast<int>(t - row * units);
-    const uint16_t* xr = x + row * H;
-    const int e0 = 24 * u;
-    uint32_t w[12];
-    if (e0 + 24 <= H) {
-      const uint4 a = ld128_stream(xr + e0), b = ld128_stream(xr + e0 + 8),
-                  c = ld128_stream(xr + e0 + 16);
-      w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w;
-      w[4] = b.x, w[5] = b.y, w[6] = b.z, w[7] = b.w;
-      w[8] = c.x, w[9] = c.y, w[10] = c.z, w[11] = c.w;
-    } else {
+  const int lane = threadIdx.x & 31;
+  const uint32_t gpr = static_cast<uint32_t>((nb + 31) >> 5);  // block groups per row
+  const int64_t items = rows * gpr;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  // (row, group) cursors, advanced by nw items without dividing again
+  const int64_t step_rows = nw / gpr;
+  const uint32_t step_g = static_cast<uint32_t>(nw - step_rows * gpr);
+  auto advance = [&](int64_t& row, uint32_t& g) {
+    row += step_rows;
+    g += step_g;
+    if (g >= gpr) g -= gpr, ++row;
+  };
+  int64_t row0 = w0 / gpr;
+  uint32_t g0 = static_cast<uint32_t>(w0 - row0 * gpr);
+  for (int64_t it0 = w0; it0 < items; it0 += nw * kPackUnroll) {
+    uint32_t wv[kPackUnroll][3];
+    int64_t blk[kPackUnroll];
+    bool act[kPackUnroll];
+    int64_t row = row0;
+    uint32_t g = g0;
 #pragma unroll
-      for (int i = 0; i < 12; ++i) {
-        const int e = e0 + 2 * i;
-        const uint32_t lo = e < H ? ld16(xr + e) : 0u;
-        const uint32_t hi = e + 1 < H ? ld16(xr + e + 1) : 0u;
-        w[i] = lo | (hi << 16);
+    for (int u = 0; u < kPackUnroll; ++u) {
+      if (u) advance(row, g);
+      const int64_t it = it0 + u * nw;
+      const int j = static_cast<int>(g) * 32 + lane;
+      act[u] = it < items && j < nb;
+      blk[u] = row * nb + j;
+      if (act[u]) {
+        const uint16_t* xr = x + row * H;
+        const int e0 = 6 * j;
+        if (e0 + 6 <= H) {
+#pragma unroll
+          for (int k = 0; k < 3; ++k) wv[u][k] = ld32_stream(xr + e0 + 2 * k);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 3; ++k) {
+            const int e = e0 + 2 * k;
+            const uint32_t lo = e < H ? ld16(xr + e) : 0u;
+            const uint32_t hi = e + 1 < H ? ld16(xr + e + 1) : 0u;
+            wv[u][k] = lo | (hi << 16);
+          }
+        }
       }
     }
-    uint4* br = blocks + row * nb;
+    advance(row, g);
+    row0 = row, g0 = g;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int j = 4 * u + b;
-      if (j < nb) st128(br + j, make_uint4(w[3 * b], w[3 * b + 1], w[3 * b + 2], epoch));
-    }
+    for (int u = 0; u < kPackUnroll; ++u)
+      if (act[u]) st128(blocks + blk[u], make_uint4(wv[u][0], wv[u][1], wv[u][2], epoch));
   }
 }
 
@@ -426,8 +456,8 @@ cudaError_t launch_pack_tagged(const void* x, int64_t rows, int H, uint32_t epoc
                                cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const int nb = (H + 5) / 6;
-  const int64_t total = rows * ((nb + 3) / 4);
-  const int grid = grid_for(total, kThreads);
+  const int64_t total = rows * ((nb + 31) / 32) * 32;  // lanes
+  const int grid = grid_for((total + kPackUnroll - 1) / kPackUnroll, kThreads);
   k_pack_tagged<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t*>(x), rows, H, nb, epoch,
                                            static_cast<uint4*>(blocks));
   return cudaGetLastError();
