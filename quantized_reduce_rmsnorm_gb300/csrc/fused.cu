@@ -237,23 +237,35 @@ __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
     uint16_t* ro = static_cast<uint16_t*>(a.res_out) + row * H;
     float ss = 0.0f;
     int64_t first_bad = LLONG_MAX;
+    // software pipeline: group gi+1's blocks and residual are in flight
+    // while group gi is summed
+    uint4 b[2][PMAX];
+    uint32_t rw[2][3];
+    auto fetch = [&](int gi, int slot) {
+      const int j = gi * 32 + lane;
+      if (gi < gpr && j < nb) {
+#pragma unroll
+        for (int p = 0; p < PMAX; ++p)
+          if (p < P) b[slot][p] = ld128_stream(static_cast<const uint4*>(a.s.codes[p]) + row * nb + j);
+        load6<true>(rr, 6 * j, H, 6 * j + 6 <= H, rw[slot]);
+      }
+    };
+    fetch(0, 0);
+#pragma unroll 2
     for (int gi = 0; gi < gpr; ++gi) {
+      const int slot = gi & 1;
+      fetch(gi + 1, slot ^ 1);
       const int j = gi * 32 + lane;
       if (j >= nb) continue;
-      uint4 b[PMAX];
-#pragma unroll
-      for (int p = 0; p < PMAX; ++p)
-        if (p < P) b[p] = ld128_stream(static_cast<const uint4*>(a.s.codes[p]) + row * nb + j);
       const int e0 = 6 * j;
       const bool full = e0 + 6 <= H;
-      uint32_t rw[3];
-      load6<true>(rr, e0, H, full, rw);
       float acc[6] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int p = 0; p < PMAX; ++p) {
         if (p < P) {
-          if (b[p].w == epoch) {
-            const uint32_t w[3] = {b[p].x, b[p].y, b[p].z};
+          const uint4 bp = b[slot][p];
+          if (bp.w == epoch) {
+            const uint32_t w[3] = {bp.x, bp.y, bp.z};
 #pragma unroll
             for (int k = 0; k < 3; ++k) {
               const float2 t = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
@@ -270,7 +282,7 @@ __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
 #pragma unroll
       for (int k = 0; k < 3; ++k) {
         const float2 h = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
-                              make_float2(bf_lo(rw[k]), bf_hi(rw[k])));
+                              make_float2(bf_lo(rw[slot][k]), bf_hi(rw[slot][k])));
         hw[k] = pack_bf2(h.x, h.y);
         const float h0 = bf_lo(hw[k]), h1 = bf_hi(hw[k]);
         ss = __fmaf_rn(h0, h0, ss);
