@@ -151,6 +151,12 @@ fc_status fc_requant_gather(const float* reduced_f32, int64_t rows, int64_t hidd
 fc_status fc_pack_tagged(const void* x_bf16, int64_t rows, int64_t hidden, uint32_t epoch,
                          void* blocks, fc_stream_t stream);
 
+/* Pack P bf16 slabs (host arrays of P device pointers, 1 <= P <= 8) in one
+ * launch: slab p reads x_bf16[p] and writes blocks[p].  Same result as P
+ * calls of fc_pack_tagged. */
+fc_status fc_pack_tagged_multi(const void* const* x_bf16, int P, int64_t rows, int64_t hidden,
+                               uint32_t epoch, void* const* blocks, fc_stream_t stream);
+
 /* The fused path: quantized All-Reduce + residual add + RMSNorm (Flash
  * Communication two-step reduce; TokenWeave fused AllReduce-RMSNorm).
  * For every row, in one kernel:

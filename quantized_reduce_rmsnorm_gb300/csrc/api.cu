@@ -220,16 +220,25 @@ fc_status fc_requant_gather(const float* reduced_f32, int64_t rows, int64_t hidd
                      "fc_requant_gather launch");
 }
 
-fc_status fc_pack_tagged(const void* x_bf16, int64_t rows, int64_t hidden, uint32_t epoch,
-                         void* blocks, fc_stream_t stream) {
+fc_status fc_pack_tagged_multi(const void* const* x_bf16, int P, int64_t rows, int64_t hidden,
+                               uint32_t epoch, void* const* blocks, fc_stream_t stream) {
   fc_qspec spec{FC_FMT_BF16_TAGGED, 0};
   if (fc_status s = check_shape(spec, rows, hidden, false)) return s;
+  if (P < 1 || P > 8) return fail(FC_ERR_INVALID, "P must be in [1, 8] (got %d)", P);
   if (rows == 0) return ok();
-  if (fc_status s = check_ptr(x_bf16, 32, "x_bf16")) return s;
-  if (fc_status s = check_ptr(blocks, 16, "blocks")) return s;
-  return cuda_status(fc::launch_pack_tagged(x_bf16, rows, static_cast<int>(hidden), epoch, blocks,
-                                            (cudaStream_t)stream),
+  if (!x_bf16 || !blocks) return fail(FC_ERR_INVALID, "x_bf16 and blocks must not be NULL");
+  for (int p = 0; p < P; ++p) {
+    if (fc_status s = check_ptr(x_bf16[p], 32, "x_bf16[p]")) return s;
+    if (fc_status s = check_ptr(blocks[p], 16, "blocks[p]")) return s;
+  }
+  return cuda_status(fc::launch_pack_tagged(x_bf16, blocks, P, rows, static_cast<int>(hidden),
+                                            epoch, (cudaStream_t)stream),
                      "fc_pack_tagged launch");
+}
+
+fc_status fc_pack_tagged(const void* x_bf16, int64_t rows, int64_t hidden, uint32_t epoch,
+                         void* blocks, fc_stream_t stream) {
+  return fc_pack_tagged_multi(&x_bf16, 1, rows, hidden, epoch, &blocks, stream);
 }
 
 fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64_t rows,

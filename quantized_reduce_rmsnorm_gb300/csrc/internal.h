@@ -67,8 +67,8 @@ cudaError_t launch_quantize(int fmt, bool in_f32, int deq_kind, const QuantJob& 
 // Sum of dequantized slabs over the 16-element chunks [c0, c1).
 cudaError_t launch_reduce(int fmt, const Slabs& s, int P, int G, int64_t c0, int64_t c1,
                           float* out, cudaStream_t st);
-cudaError_t launch_pack_tagged(const void* x, int64_t rows, int H, uint32_t epoch, void* blocks,
-                               cudaStream_t st);
+cudaError_t launch_pack_tagged(const void* const* x, void* const* blocks, int P, int64_t rows,
+                               int H, uint32_t epoch, cudaStream_t st);
 cudaError_t launch_fused(int fmt, const FusedArgs& a, int max_ctas, int path, cudaStream_t st);
 
 }  // namespace fc

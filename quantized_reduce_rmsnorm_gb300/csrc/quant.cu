@@ -287,19 +287,29 @@ __global__ void __launch_bounds__(kThreads) k_reduce(Slabs s, int P, int lpg_shi
 }
 
 // ---------------------------------------------------- tagged-block packing --
-// One warp per group of 32 consecutive blocks of a row, one lane per 16-byte
-// block.  The group's 192 input elements (384 bytes, 16-byte aligned because
-// rows are) are read with 24 coalesced 16-byte loads into a per-warp
-// shared-memory buffer; each lane then picks its block's three words (a
-// 12-byte stride: conflict-free) and the warp writes 512 contiguous output
-// bytes.  Two groups are in flight per iteration.
+// One lane per 16-byte block, one warp per 32 consecutive blocks of a row:
+// the warp reads 384 contiguous input bytes (three 4-byte loads per lane)
+// and writes 512 contiguous output bytes (one 16-byte store per lane), two
+// block groups in flight per iteration.  blockIdx.y selects the slab, so all
+// P producers pack in one launch.
 constexpr int kPackUnroll = 2;
 
-__global__ void __launch_bounds__(kThreads) k_pack_tagged(const uint16_t* __restrict__ x,
-                                                          int64_t rows, int H, int nb,
-                                                          uint32_t epoch, uint4* blocks) {
-  __shared__ uint4 stage[kThreads / 32][kPackUnroll][24];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+struct PackJob {
+  const uint16_t* x[8];
+  uint4* blocks[8];
+};
+
+__device__ __forceinline__ uint32_t ld32_stream(const void* p) {
+  uint32_t r;
+  asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads) k_pack_tagged(PackJob job, int64_t rows, int H, int nb,
+                                                          uint32_t epoch) {
+  const uint16_t* __restrict__ x = job.x[blockIdx.y];
+  uint4* blocks = job.blocks[blockIdx.y];
+  const int lane = threadIdx.x & 31;
   const uint32_t gpr = static_cast<uint32_t>((nb + 31) >> 5);  // block groups per row
   const int64_t items = rows * gpr;
   const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
@@ -315,6 +325,7 @@ __global__ void __launch_bounds__(kThreads) k_pack_tagged(const uint16_t* __rest
   int64_t row0 = w0 / gpr;
   uint32_t g0 = static_cast<uint32_t>(w0 - row0 * gpr);
   for (int64_t it0 = w0; it0 < items; it0 += nw * kPackUnroll) {
+    uint32_t wv[kPackUnroll][3];
     int64_t blk[kPackUnroll];
     bool act[kPackUnroll];
     int64_t row = row0;
@@ -322,26 +333,32 @@ __global__ void __launch_bounds__(kThreads) k_pack_tagged(const uint16_t* __rest
 #pragma unroll
     for (int u = 0; u < kPackUnroll; ++u) {
       if (u) advance(row, g);
-      const bool item = it0 + u * nw < items;
+      const int64_t it = it0 + u * nw;
       const int j = static_cast<int>(g) * 32 + lane;
-      act[u] = item && j < nb;
+      act[u] = it < items && j < nb;
       blk[u] = row * nb + j;
-      const int e = static_cast<int>(g) * 192 + 8 * lane;  // this lane's 8 input elements
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (item && lane < 24 && e < H) v = ld128_stream(x + row * H + e);  // H % 8 == 0
-      if (lane < 24) stage[wid][u][lane] = v;
+      if (act[u]) {
+        const uint16_t* xr = x + row * H;
+        const int e0 = 6 * j;
+        if (e0 + 6 <= H) {
+#pragma unroll
+          for (int k = 0; k < 3; ++k) wv[u][k] = ld32_stream(xr + e0 + 2 * k);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 3; ++k) {
+            const int e = e0 + 2 * k;
+            const uint32_t lo = e < H ? ld16(xr + e) : 0u;
+            const uint32_t hi = e + 1 < H ? ld16(xr + e + 1) : 0u;
+            wv[u][k] = lo | (hi << 16);
+          }
+        }
+      }
     }
     advance(row, g);
     row0 = row, g0 = g;
-    __syncwarp();
 #pragma unroll
-    for (int u = 0; u < kPackUnroll; ++u) {
-      const uint32_t* words = reinterpret_cast<const uint32_t*>(stage[wid][u]);
-      if (act[u])
-        st128(blocks + blk[u],
-              make_uint4(words[3 * lane], words[3 * lane + 1], words[3 * lane + 2], epoch));
-    }
-    __syncwarp();  // the buffer is reused by the next iteration
+    for (int u = 0; u < kPackUnroll; ++u)
+      if (act[u]) st128(blocks + blk[u], make_uint4(wv[u][0], wv[u][1], wv[u][2], epoch));
   }
 }
 
@@ -442,14 +459,19 @@ cudaError_t launch_reduce(int fmt, const Slabs& s, int P, int G, int64_t c0, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_pack_tagged(const void* x, int64_t rows, int H, uint32_t epoch, void* blocks,
-                               cudaStream_t st) {
+cudaError_t launch_pack_tagged(const void* const* x, void* const* blocks, int P, int64_t rows,
+                               int H, uint32_t epoch, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const int nb = (H + 5) / 6;
-  const int64_t total = rows * ((nb + 31) / 32) * 32;  // lanes
-  const int grid = grid_for((total + kPackUnroll - 1) / kPackUnroll, kThreads);
-  k_pack_tagged<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t*>(x), rows, H, nb, epoch,
-                                           static_cast<uint4*>(blocks));
+  PackJob job{};
+  for (int p = 0; p < P; ++p) {
+    job.x[p] = static_cast<const uint16_t*>(x[p]);
+    job.blocks[p] = static_cast<uint4*>(blocks[p]);
+  }
+  const int64_t lanes = rows * ((nb + 31) / 32) * 32;
+  int grid = grid_for((lanes + kPackUnroll - 1) / kPackUnroll, kThreads);
+  grid = (grid + P - 1) / P;  // the P slabs share the resident-CTA budget
+  k_pack_tagged<<<dim3(grid, P), kThreads, 0, st>>>(job, rows, H, nb, epoch);
   return cudaGetLastError();
 }
 

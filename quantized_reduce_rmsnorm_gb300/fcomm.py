@@ -24,6 +24,7 @@ STATUS_NO_INDEX = 0x7F7F7F7F
 EXPORTS = (
     "fc_codes_bytes", "fc_groups", "fc_tagged_bytes", "fc_shard_range", "fc_group_quantize",
     "fc_group_quantize_multi", "fc_reduce_dequant_sum", "fc_requant_gather", "fc_pack_tagged",
+    "fc_pack_tagged_multi",
     "fc_allreduce_residual_rmsnorm", "fc_allreduce_residual_rmsnorm_ex", "fc_status_string",
     "fc_last_error", "fc_version",
 )
@@ -91,6 +92,7 @@ def load(path: Optional[str] = None):
         "fc_reduce_dequant_sum": (i32, [P, i32, i64, i64, QS, i32, P, P]),
         "fc_requant_gather": (i32, [P, i64, i64, QS, QT, P, i32, P]),
         "fc_pack_tagged": (i32, [P, i64, i64, u32, P, P]),
+        "fc_pack_tagged_multi": (i32, [P, i32, i64, i64, u32, P, P]),
         "fc_allreduce_residual_rmsnorm": (
             i32, [P, i32, i64, i64, QS, P, P, P, f32, QT, P, u32, P, P]),
         "fc_allreduce_residual_rmsnorm_ex": (
@@ -206,6 +208,14 @@ def requant_gather(reduced: torch.Tensor, spec: QSpec, requant_out=None,
 def pack_tagged(x: torch.Tensor, epoch: int, blocks: torch.Tensor, stream=None):
     rows, hidden = _rows_hidden(x)
     _check(load().fc_pack_tagged(_ptr(x), rows, hidden, epoch, _ptr(blocks), _stream(stream)))
+
+
+def pack_tagged_multi(xs: Sequence[torch.Tensor], epoch: int, blocks: Sequence[torch.Tensor],
+                      stream=None):
+    rows, hidden = _rows_hidden(xs[0])
+    xp = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+    bp = (ctypes.c_void_p * len(blocks))(*[_ptr(b) for b in blocks])
+    _check(load().fc_pack_tagged_multi(xp, len(xs), rows, hidden, epoch, bp, _stream(stream)))
 
 
 def allreduce_residual_rmsnorm(slabs, spec: QSpec, rows: int, hidden: int,

@@ -8,7 +8,7 @@ standing in as P slabs in one GPU's HBM:
   RMSNorm (one launch) that also writes the requantized all-gather payload;
 * BF16: the fused reduce + residual add + RMSNorm on the bf16 slabs;
 * BF16_TAGGED: the producers pack every slab into epoch-tagged blocks with a
-  fresh epoch (one launch per slab), then the consumer validates and reduces
+  fresh epoch (one launch for all slabs), then the consumer validates and reduces
   them; with ``splits`` > 1 the token rows are split into that many subsets
   that run on their own streams (TokenWeave's token splitting).
 
@@ -72,7 +72,7 @@ class Pipeline:
             return 2
         if w.fmt == FMT_BF16:
             return 1
-        return w.P + max(1, w.splits)
+        return 1 + max(1, w.splits)
 
     def step(self, stream=None):
         """Launch one pass of the hot path on `stream` (default: current)."""
@@ -96,8 +96,7 @@ class Pipeline:
             fc.group_quantize_multi(self.x, self.spec, self.codes, stream=st)
         elif w.fmt == FMT_BF16_TAGGED:
             self.epoch = (self.epoch + 1) & 0xFFFFFFFF
-            for p in range(w.P):
-                fc.pack_tagged(self.x[p], self.epoch, self.blocks[p], stream=st)
+            fc.pack_tagged_multi(self.x, self.epoch, self.blocks, stream=st)
 
     def consumer(self, st):
         """Receiver side: the fused reduce + residual add + RMSNorm."""

@@ -408,6 +408,18 @@ def test_tagged_pack_bit_exact(orc):
                           f"tagged blocks {T}x{H}")
 
 
+def test_tagged_pack_multi_equals_oracle(orc):
+    T, H, P = 7, 1040, 3
+    rng = np.random.default_rng(77)
+    xs = [rng.integers(0, 1 << 16, (T, H)).astype(np.uint16) for _ in range(P)]
+    blks = [torch.empty(fc.tagged_bytes(T, H), dtype=torch.uint8, device="cuda") for _ in range(P)]
+    fc.pack_tagged_multi([dev_bf16(x) for x in xs], 12345, blks)
+    torch.cuda.synchronize()
+    for p in range(P):
+        assert_bits_equal(host(blks[p]).view(np.uint32), orc.pack_tagged(xs[p], T, H, 12345),
+                          f"slab {p}")
+
+
 def test_tagged_stale_block_is_reported(orc):
     """Blocks built on the host by the oracle; one or two tags corrupted
     before upload: the call reports FC_ERR_STALE_BLOCK and the first index,
