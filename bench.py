@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--overlap", action="store_true",
+                    help="SM-capped fused kernel beside a GEMM on another stream (one JSON line per cap)")
     ap.add_argument("--sweep", choices=["quick", "full"], default=None,
                     help="message-size sweep (16 KB..256 MB x P x format): one JSON line per point")
     return ap.parse_args()
@@ -480,8 +482,86 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_overlap(args):
+    """The fused reduce + residual + RMSNorm with its grid capped at max_ctas
+    CTAs (one per SM), alone and concurrently with a bf16 GEMM standing in for
+    the other token subset's compute (TokenWeave, abstract: communication and
+    RMSNorm on 2-8 SMs, overlapped with the other subset's computation)."""
+    import torch
+    from quantized_reduce_rmsnorm_gb300 import fcomm, synth
+    from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
+    fcomm.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    base = synth.WORKLOADS[args.workload]
+    w = synth.Workload(**{**base.__dict__, "T": base.T // max(1, base.splits), "splits": 1})
+    pipe = Pipeline(w, synth.make_inputs(w, seed=0), device=dev)
+    pipe.sender(torch.cuda.current_stream(dev))
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    A = torch.randn(4096, 8192, generator=g, device=dev).to(torch.bfloat16)
+    B = torch.randn(8192, 8192, generator=g, device=dev).to(torch.bfloat16)
+    C = torch.empty(4096, 8192, dtype=torch.bfloat16, device=dev)
+    s_ar, s_mm = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def fused(cap, st):
+        fcomm.allreduce_residual_rmsnorm(
+            pipe.blocks if w.fmt == synth.FMT_BF16_TAGGED else (pipe.codes if pipe.payload is not None else pipe.x),
+            pipe.spec, w.T, w.H, pipe.residual, pipe.residual_out, pipe.gamma, w.eps, pipe.y,
+            requant_out=pipe.payload, expected_epoch=pipe.epoch,
+            d_status=pipe.status[0] if pipe.status is not None else None, max_ctas=cap, stream=st)
+
+    def gemm(st):
+        with torch.cuda.stream(st):
+            torch.matmul(A, B, out=C)
+
+    def timed(fn, reps=10):
+        out = []
+        for i in range(reps + 3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            if i >= 3:
+                out.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(out)
+
+    def both(cap):
+        cur = torch.cuda.current_stream(dev)
+        ev0 = torch.cuda.Event()
+        ev0.record(cur)
+        s_ar.wait_event(ev0), s_mm.wait_event(ev0)
+        e_ar0, e_ar1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_ar0.record(s_ar)
+        fused(cap, s_ar)
+        e_ar1.record(s_ar)
+        gemm(s_mm)
+        cur.wait_stream(s_ar), cur.wait_stream(s_mm)
+        both.last_ar = e_ar1, e_ar0
+
+    t_mm = timed(lambda: gemm(torch.cuda.current_stream(dev)))
+    peak, _ = peaks()
+    alg = pipe.alg_bytes()["fused"]
+    for cap in (2, 4, 8, 16, 32, 64, 0):
+        t_ar = timed(lambda: fused(cap, torch.cuda.current_stream(dev)))
+        t_both = timed(lambda: both(cap))
+        e1, e0 = both.last_ar
+        t_ar_conc = e0.elapsed_time(e1) * 1e3
+        hidden = (t_ar + t_mm - t_both) / min(t_ar, t_mm)
+        print(json.dumps({"overlap": True, "workload": f"{w.name} subset {w.T}x{w.H} P={w.P}",
+                          "max_ctas": cap or "all", "fused_alone_us": round(t_ar, 1),
+                          "fused_alone_GBps": round(alg / t_ar / 1e3, 1),
+                          "gemm_alone_us": round(t_mm, 1), "both_us": round(t_both, 1),
+                          "fused_during_gemm_us": round(t_ar_conc, 1),
+                          "overlap_of_shorter": round(hidden, 3)}), flush=True)
+
+
 def main():
     args = parse()
+    if args.overlap:
+        run_overlap(args)
+        return
     if args.sweep:
         run_sweep(args)
         return
