@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--split", choices=["even", "wave"], default="even",
+                    help="token-subset boundary for workloads that split rows")
     ap.add_argument("--overlap", action="store_true",
                     help="SM-capped fused kernel beside a GEMM on another stream (one JSON line per cap)")
     ap.add_argument("--sweep", choices=["quick", "full"], default=None,
@@ -260,7 +262,7 @@ def run_ours(args):
     fcomm.load()
     w = get_workload(args)
     inputs = synth.make_inputs(w, seed=rank)
-    pipe = Pipeline(w, inputs, device=dev)
+    pipe = Pipeline(w, inputs, device=dev, split=args.split)
     alg = pipe.alg_bytes()
     step_bytes = alg["sender"] + alg["fused"]
     in_bytes = w.P * 2 * w.T * w.H  # bf16 slabs read by the first stage
@@ -308,6 +310,8 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": {**workload_config(w),
+                   **({"split": args.split, "split_rows": pipe.bounds, "wave_rows": pipe.wave_rows}
+                      if w.splits > 1 else {}),
                    "l2": ("L2 scrubbed (256 MB write) before every timed step"
                           if flush is not None else
                           f"inputs larger than L2 ({in_bytes / 2**20:.0f} MB of bf16 slabs "

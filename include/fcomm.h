@@ -207,6 +207,19 @@ fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64
                                            void* y, uint32_t expected_epoch, int32_t* d_status,
                                            const fc_launch_opts* opts, fc_stream_t stream);
 
+/* Wave-aware token split (TokenWeave, abstract: the batch's tokens are
+ * divided into two approximately equal subsets in a wave-aware manner; the
+ * work of one overlaps the other's).  A "wave" is the number of rows the
+ * fused kernel that fc_allreduce_residual_rmsnorm would launch for this
+ * shape processes concurrently on the current GPU (SMs x resident rows per
+ * SM, from the kernel's occupancy; returned in *wave_rows, may be NULL).
+ * *split receives the first subset's row count: the multiple of the wave
+ * nearest rows/2 (so the first subset is whole waves and the two subsets
+ * together take no more waves than one unsplit call), or rows/2 when rows is
+ * at most one wave.  Host-side query; launches nothing, allocates nothing. */
+fc_status fc_token_split(int P, int64_t rows, int64_t hidden, fc_qspec spec, int64_t* split,
+                         int64_t* wave_rows);
+
 /* --------------------------------------------------------------- misc --- */
 const char* fc_status_string(fc_status s);
 /* Message describing the calling thread's last non-OK status ("" if none). */

@@ -310,4 +310,37 @@ fc_status fc_allreduce_residual_rmsnorm(const fc_qtensor* slabs, int P, int64_t 
                                           nullptr, stream);
 }
 
+fc_status fc_token_split(int P, int64_t rows, int64_t hidden, fc_qspec spec, int64_t* split,
+                         int64_t* wave_rows) {
+  if (fc_status s = check_shape(spec, rows, hidden, false)) return s;
+  if (P < 2 || P > 8) return fail(FC_ERR_INVALID, "P must be in [2, 8] (got %d)", P);
+  if (!split) return fail(FC_ERR_INVALID, "split must not be NULL");
+  fc::FusedArgs a{};
+  a.P = P;
+  a.H = static_cast<int>(hidden);
+  a.G = quantized(spec.fmt) ? spec.group : 16;
+  a.rows = rows;
+  // shape-only query: the kernel choice assumes 16-byte aligned tensors
+  static const uint4 aligned_probe[1] = {};
+  for (int p = 0; p < P; ++p) {
+    a.s.codes[p] = aligned_probe;
+    a.s.scales[p] = reinterpret_cast<const float*>(aligned_probe);
+    a.s.zeros[p] = reinterpret_cast<const float*>(aligned_probe);
+  }
+  a.res_in = a.gamma = aligned_probe;
+  const int64_t w = fc::fused_wave_rows(spec.fmt, a);
+  if (w <= 0) return fail(FC_ERR_CUDA, "could not query the fused kernel's occupancy");
+  if (wave_rows) *wave_rows = w;
+  int64_t s = rows / 2;
+  if (rows > w) {
+    // the whole-wave split nearest the middle: the first subset fills whole
+    // waves and the pair needs no more waves than one unsplit call
+    const int64_t k = (rows / 2 + w / 2) / w;
+    const int64_t cand = (k < 1 ? 1 : k) * w;
+    if (cand < rows) s = cand;
+  }
+  *split = s;
+  return ok();
+}
+
 }  // extern "C"

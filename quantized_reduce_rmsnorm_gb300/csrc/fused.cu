@@ -393,6 +393,26 @@ cudaError_t launch_tagged(const FusedArgs& a, int max_ctas, cudaStream_t st) {
 
 }  // namespace
 
+// Rows the chosen fused kernel processes concurrently on the current device.
+int64_t fused_wave_rows(int fmt, const FusedArgs& a) {
+  if (fmt == kTAGGED) {
+    const void* k = a.P <= 2 ? reinterpret_cast<const void*>(k_fused_tagged<2>)
+                  : a.P <= 4 ? reinterpret_cast<const void*>(k_fused_tagged<4>)
+                             : reinterpret_cast<const void*>(k_fused_tagged<8>);
+    return static_cast<int64_t>(num_sms()) * occupancy(k, 256) * 8;  // a warp per row
+  }
+  if (fused_tma_eligible(fmt, a)) return fused_tma_wave_rows(fmt, a);
+  const int cpr = a.H >> 4;
+  int nch = 1;
+  while (nch < 8 && (cpr + nch - 1) / nch > 256) nch <<= 1;
+  const int threads = round_warp((cpr + nch - 1) / nch);
+  const void* k = nullptr;
+  if (fmt == kBF16) k = reinterpret_cast<const void*>(k_fused<kBF16, 1>);
+  else if (fmt == kINT8) k = reinterpret_cast<const void*>(k_fused<kINT8, 1>);
+  else k = reinterpret_cast<const void*>(k_fused<kINT4, 1>);
+  return static_cast<int64_t>(num_sms()) * occupancy(k, threads);
+}
+
 cudaError_t launch_fused(int fmt, const FusedArgs& a, int max_ctas, int path, cudaStream_t st) {
   if (a.rows == 0) return cudaSuccess;
   if (path != kPathStream && fused_tma_eligible(fmt, a)) return launch_fused_tma(fmt, a, max_ctas, st);

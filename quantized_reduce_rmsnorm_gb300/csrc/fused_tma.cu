@@ -289,6 +289,36 @@ bool fused_tma_eligible(int fmt, const FusedArgs& a) {
   return aligned16(a.res_in) && aligned16(a.gamma);
 }
 
+template <int FMT, int NSTAGE, int PMAX>
+int64_t wave_t(const FusedArgs& a, const TmaGeom& g, int smem) {
+  auto kern = k_fused_tma<FMT, NSTAGE, PMAX>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int cpr = a.H >> 4;
+  int threads = cpr < kTmaThreads ? ((cpr + 31) & ~31) : kTmaThreads;
+  int occ = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+  if (occ == 1 && cpr >= kTmaThreadsMax)
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kTmaThreadsMax, smem);
+  return static_cast<int64_t>(num_sms()) * (occ > 0 ? occ : 1);  // a CTA per row
+}
+
+template <int FMT>
+int64_t wave_fmt(const FusedArgs& a, const TmaGeom& g) {
+  const int two = g.stage_off + 2 * g.stage_bytes, one = g.stage_off + g.stage_bytes;
+  const bool s2 = two <= kTmaSmemLimit;
+  if (a.P <= 2) return s2 ? wave_t<FMT, 2, 2>(a, g, two) : wave_t<FMT, 1, 2>(a, g, one);
+  if (a.P <= 4) return s2 ? wave_t<FMT, 2, 4>(a, g, two) : wave_t<FMT, 1, 4>(a, g, one);
+  return s2 ? wave_t<FMT, 2, 8>(a, g, two) : wave_t<FMT, 1, 8>(a, g, one);
+}
+
+int64_t fused_tma_wave_rows(int fmt, const FusedArgs& a) {
+  TmaGeom g;
+  geometry(fmt, a, g);
+  if (fmt == kBF16) return wave_fmt<kBF16>(a, g);
+  if (fmt == kINT8) return wave_fmt<kINT8>(a, g);
+  return wave_fmt<kINT4>(a, g);
+}
+
 cudaError_t launch_fused_tma(int fmt, const FusedArgs& a, int max_ctas, cudaStream_t st) {
   TmaGeom g;
   geometry(fmt, a, g);

@@ -60,6 +60,9 @@ constexpr int kTmaSmemLimit = 224 * 1024;
 enum FusedPath : int { kPathAuto = 0, kPathStream = 1, kPathTma = 2 };
 bool fused_tma_eligible(int fmt, const FusedArgs& a);
 cudaError_t launch_fused_tma(int fmt, const FusedArgs& a, int max_ctas, cudaStream_t st);
+int64_t fused_tma_wave_rows(int fmt, const FusedArgs& a);
+// Rows the fused kernel that a call would launch processes concurrently.
+int64_t fused_wave_rows(int fmt, const FusedArgs& a);
 
 // in_f32: input is fp32 (requantization) instead of bf16; deq_kind: a DeqOut.
 cudaError_t launch_quantize(int fmt, bool in_f32, int deq_kind, const QuantJob& job,

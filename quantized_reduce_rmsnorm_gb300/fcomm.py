@@ -26,7 +26,7 @@ EXPORTS = (
     "fc_group_quantize_multi", "fc_reduce_dequant_sum", "fc_requant_gather", "fc_pack_tagged",
     "fc_pack_tagged_multi",
     "fc_allreduce_residual_rmsnorm", "fc_allreduce_residual_rmsnorm_ex", "fc_status_string",
-    "fc_last_error", "fc_version",
+    "fc_last_error", "fc_version", "fc_token_split",
 )
 
 
@@ -100,6 +100,7 @@ def load(path: Optional[str] = None):
         "fc_status_string": (ctypes.c_char_p, [i32]),
         "fc_last_error": (ctypes.c_char_p, []),
         "fc_version": (ctypes.c_char_p, []),
+        "fc_token_split": (i32, [i32, i64, i64, QS, ctypes.POINTER(i64), ctypes.POINTER(i64)]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -235,6 +236,13 @@ def allreduce_residual_rmsnorm(slabs, spec: QSpec, rows: int, hidden: int,
         qs, len(slabs), rows, hidden, spec, _ptr(residual_in), _ptr(residual_out), _ptr(gamma),
         eps, _qt(requant_out), _ptr(y), expected_epoch, _ptr(d_status), ctypes.byref(opts),
         _stream(stream)))
+
+
+def token_split(spec: QSpec, P: int, rows: int, hidden: int):
+    """(first subset's rows, wave rows) of the wave-aware token split."""
+    sp, wv = ctypes.c_int64(), ctypes.c_int64()
+    _check(load().fc_token_split(P, rows, hidden, spec, ctypes.byref(sp), ctypes.byref(wv)))
+    return sp.value, wv.value
 
 
 def version() -> str:

@@ -41,7 +41,8 @@ def qs_bytes(w: Workload, E: int) -> int:
 
 
 class Pipeline:
-    def __init__(self, w: Workload, inputs: dict, device="cuda", with_payload=True):
+    def __init__(self, w: Workload, inputs: dict, device="cuda", with_payload=True,
+                 split: str = "even"):
         self.w = w
         self.device = device
         self.spec = fc.QSpec(w.fmt, w.group)
@@ -63,6 +64,15 @@ class Pipeline:
                            for _ in range(w.P)]
             self.status = torch.zeros(max(1, w.splits), 2, dtype=torch.int32, device=device)
             self.streams = [torch.cuda.Stream(device=device) for _ in range(max(1, w.splits))]
+        # token-subset boundaries: even, or wave-aware (the first subset is
+        # whole waves of the fused kernel on this GPU)
+        n = max(1, w.splits)
+        if split == "wave" and n == 2:
+            first, self.wave_rows = fc.token_split(self.spec, w.P, w.T, w.H)
+            self.bounds = [0, first, w.T]
+        else:
+            self.wave_rows = None
+            self.bounds = [w.T * i // n for i in range(n + 1)]
         self.launches_per_step = self._launches()
 
     # ------------------------------------------------------------------
@@ -116,7 +126,7 @@ class Pipeline:
         w = self.w
         n = max(1, w.splits)
         bpr = fc.tagged_bytes(1, w.H)
-        bounds = [w.T * i // n for i in range(n + 1)]
+        bounds = self.bounds
         fork = torch.cuda.Event()
         fork.record(st)
         joins = []

@@ -485,6 +485,31 @@ def test_token_split_two_streams_equals_one_call(orc):
     assert_y_close(host_bits(y), want["y"])
 
 
+def test_wave_aware_token_split(orc):
+    """The split is whole waves of the fused kernel (nearest the middle), and
+    the two-stream step with it gives the same bits as with an even split."""
+    from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
+    for spec, P, T, H in ((fc.BF16_TAGGED, 8, 4096, 5120), (fc.INT4_G32, 4, 3000, 8192),
+                          (fc.INT8_G128, 8, 64, 8192), (fc.BF16, 2, 10000, 4096)):
+        split, wave = fc.token_split(spec, P, T, H)
+        assert wave > 0 and 0 < split < T
+        if T > wave:
+            assert split % wave == 0
+            assert abs(split - T / 2) <= wave / 2 + 1
+        else:
+            assert split == T // 2
+    w = small("token-split", T=600)
+    inp = synth.make_inputs(w, seed=31)
+    outs = []
+    for mode in ("even", "wave"):
+        pipe = Pipeline(w, inp, split=mode)
+        pipe.step()
+        outs.append(pipe.outputs())
+    assert np.array_equal(outs[0]["h"], outs[1]["h"]) and np.array_equal(outs[0]["y"], outs[1]["y"])
+    want = oracle_fused(orc, w, inp)
+    assert_bits_equal(outs[1]["h"], want["h"], "residual_out")
+
+
 # --------------------------------------------------- full-size, sampled rows --
 @pytest.mark.parametrize("name", ["prefill", "token-split", "decode"])
 def test_full_size_sampled_rows(orc, name):
