@@ -69,6 +69,9 @@ def _signatures():
         "or_pack_tagged": (None, [P, i64, i64, u32, P]),
         "or_validate_tagged": (i64, [P, i64, u32]),
         "or_unpack_tagged": (None, [P, i64, i64, P]),
+        "or_qtagged_blocks_per_group": (i32, [i32, i32]),
+        "or_pack_qtagged": (None, [i32, P, P, P, i64, i32, u32, P]),
+        "or_unpack_qtagged": (i64, [i32, P, i64, i32, u32, P, P, P]),
         "or_allreduce_residual_rmsnorm": (
             i32, [i32, P, i32, i64, i64, i32, P, P, f32, P, P, P, P, P]),
     }
@@ -233,6 +236,30 @@ class Oracle:
         x = np.empty(T * H, np.uint16)
         self.lib.or_unpack_tagged(_p(b), T, H, _p(x))
         return x.reshape(T, H)
+
+    # ------------------------------------------- tagged quantized payloads ---
+    def qtagged_blocks_per_group(self, fmt, G):
+        return int(self.lib.or_qtagged_blocks_per_group(fmt, G))
+
+    def pack_qtagged(self, fmt, q, s, z, G, epoch):
+        """uint32 words of the self-synchronizing quantized payload blocks."""
+        cdt = np.int8 if fmt == FMT_INT8_SYM else np.uint8
+        q = _c(q, cdt).ravel()
+        s = _c(s, np.float32)
+        n = q.size if fmt == FMT_INT8_SYM else q.size * 2
+        zz = _c(z, np.float32) if z is not None else np.zeros(s.size, np.float32)
+        out = np.empty((n // G) * self.qtagged_blocks_per_group(fmt, G) * 4, np.uint32)
+        self.lib.or_pack_qtagged(fmt, _p(q), _p(s), _p(zz), n, G, epoch, _p(out))
+        return out
+
+    def unpack_qtagged(self, fmt, blocks, n, G, epoch):
+        """(codes, scales, zeros-or-None, first bad block or -1)."""
+        b = _c(blocks, np.uint32).ravel()
+        q = np.empty(n if fmt == FMT_INT8_SYM else n // 2, np.int8 if fmt == FMT_INT8_SYM else np.uint8)
+        s = np.empty(n // G, np.float32)
+        z = np.empty(n // G, np.float32)
+        bad = self.lib.or_unpack_qtagged(fmt, _p(b), n, G, epoch, _p(q), _p(s), _p(z))
+        return q, s, (z if fmt == FMT_INT4_ASYM else None), int(bad)
 
     # -------------------------------------------------------- whole path ---
     def allreduce_residual_rmsnorm(self, fmt, slabs_bf16, r_bf16, gamma_bf16, T, H, G=0,

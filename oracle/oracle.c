@@ -277,6 +277,55 @@ void or_unpack_tagged(const uint32_t* blocks, int64_t T, int64_t H, uint16_t* x)
     }
 }
 
+/* --------------------------------------------- tagged quantized payloads -- */
+/* [FL] abstract (readiness evidence in every block) applied to [FC]'s
+ * quantized groups: the payload a rank sends for one group is carried by
+ * ceil(payload/12) self-validating 16-byte blocks. */
+static int qt_payload_bytes(int fmt, int G) {
+  return fmt == OR_FMT_INT8_SYM ? G + 4 : G / 2 + 8;
+}
+
+int or_qtagged_blocks_per_group(int fmt, int G) { return (qt_payload_bytes(fmt, G) + 11) / 12; }
+
+void or_pack_qtagged(int fmt, const void* codes, const float* scales, const float* zeros,
+                     int64_t n, int G, uint32_t epoch, uint32_t* blocks) {
+  int64_t ng = n / G;
+  int nbg = or_qtagged_blocks_per_group(fmt, G);
+  int cb = fmt == OR_FMT_INT8_SYM ? G : G / 2;
+  uint8_t payload[12 * 64];
+  for (int64_t g = 0; g < ng; ++g) {
+    memset(payload, 0, sizeof payload);
+    memcpy(payload, (const uint8_t*)codes + g * cb, (size_t)cb);
+    memcpy(payload + cb, &scales[g], 4);
+    if (fmt == OR_FMT_INT4_ASYM) memcpy(payload + cb + 4, &zeros[g], 4);
+    for (int b = 0; b < nbg; ++b) {
+      uint32_t* w = blocks + 4 * (g * nbg + b);
+      memcpy(w, payload + 12 * b, 12);
+      w[3] = epoch;
+    }
+  }
+}
+
+int64_t or_unpack_qtagged(int fmt, const uint32_t* blocks, int64_t n, int G, uint32_t epoch,
+                          void* codes, float* scales, float* zeros) {
+  int64_t ng = n / G;
+  int nbg = or_qtagged_blocks_per_group(fmt, G);
+  int cb = fmt == OR_FMT_INT8_SYM ? G : G / 2;
+  int64_t bad = -1;
+  uint8_t payload[12 * 64];
+  for (int64_t g = 0; g < ng; ++g) {
+    for (int b = 0; b < nbg; ++b) {
+      const uint32_t* w = blocks + 4 * (g * nbg + b);
+      if (w[3] != epoch && bad < 0) bad = g * nbg + b;
+      memcpy(payload + 12 * b, w, 12);
+    }
+    memcpy((uint8_t*)codes + g * cb, payload, (size_t)cb);
+    memcpy(&scales[g], payload + cb, 4);
+    if (fmt == OR_FMT_INT4_ASYM && zeros) memcpy(&zeros[g], payload + cb + 4, 4);
+  }
+  return bad;
+}
+
 /* --------------------------------------------------------- whole path --- */
 int or_allreduce_residual_rmsnorm(int fmt, const uint16_t* const* slabs, int P, int64_t T,
                                   int64_t H, int G, const uint16_t* r, const uint16_t* gamma,

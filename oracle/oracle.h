@@ -81,6 +81,20 @@ void or_pack_tagged(const uint16_t* x, int64_t T, int64_t H, uint32_t epoch, uin
 int64_t or_validate_tagged(const uint32_t* blocks, int64_t nblocks, uint32_t epoch);
 void or_unpack_tagged(const uint32_t* blocks, int64_t T, int64_t H, uint16_t* x);
 
+/* Self-synchronizing quantized payloads: every quantization group's payload
+ * (INT8: its G code bytes then the fp32 scale; INT4: its G/2 packed code
+ * bytes, the fp32 scale, the fp32 zero-point), zero-padded to a multiple of
+ * 12 bytes, is cut into 12-byte pieces; each goes into a 16-byte block as
+ * words 0..2 (little-endian payload bytes) with the epoch in word 3.  Groups
+ * follow each other in row-major order. */
+int or_qtagged_blocks_per_group(int fmt, int G);
+void or_pack_qtagged(int fmt, const void* codes, const float* scales, const float* zeros,
+                     int64_t n, int G, uint32_t epoch, uint32_t* blocks);
+/* Unpacks codes/scales/zeros (zeros may be NULL for INT8) and returns -1 when
+ * every block carries `epoch`, else the first bad block index. */
+int64_t or_unpack_qtagged(int fmt, const uint32_t* blocks, int64_t n, int G, uint32_t epoch,
+                          void* codes, float* scales, float* zeros);
+
 /* Whole path from bf16 partial-sum slabs (the CPU baseline):
  * quantize each slab (sender side), two-step reduce with P shards, gather,
  * residual add, RMSNorm.  fmt BF16: plain fp32 sum of the bf16 slabs, no

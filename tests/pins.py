@@ -357,6 +357,30 @@ def check_tagged_stale(orc):
     assert orc.validate_tagged(w, 10) == 0
 
 
+def check_qtagged_golden_roundtrip_and_stale(orc):
+    g = load_golden("qtagged_int4_tiny.txt")
+    G, ep = int(g["G"][0]), int(g["epoch"][0])
+    q = np.array(g["codes"], np.uint8)
+    w = orc.pack_qtagged(FMT_INT4_ASYM, q, np.array(g["scale"], np.float32),
+                         np.array(g["zero"], np.float32), G, ep)
+    assert list(w) == [int(v) for v in g["words"]]
+    assert orc.qtagged_blocks_per_group(FMT_INT8_SYM, 128) == 11
+    assert orc.qtagged_blocks_per_group(FMT_INT4_ASYM, 32) == 2
+    rng = np.random.default_rng(24)
+    for fmt, G in ((FMT_INT8_SYM, 128), (FMT_INT4_ASYM, 32), (FMT_INT8_SYM, 64)):
+        x = bf16_bits_to_float(_groups(rng, 12, G))
+        q, s, z = orc.quantize(fmt, x, G)
+        w = orc.pack_qtagged(fmt, q, s, z, G, 77)
+        q2, s2, z2, bad = orc.unpack_qtagged(fmt, w, x.size, G, 77)
+        assert bad == -1 and np.array_equal(q2, q) and np.array_equal(s2, s)
+        if z is not None:
+            assert np.array_equal(z2, z)
+        w2 = w.copy()
+        nb = orc.qtagged_blocks_per_group(fmt, G)
+        w2[4 * (3 * nb + 1) + 3] = 76
+        assert orc.unpack_qtagged(fmt, w2, x.size, G, 77)[3] == 3 * nb + 1
+
+
 # --------------------------------------------------------- whole path -----
 def check_whole_path_composition(orc):
     """The whole path equals its pinned steps composed by hand."""

@@ -32,6 +32,8 @@ MUTANTS = [
     ("tag-in-word-0", "w[3] = epoch;", "w[0] = epoch;"),
     ("tag-check-inverted", "if (blocks[4 * b + 3] != epoch) return b;",
      "if (blocks[4 * b + 3] == epoch) return b;"),
+    ("qtagged-scale-before-codes", "memcpy(payload + cb, &scales[g], 4);",
+     "memcpy(payload, &scales[g], 4);"),
 ]
 
 
