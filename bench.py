@@ -167,8 +167,9 @@ def oracle_sample(w, inputs, target_s: float):
     from quantized_reduce_rmsnorm_gb300.pipeline import qs_bytes
     from quantized_reduce_rmsnorm_gb300.synth import (FMT_BF16, FMT_BF16_TAGGED, FMT_INT4_ASYM,
                                                       FMT_INT8_SYM, Workload)
+    from quantized_reduce_rmsnorm_gb300.synth import base_format
     orc = oracle.default()
-    fmt = FMT_BF16 if w.fmt == FMT_BF16_TAGGED else w.fmt
+    fmt = FMT_BF16 if w.fmt == FMT_BF16_TAGGED else base_format(w.fmt)
 
     def run(rows):
         sl = [s[:rows] for s in inputs["slabs"]]
@@ -184,7 +185,7 @@ def oracle_sample(w, inputs, target_s: float):
     dt = run(rows)
     sub = Workload(**{**w.__dict__, "T": rows})
     E = rows * w.H
-    if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
+    if fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
         qs = qs_bytes(sub, E)
         alg = (w.P * 2 * E + w.P * qs) + (w.P * qs + 2 * E + 2 * w.H + qs + 4 * E)
     else:
@@ -297,7 +298,7 @@ def run_ours(args):
 
     value = whole_job_gbs(step_bytes, ws, step_ms)
     peak, peak_kind = peaks()
-    kern = [("sender", "k_quantize" if w.fmt in (1, 2) else "k_pack_tagged", alg["sender"],
+    kern = [("sender", "k_quantize" if w.fmt in synth.QUANTIZED else "k_pack_tagged", alg["sender"],
              statistics.mean(sender_ms)),
             ("fused", "k_fused_tagged" if w.fmt == 3 else "k_fused", alg["fused"],
              statistics.mean(fused_ms))]

@@ -69,7 +69,9 @@ typedef enum {
   FC_FMT_INT8_SYM = 1,    /* INT8 symmetric: scale = absmax/127, codes in [-127, 127] */
   FC_FMT_INT4_ASYM = 2,   /* INT4 asymmetric: scale = (max-min)/15, zero = min, codes in [0, 15] */
   FC_FMT_BF16_TAGGED = 3, /* bf16 in epoch-tagged 16-byte blocks */
-  FC_FMT_F32 = 4          /* output dtype only (fc_requant_gather) */
+  FC_FMT_F32 = 4,         /* output dtype only (fc_requant_gather) */
+  FC_FMT_INT8_TAGGED = 5, /* INT8 g128 groups as self-synchronizing blocks (11 per group) */
+  FC_FMT_INT4_TAGGED = 6  /* INT4 g32 groups as self-synchronizing blocks (2 per group) */
 } fc_format;
 
 /* Quantization spec.  group: 16..512, a multiple of 16 (INT8 uses 128 and
@@ -118,6 +120,26 @@ fc_status fc_shard_range(fc_qspec spec, int64_t rows, int64_t hidden, int P, int
  *        q = clamp(rne((x-lo)/s), 0, 15); s == 0 -> codes 0. */
 fc_status fc_group_quantize(const void* x_bf16, int64_t rows, int64_t hidden, fc_qspec spec,
                             fc_qtensor out, fc_stream_t stream);
+
+/* Self-synchronizing quantized payloads (flash-comm, abstract: every block
+ * carries evidence of its readiness; applied to Flash Communication's
+ * fine-grained quantized groups).  spec.fmt FC_FMT_INT8_TAGGED (group 128) or
+ * FC_FMT_INT4_TAGGED (group 32); other groups return FC_ERR_UNSUPPORTED.
+ * Each group's payload -- INT8: its 128 code bytes then the fp32 scale (132
+ * bytes); INT4: its 16 packed code bytes, the fp32 scale, the fp32 zero-point
+ * (24 bytes) -- is cut into 12-byte pieces carried as words 0..2 of 16-byte
+ * blocks whose word 3 is `epoch`: 11 blocks per INT8 group, 2 per INT4 group,
+ * groups in row-major order (fc_codes_bytes gives the size).  The codes and
+ * scales are exactly those fc_group_quantize computes.  P slabs (1..8, host
+ * arrays of device pointers) in one launch.  The consumer is
+ * fc_allreduce_residual_rmsnorm with the same spec: slabs[p].codes = blocks,
+ * every block checked against expected_epoch, stale blocks reported through
+ * d_status like FC_FMT_BF16_TAGGED (block index counted over the blocks of
+ * slab 0's rows, then slab 1's, ...); its requant_out (optional) is the plain
+ * INT8/INT4 payload. */
+fc_status fc_group_quantize_tagged(const void* const* x_bf16, int P, int64_t rows,
+                                   int64_t hidden, fc_qspec spec, uint32_t epoch,
+                                   void* const* blocks, fc_stream_t stream);
 
 /* Quantize P bf16 slabs in one launch; slab p reads x_bf16[p] and writes
  * out[p] (host arrays of P entries, 1 <= P <= 8).  Same result as P calls of

@@ -34,6 +34,10 @@ fc_status cuda_status(cudaError_t e, const char* what) {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool quantized(int fmt) { return fmt == FC_FMT_INT8_SYM || fmt == FC_FMT_INT4_ASYM; }
+bool qtagged(int fmt) { return fmt == FC_FMT_INT8_TAGGED || fmt == FC_FMT_INT4_TAGGED; }
+int base_fmt(int fmt) {
+  return fmt == FC_FMT_INT8_TAGGED ? FC_FMT_INT8_SYM : fmt == FC_FMT_INT4_TAGGED ? FC_FMT_INT4_ASYM : fmt;
+}
 
 // Common shape/spec checks.  needs_group: the format is quantized.
 fc_status check_shape(fc_qspec spec, int64_t rows, int64_t hidden, bool quant_only) {
@@ -44,7 +48,15 @@ fc_status check_shape(fc_qspec spec, int64_t rows, int64_t hidden, bool quant_on
   if (hidden > 65536) return fail(FC_ERR_UNSUPPORTED, "hidden > 65536 is not supported");
   if (quant_only && !quantized(spec.fmt))
     return fail(FC_ERR_INVALID, "format %d is not a quantized format", spec.fmt);
-  if (quantized(spec.fmt)) {
+  if (qtagged(spec.fmt)) {
+    const int want = spec.fmt == FC_FMT_INT8_TAGGED ? 128 : 32;
+    if (spec.group != want)
+      return fail(FC_ERR_UNSUPPORTED, "the tagged quantized format needs group %d (got %d)", want,
+                  spec.group);
+    if (hidden % want != 0)
+      return fail(FC_ERR_INVALID, "hidden (%lld) must be a multiple of group (%d)",
+                  (long long)hidden, want);
+  } else if (quantized(spec.fmt)) {
     const int G = spec.group;
     if (G < 16 || G > 512 || (G & (G - 1)) != 0)
       return fail(FC_ERR_INVALID, "group must be a power of two in [16, 512] (got %d)", G);
@@ -112,12 +124,15 @@ size_t fc_codes_bytes(fc_qspec spec, int64_t rows, int64_t hidden) {
     case FC_FMT_INT8_SYM: return n;
     case FC_FMT_INT4_ASYM: return n / 2;
     case FC_FMT_BF16_TAGGED: return fc_tagged_bytes(rows, hidden);
+    case FC_FMT_INT8_TAGGED: return n / 128 * 11 * 16;
+    case FC_FMT_INT4_TAGGED: return n / 32 * 2 * 16;
     default: return 0;
   }
 }
 
 size_t fc_groups(fc_qspec spec, int64_t rows, int64_t hidden) {
-  if (!quantized(spec.fmt) || spec.group <= 0 || rows < 0 || hidden <= 0) return 0;
+  if (!(quantized(spec.fmt) || qtagged(spec.fmt)) || spec.group <= 0 || rows < 0 || hidden <= 0)
+    return 0;
   return static_cast<size_t>(rows) * static_cast<size_t>(hidden) / static_cast<size_t>(spec.group);
 }
 
@@ -156,6 +171,30 @@ fc_status fc_group_quantize_multi(const void* const* x_bf16, int P, int64_t rows
   job.G = spec.group;
   return cuda_status(fc::launch_quantize(spec.fmt, false, fc::kDeqNone, job, (cudaStream_t)stream),
                      "fc_group_quantize launch");
+}
+
+fc_status fc_group_quantize_tagged(const void* const* x_bf16, int P, int64_t rows,
+                                   int64_t hidden, fc_qspec spec, uint32_t epoch,
+                                   void* const* blocks, fc_stream_t stream) {
+  if (!qtagged(spec.fmt))
+    return fail(FC_ERR_INVALID, "format %d is not a tagged quantized format", spec.fmt);
+  if (fc_status s = check_shape(spec, rows, hidden, false)) return s;
+  if (P < 1 || P > 8) return fail(FC_ERR_INVALID, "P must be in [1, 8] (got %d)", P);
+  if (rows == 0) return ok();
+  if (!x_bf16 || !blocks) return fail(FC_ERR_INVALID, "x_bf16 and blocks must not be NULL");
+  fc::QuantJob job{};
+  for (int p = 0; p < P; ++p) {
+    if (fc_status s = check_ptr(x_bf16[p], 32, "x_bf16[p]")) return s;
+    if (fc_status s = check_ptr(blocks[p], 16, "blocks[p]")) return s;
+    job.x[p] = x_bf16[p];
+    job.codes[p] = blocks[p];
+  }
+  job.n = rows * hidden;
+  job.P = P;
+  job.G = spec.group;
+  job.epoch = epoch;
+  return cuda_status(fc::launch_quantize_tagged(spec.fmt, job, (cudaStream_t)stream),
+                     "fc_group_quantize_tagged launch");
 }
 
 fc_status fc_group_quantize(const void* x_bf16, int64_t rows, int64_t hidden, fc_qspec spec,
@@ -267,8 +306,8 @@ fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64
     a.s.scales[p] = slabs[p].scales;
     a.s.zeros[p] = slabs[p].zeros;
   }
-  if (quantized(spec.fmt) && requant_out.codes) {
-    if (fc_status s = check_qtensor(requant_out, spec.fmt, "requant_out")) return s;
+  if ((quantized(spec.fmt) || qtagged(spec.fmt)) && requant_out.codes) {
+    if (fc_status s = check_qtensor(requant_out, base_fmt(spec.fmt), "requant_out")) return s;
     a.rq_codes = requant_out.codes;
     a.rq_scales = requant_out.scales;
     a.rq_zeros = requant_out.zeros;
@@ -280,7 +319,7 @@ fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64
   a.y = y;
   a.rows = rows;
   a.H = static_cast<int>(hidden);
-  a.G = quantized(spec.fmt) ? spec.group : 16;
+  a.G = (quantized(spec.fmt) || qtagged(spec.fmt)) ? spec.group : 16;
   a.lpg_shift = 0;
   while ((16 << a.lpg_shift) < a.G) ++a.lpg_shift;
   a.P = P;
@@ -296,7 +335,9 @@ fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64
   const int path = opts ? opts->kernel : 0;
   const cudaError_t e = fc::launch_fused(spec.fmt, a, opts ? opts->max_ctas : 0, path, st);
   if (e == cudaErrorNotSupported)
-    return fail(FC_ERR_UNSUPPORTED, "the TMA-staged kernel does not support this shape/alignment");
+    return fail(FC_ERR_UNSUPPORTED,
+                "the TMA-staged kernel (the only one for tagged quantized formats) does not support "
+                "this shape/alignment");
   return cuda_status(e, "fc_allreduce_residual_rmsnorm launch");
 }
 
@@ -318,7 +359,7 @@ fc_status fc_token_split(int P, int64_t rows, int64_t hidden, fc_qspec spec, int
   fc::FusedArgs a{};
   a.P = P;
   a.H = static_cast<int>(hidden);
-  a.G = quantized(spec.fmt) ? spec.group : 16;
+  a.G = (quantized(spec.fmt) || qtagged(spec.fmt)) ? spec.group : 16;
   a.rows = rows;
   // shape-only query: the kernel choice assumes 16-byte aligned tensors
   static const uint4 aligned_probe[1] = {};

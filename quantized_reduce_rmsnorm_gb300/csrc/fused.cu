@@ -402,6 +402,7 @@ int64_t fused_wave_rows(int fmt, const FusedArgs& a) {
     return static_cast<int64_t>(num_sms()) * occupancy(k, 256) * 8;  // a warp per row
   }
   if (fused_tma_eligible(fmt, a)) return fused_tma_wave_rows(fmt, a);
+  if (fmt == kINT8T || fmt == kINT4T) return 0;
   const int cpr = a.H >> 4;
   int nch = 1;
   while (nch < 8 && (cpr + nch - 1) / nch > 256) nch <<= 1;
@@ -415,6 +416,10 @@ int64_t fused_wave_rows(int fmt, const FusedArgs& a) {
 
 cudaError_t launch_fused(int fmt, const FusedArgs& a, int max_ctas, int path, cudaStream_t st) {
   if (a.rows == 0) return cudaSuccess;
+  if (fmt == kINT8T || fmt == kINT4T) {  // staged kernel only
+    if (path == kPathStream || !fused_tma_eligible(fmt, a)) return cudaErrorNotSupported;
+    return launch_fused_tma(fmt, a, max_ctas, st);
+  }
   if (path != kPathStream && fused_tma_eligible(fmt, a)) return launch_fused_tma(fmt, a, max_ctas, st);
   if (path == kPathTma) return cudaErrorNotSupported;
   switch (fmt) {

@@ -41,7 +41,7 @@ __device__ __forceinline__ void issue_row(const FusedArgs& a, const TmaGeom& g, 
   const int P = a.P;
   for (int p = 0; p < P; ++p) {
     bulk_load(st + p * g.cb, static_cast<const uint8_t*>(a.s.codes[p]) + row * g.cb, g.cb, bar);
-    if (FMT != kBF16)
+    if (FMT == kINT8 || FMT == kINT4)
       bulk_load(st + P * g.cb + p * g.sb,
                 reinterpret_cast<const uint8_t*>(a.s.scales[p]) + row * g.sb, g.sb, bar);
     if (FMT == kINT4)
@@ -67,6 +67,10 @@ __global__ void __launch_bounds__(kTmaThreadsMax) k_fused_tma(FusedArgs a, TmaGe
   uint8_t* stage0 = smem + g.stage_off;
   const int64_t row0 = blockIdx.x, rstride = gridDim.x;
   if (row0 >= a.rows) return;
+  // tagged quantized formats decode to the plain ones
+  constexpr int BASE = FMT == kINT8T ? kINT8 : FMT == kINT4T ? kINT4 : FMT;
+  constexpr bool QTAG = FMT == kINT8T || FMT == kINT4T;
+  const int64_t bpr = g.cb / 16;  // tagged blocks per row and slab
 
   if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s) mbar_init(&bar[s], 1);
@@ -93,6 +97,7 @@ __global__ void __launch_bounds__(kTmaThreadsMax) k_fused_tma(FusedArgs a, TmaGe
     // the group shuffles; lanes past the row end feed zeros (their groups
     // hold no real element) and touch no memory.
     float2 ss2 = make_float2(0.0f, 0.0f);
+    int64_t first_bad = LLONG_MAX;
     for (int cbase = 0; cbase < cpr; cbase += nthr) {
       const int c = cbase + tid;
       const bool act = c < cpr;
@@ -112,6 +117,36 @@ __global__ void __launch_bounds__(kTmaThreadsMax) k_fused_tma(FusedArgs a, TmaGe
                                     make_float2(bf_lo(w[k]), bf_hi(w[k])));
               acc[2 * k] = t.x, acc[2 * k + 1] = t.y;
             }
+          } else if (FMT == kINT8T) {
+            // group c>>3, lane k = c&7: code bytes 16k.. = words o.. of blocks b0, b0+1
+            const int gl = c >> 3, k = c & 7, b0 = (4 * k) / 3, o = 4 * k - 3 * b0;
+            const uint4* gb = reinterpret_cast<const uint4*>(codes + p * g.cb) + gl * kBlocksPerGroupI8;
+            const uint4 B0 = gb[b0], B1 = gb[b0 + 1], BS = gb[kBlocksPerGroupI8 - 1];
+            if (B0.w == a.epoch && B1.w == a.epoch && BS.w == a.epoch) {
+              const uint32_t W[6] = {B0.x, B0.y, B0.z, B1.x, B1.y, B1.z};
+              const uint32_t w[4] = {o == 0 ? W[0] : o == 1 ? W[1] : W[2],
+                                     o == 0 ? W[1] : o == 1 ? W[2] : W[3],
+                                     o == 0 ? W[2] : o == 1 ? W[3] : W[4],
+                                     o == 0 ? W[3] : o == 1 ? W[4] : W[5]};
+              dequant_i8_acc(w, __uint_as_float(BS.z), acc);
+            } else {
+              const int64_t base = (static_cast<int64_t>(p) * a.rows + row) * bpr + gl * kBlocksPerGroupI8;
+              const int64_t bad = base + (B0.w != a.epoch ? b0 : B1.w != a.epoch ? b0 + 1 : kBlocksPerGroupI8 - 1);
+              first_bad = bad < first_bad ? bad : first_bad;
+            }
+          } else if (FMT == kINT4T) {
+            // group c>>1: block 0 = {codes 0-3, 4-7, 8-11}, block 1 = {codes 12-15, scale, zero}
+            const int gl = c >> 1, k = c & 1;
+            const uint4* gb = reinterpret_cast<const uint4*>(codes + p * g.cb) + gl * kBlocksPerGroupI4;
+            const uint4 B0 = gb[0], B1 = gb[1];
+            if (B0.w == a.epoch && B1.w == a.epoch) {
+              const uint32_t w[2] = {k ? B0.z : B0.x, k ? B1.x : B0.y};
+              dequant_i4_acc(w, __uint_as_float(B1.y), __uint_as_float(B1.z), acc);
+            } else {
+              const int64_t bad = (static_cast<int64_t>(p) * a.rows + row) * bpr + gl * kBlocksPerGroupI4 +
+                                  (B0.w != a.epoch ? 0 : 1);
+              first_bad = bad < first_bad ? bad : first_bad;
+            }
           } else if (FMT == kINT8) {
             const uint4 q = reinterpret_cast<const uint4*>(codes + p * g.cb)[c];
             const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -126,14 +161,14 @@ __global__ void __launch_bounds__(kTmaThreadsMax) k_fused_tma(FusedArgs a, TmaGe
       }
       const int64_t gc = row * cpr + c;
       const int64_t gg = gc >> sh;
-      if (FMT == kINT8) {
+      if (BASE == kINT8) {
         uint32_t q[4];
         const float s8 = quant_i8<true>(acc, lpg, q, acc);
         if (act && a.rq_codes) {
           st128(static_cast<int8_t*>(a.rq_codes) + gc * 16, make_uint4(q[0], q[1], q[2], q[3]));
           if ((lane & (lpg - 1)) == 0) stf(a.rq_scales + gg, s8);
         }
-      } else if (FMT == kINT4) {
+      } else if (BASE == kINT4) {
         uint32_t q[2];
         float z;
         const float s4 = quant_i4<true>(acc, lpg, q, z, acc);
@@ -165,6 +200,17 @@ __global__ void __launch_bounds__(kTmaThreadsMax) k_fused_tma(FusedArgs a, TmaGe
       }
     }
 
+    if (QTAG) {  // the row's first failing block (if any) -> status
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) {
+        const int64_t o2 = __shfl_xor_sync(kFull, first_bad, m);
+        first_bad = o2 < first_bad ? o2 : first_bad;
+      }
+      if (lane == 0 && first_bad != LLONG_MAX && a.status) {
+        atomicCAS(a.status, 0, 3 /* FC_ERR_STALE_BLOCK */);
+        atomicMin(a.status + 1, first_bad < INT_MAX ? static_cast<int>(first_bad) : INT_MAX - 1);
+      }
+    }
     // ---- the row's only barrier: sum of squares + vote on the staged copy
     float v = warp_sum(__fadd_rn(ss2.x, ss2.y));
     if (lane == 0) red[i & 1][wid] = v;
@@ -214,6 +260,10 @@ int geometry(int fmt, const FusedArgs& a, TmaGeom& g) {
   const int H = a.H, P = a.P;
   if (fmt == kBF16) {
     g.cb = 2 * H, g.sb = 0, g.zb = 0;
+  } else if (fmt == kINT8T) {
+    g.cb = (H / 128) * kBlocksPerGroupI8 * 16, g.sb = 0, g.zb = 0;
+  } else if (fmt == kINT4T) {
+    g.cb = (H / 32) * kBlocksPerGroupI4 * 16, g.sb = 0, g.zb = 0;
   } else {
     g.cb = fmt == kINT8 ? H : H / 2;
     g.sb = (H / a.G) * 4;
@@ -277,13 +327,13 @@ cudaError_t launch_tma_fmt(const FusedArgs& a, const TmaGeom& g, int max_ctas, c
 }  // namespace
 
 bool fused_tma_eligible(int fmt, const FusedArgs& a) {
-  if (fmt != kBF16 && fmt != kINT8 && fmt != kINT4) return false;
+  if (fmt != kBF16 && fmt != kINT8 && fmt != kINT4 && fmt != kINT8T && fmt != kINT4T) return false;
   TmaGeom g;
   if (!geometry(fmt, a, g)) return false;
   if (g.stage_off + g.stage_bytes > kTmaSmemLimit) return false;
   for (int p = 0; p < a.P; ++p) {
     if (!aligned16(a.s.codes[p])) return false;
-    if (fmt != kBF16 && !aligned16(a.s.scales[p])) return false;
+    if ((fmt == kINT8 || fmt == kINT4) && !aligned16(a.s.scales[p])) return false;
     if (fmt == kINT4 && !aligned16(a.s.zeros[p])) return false;
   }
   return aligned16(a.res_in) && aligned16(a.gamma);
@@ -316,6 +366,8 @@ int64_t fused_tma_wave_rows(int fmt, const FusedArgs& a) {
   geometry(fmt, a, g);
   if (fmt == kBF16) return wave_fmt<kBF16>(a, g);
   if (fmt == kINT8) return wave_fmt<kINT8>(a, g);
+  if (fmt == kINT8T) return wave_fmt<kINT8T>(a, g);
+  if (fmt == kINT4T) return wave_fmt<kINT4T>(a, g);
   return wave_fmt<kINT4>(a, g);
 }
 
@@ -325,6 +377,8 @@ cudaError_t launch_fused_tma(int fmt, const FusedArgs& a, int max_ctas, cudaStre
   switch (fmt) {
     case kBF16: return launch_tma_fmt<kBF16>(a, g, max_ctas, st);
     case kINT8: return launch_tma_fmt<kINT8>(a, g, max_ctas, st);
+    case kINT8T: return launch_tma_fmt<kINT8T>(a, g, max_ctas, st);
+    case kINT4T: return launch_tma_fmt<kINT4T>(a, g, max_ctas, st);
     default: return launch_tma_fmt<kINT4>(a, g, max_ctas, st);
   }
 }

@@ -6,7 +6,13 @@
 
 namespace fc {
 
-enum Fmt : int { kBF16 = 0, kINT8 = 1, kINT4 = 2, kTAGGED = 3, kF32 = 4 };
+enum Fmt : int {
+  kBF16 = 0, kINT8 = 1, kINT4 = 2, kTAGGED = 3, kF32 = 4,
+  kINT8T = 5,  // INT8 g128 groups in epoch-tagged 16-byte blocks (11 per group)
+  kINT4T = 6   // INT4 g32 groups in epoch-tagged 16-byte blocks (2 per group)
+};
+// 16-byte blocks per quantization group of the tagged quantized formats.
+constexpr int kBlocksPerGroupI8 = 11, kBlocksPerGroupI4 = 2;
 
 // Dequantized output of a requantization: none, bf16 or fp32.
 enum DeqOut : int { kDeqNone = 0, kDeqBF16 = 1, kDeqF32 = 2 };
@@ -26,6 +32,7 @@ struct QuantJob {
   float* scales[8];
   float* zeros[8];
   void* deq;  // NULL, bf16 or fp32 [n] (P == 1 only)
+  uint32_t epoch;  // tagged quantized output only
   int64_t n;  // elements per tensor (multiple of G)
   int P;
   int G;
@@ -67,6 +74,9 @@ int64_t fused_wave_rows(int fmt, const FusedArgs& a);
 // in_f32: input is fp32 (requantization) instead of bf16; deq_kind: a DeqOut.
 cudaError_t launch_quantize(int fmt, bool in_f32, int deq_kind, const QuantJob& job,
                             cudaStream_t st);
+// Sender quantization of P bf16 slabs straight into epoch-tagged blocks
+// (fmt kINT8T / kINT4T; job.codes[p] are the block arrays).
+cudaError_t launch_quantize_tagged(int fmt, const QuantJob& job, cudaStream_t st);
 // Sum of dequantized slabs over the 16-element chunks [c0, c1).
 cudaError_t launch_reduce(int fmt, const Slabs& s, int P, int G, int64_t c0, int64_t c1,
                           float* out, cudaStream_t st);

@@ -125,11 +125,17 @@ constexpr int kWTile = 1024;  // elements per warp tile (2 KB of bf16, 2 chunks 
 constexpr int kWStages = 4;
 constexpr int kQWarps = kThreads / 32;
 
-template <int FMT>
+// TAGGED: the codes and scales go out as self-synchronizing blocks carrying
+// job.epoch: every group's payload (INT8 g128: 128 code bytes + scale = 11
+// pieces of 12 bytes; INT4 g32: 16 code bytes + scale + zero = 2 pieces) in
+// words 0..2 of a 16-byte block, the epoch in word 3.
+template <int FMT, bool TAGGED = false>
 __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int lpg_shift,
                                                            int64_t tiles_per_slab) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t bars[kQWarps][kWStages];
+  // INT8 tagged: a warp assembles its 4 groups' payloads (33 words each) here
+  __shared__ uint32_t qstage[TAGGED && FMT == kINT8 ? kQWarps : 1][4][33];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int lpg = 1 << lpg_shift;
   const int64_t total = tiles_per_slab * job.P;
@@ -215,7 +221,28 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int 
       if (FMT == kINT8) {
         uint32_t q[4];
         const float s = quant_i8<false, true>(v, lpg, q, d, bw);
-        if (act) {
+        if (TAGGED) {
+          // lpg == 8: lane = (group in warp) * 8 + k; stage the payload, then
+          // one lane per block writes it (11 blocks per group, 44 per warp)
+          uint32_t* pl = qstage[wid][lane >> 3];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) pl[4 * (lane & 7) + i] = q[i];
+          if ((lane & 7) == 0) pl[32] = __float_as_uint(s);
+          __syncwarp();
+          const int64_t g0 = ((e0 >> 4) + j * 32) >> 3;  // first group of this warp chunk
+          const int ngr = min(4, (nch - j * 32 + 7) >> 3);
+          uint4* out = static_cast<uint4*>(job.codes[p]);
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int bi = r * 32 + lane;
+            const int gr = bi / kBlocksPerGroupI8, b = bi - gr * kBlocksPerGroupI8;
+            if (bi < 44 && gr < ngr) {
+              const uint32_t* w = qstage[wid][gr] + 3 * b;
+              st128(out + (g0 + gr) * kBlocksPerGroupI8 + b, make_uint4(w[0], w[1], w[2], job.epoch));
+            }
+          }
+          __syncwarp();
+        } else if (act) {
           st128(static_cast<int8_t*>(job.codes[p]) + c * 16, make_uint4(q[0], q[1], q[2], q[3]));
           if ((lane & (lpg - 1)) == 0) stf(job.scales[p] + (c >> lpg_shift), s);
         }
@@ -223,7 +250,18 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int 
         uint32_t q[2];
         float z;
         const float s = quant_i4<false, true>(v, lpg, q, z, d, bw);
-        if (act) {
+        if (TAGGED) {
+          // lpg == 2: the even lane writes block 0 {its two code words, the odd
+          // lane's first}, the odd lane block 1 {its second, scale, zero}
+          const uint32_t other = __shfl_xor_sync(kFull, q[0], 1);
+          if (act) {
+            uint4* out = static_cast<uint4*>(job.codes[p]) + (c >> 1) * kBlocksPerGroupI4;
+            if ((lane & 1) == 0)
+              st128(out, make_uint4(q[0], q[1], other, job.epoch));
+            else
+              st128(out + 1, make_uint4(q[1], __float_as_uint(s), __float_as_uint(z), job.epoch));
+          }
+        } else if (act) {
           st64(static_cast<uint8_t*>(job.codes[p]) + c * 8, make_uint2(q[0], q[1]));
           if ((lane & (lpg - 1)) == 0) {
             stf(job.scales[p] + (c >> lpg_shift), s);
@@ -402,27 +440,27 @@ int num_sms() {
   return sms[dev];
 }
 
-template <int FMT>
+template <int FMT, bool TAGGED = false>
 cudaError_t launch_quantize_tma(const QuantJob& job, cudaStream_t st) {
   const int smem = kQWarps * kWStages * kWTile * 2;
+  auto kern = k_quantize_tma<FMT, TAGGED>;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   dev = dev < 64 ? dev : 63;
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_quantize_tma<FMT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   int occ = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_quantize_tma<FMT>, kThreads, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
   if (occ < 1) return cudaErrorInvalidConfiguration;
   const int64_t tps = (job.n + kWTile - 1) / kWTile;
   int64_t grid = static_cast<int64_t>(num_sms()) * occ;
   const int64_t need = (tps * job.P + kQWarps - 1) / kQWarps;
   if (grid > need) grid = need;
-  k_quantize_tma<FMT><<<static_cast<int>(grid), kThreads, smem, st>>>(job, log2_lanes(job.G), tps);
+  kern<<<static_cast<int>(grid), kThreads, smem, st>>>(job, log2_lanes(job.G), tps);
   return cudaGetLastError();
 }
 
@@ -446,6 +484,12 @@ cudaError_t launch_quantize(int fmt, bool in_f32, int deq, const QuantJob& job, 
   if (deq == kDeqBF16) return launch_quantize_t<kINT4, true, kDeqBF16>(job, st);
   if (deq == kDeqF32) return launch_quantize_t<kINT4, true, kDeqF32>(job, st);
   return launch_quantize_t<kINT4, true, kDeqNone>(job, st);
+}
+
+cudaError_t launch_quantize_tagged(int fmt, const QuantJob& job, cudaStream_t st) {
+  if (job.n == 0) return cudaSuccess;
+  return fmt == kINT8T ? launch_quantize_tma<kINT8, true>(job, st)
+                       : launch_quantize_tma<kINT4, true>(job, st);
 }
 
 cudaError_t launch_reduce(int fmt, const Slabs& s, int P, int G, int64_t c0, int64_t c1,

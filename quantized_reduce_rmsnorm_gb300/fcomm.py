@@ -17,6 +17,7 @@ import torch
 from . import build as _build
 
 FMT_BF16, FMT_INT8_SYM, FMT_INT4_ASYM, FMT_BF16_TAGGED, FMT_F32 = 0, 1, 2, 3, 4
+FMT_INT8_TAGGED, FMT_INT4_TAGGED = 5, 6
 FC_OK, FC_ERR_INVALID, FC_ERR_CUDA, FC_ERR_STALE_BLOCK, FC_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
 STATUS_NO_INDEX = 0x7F7F7F7F
 
@@ -24,7 +25,7 @@ STATUS_NO_INDEX = 0x7F7F7F7F
 EXPORTS = (
     "fc_codes_bytes", "fc_groups", "fc_tagged_bytes", "fc_shard_range", "fc_group_quantize",
     "fc_group_quantize_multi", "fc_reduce_dequant_sum", "fc_requant_gather", "fc_pack_tagged",
-    "fc_pack_tagged_multi",
+    "fc_pack_tagged_multi", "fc_group_quantize_tagged",
     "fc_allreduce_residual_rmsnorm", "fc_allreduce_residual_rmsnorm_ex", "fc_status_string",
     "fc_last_error", "fc_version", "fc_token_split",
 )
@@ -63,6 +64,8 @@ INT8_G128 = QSpec(FMT_INT8_SYM, 128)
 INT4_G32 = QSpec(FMT_INT4_ASYM, 32)
 BF16 = QSpec(FMT_BF16, 0)
 BF16_TAGGED = QSpec(FMT_BF16_TAGGED, 0)
+INT8_G128_TAGGED = QSpec(FMT_INT8_TAGGED, 128)
+INT4_G32_TAGGED = QSpec(FMT_INT4_TAGGED, 32)
 
 _lib = None
 
@@ -93,6 +96,7 @@ def load(path: Optional[str] = None):
         "fc_requant_gather": (i32, [P, i64, i64, QS, QT, P, i32, P]),
         "fc_pack_tagged": (i32, [P, i64, i64, u32, P, P]),
         "fc_pack_tagged_multi": (i32, [P, i32, i64, i64, u32, P, P]),
+        "fc_group_quantize_tagged": (i32, [P, i32, i64, i64, QS, u32, P, P]),
         "fc_allreduce_residual_rmsnorm": (
             i32, [P, i32, i64, i64, QS, P, P, P, f32, QT, P, u32, P, P]),
         "fc_allreduce_residual_rmsnorm_ex": (
@@ -209,6 +213,16 @@ def requant_gather(reduced: torch.Tensor, spec: QSpec, requant_out=None,
 def pack_tagged(x: torch.Tensor, epoch: int, blocks: torch.Tensor, stream=None):
     rows, hidden = _rows_hidden(x)
     _check(load().fc_pack_tagged(_ptr(x), rows, hidden, epoch, _ptr(blocks), _stream(stream)))
+
+
+def group_quantize_tagged(xs: Sequence[torch.Tensor], spec: QSpec, epoch: int,
+                          blocks: Sequence[torch.Tensor], stream=None):
+    """Quantize P bf16 slabs straight into self-synchronizing blocks."""
+    rows, hidden = _rows_hidden(xs[0])
+    xp = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+    bp = (ctypes.c_void_p * len(blocks))(*[_ptr(b) for b in blocks])
+    _check(load().fc_group_quantize_tagged(xp, len(xs), rows, hidden, spec, epoch, bp,
+                                           _stream(stream)))
 
 
 def pack_tagged_multi(xs: Sequence[torch.Tensor], epoch: int, blocks: Sequence[torch.Tensor],

@@ -22,7 +22,8 @@ import numpy as np
 import torch
 
 from . import fcomm as fc
-from .synth import FMT_BF16, FMT_BF16_TAGGED, FMT_INT4_ASYM, FMT_INT8_SYM, Workload
+from .synth import (FMT_BF16, FMT_BF16_TAGGED, FMT_INT4_ASYM, FMT_INT8_SYM, QTAGGED, Workload,
+                    base_format)
 
 
 def _bf16_dev(bits: np.ndarray, device) -> torch.Tensor:
@@ -33,9 +34,10 @@ def _bf16_dev(bits: np.ndarray, device) -> torch.Tensor:
 def qs_bytes(w: Workload, E: int) -> int:
     """Bytes of one quantized slab of E elements: codes + scales (+ zeros)."""
     ng = E // w.group
-    if w.fmt == FMT_INT8_SYM:
+    fmt = base_format(w.fmt)
+    if fmt == FMT_INT8_SYM:
         return E + 4 * ng
-    if w.fmt == FMT_INT4_ASYM:
+    if fmt == FMT_INT4_ASYM:
         return E // 2 + 8 * ng
     raise ValueError(w.fmt)
 
@@ -59,6 +61,12 @@ class Pipeline:
             self.codes = [fc.alloc_qtensor(self.spec, T, H, device) for _ in range(w.P)]
             if with_payload:
                 self.payload = fc.alloc_qtensor(self.spec, T, H, device)
+        elif w.fmt in QTAGGED:
+            self.blocks = [torch.empty(fc.codes_bytes(self.spec, T, H), dtype=torch.uint8,
+                                       device=device) for _ in range(w.P)]
+            self.status = torch.zeros(1, 2, dtype=torch.int32, device=device)
+            if with_payload:
+                self.payload = fc.alloc_qtensor(fc.QSpec(base_format(w.fmt), w.group), T, H, device)
         elif w.fmt == FMT_BF16_TAGGED:
             self.blocks = [torch.empty(fc.tagged_bytes(T, H), dtype=torch.uint8, device=device)
                            for _ in range(w.P)]
@@ -78,7 +86,7 @@ class Pipeline:
     # ------------------------------------------------------------------
     def _launches(self) -> int:
         w = self.w
-        if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
+        if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM) or w.fmt in QTAGGED:
             return 2
         if w.fmt == FMT_BF16:
             return 1
@@ -104,6 +112,9 @@ class Pipeline:
         w = self.w
         if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
             fc.group_quantize_multi(self.x, self.spec, self.codes, stream=st)
+        elif w.fmt in QTAGGED:
+            self.epoch = (self.epoch + 1) & 0xFFFFFFFF
+            fc.group_quantize_tagged(self.x, self.spec, self.epoch, self.blocks, stream=st)
         elif w.fmt == FMT_BF16_TAGGED:
             self.epoch = (self.epoch + 1) & 0xFFFFFFFF
             fc.pack_tagged_multi(self.x, self.epoch, self.blocks, stream=st)
@@ -115,6 +126,11 @@ class Pipeline:
             fc.allreduce_residual_rmsnorm(self.codes, self.spec, w.T, w.H, self.residual,
                                           self.residual_out, self.gamma, w.eps, self.y,
                                           requant_out=self.payload, stream=st)
+        elif w.fmt in QTAGGED:
+            fc.allreduce_residual_rmsnorm(self.blocks, self.spec, w.T, w.H, self.residual,
+                                          self.residual_out, self.gamma, w.eps, self.y,
+                                          requant_out=self.payload, expected_epoch=self.epoch,
+                                          d_status=self.status[0], stream=st)
         elif w.fmt == FMT_BF16:
             fc.allreduce_residual_rmsnorm(self.x, self.spec, w.T, w.H, self.residual,
                                           self.residual_out, self.gamma, w.eps, self.y,
@@ -152,6 +168,12 @@ class Pipeline:
             qs = qs_bytes(w, E)
             return {"sender": P * 2 * E + P * qs,
                     "fused": P * qs + 2 * E + 2 * H + (qs if self.payload is not None else 0)
+                    + 4 * E}
+        if w.fmt in QTAGGED:
+            tb = fc.codes_bytes(self.spec, w.T, w.H)
+            qs = qs_bytes(w, E)
+            return {"sender": P * 2 * E + P * tb,
+                    "fused": P * tb + 2 * E + 2 * H + (qs if self.payload is not None else 0)
                     + 4 * E}
         if w.fmt == FMT_BF16:
             return {"sender": 0, "fused": P * 2 * E + 2 * E + 2 * H + 4 * E}

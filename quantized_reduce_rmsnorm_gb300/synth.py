@@ -23,6 +23,8 @@ models; no dataset or weights are involved):
   blocks, processed as two subsets of 2048 rows.
 * ``sweep``: message 16 KB .. 256 MB, hidden 4096 or 8192, P in {2,4,8},
   format in {bf16, INT8 g128, INT4 g32}, N(0,1).
+* ``decode-qtagged`` / ``prefill-qtagged``: decode / prefill with the quantized
+  groups sent as self-synchronizing (epoch-tagged) 16-byte blocks.
 
 Every workload: residual N(0,1), gamma N(1, 0.1), eps 1e-5.
 """
@@ -41,8 +43,17 @@ ROW_CHUNK = 64
 _S_RESIDUAL, _S_GAMMA, _S_OUTLIER = 100, 101, 102
 
 FMT_BF16, FMT_INT8_SYM, FMT_INT4_ASYM, FMT_BF16_TAGGED = 0, 1, 2, 3
+FMT_INT8_TAGGED, FMT_INT4_TAGGED = 5, 6
 FMT_NAMES = {FMT_BF16: "bf16", FMT_INT8_SYM: "int8_sym_g128",
-             FMT_INT4_ASYM: "int4_asym_g32", FMT_BF16_TAGGED: "bf16_tagged"}
+             FMT_INT4_ASYM: "int4_asym_g32", FMT_BF16_TAGGED: "bf16_tagged",
+             FMT_INT8_TAGGED: "int8_sym_g128_tagged", FMT_INT4_TAGGED: "int4_asym_g32_tagged"}
+QUANTIZED = (FMT_INT8_SYM, FMT_INT4_ASYM, FMT_INT8_TAGGED, FMT_INT4_TAGGED)
+QTAGGED = (FMT_INT8_TAGGED, FMT_INT4_TAGGED)
+
+
+def base_format(fmt: int) -> int:
+    """The plain quantized format a tagged quantized format carries."""
+    return {FMT_INT8_TAGGED: FMT_INT8_SYM, FMT_INT4_TAGGED: FMT_INT4_ASYM}.get(fmt, fmt)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -72,6 +83,12 @@ WORKLOADS = {
                         outlier_frac=0.005, outlier_scale=20.0),
     "token-split": Workload("token-split", P=8, T=4096, H=5120, fmt=FMT_BF16_TAGGED, group=0,
                             splits=2),
+    # the decode and prefill workloads with self-synchronizing quantized payloads
+    "decode-qtagged": Workload("decode-qtagged", P=8, T=64, H=8192, fmt=FMT_INT8_TAGGED,
+                               group=128, dist="student_t3", outlier_frac=0.001,
+                               outlier_scale=50.0),
+    "prefill-qtagged": Workload("prefill-qtagged", P=4, T=8192, H=8192, fmt=FMT_INT4_TAGGED,
+                                group=32, outlier_frac=0.005, outlier_scale=20.0),
 }
 
 

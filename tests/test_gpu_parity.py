@@ -18,6 +18,7 @@ from gpu_util import (assert_bits_equal, assert_y_close, bf16_float, dev, dev_bf
 pytestmark = pytest.mark.gpu
 
 I8, I4, BF, TG = synth.FMT_INT8_SYM, synth.FMT_INT4_ASYM, synth.FMT_BF16, synth.FMT_BF16_TAGGED
+I8T, I4T = synth.FMT_INT8_TAGGED, synth.FMT_INT4_TAGGED
 
 
 def spec_of(fmt, G):
@@ -285,7 +286,7 @@ def run_fused(w, inp, seed_payload=True, max_ctas=0, alias=False, epoch=7, kerne
 
 
 def oracle_fused(orc, w, inp):
-    fmt = BF if w.fmt == TG else w.fmt
+    fmt = BF if w.fmt == TG else synth.base_format(w.fmt)
     return orc.allreduce_residual_rmsnorm(fmt, inp["slabs"], inp["residual"], inp["gamma"],
                                           w.T, w.H, w.group, w.eps)
 
@@ -510,8 +511,73 @@ def test_wave_aware_token_split(orc):
     assert_bits_equal(outs[1]["h"], want["h"], "residual_out")
 
 
+# ---------------------------------------- self-synchronizing quantized payloads --
+QT_CASES = [("decode-qtagged", {"T": 12}), ("prefill-qtagged", {"T": 10}),
+            ("i8t-p3", {"P": 3, "T": 5, "H": 1152, "fmt": I8T, "group": 128}),
+            ("i4t-p5", {"P": 5, "T": 7, "H": 4128, "fmt": I4T, "group": 32})]
+
+
+@pytest.mark.parametrize("name,kw", QT_CASES, ids=[c[0] for c in QT_CASES])
+def test_quantized_tagged_producer_and_consumer(orc, name, kw):
+    """Producer: the blocks equal the oracle's packing of the oracle's codes.
+    Consumer: the fused path equals the oracle (same math as untagged)."""
+    from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
+    w = small(name, **kw)
+    inp = synth.make_inputs(w, seed=41)
+    pipe = Pipeline(w, inp)
+    pipe.step()
+    got = pipe.outputs()
+    base = synth.base_format(w.fmt)
+    for p in range(w.P):
+        q, s, z = oracle_quant(orc, synth.Workload(**{**w.__dict__, "fmt": base}), inp["slabs"][p])
+        want = orc.pack_qtagged(base, q, s, z, w.group, pipe.epoch)
+        assert_bits_equal(host(pipe.blocks[p]).view(np.uint32), want, f"blocks slab {p}")
+    check_fused(orc, synth.Workload(**{**w.__dict__, "fmt": base}), got, oracle_fused(orc, w, inp))
+    assert got["status"].tolist() == [[fc.FC_OK, fc.STATUS_NO_INDEX]]
+
+
+@pytest.mark.parametrize("fmt,G,nbg", [(I8T, 128, 11), (I4T, 32, 2)])
+def test_quantized_tagged_stale_blocks(orc, fmt, G, nbg):
+    """Blocks built on the host by the oracle, one tag corrupted before upload."""
+    base = synth.base_format(fmt)
+    w = synth.Workload("qtstale", P=3, T=4, H=1024, fmt=fmt, group=G)
+    inp = synth.make_inputs(w, seed=42)
+    ep = 5
+    blocks = []
+    for s_ in inp["slabs"]:
+        q, s, z = orc.quantize(base, bf16_float(s_).ravel(), G)
+        blocks.append(orc.pack_qtagged(base, q, s, z, G, ep))
+    spec = spec_of(fmt, G)
+    r_in, gam = dev_bf16(inp["residual"]), dev_bf16(inp["gamma"])
+    r_out, y = torch.empty_like(r_in), torch.empty_like(r_in)
+    st = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+
+    def call(bl):
+        fc.allreduce_residual_rmsnorm([dev(b.view(np.int32)) for b in bl], spec, w.T, w.H, r_in, r_out,
+                                      gam, w.eps, y, expected_epoch=ep, d_status=st)
+        torch.cuda.synchronize()
+        return list(host(st))
+
+    assert call(blocks) == [fc.FC_OK, fc.STATUS_NO_INDEX]
+    want = oracle_fused(orc, w, inp)
+    assert_bits_equal(host_bits(r_out), want["h"], "residual_out")
+    bpr = (w.H // G) * nbg
+    for slab, row, blk in ((1, 2, 5), (2, 3, bpr - 1), (0, 0, nbg - 1)):
+        bad = [b.copy() for b in blocks]
+        bad[slab][4 * (row * bpr + blk) + 3] = ep + 1
+        assert call(bad) == [fc.FC_ERR_STALE_BLOCK, (slab * w.T + row) * bpr + blk]
+
+
+def test_quantized_tagged_rejects_other_groups():
+    x = torch.zeros(2, 4096, dtype=torch.bfloat16, device="cuda")
+    b = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fc.FcommError) as e:
+        fc.group_quantize_tagged([x], fc.QSpec(I8T, 64), 1, [b])
+    assert e.value.status == fc.FC_ERR_UNSUPPORTED
+
+
 # --------------------------------------------------- full-size, sampled rows --
-@pytest.mark.parametrize("name", ["prefill", "token-split", "decode"])
+@pytest.mark.parametrize("name", ["prefill", "token-split", "decode", "prefill-qtagged"])
 def test_full_size_sampled_rows(orc, name):
     """The full-size workloads through the same Pipeline.step() the
     benchmark times (token-split: two subsets on two streams); the oracle
@@ -528,12 +594,14 @@ def test_full_size_sampled_rows(orc, name):
     want = oracle_fused(orc, sub, synth.make_inputs(w, seed=0, rows=rows))
     assert_bits_equal(got["h"][rows], want["h"], "residual_out")
     assert_y_close(got["y"][rows], want["y"])
-    if w.fmt in (I8, I4):
+    if w.fmt in (I8, I4, I8T, I4T):
         codes = got["codes"].reshape(w.T, -1)[rows]
         assert_bits_equal(codes, want["codes"], "payload codes")
         assert_bits_equal(got["scales"].reshape(w.T, -1)[rows], want["scales"], "payload scales")
-        if w.fmt == I4:
+        if w.fmt in (I4, I4T):
             assert_bits_equal(got["zeros"].reshape(w.T, -1)[rows], want["zeros"], "payload zeros")
+    if w.fmt in (I8T, I4T):
+        assert got["status"].tolist() == [[fc.FC_OK, fc.STATUS_NO_INDEX]]
     if w.fmt == TG:
         assert got["status"].tolist() == [[fc.FC_OK, fc.STATUS_NO_INDEX]] * w.splits
 
