@@ -242,6 +242,31 @@ fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64
 fc_status fc_token_split(int P, int64_t rows, int64_t hidden, fc_qspec spec, int64_t* split,
                          int64_t* wave_rows);
 
+/* Cost-guided protocol choice (flash-comm, abstract: a selector adapts the
+ * readiness encoding to the message size and the number of GPUs, balancing
+ * synchronization overhead against additional data-transfer cost).  One-GPU
+ * analogue: for P ranks reducing rows x hidden bf16 partial sums, estimate
+ * for every format whose bit width is >= min_bits (16: bf16 only; 8: + INT8;
+ * 4: + INT4) and its tagged variant
+ *   t = t_fixed + fused_bytes(format) / rate(format)          (this GPU)
+ *     + [t_fixed + sender_bytes(format) / sender_rate(format)] (quantize/pack)
+ *     + 2 (P-1)/P * payload(format) / link_gbps               (wire, optional)
+ *     + (untagged ? 2 * barrier_us : 0)                        (readiness)
+ * where rate(format) is the fused kernel's measured algorithmic rate on
+ * GB300 (message-size sweep, 64-256 MB points) and t_fixed its measured
+ * per-call floor; tagged formats pay 16/12 of the payload and need no
+ * barrier.  link == NULL models one GPU (no wire, no barrier): then plain
+ * bf16 wins, since quantizing only pays off when the wire is the bottleneck.
+ * *choice receives the fastest format (group 128 for INT8, 32 for
+ * INT4), *est_us its estimate.  Host-only; no GPU needed. */
+typedef struct {
+  double link_gbps;  /* per-GPU interconnect bandwidth, GB/s (> 0) */
+  double barrier_us; /* cost of one all-rank readiness barrier, us (>= 0) */
+} fc_link_model;
+
+fc_status fc_select_protocol(int64_t rows, int64_t hidden, int P, int min_bits,
+                             const fc_link_model* link, fc_qspec* choice, double* est_us);
+
 /* --------------------------------------------------------------- misc --- */
 const char* fc_status_string(fc_status s);
 /* Message describing the calling thread's last non-OK status ("" if none). */

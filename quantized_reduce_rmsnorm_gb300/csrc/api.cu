@@ -384,4 +384,56 @@ fc_status fc_token_split(int P, int64_t rows, int64_t hidden, fc_qspec spec, int
   return ok();
 }
 
+fc_status fc_select_protocol(int64_t rows, int64_t hidden, int P, int min_bits,
+                             const fc_link_model* link, fc_qspec* choice, double* est_us) {
+  if (rows <= 0 || hidden <= 0 || hidden % 128 != 0)
+    return fail(FC_ERR_INVALID, "need rows > 0 and hidden a positive multiple of 128");
+  if (P < 2 || P > 8) return fail(FC_ERR_INVALID, "P must be in [2, 8] (got %d)", P);
+  if (min_bits != 4 && min_bits != 8 && min_bits != 16)
+    return fail(FC_ERR_INVALID, "min_bits must be 4, 8 or 16 (got %d)", min_bits);
+  if (!choice) return fail(FC_ERR_INVALID, "choice must not be NULL");
+  if (link && (!(link->link_gbps > 0.0) || !(link->barrier_us >= 0.0)))
+    return fail(FC_ERR_INVALID, "link_gbps must be > 0 and barrier_us >= 0");
+  const double E = static_cast<double>(rows) * static_cast<double>(hidden);
+  struct Cand {
+    int fmt, group, bits;
+    double payload;  // bytes one rank sends for its whole slab
+    double rate;     // fused kernel, algorithmic GB/s on GB300 (measured)
+    double srate;    // sender (quantize / pack) kernel, GB/s (measured); 0: none
+    bool tagged;
+  };
+  // payload per slab: bf16 2E; INT8 g128 E + 4E/128; INT4 g32 E/2 + 8E/32;
+  // the tagged encodings carry 12 payload bytes in every 16.
+  const Cand cands[] = {
+      {FC_FMT_BF16, 0, 16, 2 * E, 5800.0, 0.0, false},
+      {FC_FMT_BF16_TAGGED, 0, 16, 2 * E * 16 / 12, 4400.0, 5600.0, true},
+      {FC_FMT_INT8_SYM, 128, 8, E + 4 * E / 128, 4300.0, 4000.0, false},
+      {FC_FMT_INT8_TAGGED, 128, 8, (E + 4 * E / 128) * 16 / 12, 4000.0, 4000.0, true},
+      {FC_FMT_INT4_ASYM, 32, 4, E / 2 + 8 * E / 32, 3300.0, 3500.0, false},
+      {FC_FMT_INT4_TAGGED, 32, 4, (E / 2 + 8 * E / 32) * 16 / 12, 3300.0, 3900.0, true},
+  };
+  const double t_fixed = 9.0;  // us: measured per-call floor of the fused kernel
+  double best = 1e300;
+  const Cand* pick = nullptr;
+  for (const Cand& c : cands) {
+    if (c.bits < min_bits) continue;
+    // requant payload (quantized only) + residual in, residual_out + y out
+    const double requant = c.bits < 16 ? (c.fmt == FC_FMT_INT8_SYM || c.fmt == FC_FMT_INT8_TAGGED
+                                              ? E + 4 * E / 128 : E / 2 + 8 * E / 32)
+                                        : 0.0;
+    const double fused_bytes = P * c.payload + 2 * E + requant + 4 * E;
+    double t = t_fixed + fused_bytes / (c.rate * 1e3);
+    if (c.srate > 0.0) t += t_fixed + P * (2 * E + c.payload) / (c.srate * 1e3);  // sender
+    if (link) {
+      t += 2.0 * (P - 1) / P * c.payload / (link->link_gbps * 1e3);
+      if (!c.tagged) t += 2.0 * link->barrier_us;
+    }
+    if (t < best) best = t, pick = &c;
+  }
+  choice->fmt = pick->fmt;
+  choice->group = pick->group;
+  if (est_us) *est_us = best;
+  return ok();
+}
+
 }  // extern "C"

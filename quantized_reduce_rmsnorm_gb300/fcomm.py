@@ -27,7 +27,7 @@ EXPORTS = (
     "fc_group_quantize_multi", "fc_reduce_dequant_sum", "fc_requant_gather", "fc_pack_tagged",
     "fc_pack_tagged_multi", "fc_group_quantize_tagged",
     "fc_allreduce_residual_rmsnorm", "fc_allreduce_residual_rmsnorm_ex", "fc_status_string",
-    "fc_last_error", "fc_version", "fc_token_split",
+    "fc_last_error", "fc_version", "fc_token_split", "fc_select_protocol",
 )
 
 
@@ -51,6 +51,10 @@ class QSpec(ctypes.Structure):
 class QTensor(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("zeros", ctypes.c_void_p)]
+
+
+class LinkModel(ctypes.Structure):
+    _fields_ = [("link_gbps", ctypes.c_double), ("barrier_us", ctypes.c_double)]
 
 
 class LaunchOpts(ctypes.Structure):
@@ -105,6 +109,8 @@ def load(path: Optional[str] = None):
         "fc_last_error": (ctypes.c_char_p, []),
         "fc_version": (ctypes.c_char_p, []),
         "fc_token_split": (i32, [i32, i64, i64, QS, ctypes.POINTER(i64), ctypes.POINTER(i64)]),
+        "fc_select_protocol": (i32, [i64, i64, i32, i32, P, ctypes.POINTER(QSpec),
+                                     ctypes.POINTER(ctypes.c_double)]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -257,6 +263,17 @@ def token_split(spec: QSpec, P: int, rows: int, hidden: int):
     sp, wv = ctypes.c_int64(), ctypes.c_int64()
     _check(load().fc_token_split(P, rows, hidden, spec, ctypes.byref(sp), ctypes.byref(wv)))
     return sp.value, wv.value
+
+
+def select_protocol(rows: int, hidden: int, P: int, min_bits: int,
+                    link_gbps: Optional[float] = None, barrier_us: float = 0.0):
+    """(QSpec, estimated us) of the cost-guided format choice."""
+    link = LinkModel(link_gbps, barrier_us) if link_gbps is not None else None
+    choice, est = QSpec(), ctypes.c_double()
+    _check(load().fc_select_protocol(rows, hidden, P, min_bits,
+                                     ctypes.byref(link) if link is not None else None,
+                                     ctypes.byref(choice), ctypes.byref(est)))
+    return choice, est.value
 
 
 def version() -> str:

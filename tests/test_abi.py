@@ -127,3 +127,28 @@ def test_product_package_never_imports_the_oracle():
                 txt = open(os.path.join(root, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", txt, re.M), f
                 assert "liboracle" not in txt and "oracle.h" not in txt, f
+
+
+def test_protocol_selector_trades_barriers_against_bytes():
+    """One GPU (no wire, no barrier): plain bf16, since quantizing costs
+    compute and saves nothing.  With a link, large messages quantize; with a
+    slow barrier, small messages take a tagged encoding and large ones do not;
+    the bit-width floor is always respected."""
+    F = fc.fcomm
+    for bits in (4, 8, 16):
+        c, t = fc.select_protocol(8192, 8192, 4, bits)
+        assert c.fmt == F.FMT_BF16 and t > 0
+    c, _ = fc.select_protocol(8192, 8192, 8, 4, link_gbps=100.0, barrier_us=0.0)
+    assert c.fmt == F.FMT_INT4_ASYM
+    small, _ = fc.select_protocol(1, 4096, 8, 8, link_gbps=450.0, barrier_us=8.0)
+    large, _ = fc.select_protocol(16384, 8192, 8, 8, link_gbps=450.0, barrier_us=8.0)
+    assert small.fmt in (F.FMT_INT8_TAGGED, F.FMT_BF16_TAGGED)
+    assert large.fmt in (F.FMT_INT8_SYM, F.FMT_INT4_ASYM, F.FMT_BF16)
+    for bits in (4, 8, 16):
+        for rows in (1, 64, 4096):
+            c, _ = fc.select_protocol(rows, 8192, 4, bits, link_gbps=100.0, barrier_us=5.0)
+            width = {F.FMT_BF16: 16, F.FMT_BF16_TAGGED: 16, F.FMT_INT8_SYM: 8,
+                     F.FMT_INT8_TAGGED: 8, F.FMT_INT4_ASYM: 4, F.FMT_INT4_TAGGED: 4}[c.fmt]
+            assert width >= bits
+    with pytest.raises(fc.FcommError):
+        fc.select_protocol(1, 4096, 8, 3)
