@@ -160,16 +160,61 @@ __device__ __forceinline__ void unpack16(const V8& v, float f[16]) {
   }
 }
 
+// Mixed-precision arithmetic (sm_100 and later): one operand is the bf16 in
+// the low or high half of a 32-bit word, converted exactly to binary32 inside
+// the instruction, so the result is the same single IEEE rounding as the
+// binary32 operation on the unpacked value, without the unpacking.
+//   add_bf_{lo,hi}(w, c)     = fl(bf16(w) + c)
+//   fma_bf_{lo,hi}(w, g, c)  = fl(bf16(w) * bf16(g) + c)   (both halves alike)
+__device__ __forceinline__ float add_bf_lo(uint32_t w, float c) {
+  float d;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n add.rn.f32.bf16 %0, l, %2;\n}"
+      : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float add_bf_hi(uint32_t w, float c) {
+  float d;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n add.rn.f32.bf16 %0, h, %2;\n}"
+      : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf_lo(uint32_t w, uint32_t g, float c) {
+  float d;
+  asm("{\n .reg .b16 l, h, gl, gh;\n mov.b32 {l, h}, %1;\n mov.b32 {gl, gh}, %2;\n"
+      " fma.rn.f32.bf16 %0, l, gl, %3;\n}"
+      : "=f"(d) : "r"(w), "r"(g), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf_hi(uint32_t w, uint32_t g, float c) {
+  float d;
+  asm("{\n .reg .b16 l, h, gl, gh;\n mov.b32 {l, h}, %1;\n mov.b32 {gl, gh}, %2;\n"
+      " fma.rn.f32.bf16 %0, h, gh, %3;\n}"
+      : "=f"(d) : "r"(w), "r"(g), "f"(c));
+  return d;
+}
+
+// Three-input minimum / maximum (sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // -------------------------------------------------- packed fp32 pairs --
 // Blackwell issues two binary32 operations per instruction on a register
 // pair (.f32x2); each half is an IEEE round-to-nearest operation.  The
 // compiler may fuse a packed multiply whose product has one use with a
-// following packed add into one fused multiply-add, so packed pairs are
-// used only where that cannot change a result: additions of loaded values,
-// the rounding fast path of the quantizers (its exactness test covers either
-// form), and the tolerance-checked RMSNorm output.  Multiply-then-add chains
-// that must round twice (dequantization, the residual add after it) use the
-// scalar __fmul_rn / __fadd_rn intrinsics, which are never contracted.
+// following packed add into one fused multiply-add, so a packed multiply is
+// used only where that cannot change a result (the tolerance-checked RMSNorm
+// output).  Packed adds and packed fused multiply-adds cannot be contracted
+// any further, so exact chains are written with them: a product that must be
+// rounded on its own is formed as fma(2^23 + q, s, -2^23 * s), whose exact
+// value is q * s (see the dequantizers).
 __device__ __forceinline__ float2 padd(float2 a, float2 b) {
   float2 r;
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
@@ -210,14 +255,32 @@ __device__ __forceinline__ float byte_in_two23(uint32_t w, int k) {
 }
 
 // acc[i] += q_i * s for the 16 INT8 codes in w[4] (code i = byte i%4 of w[i/4]).
+// With b = q + 128 (exact, from the sign-flipped byte in the low bits of
+// 2^23), fma(b, s, -128 * s) has the exact value q * s and rounds it once, so
+// it equals fl(q * s) (for s < 2^100, where 128 * s is exact and finite;
+// larger scales take the plain product).  Packed in pairs.
 __device__ __forceinline__ void dequant_i8_acc(const uint32_t w[4], float s, float acc[16]) {
+  if (s < 1.2676506e30f) {  // 2^100
+    const float2 S = dup2(s), N = dup2(__fmul_rn(-128.0f, s)), M = dup2(-kTwo23);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t x = w[j] ^ 0x80808080u;  // int8 -> q + 128
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t x = w[j] ^ 0x80808080u;  // int8 -> q + 128
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float q = __fadd_rn(byte_in_two23(x, k), -kTwo23p128);
-      acc[4 * j + k] = __fadd_rn(acc[4 * j + k], __fmul_rn(q, s));
+      for (int k = 0; k < 4; k += 2) {
+        const float2 b = padd(make_float2(byte_in_two23(x, k), byte_in_two23(x, k + 1)), M);
+        const float2 t = padd(make_float2(acc[4 * j + k], acc[4 * j + k + 1]), pfma(b, S, N));
+        acc[4 * j + k] = t.x, acc[4 * j + k + 1] = t.y;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t x = w[j] ^ 0x80808080u;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float q = __fadd_rn(byte_in_two23(x, k), -kTwo23p128);
+        acc[4 * j + k] = __fadd_rn(acc[4 * j + k], __fmul_rn(q, s));
+      }
     }
   }
 }
@@ -227,10 +290,12 @@ __device__ __forceinline__ void dequant_i8_acc(const uint32_t w[4], float s, flo
 // (exact while 2^23 * s does not overflow, i.e. s < 2^100 here),
 // fma(U, s, nms) rounds the exact value q*s once: it equals the separately
 // rounded product fl(q*s).  Larger scales take the plain product.
+// The fused form runs on packed pairs (codes 2k and 2k + 1 are neighbours).
 template <bool FUSED>
 __device__ __forceinline__ void dequant_i4_acc_t(const uint32_t w[2], float s, float z,
                                                  float acc[16]) {
   const float nms = __fmul_rn(-kTwo23, s);
+  const float2 S = dup2(s), N = dup2(nms), Z = dup2(z);
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const uint32_t ev = w[j] & 0x0F0F0F0Fu;         // codes 8j + 2k
@@ -238,10 +303,17 @@ __device__ __forceinline__ void dequant_i4_acc_t(const uint32_t w[2], float s, f
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float u0 = byte_in_two23(ev, k), u1 = byte_in_two23(od, k);
-      const float p0 = FUSED ? __fmaf_rn(u0, s, nms) : __fmul_rn(__fadd_rn(u0, -kTwo23), s);
-      const float p1 = FUSED ? __fmaf_rn(u1, s, nms) : __fmul_rn(__fadd_rn(u1, -kTwo23), s);
-      acc[8 * j + 2 * k] = __fadd_rn(acc[8 * j + 2 * k], __fadd_rn(p0, z));
-      acc[8 * j + 2 * k + 1] = __fadd_rn(acc[8 * j + 2 * k + 1], __fadd_rn(p1, z));
+      float* a = acc + 8 * j + 2 * k;
+      if (FUSED) {
+        const float2 d = padd(pfma(make_float2(u0, u1), S, N), Z);
+        const float2 t = padd(make_float2(a[0], a[1]), d);
+        a[0] = t.x, a[1] = t.y;
+      } else {
+        const float p0 = __fmul_rn(__fadd_rn(u0, -kTwo23), s);
+        const float p1 = __fmul_rn(__fadd_rn(u1, -kTwo23), s);
+        a[0] = __fadd_rn(a[0], __fadd_rn(p0, z));
+        a[1] = __fadd_rn(a[1], __fadd_rn(p1, z));
+      }
     }
   }
 }
@@ -274,22 +346,24 @@ __device__ __forceinline__ float warp_sum(float v) {
 // ------------------------------------------------------------ quantizers --
 // Codes are rne(fl(v / s)), v = x (INT8) or v = fl(x - lo) (INT4): an IEEE
 // division per element by definition.  Computed without one:
-//  1. r ~ 1/s from the hardware reciprocal (relative error <= 2^-23) and
-//     t = v * r; |t| <= 128, so |t - v/s| <= 2^-15.4 and fl(v/s) is within
-//     2^-17 of v/s.  t is rounded by adding 1.5*2^23 (INT8) or 2^23 (INT4),
-//     which leaves rint(t) in the low mantissa bits; e = t - rint(t).
-//  2. If |e| < 1/2 - 2^-13, t is farther than 2^-14 from every half-integer
-//     and rne(fl(v/s)) = rint(t).  (Whether the compiler fuses t into the
-//     following add or not, this holds: the errors above cover both forms.)
-//  3. Otherwise v/s lies within 2^-12 of the half-integer m next to t.  Then
-//     D = v - m*s is an integer multiple of 2^(e_s - 25) smaller than
+//  1. r ~ 1/s from the hardware reciprocal (relative error <= 2^-23), so the
+//     exact product v * r is within |v/s| * 2^-23 <= 2^-16 of v/s, and fl(v/s)
+//     is within 2^-17 of v/s.  u = fma(v, r, M) with M = 1.5*2^23 (INT8) or
+//     2^23 (INT4) rounds v * r to the nearest integer c and leaves it in the
+//     low mantissa bits of u (which also pack directly into bytes/nibbles);
+//     c = u - M exactly, and n = fma(v, -r, c) = fl(c - v * r).
+//  2. If |n| < 1/2 - 2^-13, v * r is farther than 2^-13 - 2^-25 from every
+//     half-integer, so fl(v/s) is on the same side of each as v * r and
+//     rne(fl(v/s)) = c.
+//  3. Otherwise v/s lies within 2^-12 of the half-integer m next to v * r.
+//     Then D = v - m*s is an integer multiple of 2^(e_s - 25) smaller than
 //     2^(e_s - 11), so it fits in 24 bits and fma(-m, s, v) gives it exactly
 //     (for s >= 2^-100).  fl(v/s) == m exactly when D lies in m's half-ulp
 //     band [-hd, +hu] (hu = 2^(E-24) s for m = +-2^E...; hd = hu/2 only for
 //     |m| = 1/2), ties at the band edges going to m (its significand is
 //     even).  So the code is the even neighbour of m inside the band, and the
 //     neighbour on D's side outside it.
-//  4. Groups where the bound t <= 127.25 (INT8) / 15.25 (INT4) fails or
+//  4. Groups where the bound v * r <= 127.25 (INT8) / 15.25 (INT4) fails or
 //     s < 2^-100 take the IEEE division for every element (never seen on
 //     finite activations; it keeps denormal scales exact).
 constexpr float kMagicI8 = 12582912.0f;         // 1.5 * 2^23, bits 0x4B400000
@@ -351,55 +425,57 @@ __device__ __forceinline__ void bf16_minmax16(const uint32_t w[8], float& lo, fl
 }
 
 // Tree reductions over 16 floats (max of |v|, min and max).
+// (Three-input steps: 16 -> 6 -> 2 -> 1.)
 __device__ __forceinline__ float absmax16(const float v[16]) {
-  float m[8];
+  float a[16];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) m[i] = fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
-#pragma unroll
-  for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
-  return m[0];
+  for (int i = 0; i < 16; ++i) a[i] = fabsf(v[i]);
+  const float m0 = fmax3(a[0], a[1], a[2]), m1 = fmax3(a[3], a[4], a[5]);
+  const float m2 = fmax3(a[6], a[7], a[8]), m3 = fmax3(a[9], a[10], a[11]);
+  const float m4 = fmax3(a[12], a[13], a[14]);
+  return fmaxf(fmax3(m0, m1, m2), fmax3(m3, m4, a[15]));
 }
 __device__ __forceinline__ void minmax16(const float v[16], float& lo, float& hi) {
-  float a[8], b[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) a[i] = fminf(v[2 * i], v[2 * i + 1]), b[i] = fmaxf(v[2 * i], v[2 * i + 1]);
-#pragma unroll
-  for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) a[i] = fminf(a[i], a[i + w]), b[i] = fmaxf(b[i], b[i + w]);
-  lo = a[0], hi = b[0];
+  const float a0 = fmin3(v[0], v[1], v[2]), a1 = fmin3(v[3], v[4], v[5]);
+  const float a2 = fmin3(v[6], v[7], v[8]), a3 = fmin3(v[9], v[10], v[11]);
+  const float a4 = fmin3(v[12], v[13], v[14]);
+  const float b0 = fmax3(v[0], v[1], v[2]), b1 = fmax3(v[3], v[4], v[5]);
+  const float b2 = fmax3(v[6], v[7], v[8]), b3 = fmax3(v[9], v[10], v[11]);
+  const float b4 = fmax3(v[12], v[13], v[14]);
+  lo = fminf(fmin3(a0, a1, a2), fmin3(a3, a4, v[15]));
+  hi = fmaxf(fmax3(b0, b1, b2), fmax3(b3, b4, v[15]));
 }
 
-// Rounds the 16 quotients v[i] / s; ub[i] gets the code in its low byte (or
-// low nibble), qf[i] the code as a float.  group_ok: fl(vmax * r) is within
-// the code range and s >= 2^-100 (else every element takes the division);
-// s == 0 is passed as r == 0 with group_ok set, which yields codes 0.
-// Every lane of the warp must call this: the near-half-integer pass is
-// entered by warp vote and runs converged, one vote per element index.
+// Rounds the 16 quotients v[i] / s; ub[i] gets the bits of M + code (the
+// code in its low byte or nibble), qf[i] the code as a float.  group_ok:
+// fl(vmax * r) is within the code range and s >= 2^-100 (else every element
+// takes the division); s == 0 is passed as r == 0 with group_ok set, which
+// yields codes 0.  Every lane of the warp must call this: the
+// near-half-integer pass is entered by warp vote and runs converged, one
+// vote per element index.
 template <bool SIGNED>
 __device__ __forceinline__ void round_codes(const float v[16], float s, float r, bool group_ok,
                                             uint32_t ub[16], float qf[16]) {
   const float magic = SIGNED ? kMagicI8 : 8388608.0f;
-  float e[16];  // t - rint(t), kept for the near-half-integer pass
+  const float2 R = dup2(r), NR = dup2(-r), M = dup2(magic), NM = dup2(-magic);
+  float n[16];  // fl(code - v * r), kept for the near-half-integer pass
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
-    const float2 t = pmul(make_float2(v[i], v[i + 1]), dup2(r));
-    const float2 u = padd(t, dup2(magic));
-    const float2 c = padd(u, dup2(-magic));
-    const float2 d = padd(t, make_float2(-c.x, -c.y));
-    e[i] = d.x, e[i + 1] = d.y;
+    const float2 x = make_float2(v[i], v[i + 1]);
+    const float2 u = pfma(x, R, M);
+    const float2 c = padd(u, NM);
+    const float2 d = pfma(x, NR, c);
+    n[i] = d.x, n[i + 1] = d.y;
     ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
     qf[i] = c.x, qf[i + 1] = c.y;
   }
-  const float emax = absmax16(e);
-  if (__any_sync(kFull, group_ok && !(emax < kTieGuard))) {
+  const float nmax = absmax16(n);
+  if (__any_sync(kFull, group_ok && !(nmax < kTieGuard))) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const bool near = group_ok && !(fabsf(e[i]) < kTieGuard);
+      const bool near = group_ok && !(fabsf(n[i]) < kTieGuard);
       if (__any_sync(kFull, near)) {
-        const float res = resolve_near_half(v[i], s, qf[i], e[i]);
+        const float res = resolve_near_half(v[i], s, qf[i], -n[i]);
         if (near) {
           qf[i] = res;
           ub[i] = __float_as_uint(__fadd_rn(res, magic));
@@ -412,8 +488,8 @@ __device__ __forceinline__ void round_codes(const float v[16], float s, float r,
     for (int i = 0; i < 16; ++i) {
       const int c = SIGNED ? max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], s))))
                            : max(0, min(15, __float2int_rn(__fdiv_rn(v[i], s))));
-      ub[i] = static_cast<uint32_t>(c);
       qf[i] = static_cast<float>(c);
+      ub[i] = __float_as_uint(__fadd_rn(qf[i], magic));
     }
   }
 }
@@ -463,11 +539,16 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
   z = lo;
   uint32_t ub[16];
   float qf[16];
-  float num[16];
+  float num[16];  // fl(x - lo)
+  if (BFW) {
 #pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    const float2 n = padd(make_float2(v[i], v[i + 1]), dup2(-lo));
-    num[i] = n.x, num[i + 1] = n.y;
+    for (int i = 0; i < 8; ++i) num[2 * i] = add_bf_lo(bw[i], -lo), num[2 * i + 1] = add_bf_hi(bw[i], -lo);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const float2 n = padd(make_float2(v[i], v[i + 1]), dup2(-lo));
+      num[i] = n.x, num[i + 1] = n.y;
+    }
   }
   const float r = s == 0.0f ? 0.0f : rcp_approx(s);
   round_codes<false>(num, s, r, s == 0.0f || (__fmul_rn(span, r) <= 15.25f && s >= kTwoM100), ub, qf);
@@ -477,9 +558,19 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
     const uint32_t od = low_bytes4(ub[8 * j + 1], ub[8 * j + 3], ub[8 * j + 5], ub[8 * j + 7]);
     q[j] = ev | (od << 4);
   }
-  if (DEQ) {
+  if (DEQ) {  // d = fl(fl(q * s) + z); fl(q * s) = fma(2^23 + q, s, -2^23 * s) for s < 2^100
+    if (s < 1.2676506e30f) {
+      const float2 S = dup2(s), N = dup2(__fmul_rn(-kTwo23, s)), Z = dup2(z);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) d[i] = __fadd_rn(__fmul_rn(qf[i], s), z);
+      for (int i = 0; i < 16; i += 2) {
+        const float2 t =
+            padd(pfma(make_float2(__uint_as_float(ub[i]), __uint_as_float(ub[i + 1])), S, N), Z);
+        d[i] = t.x, d[i + 1] = t.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) d[i] = __fadd_rn(__fmul_rn(qf[i], s), z);
+    }
   }
   return s;
 }

@@ -24,6 +24,7 @@ namespace {
 
 constexpr int kTmaThreads = 256;     // per CTA when two or more CTAs fit an SM
 constexpr int kTmaThreadsMax = 512;  // when only one does
+constexpr int kGammaRegChunks = 2;   // gamma chunks a thread keeps in registers
 
 struct TmaGeom {
   int cb;           // code (or bf16 data) bytes of one slab row
@@ -80,6 +81,21 @@ __global__ void __launch_bounds__(kTmaThreadsMax) k_fused_tma(FusedArgs a, TmaGe
         issue_row<FMT>(a, g, stage0 + s * g.stage_bytes, &bar[s], row0 + s * rstride);
   }
   __syncthreads();
+
+  // gamma of this thread's first chunks, read once: every row uses the same chunks
+  uint32_t greg[kGammaRegChunks][8];
+#pragma unroll
+  for (int j = 0; j < kGammaRegChunks; ++j) {
+    const int c = tid + j * nthr;
+    if (c < cpr) {
+      const V8 gv = ld256_keep(static_cast<const uint16_t*>(a.gamma) + c * 16);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) greg[j][k] = gv.w[k];
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) greg[j][k] = 0u;
+    }
+  }
 
   bool all_ok = true;
   int i = 0;
@@ -181,21 +197,22 @@ __global__ void __launch_bounds__(kTmaThreadsMax) k_fused_tma(FusedArgs a, TmaGe
         }
       }
       if (act) {
+        // h = bf16(fl(o + R)) straight from the packed residual; sum of h^2
+        // straight from the packed h
         const uint4 r0 = rrow[2 * c], r1 = rrow[2 * c + 1];
         const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
         V8 hv;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          hv.w[k] = pack_bf2(__fadd_rn(acc[2 * k], bf_lo(rw[k])),
-                             __fadd_rn(acc[2 * k + 1], bf_hi(rw[k])));
+          hv.w[k] = pack_bf2(add_bf_lo(rw[k], acc[2 * k]), add_bf_hi(rw[k], acc[2 * k + 1]));
         uint4* hp = reinterpret_cast<uint4*>(hbuf) + 2 * c;
         hp[0] = make_uint4(hv.w[0], hv.w[1], hv.w[2], hv.w[3]);
         hp[1] = make_uint4(hv.w[4], hv.w[5], hv.w[6], hv.w[7]);
         st256(static_cast<uint16_t*>(a.res_out) + gc * 16, hv);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float2 h = make_float2(bf_lo(hv.w[k]), bf_hi(hv.w[k]));
-          ss2 = pfma(h, h, ss2);
+          ss2.x = fma_bf_lo(hv.w[k], hv.w[k], ss2.x);
+          ss2.y = fma_bf_hi(hv.w[k], hv.w[k], ss2.y);
         }
       }
     }
@@ -229,20 +246,26 @@ __global__ void __launch_bounds__(kTmaThreadsMax) k_fused_tma(FusedArgs a, TmaGe
       }
     }
 
-    // ---- pass 2: y = bf16((h * inv) * gamma)
-    for (int c = tid; c < cpr; c += nthr) {
+    // ---- pass 2: y = bf16(fl(h * gamma) * inv); h * gamma is exact in binary32
+    auto out_chunk = [&](int c, const uint32_t gw[8]) {
       const uint4* hp = reinterpret_cast<const uint4*>(hbuf) + 2 * c;
       const uint4 h0 = hp[0], h1 = hp[1];
-      const V8 gv = ld256_keep(static_cast<const uint16_t*>(a.gamma) + c * 16);
       const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
       V8 yv;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const float2 y = pmul(pmul(make_float2(bf_lo(hw[k]), bf_hi(hw[k])), dup2(inv)),
-                              make_float2(bf_lo(gv.w[k]), bf_hi(gv.w[k])));
+        const float2 y = pmul(make_float2(fma_bf_lo(hw[k], gw[k], -0.0f), fma_bf_hi(hw[k], gw[k], -0.0f)),
+                              dup2(inv));
         yv.w[k] = pack_bf2(y.x, y.y);
       }
       st256(static_cast<uint16_t*>(a.y) + (row * cpr + c) * 16, yv);
+    };
+#pragma unroll
+    for (int j = 0; j < kGammaRegChunks; ++j)
+      if (tid + j * nthr < cpr) out_chunk(tid + j * nthr, greg[j]);
+    for (int c = tid + kGammaRegChunks * nthr; c < cpr; c += nthr) {
+      const V8 gv = ld256_keep(static_cast<const uint16_t*>(a.gamma) + c * 16);
+      out_chunk(c, gv.w);
     }
   }
   if (!all_ok && tid == 0) {
