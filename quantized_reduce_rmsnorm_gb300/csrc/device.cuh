@@ -15,6 +15,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace fc {
 
 constexpr int kMaxP = 8;
@@ -367,7 +369,10 @@ __device__ __forceinline__ float warp_sum(float v) {
 //     s < 2^-100 take the IEEE division for every element (never seen on
 //     finite activations; it keeps denormal scales exact).
 constexpr float kMagicI8 = 12582912.0f;         // 1.5 * 2^23, bits 0x4B400000
-constexpr float kTieGuard = 0.5f - 1.0f / 8192;  // |e| below this: not near a half-integer
+// |n| >= 1/2 - 2^-13 (near a half-integer) <=> n*n - kNearSq >= 0; kNearSq =
+// (1/2 - 2^-13)^2 is exact in binary32 and fma(n, n, -kNearSq) has the sign
+// of the exact difference.
+constexpr float kNearSq = 0.24987794458866119384765625f;  // 2^-2 - 2^-13 + 2^-26
 constexpr float kTwoM24 = 5.9604644775390625e-08f;  // 2^-24
 constexpr float kTwoM100 = 7.888609052210118e-31f;  // 2^-100
 
@@ -382,20 +387,25 @@ __device__ __forceinline__ uint32_t low_bytes4(uint32_t a, uint32_t b, uint32_t 
 }
 
 // Exact code for an element whose fast-path value sits next to a half-integer
-// (step 3 above).  c: the fast-path integer, e = t - c, v the numerator.
+// (step 3 above).  c: the fast-path integer, e = v * r - c (up to rounding),
+// v the numerator.
 __device__ __forceinline__ float resolve_near_half(float v, float s, float c, float e) {
-  const float m = __fadd_rn(c, copysignf(0.5f, e));   // the half-integer next to t (exact)
+  const uint32_t sm = 0x80000000u;
+  // the half-integer next to v * r, on e's side of c (exact)
+  const float m = __fadd_rn(c, __uint_as_float(0x3F000000u | (__float_as_uint(e) & sm)));
   const float am = fabsf(m);
-  const float d = __fmaf_rn(-m, s, v);                // v - m*s, exact
+  const float d = __fmaf_rn(-m, s, v);  // v - m*s, exact
   const float hu = __fmul_rn(__fmul_rn(__uint_as_float(__float_as_uint(am) & 0x7F800000u), kTwoM24), s);
   const float hd = am == 0.5f ? __fmul_rn(hu, 0.5f) : hu;
-  const float dp = m > 0.0f ? d : -d;                 // > 0: |v/s| beyond |m|
-  const float away = __fadd_rn(m, copysignf(0.5f, m));
-  const float toward = __fadd_rn(m, -copysignf(0.5f, m));
-  if (dp > hu) return away;
-  if (dp < -hd) return toward;
-  // fl(v/s) == m: ties to the even integer
-  return (__float2int_rz(away) & 1) ? toward : away;
+  // > 0: |v/s| lies beyond |m| (d with the sign of m folded in)
+  const float dp = __uint_as_float(__float_as_uint(d) ^ (__float_as_uint(m) & sm));
+  const float half_m = __uint_as_float(0x3F000000u | (__float_as_uint(m) & sm));
+  const float away = __fadd_rn(m, half_m);
+  const float toward = __fsub_rn(m, half_m);
+  // fl(v/s) == m inside the band: ties to the even integer
+  const bool away_even = (__float_as_uint(__fadd_rn(away, kMagicI8)) & 1u) == 0u;
+  const float tie = away_even ? away : toward;
+  return dp > hu ? away : (dp < -hd ? toward : tie);
 }
 
 // Lane-local group statistics on the 16 bf16 inputs packed in w[8] with
@@ -447,72 +457,129 @@ __device__ __forceinline__ void minmax16(const float v[16], float& lo, float& hi
 }
 
 // Rounds the 16 quotients v[i] / s; ub[i] gets the bits of M + code (the
-// code in its low byte or nibble), qf[i] the code as a float.  group_ok:
+// code in its low byte or nibble; the code itself is M + code - M).  group_ok:
 // fl(vmax * r) is within the code range and s >= 2^-100 (else every element
 // takes the division); s == 0 is passed as r == 0 with group_ok set, which
 // yields codes 0.  Every lane of the warp must call this: the
 // near-half-integer pass is entered by warp vote and runs converged, one
 // vote per element index.
+// Near-half-integer and division elements are settled after the fast path:
+// round_codes returns a 16-bit mask of the lane's elements that need it (bit
+// 8b + w for element 4w + b: the sign bytes of four values gathered by byte
+// permutes), settle_codes ORs the masks over the warp and one uniform loop
+// visits only the element indices set in some lane, each with a single
+// shared copy of the exact code (steps 3 and 4).  pick(i) supplies the
+// lane's v_i, put(i, u) stores its exact code (u = bits of M + code).
 template <bool SIGNED>
-__device__ __forceinline__ void round_codes(const float v[16], float s, float r, bool group_ok,
-                                            uint32_t ub[16], float qf[16]) {
+__device__ __forceinline__ uint32_t round_codes(const float v[16], float r, bool group_ok,
+                                                uint32_t ub[16]) {
   const float magic = SIGNED ? kMagicI8 : 8388608.0f;
-  const float2 R = dup2(r), NR = dup2(-r), M = dup2(magic), NM = dup2(-magic);
-  float n[16];  // fl(code - v * r), kept for the near-half-integer pass
+  const float2 R = dup2(r), NR = dup2(-r), M = dup2(magic), NM = dup2(-magic), NQ = dup2(-kNearSq);
+  uint32_t notnear = 0;  // bit w of byte b: sign of fl(n^2 - kNearSq) for element 4w + b
 #pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    const float2 x = make_float2(v[i], v[i + 1]);
-    const float2 u = pfma(x, R, M);
-    const float2 c = padd(u, NM);
-    const float2 d = pfma(x, NR, c);
-    n[i] = d.x, n[i + 1] = d.y;
-    ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
-    qf[i] = c.x, qf[i + 1] = c.y;
-  }
-  const float nmax = absmax16(n);
-  if (__any_sync(kFull, group_ok && !(nmax < kTieGuard))) {
+  for (int w = 0; w < 4; ++w) {
+    uint32_t sgn[2];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const bool near = group_ok && !(fabsf(n[i]) < kTieGuard);
-      if (__any_sync(kFull, near)) {
-        const float res = resolve_near_half(v[i], s, qf[i], -n[i]);
-        if (near) {
-          qf[i] = res;
-          ub[i] = __float_as_uint(__fadd_rn(res, magic));
-        }
-      }
+    for (int h = 0; h < 2; ++h) {
+      const int i = 4 * w + 2 * h;
+      const float2 x = make_float2(v[i], v[i + 1]);
+      const float2 u = pfma(x, R, M);
+      const float2 n = pfma(x, NR, padd(u, NM));  // fl(code - v * r)
+      const float2 q = pfma(n, n, NQ);
+      ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
+      sgn[h] = __byte_perm(__float_as_uint(q.x), __float_as_uint(q.y), 0x0073u);
     }
+    notnear |= (__byte_perm(sgn[0], sgn[1], 0x5410u) >> (7 - w)) & (0x01010101u << w);
   }
-  if (!group_ok) {  // per lane; never taken on finite activations
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int c = SIGNED ? max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], s))))
-                           : max(0, min(15, __float2int_rn(__fdiv_rn(v[i], s))));
-      qf[i] = static_cast<float>(c);
-      ub[i] = __float_as_uint(__fadd_rn(qf[i], magic));
-    }
+  return group_ok ? (~notnear & 0x0F0F0F0Fu) : 0x0F0F0F0Fu;
+}
+
+template <bool SIGNED>
+__device__ __forceinline__ float exact_code(float v, float s, float c, float e, bool group_ok) {
+  if (group_ok) return resolve_near_half(v, s, c, e);
+  const float q = rintf(__fdiv_rn(v, s));  // the definition, for groups outside the fast path's bounds
+  return SIGNED ? fminf(127.0f, fmaxf(-127.0f, q)) : fminf(15.0f, fmaxf(0.0f, q));
+}
+
+template <bool SIGNED, class Pick, class Put>
+__device__ __forceinline__ void settle_codes(uint32_t mask, float s, float r, bool group_ok,
+                                             Pick pick, Put put) {
+  const float magic = SIGNED ? kMagicI8 : 8388608.0f;
+  uint32_t todo = __reduce_or_sync(kFull, mask);
+  while (todo) {  // warp-uniform
+    const int pos = __ffs(todo) - 1;
+    todo &= todo - 1;
+    const int i = 4 * (pos & 7) + (pos >> 3);
+    const float vi = pick(i);
+    const float ci = __fsub_rn(__fmaf_rn(vi, r, magic), magic);  // the fast path's code, recomputed
+    const float res = exact_code<SIGNED>(vi, s, ci, __fmaf_rn(vi, r, -ci), group_ok);
+    if ((mask >> pos) & 1u) put(i, __float_as_uint(__fadd_rn(res, magic)));
   }
 }
+
+// pick / put over the register arrays (a switch on the warp-uniform index)
+struct RegSettle {
+  const float* v;
+  uint32_t* ub;
+  __device__ __forceinline__ float operator()(int i) const {
+    switch (i) {
+#define FC_PICK(k) \
+  case k: return v[k];
+      FC_PICK(0) FC_PICK(1) FC_PICK(2) FC_PICK(3) FC_PICK(4) FC_PICK(5) FC_PICK(6) FC_PICK(7)
+      FC_PICK(8) FC_PICK(9) FC_PICK(10) FC_PICK(11) FC_PICK(12) FC_PICK(13) FC_PICK(14) FC_PICK(15)
+#undef FC_PICK
+    }
+    return 0.0f;
+  }
+  __device__ __forceinline__ void operator()(int i, uint32_t rb) const {
+    switch (i) {
+#define FC_PUT(k) \
+  case k: ub[k] = rb; break;
+      FC_PUT(0) FC_PUT(1) FC_PUT(2) FC_PUT(3) FC_PUT(4) FC_PUT(5) FC_PUT(6) FC_PUT(7)
+      FC_PUT(8) FC_PUT(9) FC_PUT(10) FC_PUT(11) FC_PUT(12) FC_PUT(13) FC_PUT(14) FC_PUT(15)
+#undef FC_PUT
+    }
+  }
+};
+
+// Without a reload source the exact pass works on the register arrays.  A
+// Reload functor instead returns element i's bf16 bits (low 16 bits) from
+// memory the caller still holds (the sender's staged tile), and the exact
+// codes are patched into the packed words.
+struct NoReload {
+  __device__ __forceinline__ uint32_t operator()(int) const { return 0u; }
+};
 
 // INT8 symmetric on this lane's 16 values of a group spread over lpg lanes:
 //   s = max|x| / 127;  q = clamp(rne(x / s), -127, 127);  s == 0 -> q = 0.
 // Writes the codes packed in q[4]; with DEQ also d[i] = q_i * s.  Returns s.
 // With BFW, the lane's max|x| is taken from the packed bf16 inputs bw[8].
-template <bool DEQ, bool BFW = false>
+template <bool DEQ, bool BFW = false, class Reload = NoReload>
 __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q[4], float d[16],
-                                          const uint32_t* bw = nullptr) {
+                                          const uint32_t* bw = nullptr, Reload reload = Reload()) {
   float a = BFW ? bf16_absmax16(bw) : absmax16(v);
   a = group_max(a, lpg);
   const float s = __fdiv_rn(a, 127.0f);
   uint32_t ub[16];  // low byte: the code
-  float qf[16];     // the code as a float
   const float r = s == 0.0f ? 0.0f : rcp_approx(s);
-  round_codes<true>(v, s, r, s == 0.0f || (__fmul_rn(a, r) <= 127.25f && s >= kTwoM100), ub, qf);
+  const bool ok = s == 0.0f || (__fmul_rn(a, r) <= 127.25f && s >= kTwoM100);
+  const uint32_t mask = round_codes<true>(v, r, ok, ub);
+  constexpr bool kReload = !std::is_same<Reload, NoReload>::value;
+  if (!kReload) settle_codes<true>(mask, s, r, ok, RegSettle{v, ub}, RegSettle{v, ub});
 #pragma unroll
   for (int j = 0; j < 4; ++j) q[j] = low_bytes4(ub[4 * j], ub[4 * j + 1], ub[4 * j + 2], ub[4 * j + 3]);
+  if (kReload)
+    settle_codes<true>(
+        mask, s, r, ok, [&](int i) { return __uint_as_float(reload(i) << 16); },
+        [&](int i, uint32_t rb) {
+          const int sh = 8 * (i & 3);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (k == (i >> 2)) q[k] = (q[k] & ~(0xFFu << sh)) | ((rb & 0xFFu) << sh);
+        });
   if (DEQ) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) d[i] = __fmul_rn(qf[i], s);
+    for (int i = 0; i < 16; ++i) d[i] = __fmul_rn(__fsub_rn(__uint_as_float(ub[i]), kMagicI8), s);
   }
   return s;
 }
@@ -522,9 +589,10 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
 // Element 2i in the low nibble of byte i.  Returns s, writes z; with DEQ also
 // d[i] = (q_i * s) + z.  With BFW, the lane's min and max come from the
 // packed bf16 inputs bw[8].
-template <bool DEQ, bool BFW = false>
+template <bool DEQ, bool BFW = false, class Reload = NoReload>
 __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q[2], float& z,
-                                          float d[16], const uint32_t* bw = nullptr) {
+                                          float d[16], const uint32_t* bw = nullptr,
+                                          Reload reload = Reload()) {
   float lo, hi;
   if (BFW)
     bf16_minmax16(bw, lo, hi);
@@ -538,7 +606,6 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
   const float s = __fdiv_rn(span, 15.0f);
   z = lo;
   uint32_t ub[16];
-  float qf[16];
   float num[16];  // fl(x - lo)
   if (BFW) {
 #pragma unroll
@@ -551,13 +618,25 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
     }
   }
   const float r = s == 0.0f ? 0.0f : rcp_approx(s);
-  round_codes<false>(num, s, r, s == 0.0f || (__fmul_rn(span, r) <= 15.25f && s >= kTwoM100), ub, qf);
+  const bool ok = s == 0.0f || (__fmul_rn(span, r) <= 15.25f && s >= kTwoM100);
+  const uint32_t mask = round_codes<false>(num, r, ok, ub);
+  constexpr bool kReload = !std::is_same<Reload, NoReload>::value;
+  if (!kReload) settle_codes<false>(mask, s, r, ok, RegSettle{num, ub}, RegSettle{num, ub});
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const uint32_t ev = low_bytes4(ub[8 * j], ub[8 * j + 2], ub[8 * j + 4], ub[8 * j + 6]);
     const uint32_t od = low_bytes4(ub[8 * j + 1], ub[8 * j + 3], ub[8 * j + 5], ub[8 * j + 7]);
     q[j] = ev | (od << 4);
   }
+  if (kReload)
+    settle_codes<false>(
+        mask, s, r, ok, [&](int i) { return add_bf_lo(reload(i), -lo); },
+        [&](int i, uint32_t rb) {
+          const int sh = 4 * (i & 7);
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            if (k == (i >> 3)) q[k] = (q[k] & ~(0xFu << sh)) | ((rb & 0xFu) << sh);
+        });
   if (DEQ) {  // d = fl(fl(q * s) + z); fl(q * s) = fma(2^23 + q, s, -2^23 * s) for s < 2^100
     if (s < 1.2676506e30f) {
       const float2 S = dup2(s), N = dup2(__fmul_rn(-kTwo23, s)), Z = dup2(z);
@@ -569,7 +648,8 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) d[i] = __fadd_rn(__fmul_rn(qf[i], s), z);
+      for (int i = 0; i < 16; ++i)
+        d[i] = __fadd_rn(__fmul_rn(__fsub_rn(__uint_as_float(ub[i]), kTwo23), s), z);
     }
   }
   return s;

@@ -218,9 +218,12 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int 
       for (int i = 0; i < 8; ++i) v[2 * i] = bf_lo(bw[i]), v[2 * i + 1] = bf_hi(bw[i]);
       const int64_t c = (e0 >> 4) + cl;  // global chunk of slab p
       float d[16];
+      // the exact pass re-reads an element's bf16 from the staged tile
+      const uint16_t* xs = reinterpret_cast<const uint16_t*>(tile) + 16 * cl;
+      auto reload = [xs](int i) { return static_cast<uint32_t>(xs[i]); };
       if (FMT == kINT8) {
         uint32_t q[4];
-        const float s = quant_i8<false, true>(v, lpg, q, d, bw);
+        const float s = quant_i8<false, true>(v, lpg, q, d, bw, reload);
         if (TAGGED) {
           // lpg == 8: lane = (group in warp) * 8 + k; stage the payload, then
           // one lane per block writes it (11 blocks per group, 44 per warp)
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int 
       } else {
         uint32_t q[2];
         float z;
-        const float s = quant_i4<false, true>(v, lpg, q, z, d, bw);
+        const float s = quant_i4<false, true>(v, lpg, q, z, d, bw, reload);
         if (TAGGED) {
           // lpg == 2: the even lane writes block 0 {its two code words, the odd
           // lane's first}, the odd lane block 1 {its second, scale, zero}
