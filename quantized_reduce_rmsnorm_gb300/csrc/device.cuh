@@ -517,6 +517,27 @@ __device__ __forceinline__ void settle_codes(uint32_t mask, float s, float r, bo
   }
 }
 
+// The same with each lane settling its own flagged elements in turn (the
+// index differs between lanes), for callers that can fetch any element by a
+// lane-varying index: the warp loops max-over-lanes times, not once per
+// distinct index.
+template <bool SIGNED, class Pick, class Put>
+__device__ __forceinline__ void settle_codes_lanewise(uint32_t mask, float s, float r, bool group_ok,
+                                                      Pick pick, Put put) {
+  const float magic = SIGNED ? kMagicI8 : 8388608.0f;
+  while (__any_sync(kFull, mask != 0u)) {
+    if (mask) {
+      const int pos = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const int i = 4 * (pos & 7) + (pos >> 3);
+      const float vi = pick(i);
+      const float ci = __fsub_rn(__fmaf_rn(vi, r, magic), magic);  // the fast path's code, recomputed
+      const float res = exact_code<SIGNED>(vi, s, ci, __fmaf_rn(vi, r, -ci), group_ok);
+      put(i, __float_as_uint(__fadd_rn(res, magic)));
+    }
+  }
+}
+
 // pick / put over the register arrays (a switch on the warp-uniform index)
 struct RegSettle {
   const float* v;
@@ -569,7 +590,7 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
 #pragma unroll
   for (int j = 0; j < 4; ++j) q[j] = low_bytes4(ub[4 * j], ub[4 * j + 1], ub[4 * j + 2], ub[4 * j + 3]);
   if (kReload)
-    settle_codes<true>(
+    settle_codes_lanewise<true>(
         mask, s, r, ok, [&](int i) { return __uint_as_float(reload(i) << 16); },
         [&](int i, uint32_t rb) {
           const int sh = 8 * (i & 3);
@@ -629,7 +650,7 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
     q[j] = ev | (od << 4);
   }
   if (kReload)
-    settle_codes<false>(
+    settle_codes_lanewise<false>(
         mask, s, r, ok, [&](int i) { return add_bf_lo(reload(i), -lo); },
         [&](int i, uint32_t rb) {
           const int sh = 4 * (i & 7);

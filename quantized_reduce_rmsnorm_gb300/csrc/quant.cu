@@ -129,7 +129,9 @@ constexpr int kQWarps = kThreads / 32;
 // job.epoch: every group's payload (INT8 g128: 128 code bytes + scale = 11
 // pieces of 12 bytes; INT4 g32: 16 code bytes + scale + zero = 2 pieces) in
 // words 0..2 of a 16-byte block, the epoch in word 3.
-template <int FMT, bool TAGGED = false>
+// LPG: lanes per group when known at compile time (the two standard group
+// sizes), 0 to take it from lpg_shift.
+template <int FMT, bool TAGGED = false, int LPG = 0>
 __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int lpg_shift,
                                                            int64_t tiles_per_slab) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int 
   // INT8 tagged: a warp assembles its 4 groups' payloads (33 words each) here
   __shared__ uint32_t qstage[TAGGED && FMT == kINT8 ? kQWarps : 1][4][33];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int lpg = 1 << lpg_shift;
+  const int lpg = LPG ? LPG : 1 << lpg_shift;
   const int64_t total = tiles_per_slab * job.P;
   const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kQWarps + wid;
   const int64_t wstride = static_cast<int64_t>(gridDim.x) * kQWarps;
@@ -443,10 +445,10 @@ int num_sms() {
   return sms[dev];
 }
 
-template <int FMT, bool TAGGED = false>
-cudaError_t launch_quantize_tma(const QuantJob& job, cudaStream_t st) {
+template <int FMT, bool TAGGED, int LPG>
+cudaError_t launch_quantize_tma_t(const QuantJob& job, cudaStream_t st) {
   const int smem = kQWarps * kWStages * kWTile * 2;
-  auto kern = k_quantize_tma<FMT, TAGGED>;
+  auto kern = k_quantize_tma<FMT, TAGGED, LPG>;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -465,6 +467,14 @@ cudaError_t launch_quantize_tma(const QuantJob& job, cudaStream_t st) {
   if (grid > need) grid = need;
   kern<<<static_cast<int>(grid), kThreads, smem, st>>>(job, log2_lanes(job.G), tps);
   return cudaGetLastError();
+}
+
+// INT8 g128 (8 lanes per group) and INT4 g32 (2 lanes) are specialised
+template <int FMT, bool TAGGED = false>
+cudaError_t launch_quantize_tma(const QuantJob& job, cudaStream_t st) {
+  constexpr int kStdLanes = FMT == kINT8 ? 8 : 2;
+  if (TAGGED || job.G == 16 * kStdLanes) return launch_quantize_tma_t<FMT, TAGGED, kStdLanes>(job, st);
+  return launch_quantize_tma_t<FMT, false, 0>(job, st);
 }
 
 bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
