@@ -376,6 +376,24 @@ constexpr float kNearSq = 0.24987794458866119384765625f;  // 2^-2 - 2^-13 + 2^-2
 constexpr float kTwoM24 = 5.9604644775390625e-08f;  // 2^-24
 constexpr float kTwoM100 = 7.888609052210118e-31f;  // 2^-100
 
+// fl(x / 15) and fl(x / 127) for the scales, without a division: with
+// zh = fl(1/y) and zl = fl(1/y - zh), q = fma(x, zh, fl(x * zl)) is the
+// correctly rounded quotient (the method of Brisebarre, Muller and Raina,
+// "Accelerating correctly rounded floating-point division when the divisor
+// is known in advance", IEEE Trans. Computers 53(8), 2004).  For y = 15 and
+// y = 127 this was checked against the IEEE quotient for every binary32
+// significand; the check scales to every x >= 2^-98 (quotient and x * zl
+// stay normal).  Smaller x take the division.
+constexpr uint32_t kInv15Hi = 0x3D888889u, kInv15Lo = 0xB16EEEEFu;
+constexpr uint32_t kInv127Hi = 0x3C010204u, kInv127Lo = 0x2E010204u;
+template <uint32_t HI, uint32_t LO>
+__device__ __forceinline__ float div_by_const(float x, float y) {
+  if (!(x >= __uint_as_float(0x0E800000u))) return __fdiv_rn(x, y);  // below 2^-98 (or 0)
+  return __fmaf_rn(x, __uint_as_float(HI), __fmul_rn(x, __uint_as_float(LO)));
+}
+__device__ __forceinline__ float div15(float x) { return div_by_const<kInv15Hi, kInv15Lo>(x, 15.0f); }
+__device__ __forceinline__ float div127(float x) { return div_by_const<kInv127Hi, kInv127Lo>(x, 127.0f); }
+
 __device__ __forceinline__ float rcp_approx(float x) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -580,7 +598,7 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
                                           const uint32_t* bw = nullptr, Reload reload = Reload()) {
   float a = BFW ? bf16_absmax16(bw) : absmax16(v);
   a = group_max(a, lpg);
-  const float s = __fdiv_rn(a, 127.0f);
+  const float s = div127(a);
   uint32_t ub[16];  // low byte: the code
   const float r = s == 0.0f ? 0.0f : rcp_approx(s);
   const bool ok = s == 0.0f || (__fmul_rn(a, r) <= 127.25f && s >= kTwoM100);
@@ -624,7 +642,7 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
   if (lo == 0.0f) lo = 0.0f;  // -0 -> +0
   if (hi == 0.0f) hi = 0.0f;
   const float span = __fsub_rn(hi, lo);
-  const float s = __fdiv_rn(span, 15.0f);
+  const float s = div15(span);
   z = lo;
   uint32_t ub[16];
   float num[16];  // fl(x - lo)
