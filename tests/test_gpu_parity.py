@@ -337,6 +337,9 @@ TMA_CASES = [
     ("i4-ragged-h", {"P": 3, "T": 13, "H": 4224, "fmt": I4, "group": 32}),  # 132 groups/row
     ("i8-cpr-not-warp-multiple", {"P": 2, "T": 7, "H": 1152, "fmt": I8, "group": 32}),
     ("i4-wide-h", {"P": 2, "T": 5, "H": 16384, "fmt": I4, "group": 32}),
+    # short rows, many per CTA at max_ctas 1 and 3
+    ("i4-short-rows", {"P": 2, "T": 37, "H": 4096, "fmt": I4, "group": 32}),
+    ("i8-short-rows", {"P": 2, "T": 29, "H": 2048, "fmt": I8, "group": 128}),
 ]
 
 
