@@ -22,8 +22,7 @@ namespace fc {
 
 namespace {
 
-constexpr int kTmaThreads = 256;     // per CTA when two or more CTAs fit an SM
-constexpr int kTmaThreadsMax = 512;  // when only one does
+constexpr int kTmaThreadsMax = 512;  // threads per CTA at most
 constexpr int kGammaRegChunks = 2;   // gamma chunks a thread keeps in registers
 
 struct TmaGeom {
@@ -301,41 +300,73 @@ int geometry(int fmt, const FusedArgs& a, TmaGeom& g) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Launch shape of one instantiation: threads per CTA and resident CTAs per SM.
+struct TmaShape {
+  int nstage = 0, threads = 0, occ = 0, smem = 0;
+};
+
+// Threads per CTA, from the work a thread does per row and barrier (measured
+// on GB300 across the message-size sweep): where a chunk carries little
+// arithmetic (INT4, INT8 with up to four slabs) two 16-element chunks per
+// thread and row; where it carries more (INT8 with more slabs) or the row is
+// plain bf16, up to 256 threads, i.e. one chunk per thread for rows up to
+// 4096 elements.
+int tma_threads(int fmt, int P, int H) {
+  const int cpr = H >> 4;
+  const bool heavy = fmt == kBF16 || ((fmt == kINT8 || fmt == kINT8T) && P > 4);
+  int t = heavy ? (cpr < 256 ? cpr : 256) : (cpr + 1) / 2;
+  t = (t + 31) & ~31;
+  return t < 32 ? 32 : (t > kTmaThreadsMax ? kTmaThreadsMax : t);
+}
+
 template <int FMT, int NSTAGE, int PMAX>
-cudaError_t launch_tma_t(const FusedArgs& a, const TmaGeom& g, int smem, int max_ctas,
-                         cudaStream_t st) {
+TmaShape shape_t(const FusedArgs& a, const TmaGeom& g) {
+  TmaShape sh;
+  sh.nstage = NSTAGE;
+  sh.smem = g.stage_off + NSTAGE * g.stage_bytes;
+  if (sh.smem > kTmaSmemLimit) return sh;
   auto kern = k_fused_tma<FMT, NSTAGE, PMAX>;
   static int configured_smem[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   dev = dev < 64 ? dev : 63;
-  if (configured_smem[dev] < smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured_smem[dev] = smem;
+  if (configured_smem[dev] < sh.smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sh.smem) != cudaSuccess)
+      return sh;
+    configured_smem[dev] = sh.smem;
   }
-  const int cpr = a.H >> 4;
-  int threads = cpr < kTmaThreads ? ((cpr + 31) & ~31) : kTmaThreads;
-  int occ = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
-  if (occ == 1 && cpr >= kTmaThreadsMax) {
-    // shared memory admits a single CTA per SM: give it more warps instead
-    threads = kTmaThreadsMax;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
-  }
-  if (occ < 1) return cudaErrorInvalidConfiguration;
-  int64_t grid = static_cast<int64_t>(num_sms()) * occ;
-  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
-  if (grid > a.rows) grid = a.rows;
-  kern<<<static_cast<int>(grid), threads, smem, st>>>(a, g);
-  return cudaGetLastError();
+  sh.threads = tma_threads(FMT, a.P, a.H);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.occ, kern, sh.threads, sh.smem) != cudaSuccess)
+    sh.occ = 0;
+  return sh;
+}
+
+// A two-row ring (the next row streams in while this one is computed).  For
+// the quantized formats, when that ring leaves room for a single CTA per SM,
+// two single-stage CTAs (which overlap each other's copies and row
+// barriers) were measured faster; for bf16 rows the two-row ring stays.
+template <int FMT, int PMAX>
+TmaShape choose_shape(const FusedArgs& a, const TmaGeom& g) {
+  const TmaShape two = shape_t<FMT, 2, PMAX>(a, g);
+  if (FMT == kBF16 && two.occ >= 1) return two;
+  const TmaShape one = shape_t<FMT, 1, PMAX>(a, g);
+  if (two.occ >= 1 && (two.occ >= 2 || one.occ <= two.occ)) return two;
+  return one;
 }
 
 template <int FMT, int PMAX>
 cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cudaStream_t st) {
-  const int two = g.stage_off + 2 * g.stage_bytes, one = g.stage_off + g.stage_bytes;
-  if (two <= kTmaSmemLimit) return launch_tma_t<FMT, 2, PMAX>(a, g, two, max_ctas, st);
-  return launch_tma_t<FMT, 1, PMAX>(a, g, one, max_ctas, st);
+  const TmaShape sh = choose_shape<FMT, PMAX>(a, g);
+  if (sh.occ < 1) return cudaErrorInvalidConfiguration;
+  int64_t grid = static_cast<int64_t>(num_sms()) * sh.occ;
+  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+  if (grid > a.rows) grid = a.rows;
+  const dim3 gr(static_cast<unsigned>(grid));
+  if (sh.nstage == 2)
+    k_fused_tma<FMT, 2, PMAX><<<gr, sh.threads, sh.smem, st>>>(a, g);
+  else
+    k_fused_tma<FMT, 1, PMAX><<<gr, sh.threads, sh.smem, st>>>(a, g);
+  return cudaGetLastError();
 }
 
 // The slab loop is unrolled to PMAX (2, 4 or 8) slots, so no instruction is
@@ -362,26 +393,12 @@ bool fused_tma_eligible(int fmt, const FusedArgs& a) {
   return aligned16(a.res_in) && aligned16(a.gamma);
 }
 
-template <int FMT, int NSTAGE, int PMAX>
-int64_t wave_t(const FusedArgs& a, const TmaGeom& g, int smem) {
-  auto kern = k_fused_tma<FMT, NSTAGE, PMAX>;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  const int cpr = a.H >> 4;
-  int threads = cpr < kTmaThreads ? ((cpr + 31) & ~31) : kTmaThreads;
-  int occ = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
-  if (occ == 1 && cpr >= kTmaThreadsMax)
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kTmaThreadsMax, smem);
-  return static_cast<int64_t>(num_sms()) * (occ > 0 ? occ : 1);  // a CTA per row
-}
-
 template <int FMT>
 int64_t wave_fmt(const FusedArgs& a, const TmaGeom& g) {
-  const int two = g.stage_off + 2 * g.stage_bytes, one = g.stage_off + g.stage_bytes;
-  const bool s2 = two <= kTmaSmemLimit;
-  if (a.P <= 2) return s2 ? wave_t<FMT, 2, 2>(a, g, two) : wave_t<FMT, 1, 2>(a, g, one);
-  if (a.P <= 4) return s2 ? wave_t<FMT, 2, 4>(a, g, two) : wave_t<FMT, 1, 4>(a, g, one);
-  return s2 ? wave_t<FMT, 2, 8>(a, g, two) : wave_t<FMT, 1, 8>(a, g, one);
+  const TmaShape sh = a.P <= 2 ? choose_shape<FMT, 2>(a, g)
+                      : a.P <= 4 ? choose_shape<FMT, 4>(a, g)
+                                 : choose_shape<FMT, 8>(a, g);
+  return static_cast<int64_t>(num_sms()) * (sh.occ > 0 ? sh.occ : 1);  // a CTA per row
 }
 
 int64_t fused_tma_wave_rows(int fmt, const FusedArgs& a) {
