@@ -64,6 +64,7 @@ def _signatures():
         "or_dequant_i4a": (None, [P, P, P, i64, i32, P]),
         "or_reduce_sum": (None, [P, i32, i64, P]),
         "or_two_step": (i32, [i32, P, P, P, i32, i64, i32, i32, P, P, P, P, P]),
+        "or_allgather_dequant": (i32, [i32, P, P, P, i32, i64, i32, P]),
         "or_residual_rmsnorm": (None, [P, P, P, i64, i64, f32, P, P]),
         "or_tagged_blocks_per_row": (i64, [i64]),
         "or_pack_tagged": (None, [P, i64, i64, u32, P]),
@@ -203,6 +204,24 @@ class Oracle:
             raise ValueError("or_two_step rejected its arguments")
         return dict(reduced=red, codes=rq, scales=rs,
                     zeros=rz if fmt == FMT_INT4_ASYM else None, gathered=gath)
+
+    def allgather_dequant(self, fmt, shards, n, G):
+        """Standalone all-gather: shards = [(codes, scales, zeros), ...], shard j
+        holding groups [j*per, min((j+1)*per, n_g)) from its own index 0.
+        Returns the n dequantized fp32 values of the whole tensor."""
+        P = len(shards)
+        cdt = np.int8 if fmt == FMT_INT8_SYM else np.uint8
+        keep = []
+        for c, s_, z in shards:
+            keep.append((_c(c, cdt).ravel() if c is not None else np.zeros(1, cdt),
+                         _c(s_, np.float32) if s_ is not None else np.zeros(1, np.float32),
+                         _c(z, np.float32) if z is not None else np.zeros(1, np.float32)))
+        out = np.empty(n, np.float32)
+        rc = self.lib.or_allgather_dequant(fmt, _ptrs([k[0] for k in keep]), _ptrs([k[1] for k in keep]),
+                                           _ptrs([k[2] for k in keep]), P, n, G, _p(out))
+        if rc != 0:
+            raise ValueError("or_allgather_dequant rejected its arguments")
+        return out
 
     # ---------------------------------------------------- residual, norm ---
     def residual_rmsnorm(self, o, r_bf16, gamma_bf16, T, H, eps=1e-5):

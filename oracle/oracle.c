@@ -210,6 +210,30 @@ int or_two_step(int fmt, const void* const* codes, const float* const* scales,
   return 0;
 }
 
+/* ------------------------------------------------- standalone all-gather -- */
+/* [FL] abstract (the all-gather collective) and [FC] "Core ideas" (its
+ * second step): each of P ranks holds the quantized payload of one shard --
+ * the contiguous groups [j*per, min((j+1)*per, n_g)), per = ceil(n_g/P), the
+ * same partition as the reduce-scatter -- indexed from the shard's own first
+ * group.  Every rank receives all shards and dequantizes them. */
+int or_allgather_dequant(int fmt, const void* const* codes, const float* const* scales,
+                         const float* const* zeros, int P, int64_t n, int G, float* out) {
+  if (fmt != OR_FMT_INT8_SYM && fmt != OR_FMT_INT4_ASYM) return -1;
+  if (P < 1 || G < 1 || n < 0 || n % G != 0) return -1;
+  if (fmt == OR_FMT_INT4_ASYM && (G % 2) != 0) return -1;
+  int64_t ng = n / G;
+  int64_t per = (ng + P - 1) / P;
+  for (int j = 0; j < P; ++j) {
+    int64_t g0 = (int64_t)j * per, g1 = g0 + per;
+    if (g1 > ng) g1 = ng;
+    if (g0 >= g1) continue; /* an empty shard */
+    int64_t local_n = (g1 - g0) * G;
+    for (int64_t e = 0; e < local_n; ++e)
+      out[g0 * G + e] = deq_one(fmt, codes[j], scales[j], zeros ? zeros[j] : NULL, e, G);
+  }
+  return 0;
+}
+
 /* ------------------------------------------------ residual add, RMSNorm -- */
 /* [TW] abstract: the RMSNorm that follows each tensor-parallel All-Reduce is
  * fused into it.  h = bf16(o + R) is the new residual stream (the sum is the

@@ -67,6 +67,14 @@ int or_two_step(int fmt, const void* const* codes, const float* const* scales,
                 float* reduced, void* rq_codes, float* rq_scales, float* rq_zeros,
                 float* gathered);
 
+/* Standalone all-gather: shard j (of P) holds the payload of groups
+ * [j*per, min((j+1)*per, n_g)), per = ceil(n_g/P), indexed from its own first
+ * group (codes[j], scales[j], zeros[j]; zeros may be NULL for INT8).  out gets
+ * the n dequantized values of the whole tensor.  Returns 0, or -1 on a bad
+ * argument. */
+int or_allgather_dequant(int fmt, const void* const* codes, const float* const* scales,
+                         const float* const* zeros, int P, int64_t n, int G, float* out);
+
 /* Residual add and RMSNorm over T rows of H: h = bf16(o + R) (fp32 add),
  * y = bf16(h / sqrt(mean(h^2) + eps) * gamma) (binary64). */
 void or_residual_rmsnorm(const float* o, const uint16_t* r, const uint16_t* gamma, int64_t T,

@@ -271,6 +271,52 @@ def check_two_step_equals_direct(orc):
             assert n == direct["reduced"].size
 
 
+def check_allgather_golden(orc):
+    g = load_golden("allgather_tiny.txt")
+    for fmt, pre, cdt in ((FMT_INT8_SYM, "i8", np.int8), (FMT_INT4_ASYM, "i4", np.uint8)):
+        G, P = int(g[pre + "_G"][0]), int(g[pre + "_P"][0])
+        shards = []
+        for j in range(P):
+            c = np.array([int(v) for v in g[f"{pre}_shard{j}_codes"]], np.int64).astype(cdt)
+            sc = np.array(g[f"{pre}_shard{j}_scales"], np.float32)
+            z = np.array(g[f"{pre}_shard{j}_zeros"], np.float32) if fmt == FMT_INT4_ASYM else None
+            shards.append((c, sc, z))
+        want = np.array(g[pre + "_out"], np.float32)
+        got = orc.allgather_dequant(fmt, shards, want.size, G)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def check_allgather_equals_dequant_of_slices(orc):
+    """Gathering the shard slices of a payload dequantizes the whole payload,
+    for every shard count (incl. more shards than groups, i.e. empty shards),
+    and gathering the shards of the two-step reduce's requantized payload gives
+    its gathered result."""
+    rng = np.random.default_rng(29)
+    for fmt, G in ((FMT_INT8_SYM, 128), (FMT_INT4_ASYM, 32), (FMT_INT4_ASYM, 16)):
+        ng = 37
+        x = bf16_bits_to_float(_groups(rng, ng, G))
+        q, s, z = orc.quantize(fmt, x, G)
+        cb = G if fmt == FMT_INT8_SYM else G // 2
+        whole = orc.dequantize(fmt, q, s, z, G)
+        for P in (1, 2, 3, 5, 8, 40):
+            per = -(-ng // P)
+            shards = []
+            for j in range(P):
+                g0, g1 = min(j * per, ng), min((j + 1) * per, ng)
+                shards.append((q[g0 * cb:g1 * cb], s[g0:g1], None if z is None else z[g0:g1]))
+            got = orc.allgather_dequant(fmt, shards, x.size, G)
+            assert np.array_equal(got.view(np.uint32), whole.view(np.uint32)), (fmt, G, P)
+        slabs = [orc.quantize(fmt, bf16_bits_to_float(_groups(rng, ng, G)), G) for _ in range(3)]
+        two = orc.two_step(fmt, slabs, G, shards=3)
+        per = -(-ng // 3)
+        shards = [(two["codes"][j * per * cb:min((j + 1) * per, ng) * cb],
+                   two["scales"][j * per:min((j + 1) * per, ng)],
+                   None if two["zeros"] is None else two["zeros"][j * per:min((j + 1) * per, ng)])
+                  for j in range(3)]
+        got = orc.allgather_dequant(fmt, shards, x.size, G)
+        assert np.array_equal(got.view(np.uint32), two["gathered"].view(np.uint32))
+
+
 # ------------------------------------------------------ residual, norm ----
 def check_residual_add(orc):
     """h = bf16(o + R) equals torch's fp32 add and bf16 conversion."""

@@ -34,6 +34,9 @@ MUTANTS = [
      "if (blocks[4 * b + 3] == epoch) return b;"),
     ("qtagged-scale-before-codes", "memcpy(payload + cb, &scales[g], 4);",
      "memcpy(payload, &scales[g], 4);"),
+    ("gather-forgets-shard-offset", "out[g0 * G + e] = deq_one(", "out[e] = deq_one("),
+    ("gather-shard-size-floor", "int64_t per = (ng + P - 1) / P;\n  for (int j = 0; j < P; ++j) {\n    int64_t g0 = (int64_t)j * per, g1 = g0 + per;\n    if (g1 > ng) g1 = ng;\n    if (g0 >= g1) continue; /* an empty shard */",
+     "int64_t per = ng / P ? ng / P : 1;\n  for (int j = 0; j < P; ++j) {\n    int64_t g0 = (int64_t)j * per, g1 = g0 + per;\n    if (g1 > ng) g1 = ng;\n    if (g0 >= g1) continue; /* an empty shard */"),
 ]
 
 
