@@ -54,6 +54,8 @@ def parse():
                     help="token-subset boundary for workloads that split rows")
     ap.add_argument("--overlap", action="store_true",
                     help="SM-capped fused kernel beside a GEMM on another stream (one JSON line per cap)")
+    ap.add_argument("--gather", action="store_true",
+                    help="standalone quantized all-gather (shards -> whole dequantized tensor): one JSON line per case")
     ap.add_argument("--sweep", choices=["quick", "full"], default=None,
                     help="message-size sweep (16 KB..256 MB x P x format): one JSON line per point")
     return ap.parse_args()
@@ -487,6 +489,55 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_gather(args):
+    """The standalone quantized all-gather (fc_allgather_dequant): P shard
+    payloads of a prefill-sized and a decode-sized tensor (quantized on the
+    device from seeded N(0,1) bf16), gathered and dequantized to bf16 and to
+    fp32; CUDA events, median of the repetitions, a 256 MB L2 scrub before
+    each repetition when the point fits in L2."""
+    import torch
+    from quantized_reduce_rmsnorm_gb300 import fcomm, synth
+    fcomm.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, kind = peaks()
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    gen = torch.Generator(device=dev)
+    for name, T, H, P, spec in (("prefill", 8192, 8192, 4, fcomm.INT4_G32),
+                                ("prefill", 8192, 8192, 4, fcomm.INT8_G128),
+                                ("decode", 64, 8192, 8, fcomm.INT8_G128)):
+        gen.manual_seed(T ^ P)
+        x = torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16)
+        whole = fcomm.alloc_qtensor(spec, T, H, dev)
+        fcomm.group_quantize(x, spec, whole)
+        shards = fcomm.shard_views(whole, spec, T, H, P)
+        E = T * H
+        qs = fcomm.codes_bytes(spec, T, H) + fcomm.groups(spec, T, H) * (8 if spec.fmt == fcomm.FMT_INT4_ASYM else 4)
+        for odt, osz in ((torch.bfloat16, 2), (torch.float32, 4)):
+            out = torch.empty(T, H, dtype=odt, device=dev)
+            small = qs + osz * E < 2 * L2_BYTES
+            times = []
+            for i in range(max(args.steps, 5) + 3):
+                if small:
+                    flush.add_(1.0)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fcomm.allgather_dequant(shards, spec, T, H, out)
+                b.record()
+                b.synchronize()
+                if i >= 3:
+                    times.append(a.elapsed_time(b) * 1e3)
+            us = statistics.median(times)
+            alg = qs + osz * E
+            print(json.dumps({"gather": True, "workload": name, "rows": T, "hidden": H, "P": P,
+                              "format": synth.FMT_NAMES[spec.fmt], "out": str(odt).split(".")[-1],
+                              "us": round(us, 2), "alg_bytes": alg, "GB/s": round(alg / us / 1e3, 1),
+                              "frac": round(alg / us / 1e3 / peak, 4), "peak_kind": kind,
+                              "l2_scrubbed": small}), flush=True)
+        del x, whole, shards, out
+        torch.cuda.empty_cache()
+
+
 def run_overlap(args):
     """The fused reduce + residual + RMSNorm with its grid capped at max_ctas
     CTAs (one per SM), alone and concurrently with a bf16 GEMM standing in for
@@ -564,6 +615,9 @@ def run_overlap(args):
 
 def main():
     args = parse()
+    if args.gather:
+        run_gather(args)
+        return
     if args.overlap:
         run_overlap(args)
         return

@@ -229,6 +229,29 @@ fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64
                                            void* y, uint32_t expected_epoch, int32_t* d_status,
                                            const fc_launch_opts* opts, fc_stream_t stream);
 
+/* Standalone quantized all-gather (flash-comm, abstract: the all-gather
+ * collective; Flash Communication, "Core ideas": the second step of the
+ * two-step All-Reduce, in which every rank receives all requantized shards
+ * and dequantizes them).  Shard p (of P, 1..8) holds the payload of the
+ * contiguous groups [p*per, min((p+1)*per, n_g)), per = ceil(n_g/P) -- the
+ * partition of fc_shard_range -- indexed from its own first group: for
+ * FC_FMT_INT8_SYM / FC_FMT_INT4_ASYM, shards[p] = {codes, scales, zeros}
+ * (codes 16-byte aligned for INT8, 8-byte for INT4; scales and zeros 4-byte);
+ * for FC_FMT_INT8_TAGGED / FC_FMT_INT4_TAGGED, shards[p].codes is its
+ * epoch-tagged blocks (16-byte aligned; fc_group_quantize_tagged's layout) and
+ * every block is checked against expected_epoch before use.  An empty shard
+ * (p*per >= n_g) may have NULL buffers.  out: the whole [rows, hidden] tensor,
+ * out_dtype FC_FMT_BF16 (round to nearest even) or FC_FMT_F32, 32-byte
+ * aligned; element e = dequant of e's code (INT8: q*s; INT4: q*s + z, two
+ * roundings).  d_status (optional, two int32 words, reset by the call):
+ * {FC_OK, 0x7F7F7F7F}, or {FC_ERR_STALE_BLOCK, first stale block index}
+ * counting shard 0's blocks, then shard 1's, ...; the outputs of a group
+ * with a stale block are unspecified (the chunks read from it are not
+ * written), every other group's are exact. */
+fc_status fc_allgather_dequant(const fc_qtensor* shards, int P, int64_t rows, int64_t hidden,
+                               fc_qspec spec, int32_t out_dtype, void* out, uint32_t expected_epoch,
+                               int32_t* d_status, fc_stream_t stream);
+
 /* Wave-aware token split (TokenWeave, abstract: the batch's tokens are
  * divided into two approximately equal subsets in a wave-aware manner; the
  * work of one overlaps the other's).  A "wave" is the number of rows the

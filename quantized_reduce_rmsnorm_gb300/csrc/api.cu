@@ -6,6 +6,8 @@
 #include <cstdio>
 #include <cstring>
 
+#include <algorithm>
+
 #include "fcomm.h"
 #include "internal.h"
 
@@ -257,6 +259,61 @@ fc_status fc_requant_gather(const float* reduced_f32, int64_t rows, int64_t hidd
   job.G = spec.group;
   return cuda_status(fc::launch_quantize(spec.fmt, true, deq, job, (cudaStream_t)stream),
                      "fc_requant_gather launch");
+}
+
+fc_status fc_allgather_dequant(const fc_qtensor* shards, int P, int64_t rows, int64_t hidden,
+                               fc_qspec spec, int32_t out_dtype, void* out, uint32_t expected_epoch,
+                               int32_t* d_status, fc_stream_t stream) {
+  if (fc_status s = check_shape(spec, rows, hidden, false)) return s;
+  if (!quantized(spec.fmt) && !qtagged(spec.fmt))
+    return fail(FC_ERR_INVALID, "format %d is not a quantized format", spec.fmt);
+  if (P < 1 || P > 8) return fail(FC_ERR_INVALID, "P must be in [1, 8] (got %d)", P);
+  if (out_dtype != FC_FMT_BF16 && out_dtype != FC_FMT_F32)
+    return fail(FC_ERR_INVALID, "out_dtype must be FC_FMT_BF16 or FC_FMT_F32");
+  if (rows == 0) return ok();
+  if (!shards) return fail(FC_ERR_INVALID, "shards must not be NULL");
+  if (fc_status s = check_ptr(out, 32, "out")) return s;
+  if (d_status && !aligned(d_status, 4)) return fail(FC_ERR_INVALID, "d_status must be 4-byte aligned");
+  const bool tagged = qtagged(spec.fmt);
+  const int G = spec.group, lpg = G / 16;
+  const int nbg = spec.fmt == FC_FMT_INT8_TAGGED ? fc::kBlocksPerGroupI8 : fc::kBlocksPerGroupI4;
+  const int64_t ng = rows * hidden / G, per = (ng + P - 1) / P;
+  fc::GatherJob j{};
+  int64_t blk = 0;
+  for (int p = 0; p < P; ++p) {
+    const int64_t g0 = std::min<int64_t>(p * per, ng), g1 = std::min<int64_t>(g0 + per, ng);
+    j.first[p] = g0 * lpg;
+    j.blk0[p] = blk;
+    if (g1 > g0) {  // an empty shard needs no buffers
+      const size_t calign = tagged || spec.fmt == FC_FMT_INT8_SYM ? 16 : 8;
+      if (fc_status s = check_ptr(shards[p].codes, calign, "shards[p].codes")) return s;
+      if (!tagged) {
+        if (fc_status s = check_ptr(shards[p].scales, 4, "shards[p].scales")) return s;
+        if (spec.fmt == FC_FMT_INT4_ASYM)
+          if (fc_status s = check_ptr(shards[p].zeros, 4, "shards[p].zeros")) return s;
+      }
+      if (tagged) blk += (g1 - g0) * nbg;
+    }
+    j.codes[p] = shards[p].codes;
+    j.scales[p] = shards[p].scales;
+    j.zeros[p] = shards[p].zeros;
+  }
+  j.first[P] = ng * lpg;
+  j.chunks = ng * lpg;
+  j.P = P;
+  j.lpg_shift = 0;
+  while ((1 << j.lpg_shift) < lpg) ++j.lpg_shift;
+  j.out = out;
+  j.epoch = expected_epoch;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (d_status) {
+    j.status = d_status;
+    cudaError_t e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_status + 1, 0x7F, sizeof(int32_t), st);
+    if (e != cudaSuccess) return cuda_status(e, "d_status reset");
+  }
+  return cuda_status(fc::launch_allgather(spec.fmt, out_dtype == FC_FMT_F32, j, st),
+                     "fc_allgather_dequant launch");
 }
 
 fc_status fc_pack_tagged_multi(const void* const* x_bf16, int P, int64_t rows, int64_t hidden,

@@ -78,6 +78,24 @@ cudaError_t launch_quantize(int fmt, bool in_f32, int deq_kind, const QuantJob& 
 // (fmt kINT8T / kINT4T; job.codes[p] are the block arrays).
 cudaError_t launch_quantize_tagged(int fmt, const QuantJob& job, cudaStream_t st);
 // Sum of dequantized slabs over the 16-element chunks [c0, c1).
+// Standalone all-gather: shard p holds chunks [first[p], first[p+1]) of the
+// whole tensor (16-element chunks), indexed from its own chunk 0; for the
+// tagged formats codes[p] are its blocks and blk0[p] the global index of its
+// first block (for stale reports).
+struct GatherJob {
+  const void* codes[8];
+  const float* scales[8];
+  const float* zeros[8];
+  int64_t first[9];
+  int64_t blk0[8];
+  void* out;
+  int32_t* status;
+  int64_t chunks;
+  int P, lpg_shift;
+  uint32_t epoch;
+};
+cudaError_t launch_allgather(int fmt, bool out_f32, const GatherJob& j, cudaStream_t st);
+
 cudaError_t launch_reduce(int fmt, const Slabs& s, int P, int G, int64_t c0, int64_t c1,
                           float* out, cudaStream_t st);
 cudaError_t launch_pack_tagged(const void* const* x, void* const* blocks, int P, int64_t rows,

@@ -27,7 +27,7 @@ EXPORTS = (
     "fc_group_quantize_multi", "fc_reduce_dequant_sum", "fc_requant_gather", "fc_pack_tagged",
     "fc_pack_tagged_multi", "fc_group_quantize_tagged",
     "fc_allreduce_residual_rmsnorm", "fc_allreduce_residual_rmsnorm_ex", "fc_status_string",
-    "fc_last_error", "fc_version", "fc_token_split", "fc_select_protocol",
+    "fc_last_error", "fc_version", "fc_token_split", "fc_select_protocol", "fc_allgather_dequant",
 )
 
 
@@ -98,6 +98,7 @@ def load(path: Optional[str] = None):
         "fc_group_quantize_multi": (i32, [P, i32, i64, i64, QS, P, P]),
         "fc_reduce_dequant_sum": (i32, [P, i32, i64, i64, QS, i32, P, P]),
         "fc_requant_gather": (i32, [P, i64, i64, QS, QT, P, i32, P]),
+        "fc_allgather_dequant": (i32, [ctypes.POINTER(QT), i32, i64, i64, QS, i32, P, u32, P, P]),
         "fc_pack_tagged": (i32, [P, i64, i64, u32, P, P]),
         "fc_pack_tagged_multi": (i32, [P, i32, i64, i64, u32, P, P]),
         "fc_group_quantize_tagged": (i32, [P, i32, i64, i64, QS, u32, P, P]),
@@ -214,6 +215,41 @@ def requant_gather(reduced: torch.Tensor, spec: QSpec, requant_out=None,
     rows, hidden = _rows_hidden(reduced)
     _check(load().fc_requant_gather(_ptr(reduced), rows, hidden, spec, _qt(requant_out),
                                     _ptr(out), out_dtype, _stream(stream)))
+
+
+def allgather_dequant(shards, spec: QSpec, rows: int, hidden: int, out: torch.Tensor,
+                      expected_epoch: int = 0, d_status: Optional[torch.Tensor] = None,
+                      stream=None):
+    """Standalone quantized all-gather: shards = P (codes, scales, zeros) tuples
+    (or tagged-block tensors), shard p holding groups [p*per, min((p+1)*per,
+    n_g)) from its own index 0; out = the whole dequantized [rows, hidden]
+    tensor (bf16 or fp32, by its dtype)."""
+    qs = (QTensor * len(shards))(*[_qt(s if isinstance(s, (tuple, list)) else (s,))
+                                   for s in shards])
+    od = FMT_F32 if out.dtype == torch.float32 else FMT_BF16
+    _check(load().fc_allgather_dequant(qs, len(shards), rows, hidden, spec, od, _ptr(out),
+                                       expected_epoch, _ptr(d_status), _stream(stream)))
+
+
+def shard_views(q, spec: QSpec, rows: int, hidden: int, P: int):
+    """The P shard payloads (views, no copy) of a whole payload q = (codes,
+    scales, zeros) or tagged blocks, in the partition fc_allgather_dequant reads."""
+    ng = groups(spec, rows, hidden)
+    per = -(-ng // P)
+    if spec.fmt in (FMT_INT8_TAGGED, FMT_INT4_TAGGED):
+        nbg = 11 if spec.fmt == FMT_INT8_TAGGED else 2
+        b = q if isinstance(q, torch.Tensor) else q[0]
+        return [b[min(j * per, ng) * nbg * 16:min((j + 1) * per, ng) * nbg * 16] for j in range(P)]
+    cb = spec.group if spec.fmt == FMT_INT8_SYM else spec.group // 2
+    codes, scales, zeros = (tuple(q) + (None, None, None))[:3]
+    out = []
+    for j in range(P):
+        g0, g1 = min(j * per, ng), min((j + 1) * per, ng)
+        if g1 <= g0:
+            out.append((None, None, None))
+            continue
+        out.append((codes[g0 * cb:g1 * cb], scales[g0:g1], None if zeros is None else zeros[g0:g1]))
+    return out
 
 
 def pack_tagged(x: torch.Tensor, epoch: int, blocks: torch.Tensor, stream=None):

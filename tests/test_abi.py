@@ -152,3 +152,25 @@ def test_protocol_selector_trades_barriers_against_bytes():
             assert width >= bits
     with pytest.raises(fc.FcommError):
         fc.select_protocol(1, 4096, 8, 3)
+
+
+def test_allgather_rejects_bad_arguments():
+    lib = fc.fcomm.load()
+    shards = (fc.QTensor * 8)(*[fc.QTensor(64, 128, 256)] * 8)
+    for P in (0, 9):
+        assert lib.fc_allgather_dequant(shards, P, 4, 4096, fc.INT8_G128, 0, 64, 0, None,
+                                        None) == fc.FC_ERR_INVALID
+    # bf16 is not a quantized payload; out_dtype must be bf16 or f32
+    assert lib.fc_allgather_dequant(shards, 2, 4, 4096, fc.BF16, 0, 64, 0, None, None) == \
+        fc.FC_ERR_INVALID
+    assert lib.fc_allgather_dequant(shards, 2, 4, 4096, fc.INT8_G128, 1, 64, 0, None, None) == \
+        fc.FC_ERR_INVALID
+    # misaligned output, NULL codes of a non-empty shard
+    assert lib.fc_allgather_dequant(shards, 2, 4, 4096, fc.INT8_G128, 0, 48, 0, None, None) == \
+        fc.FC_ERR_INVALID
+    bad = (fc.QTensor * 2)(fc.QTensor(64, 128, 256), fc.QTensor(None, 128, 256))
+    assert lib.fc_allgather_dequant(bad, 2, 4, 4096, fc.INT8_G128, 0, 64, 0, None, None) == \
+        fc.FC_ERR_INVALID
+    assert "shards" in lib.fc_last_error().decode()
+    # an empty shard may have NULL buffers (checked before any launch: rows = 0)
+    assert lib.fc_allgather_dequant(bad, 2, 0, 4096, fc.INT8_G128, 0, 64, 0, None, None) == fc.FC_OK

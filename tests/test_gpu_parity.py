@@ -580,6 +580,116 @@ def test_quantized_tagged_rejects_other_groups():
 
 
 # --------------------------------------------------- full-size, sampled rows --
+# ----------------------------------------------------- standalone gather ---
+def _gather_shards_host(orc, fmt, G, T, H, P, seed):
+    """The oracle's payload of a seeded bf16 tensor, cut into P shards."""
+    w = synth.Workload("gather", P=1, T=T, H=H, fmt=fmt, group=G, outlier_frac=0.01,
+                       outlier_scale=30.0)
+    x = bf16_float(synth.make_inputs(w, seed=seed)["slabs"][0]).ravel()
+    q, s, z = orc.quantize(fmt, x, G)
+    ng = x.size // G
+    per = -(-ng // P)
+    cb = G if fmt == I8 else G // 2
+    shards = []
+    for j in range(P):
+        g0, g1 = min(j * per, ng), min((j + 1) * per, ng)
+        shards.append((q[g0 * cb:g1 * cb], s[g0:g1], None if z is None else z[g0:g1]))
+    return x.size, shards
+
+
+def _dev_shards(shards):
+    return [(None, None, None) if c.size == 0 else
+            (dev(c.view(np.uint8)), dev(s_), None if z is None else dev(z)) for c, s_, z in shards]
+
+
+GATHER_CASES = [(I8, 128, 1), (I8, 128, 3), (I8, 128, 8), (I4, 32, 2), (I4, 32, 5), (I4, 32, 8),
+                (I8, 32, 4), (I4, 16, 3), (I4, 128, 8)]
+
+
+@pytest.mark.parametrize("fmt,G,P", GATHER_CASES)
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_allgather_dequant_bit_exact(orc, fmt, G, P, out_dtype):
+    """Ragged shards (the group count is not a multiple of P) of a payload the
+    oracle built on the host; fp32 output bit-exact, bf16 = its RNE rounding."""
+    T, H = 7, 1152
+    n, shards = _gather_shards_host(orc, fmt, G, T, H, P, seed=60 + P)
+    want = orc.allgather_dequant(fmt, shards, n, G)
+    out = torch.empty(T, H, dtype=out_dtype, device="cuda")
+    fc.allgather_dequant(_dev_shards(shards), spec_of(fmt, G), T, H, out)
+    torch.cuda.synchronize()
+    if out_dtype == torch.float32:
+        assert_bits_equal(host(out), want, "gathered fp32")
+    else:
+        assert_bits_equal(host_bits(out), orc.f32_to_bf16_array(want), "gathered bf16")
+
+
+def test_allgather_more_shards_than_groups(orc):
+    """P = 8 shards of a 5-group tensor: shards 5..7 are empty (NULL buffers)."""
+    T, H, G = 1, 640, 128
+    n, shards = _gather_shards_host(orc, I8, G, T, H, 8, seed=70)
+    assert [c.size for c, _, _ in shards][5:] == [0, 0, 0]
+    out = torch.empty(T, H, dtype=torch.float32, device="cuda")
+    fc.allgather_dequant(_dev_shards(shards), spec_of(I8, G), T, H, out)
+    torch.cuda.synchronize()
+    assert_bits_equal(host(out), orc.allgather_dequant(I8, shards, n, G), "gathered")
+
+
+@pytest.mark.parametrize("fmt,G,nbg", [(I8T, 128, 11), (I4T, 32, 2)])
+def test_allgather_tagged_shards_and_stale_blocks(orc, fmt, G, nbg):
+    """Self-synchronizing shards (blocks built by the oracle on the host): every
+    group bit-exact; a corrupted tag is reported with its index (shard 0's
+    blocks first), and every group but the stale block's stays exact."""
+    base = synth.base_format(fmt)
+    T, H, P, ep = 5, 1024, 3, 9
+    n, shards = _gather_shards_host(orc, base, G, T, H, P, seed=80)
+    blocks = [orc.pack_qtagged(base, c, s_, z, G, ep) for c, s_, z in shards]
+    want = orc.allgather_dequant(base, shards, n, G)
+    spec = spec_of(fmt, G)
+    st = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+
+    def call(bl):
+        out = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+        fc.allgather_dequant([dev(b.view(np.int32)) for b in bl], spec, T, H, out,
+                             expected_epoch=ep, d_status=st)
+        torch.cuda.synchronize()
+        return host(out).ravel(), list(host(st))
+
+    got, status = call(blocks)
+    assert status == [fc.FC_OK, fc.STATUS_NO_INDEX]
+    assert_bits_equal(got, want, "gathered")
+    nblk = [b.size // 4 for b in blocks]
+    for shard, blk in ((1, 3), (2, nblk[2] - 1), (0, 0)):
+        bad = [b.copy() for b in blocks]
+        bad[shard][4 * blk + 3] = ep + 1
+        got, status = call(bad)
+        assert status == [fc.FC_ERR_STALE_BLOCK, sum(nblk[:shard]) + blk]
+        g = sum(nblk[:shard]) // nbg + blk // nbg  # the global group of the stale block
+        keep = np.ones(n, bool)
+        keep[g * G:(g + 1) * G] = False
+        assert_bits_equal(got[keep], want[keep], "gathered, other groups")
+
+
+def test_allgather_full_size_sampled(orc):
+    """A prefill-sized INT4 payload (8192 x 8192, P = 4 shards) of random codes,
+    scales and zero-points drawn on the host; sampled rows against the oracle."""
+    T, H, G, P = 8192, 8192, 32, 4
+    rng = np.random.default_rng(90)
+    ng = T * H // G
+    codes = rng.integers(0, 256, T * H // 2, dtype=np.uint8)
+    scales = (rng.random(ng, dtype=np.float32) * 0.5).astype(np.float32)
+    zeros = rng.standard_normal(ng).astype(np.float32)
+    spec = spec_of(I4, G)
+    whole = (dev(codes), dev(scales), dev(zeros))
+    out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    fc.allgather_dequant(fc.shard_views(whole, spec, T, H, P), spec, T, H, out)
+    torch.cuda.synchronize()
+    gpb = H // G
+    for r in (0, 1, 2047, 2048, 4095, 6000, 8191):
+        want = orc.dequantize(I4, codes[r * H // 2:(r + 1) * H // 2], scales[r * gpb:(r + 1) * gpb],
+                              zeros[r * gpb:(r + 1) * gpb], G)
+        assert_bits_equal(host_bits(out[r]), orc.f32_to_bf16_array(want), f"row {r}")
+
+
 @pytest.mark.parametrize("name", ["prefill", "token-split", "decode", "prefill-qtagged"])
 def test_full_size_sampled_rows(orc, name):
     """The full-size workloads through the same Pipeline.step() the
