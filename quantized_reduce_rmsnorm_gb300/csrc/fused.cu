@@ -75,9 +75,8 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
           if (p < P && act) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float2 t = padd(make_float2(acc[2 * i], acc[2 * i + 1]),
-                                    make_float2(bf_lo(xv[p].w[i]), bf_hi(xv[p].w[i])));
-              acc[2 * i] = t.x, acc[2 * i + 1] = t.y;
+              acc[2 * i] = add_bf_lo(xv[p].w[i], acc[2 * i]);
+              acc[2 * i + 1] = add_bf_hi(xv[p].w[i], acc[2 * i + 1]);
             }
           }
         }
@@ -137,14 +136,14 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
         V8 hv;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          hb[k][i] = hv.w[i] = pack_bf2(__fadd_rn(acc[2 * i], bf_lo(rv.w[i])),
-                                        __fadd_rn(acc[2 * i + 1], bf_hi(rv.w[i])));
+          hb[k][i] = hv.w[i] = pack_bf2(add_bf_lo(rv.w[i], acc[2 * i]),
+                                        add_bf_hi(rv.w[i], acc[2 * i + 1]));
         }
         st256(static_cast<uint16_t*>(a.res_out) + gc * 16, hv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float2 h = make_float2(bf_lo(hb[k][i]), bf_hi(hb[k][i]));
-          ss2 = pfma(h, h, ss2);
+          ss2.x = fma_bf_lo(hb[k][i], hb[k][i], ss2.x);
+          ss2.y = fma_bf_hi(hb[k][i], hb[k][i], ss2.y);
         }
       }
     }
@@ -152,7 +151,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
     const float ss = __fadd_rn(ss2.x, ss2.y);
     const float inv = inv_rms(block_sum(ss, red, parity), a.H, a.eps);
 
-    // ---- y = bf16((h * inv) * gamma)
+    // ---- y = bf16(fl(h * gamma) * inv); h * gamma is exact in binary32
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
       const int c = k * nthr + tid;
@@ -161,8 +160,9 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
         V8 yv;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float2 y = pmul(pmul(make_float2(bf_lo(hb[k][i]), bf_hi(hb[k][i])), dup2(inv)),
-                                make_float2(bf_lo(gv.w[i]), bf_hi(gv.w[i])));
+          const float2 y = pmul(make_float2(fma_bf_lo(hb[k][i], gv.w[i], -0.0f),
+                                            fma_bf_hi(hb[k][i], gv.w[i], -0.0f)),
+                                dup2(inv));
           yv.w[i] = pack_bf2(y.x, y.y);
         }
         st256(static_cast<uint16_t*>(a.y) + (row * cpr + c) * 16, yv);
@@ -312,8 +312,8 @@ __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
       load6<true>(static_cast<const uint16_t*>(a.gamma), e0, H, full, gw);
 #pragma unroll
       for (int k = 0; k < 3; ++k) {
-        const float2 y = pmul(pmul(make_float2(bf_lo(hw[k]), bf_hi(hw[k])), dup2(inv)),
-                              make_float2(bf_lo(gw[k]), bf_hi(gw[k])));
+        const float2 y = pmul(make_float2(fma_bf_lo(hw[k], gw[k], -0.0f), fma_bf_hi(hw[k], gw[k], -0.0f)),
+                              dup2(inv));
         yw[k] = pack_bf2(y.x, y.y);
       }
       store6(static_cast<uint16_t*>(a.y) + row * H, e0, H, full, yw);
