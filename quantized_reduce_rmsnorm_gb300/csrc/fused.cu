@@ -221,9 +221,29 @@ __device__ __forceinline__ void store6(uint16_t* row, int e0, int H, bool full, 
   }
 }
 
+// Async copies (cp.async, 16 bytes per lane, completion tracked per thread
+// in commit groups) into a warp's own shared-memory ring: the loads need no
+// registers, so two block groups of every slab stay in flight per warp while
+// a third is summed.
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+constexpr int kTagStages = 3;  // block groups in a warp's ring
+constexpr int kTagWarps = 8;
+template <int PMAX>
+__host__ __device__ constexpr int tag_stage_bytes() { return PMAX * 32 * 16 + 384; }  // 32 blocks per slab + residual
+
 template <int PMAX>
 __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
-  const int lane = threadIdx.x & 31;
+  extern __shared__ __align__(16) uint8_t tsmem[];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int H = a.H;
@@ -231,65 +251,91 @@ __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
   const int gpr = (nb + 31) >> 5;
   const int P = a.P;
   const uint32_t epoch = a.epoch;
+  constexpr int kStage = tag_stage_bytes<PMAX>();
+  uint8_t* ring = tsmem + wid * (kTagStages * kStage);
 
   for (int64_t row = w0; row < a.rows; row += nw) {
     const uint16_t* rr = static_cast<const uint16_t*>(a.res_in) + row * H;
     uint16_t* ro = static_cast<uint16_t*>(a.res_out) + row * H;
     float ss = 0.0f;
     int64_t first_bad = LLONG_MAX;
-    // software pipeline: group gi+1's blocks and residual are in flight
-    // while group gi is summed
-    uint4 b[2][PMAX];
-    uint32_t rw[2][3];
-    auto fetch = [&](int gi, int slot) {
-      const int j = gi * 32 + lane;
-      if (gi < gpr && j < nb) {
+    // every lane copies its own block of each slab and 16 bytes of the
+    // group's residual chunk (384 bytes = 32 lanes x 6 bf16, 16-byte aligned)
+    auto issue = [&](int gi) {
+      if (gi < gpr) {
+        uint8_t* st = ring + (gi % kTagStages) * kStage;
+        const int j = gi * 32 + lane;
+        if (j < nb) {
 #pragma unroll
-        for (int p = 0; p < PMAX; ++p)
-          if (p < P) b[slot][p] = ld128_stream(static_cast<const uint4*>(a.s.codes[p]) + row * nb + j);
-        load6<true>(rr, 6 * j, H, 6 * j + 6 <= H, rw[slot]);
+          for (int p = 0; p < PMAX; ++p)
+            if (p < P)
+              cp_async16(st + (p * 32 + lane) * 16, static_cast<const uint4*>(a.s.codes[p]) + row * nb + j);
+        }
+        const int rbytes = 2 * H - 384 * gi < 384 ? 2 * H - 384 * gi : 384;
+        if (16 * lane < rbytes)
+          cp_async16(st + PMAX * 512 + 16 * lane, reinterpret_cast<const uint8_t*>(rr) + 384 * gi + 16 * lane);
       }
+      cp_async_commit();  // one commit group per block group (possibly empty)
     };
-    fetch(0, 0);
-#pragma unroll 2
+#pragma unroll
+    for (int gi = 0; gi < kTagStages - 1; ++gi) issue(gi);
     for (int gi = 0; gi < gpr; ++gi) {
-      const int slot = gi & 1;
-      fetch(gi + 1, slot ^ 1);
+      issue(gi + kTagStages - 1);
+      cp_async_wait<kTagStages - 1>();  // this lane's copies of group gi have landed
+      __syncwarp();                     // and every lane's (the residual chunk is shared)
+      const uint8_t* st = ring + (gi % kTagStages) * kStage;
       const int j = gi * 32 + lane;
-      if (j >= nb) continue;
-      const int e0 = 6 * j;
-      const bool full = e0 + 6 <= H;
-      float acc[6] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+      if (j < nb) {
+        const int e0 = 6 * j;
+        const bool full = e0 + 6 <= H;
+        float acc[6] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int p = 0; p < PMAX; ++p) {
-        if (p < P) {
-          const uint4 bp = b[slot][p];
-          if (bp.w == epoch) {
-            const uint32_t w[3] = {bp.x, bp.y, bp.z};
+        for (int p = 0; p < PMAX; ++p) {
+          if (p < P) {
+            const uint4 bp = *reinterpret_cast<const uint4*>(st + (p * 32 + lane) * 16);
+            if (bp.w == epoch) {
+              const uint32_t w[3] = {bp.x, bp.y, bp.z};
 #pragma unroll
-            for (int k = 0; k < 3; ++k) {
-              const float2 t = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
-                                    make_float2(bf_lo(w[k]), bf_hi(w[k])));
-              acc[2 * k] = t.x, acc[2 * k + 1] = t.y;
+              for (int k = 0; k < 3; ++k) {
+                const float2 t = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
+                                      make_float2(bf_lo(w[k]), bf_hi(w[k])));
+                acc[2 * k] = t.x, acc[2 * k + 1] = t.y;
+              }
+            } else {
+              const int64_t idx = (static_cast<int64_t>(p) * a.rows + row) * nb + j;
+              first_bad = idx < first_bad ? idx : first_bad;
             }
-          } else {
-            const int64_t idx = (static_cast<int64_t>(p) * a.rows + row) * nb + j;
-            first_bad = idx < first_bad ? idx : first_bad;
           }
         }
-      }
-      uint32_t hw[3];
+        const uint8_t* rs = st + PMAX * 512 + 12 * lane;  // this lane's 6 residual values
+        uint32_t rw[3];
+        if (full) {
 #pragma unroll
-      for (int k = 0; k < 3; ++k) {
-        const float2 h = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
-                              make_float2(bf_lo(rw[slot][k]), bf_hi(rw[slot][k])));
-        hw[k] = pack_bf2(h.x, h.y);
-        const float h0 = bf_lo(hw[k]), h1 = bf_hi(hw[k]);
-        ss = __fmaf_rn(h0, h0, ss);
-        ss = __fmaf_rn(h1, h1, ss);
+          for (int k = 0; k < 3; ++k) rw[k] = *reinterpret_cast<const uint32_t*>(rs + 4 * k);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 3; ++k) {
+            const int e = e0 + 2 * k;
+            const uint32_t lo = e < H ? *reinterpret_cast<const uint16_t*>(rs + 4 * k) : 0u;
+            const uint32_t hi = e + 1 < H ? *reinterpret_cast<const uint16_t*>(rs + 4 * k + 2) : 0u;
+            rw[k] = lo | (hi << 16);
+          }
+        }
+        uint32_t hw[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const float2 h = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
+                                make_float2(bf_lo(rw[k]), bf_hi(rw[k])));
+          hw[k] = pack_bf2(h.x, h.y);
+          const float h0 = bf_lo(hw[k]), h1 = bf_hi(hw[k]);
+          ss = __fmaf_rn(h0, h0, ss);
+          ss = __fmaf_rn(h1, h1, ss);
+        }
+        store6(ro, e0, H, full, hw);
       }
-      store6(ro, e0, H, full, hw);
+      __syncwarp();  // every lane is done with this slot before it is refilled
     }
+    cp_async_wait<0>();
     ss = warp_sum(ss);
     // first failing block of the row (lanes agree via a min-reduction)
 #pragma unroll
@@ -302,21 +348,37 @@ __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
       atomicMin(a.status + 1, first_bad < INT_MAX ? static_cast<int>(first_bad) : INT_MAX - 1);
     }
     const float inv = inv_rms(ss, H, a.eps);
-    for (int gi = 0; gi < gpr; ++gi) {
-      const int j = gi * 32 + lane;
-      if (j >= nb) continue;
-      const int e0 = 6 * j;
-      const bool full = e0 + 6 <= H;
-      uint32_t hw[3], gw[3], yw[3];
-      load6<false>(ro, e0, H, full, hw);  // this lane's own h, written above
-      load6<true>(static_cast<const uint16_t*>(a.gamma), e0, H, full, gw);
+    // pass 2 in batches of kOutBatch block groups: all their loads (h, which
+    // this lane wrote above and is in L2, and gamma) are issued before any
+    // is used, so the L2 latency is paid once per batch
+    constexpr int kOutBatch = 4;
+    for (int gb = 0; gb < gpr; gb += kOutBatch) {
+      uint32_t hw[kOutBatch][3], gw[kOutBatch][3];
 #pragma unroll
-      for (int k = 0; k < 3; ++k) {
-        const float2 y = pmul(make_float2(fma_bf_lo(hw[k], gw[k], -0.0f), fma_bf_hi(hw[k], gw[k], -0.0f)),
-                              dup2(inv));
-        yw[k] = pack_bf2(y.x, y.y);
+      for (int u = 0; u < kOutBatch; ++u) {
+        const int j = (gb + u) * 32 + lane;
+        if (gb + u < gpr && j < nb) {
+          const int e0 = 6 * j;
+          load6<false>(ro, e0, H, e0 + 6 <= H, hw[u]);
+          load6<true>(static_cast<const uint16_t*>(a.gamma), e0, H, e0 + 6 <= H, gw[u]);
+        }
       }
-      store6(static_cast<uint16_t*>(a.y) + row * H, e0, H, full, yw);
+#pragma unroll
+      for (int u = 0; u < kOutBatch; ++u) {
+        const int j = (gb + u) * 32 + lane;
+        if (gb + u < gpr && j < nb) {
+          const int e0 = 6 * j;
+          uint32_t yw[3];
+#pragma unroll
+          for (int k = 0; k < 3; ++k) {
+            const float2 y = pmul(make_float2(fma_bf_lo(hw[u][k], gw[u][k], -0.0f),
+                                              fma_bf_hi(hw[u][k], gw[u][k], -0.0f)),
+                                  dup2(inv));
+            yw[k] = pack_bf2(y.x, y.y);
+          }
+          store6(static_cast<uint16_t*>(a.y) + row * H, e0, H, e0 + 6 <= H, yw);
+        }
+      }
     }
   }
 }
@@ -385,10 +447,34 @@ cudaError_t launch_warp_rows(K kernel, const FusedArgs& a, int max_ctas, cudaStr
   return cudaGetLastError();
 }
 
+template <int PMAX>
+int tagged_occupancy() {
+  constexpr int smem = kTagWarps * kTagStages * tag_stage_bytes<PMAX>();
+  static int occ = 0;
+  if (!occ) {
+    cudaFuncSetAttribute(k_fused_tagged<PMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_fused_tagged<PMAX>, kTagWarps * 32, smem) !=
+            cudaSuccess || occ < 1)
+      occ = 1;
+  }
+  return occ;
+}
+
+template <int PMAX>
+cudaError_t launch_tagged_p(const FusedArgs& a, int max_ctas, cudaStream_t st) {
+  constexpr int smem = kTagWarps * kTagStages * tag_stage_bytes<PMAX>();
+  int64_t grid = static_cast<int64_t>(num_sms()) * tagged_occupancy<PMAX>();
+  const int64_t need = (a.rows + kTagWarps - 1) / kTagWarps;
+  if (grid > need) grid = need;
+  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+  k_fused_tagged<PMAX><<<static_cast<int>(grid), kTagWarps * 32, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_tagged(const FusedArgs& a, int max_ctas, cudaStream_t st) {
-  if (a.P <= 2) return launch_warp_rows(k_fused_tagged<2>, a, max_ctas, st);
-  if (a.P <= 4) return launch_warp_rows(k_fused_tagged<4>, a, max_ctas, st);
-  return launch_warp_rows(k_fused_tagged<8>, a, max_ctas, st);
+  if (a.P <= 2) return launch_tagged_p<2>(a, max_ctas, st);
+  if (a.P <= 4) return launch_tagged_p<4>(a, max_ctas, st);
+  return launch_tagged_p<8>(a, max_ctas, st);
 }
 
 }  // namespace
@@ -396,10 +482,8 @@ cudaError_t launch_tagged(const FusedArgs& a, int max_ctas, cudaStream_t st) {
 // Rows the chosen fused kernel processes concurrently on the current device.
 int64_t fused_wave_rows(int fmt, const FusedArgs& a) {
   if (fmt == kTAGGED) {
-    const void* k = a.P <= 2 ? reinterpret_cast<const void*>(k_fused_tagged<2>)
-                  : a.P <= 4 ? reinterpret_cast<const void*>(k_fused_tagged<4>)
-                             : reinterpret_cast<const void*>(k_fused_tagged<8>);
-    return static_cast<int64_t>(num_sms()) * occupancy(k, 256) * 8;  // a warp per row
+    const int occ = a.P <= 2 ? tagged_occupancy<2>() : a.P <= 4 ? tagged_occupancy<4>() : tagged_occupancy<8>();
+    return static_cast<int64_t>(num_sms()) * occ * kTagWarps;  // a warp per row
   }
   if (fused_tma_eligible(fmt, a)) return fused_tma_wave_rows(fmt, a);
   if (fmt == kINT8T || fmt == kINT4T) return 0;
