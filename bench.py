@@ -416,10 +416,8 @@ def run_sweep(args):
 
     Inputs are seeded N(0,1) bf16 generated on the device (a measurement,
     not a parity case); each point is timed with CUDA events, median of
-    repetitions.  Points whose buffers fit in L2 rotate through several
-    copies of their inputs and outputs (together larger than L2), so no
-    timed call finds its inputs in L2; points too small for that write a
-    256 MB buffer (scrubbing L2) before each call."""
+    repetitions, with a 256 MB L2 scrub before every repetition when the
+    point's inputs fit in L2."""
     import torch
     from quantized_reduce_rmsnorm_gb300 import fcomm, synth
     from quantized_reduce_rmsnorm_gb300.pipeline import qs_bytes
@@ -438,57 +436,37 @@ def run_sweep(args):
         gen.manual_seed(msg ^ (H << 8) ^ (P << 4) ^ fmt)
         w = synth.sweep_workload(H, T, P, fmt, G)
         spec = fcomm.QSpec(fmt, G)
+        xs = [torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16) for _ in range(P)]
+        res = torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16)
+        gam = (1 + 0.1 * torch.randn(H, generator=gen, device=dev)).to(torch.bfloat16)
+        r_out, y = torch.empty_like(res), torch.empty_like(res)
         E = T * H
-        quant = fmt in (synth.FMT_INT8_SYM, synth.FMT_INT4_ASYM)
-        qs = qs_bytes(w, E) if quant else 0
-        point = P * 2 * E + P * qs + 2 * E + 2 * H + qs + 4 * E  # every buffer the step touches
-        # inputs larger than L2: when one copy fits, rotate through enough
-        # copies that together they exceed it, so every timed call reads
-        # inputs that are not in L2; points too small for that (under ~16 MB
-        # of buffers) scrub L2 by writing 256 MB before each call instead
-        need = -(-(2 * L2_BYTES) // point) + 1
-        copies = 1 if point > 2 * L2_BYTES else (need if need <= 16 else 1)
-        scrub = point <= 2 * L2_BYTES and copies == 1
-        sets = []
-        for _ in range(copies):
-            xs = [torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16) for _ in range(P)]
-            res = torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16)
-            gam = (1 + 0.1 * torch.randn(H, generator=gen, device=dev)).to(torch.bfloat16)
-            r_out, y = torch.empty_like(res), torch.empty_like(res)
-            codes = [fcomm.alloc_qtensor(spec, T, H, dev) for _ in range(P)] if quant else None
-            payload = fcomm.alloc_qtensor(spec, T, H, dev) if quant else None
-            sets.append((xs, res, gam, r_out, y, codes, payload))
-        if quant:
+        if fmt in (synth.FMT_INT8_SYM, synth.FMT_INT4_ASYM):
+            codes = [fcomm.alloc_qtensor(spec, T, H, dev) for _ in range(P)]
+            payload = fcomm.alloc_qtensor(spec, T, H, dev)
+            qs = qs_bytes(w, E)
             sender_bytes = P * 2 * E + P * qs
             fused_bytes = P * qs + 2 * E + 2 * H + qs + 4 * E
-
-            def send(k):
-                xs, codes = sets[k][0], sets[k][5]
-                fcomm.group_quantize_multi(xs, spec, codes)
-
-            def fuse(k):
-                xs, res, gam, r_out, y, codes, payload = sets[k]
-                fcomm.allreduce_residual_rmsnorm(codes, spec, T, H, res, r_out, gam, 1e-5, y,
-                                                 requant_out=payload)
+            send = lambda: fcomm.group_quantize_multi(xs, spec, codes)
+            fuse = lambda: fcomm.allreduce_residual_rmsnorm(codes, spec, T, H, res, r_out, gam,
+                                                            1e-5, y, requant_out=payload)
         else:
             sender_bytes = 0
             fused_bytes = P * 2 * E + 2 * E + 2 * H + 4 * E
             send = None
-
-            def fuse(k):
-                xs, res, gam, r_out, y, _, _ = sets[k]
-                fcomm.allreduce_residual_rmsnorm(xs, spec, T, H, res, r_out, gam, 1e-5, y)
+            fuse = lambda: fcomm.allreduce_residual_rmsnorm(xs, spec, T, H, res, r_out, gam,
+                                                            1e-5, y)
+        small = (P * 2 + 6) * E < 2 * L2_BYTES
         reps = 15 if E * P * 2 < (64 << 20) else 7
 
         def timed(fn):
             out = []
             for i in range(reps + 2):
-                if scrub:
+                if small:
                     flush.add_(1.0)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                k = i % copies
                 a.record()
-                fn(k)
+                fn()
                 b.record()
                 b.synchronize()
                 if i >= 2:
@@ -503,9 +481,11 @@ def run_sweep(args):
                 "fused_frac": round(fused_bytes / fu / 1e3 / peak, 4),
                 "sender_us": None if su is None else round(su, 2),
                 "sender_GBps": None if su is None else round(sender_bytes / su / 1e3, 1),
-                "input_copies": copies, "l2_scrubbed": scrub}
+                "l2_scrubbed": small}
         print(json.dumps(line), flush=True)
-        del sets
+        del xs, res, gam, r_out, y
+        if send:
+            del codes, payload
         torch.cuda.empty_cache()
 
 
