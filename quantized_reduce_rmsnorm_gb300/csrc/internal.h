@@ -67,6 +67,9 @@ constexpr int kTmaSmemLimit = 224 * 1024;
 enum FusedPath : int { kPathAuto = 0, kPathStream = 1, kPathTma = 2 };
 bool fused_tma_eligible(int fmt, const FusedArgs& a);
 cudaError_t launch_fused_tma(int fmt, const FusedArgs& a, int max_ctas, cudaStream_t st);
+// Row-starved calls: each row shared by a cluster of CTAs (segments of the
+// row); cudaErrorNotSupported when the row cannot be cut into such segments.
+cudaError_t launch_fused_tma_cluster(int fmt, const FusedArgs& a, cudaStream_t st);
 int64_t fused_tma_wave_rows(int fmt, const FusedArgs& a);
 // Rows the fused kernel that a call would launch processes concurrently.
 int64_t fused_wave_rows(int fmt, const FusedArgs& a);
