@@ -121,11 +121,19 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
 // and its 32 lanes quantize the current tile out of shared memory and store
 // codes and scales directly.  Warps never wait for each other: no CTA-wide
 // barrier is used.  Tiles cover the flattened (slab, tile) space.
-// Measured on GB300 (prefill, 4 x 8192 x 8192): 2048-element tiles in a
-// two-deep ring (4 KB in flight per warp, three CTAs per SM) beat 1024-element
-// tiles four deep by 8%: half the per-tile waits and cursor steps.
-constexpr int kWTile = 2048;  // elements per warp tile (4 KB of bf16, 4 chunks per lane)
-constexpr int kWStages = 2;
+// TILE: elements per warp tile.  Measured on GB300: for large calls (prefill,
+// 4 x 8192 x 8192) 2048-element tiles in a two-deep ring (three CTAs per SM)
+// beat 1024-element tiles four deep by 8% -- half the per-tile waits and
+// cursor steps; calls with fewer 2048-element tiles than resident warps
+// (decode) keep the smaller tiles, which spread over more warps.  Both use
+// 8 KB of ring per warp.
+template <int TILE>
+struct WRing {
+  static constexpr int kStages = TILE == 1024 ? 4 : 2;
+  static constexpr int kBytes = kStages * TILE * 2;
+};
+constexpr int kWRingBytes = WRing<2048>::kBytes;
+static_assert(WRing<1024>::kBytes == WRing<2048>::kBytes, "one shared-memory size for both tilings");
 constexpr int kQWarps = kThreads / 32;
 
 // TAGGED: the codes and scales go out as self-synchronizing blocks carrying
@@ -134,11 +142,12 @@ constexpr int kQWarps = kThreads / 32;
 // words 0..2 of a 16-byte block, the epoch in word 3.
 // LPG: lanes per group when known at compile time (the two standard group
 // sizes), 0 to take it from lpg_shift.
-template <int FMT, bool TAGGED = false, int LPG = 0>
+template <int FMT, bool TAGGED = false, int LPG = 0, int TILE = 2048>
 __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int lpg_shift,
                                                            int64_t tiles_per_slab) {
+  constexpr int kWTile = TILE, kWStages = WRing<TILE>::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint64_t bars[kQWarps][kWStages];
+  __shared__ uint64_t bars[kQWarps][WRing<TILE>::kStages];
   // INT8 tagged: a warp assembles its 4 groups' payloads (33 words each) here
   __shared__ uint32_t qstage[TAGGED && FMT == kINT8 ? kQWarps : 1][4][33];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -147,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int 
   const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kQWarps + wid;
   const int64_t wstride = static_cast<int64_t>(gridDim.x) * kQWarps;
   if (w0 >= total) return;  // whole warp
-  uint8_t* ring = smem + wid * (kWStages * kWTile * 2);
+  uint8_t* ring = smem + wid * kWRingBytes;
   uint64_t* bar = bars[wid];
 
   // A cursor over the flattened (slab, tile) space that only moves forward by
@@ -448,10 +457,11 @@ int num_sms() {
   return sms[dev];
 }
 
-template <int FMT, bool TAGGED, int LPG>
+template <int FMT, bool TAGGED, int LPG, int TILE>
 cudaError_t launch_quantize_tma_t(const QuantJob& job, cudaStream_t st) {
-  const int smem = kQWarps * kWStages * kWTile * 2;
-  auto kern = k_quantize_tma<FMT, TAGGED, LPG>;
+  constexpr int kWTile = TILE;
+  const int smem = kQWarps * kWRingBytes;
+  auto kern = k_quantize_tma<FMT, TAGGED, LPG, TILE>;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -473,11 +483,20 @@ cudaError_t launch_quantize_tma_t(const QuantJob& job, cudaStream_t st) {
 }
 
 // INT8 g128 (8 lanes per group) and INT4 g32 (2 lanes) are specialised
+template <int FMT, bool TAGGED, int LPG>
+cudaError_t launch_quantize_tma_tile(const QuantJob& job, cudaStream_t st) {
+  // resident warps: three CTAs of kQWarps per SM
+  const int64_t big_tiles = (job.n + 2047) / 2048 * job.P;
+  if (big_tiles < static_cast<int64_t>(num_sms()) * 3 * kQWarps)
+    return launch_quantize_tma_t<FMT, TAGGED, LPG, 1024>(job, st);
+  return launch_quantize_tma_t<FMT, TAGGED, LPG, 2048>(job, st);
+}
+
 template <int FMT, bool TAGGED = false>
 cudaError_t launch_quantize_tma(const QuantJob& job, cudaStream_t st) {
   constexpr int kStdLanes = FMT == kINT8 ? 8 : 2;
-  if (TAGGED || job.G == 16 * kStdLanes) return launch_quantize_tma_t<FMT, TAGGED, kStdLanes>(job, st);
-  return launch_quantize_tma_t<FMT, false, 0>(job, st);
+  if (TAGGED || job.G == 16 * kStdLanes) return launch_quantize_tma_tile<FMT, TAGGED, kStdLanes>(job, st);
+  return launch_quantize_tma_tile<FMT, false, 0>(job, st);
 }
 
 bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
