@@ -327,6 +327,13 @@ __device__ __forceinline__ void dequant_i4_acc(const uint32_t w[2], float s, flo
     dequant_i4_acc_t<false>(w, s, z, acc);
 }
 
+// RMSNorm's inverse root mean square, 1/sqrt(ss/H + eps), for an output held
+// to one bf16 ulp: ss * (1/H) and the hardware reciprocal square root
+// (a few binary32 ulps) instead of two IEEE divisions and a square root.
+__device__ __forceinline__ float inv_rms(float ss, float inv_h, float eps) {
+  return rsqrtf(__fadd_rn(__fmul_rn(ss, inv_h), eps));
+}
+
 // ------------------------------------------------------- group reductions --
 // Reductions across the `lpg` lanes (a power of two, 1..32) holding one group.
 // Every lane of the warp must call these (inactive lanes with neutral data).

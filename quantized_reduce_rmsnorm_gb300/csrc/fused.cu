@@ -8,7 +8,7 @@
 //           it, add the residual, round to bf16 (written as residual_out and
 //           kept in registers), accumulate the sum of squares;
 //   block reduction of the sum of squares;
-//   pass 2: y = bf16((h * inv_rms) * gamma) from the registers.
+//   pass 2: y = bf16(fl(h * gamma) * inv_rms) from the registers.
 // Nothing but y, residual_out and the optional payload leaves the SM; the
 // reduced fp32 row never touches HBM.
 #include <climits>
@@ -34,9 +34,6 @@ __device__ __forceinline__ float block_sum(float v, float (*red)[32], int parity
   return t;
 }
 
-__device__ __forceinline__ float inv_rms(float ss, int H, float eps) {
-  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(H)), eps)));
-}
 
 // ------------------------------------------------ BF16 / INT8 / INT4 path --
 template <int FMT, int NCH>
@@ -149,7 +146,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
     }
 
     const float ss = __fadd_rn(ss2.x, ss2.y);
-    const float inv = inv_rms(block_sum(ss, red, parity), a.H, a.eps);
+    const float inv = inv_rms(block_sum(ss, red, parity), 1.0f / static_cast<float>(a.H), a.eps);
 
     // ---- y = bf16(fl(h * gamma) * inv); h * gamma is exact in binary32
 #pragma unroll
@@ -347,7 +344,7 @@ __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
       atomicCAS(a.status, 0, 3 /* FC_ERR_STALE_BLOCK */);
       atomicMin(a.status + 1, first_bad < INT_MAX ? static_cast<int>(first_bad) : INT_MAX - 1);
     }
-    const float inv = inv_rms(ss, H, a.eps);
+    const float inv = inv_rms(ss, 1.0f / static_cast<float>(H), a.eps);
     // pass 2 in batches of kOutBatch block groups: all their loads (h, which
     // this lane wrote above and is in L2, and gamma) are issued before any
     // is used, so the L2 latency is paid once per batch

@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kTmaThreadsMax) k_fused_tma(FusedArgs a, TmaGe
   const int H = a.H, cpr = H >> 4, P = a.P;
   const int rank = CL > 1 ? static_cast<int>(cluster_rank()) : 0;
   const int cps = g.cps, c0 = rank * cps;  // this CTA's chunks of every row
+  const float inv_h = 1.0f / static_cast<float>(H);
   const int lpg = a.G >> 4, sh = a.lpg_shift;
   // h (the bf16 row) lives in its own buffer: each thread reads back only the
   // chunks it wrote, so it needs no barrier and frees the stage early.
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(kTmaThreadsMax) k_fused_tma(FusedArgs a, TmaGe
       }
     }
     if (!all_ok) break;
-    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, static_cast<float>(H)), a.eps)));
+    const float inv = inv_rms(tot, inv_h, a.eps);
 
     // every thread is past its reads of stage s: refill it NSTAGE rows ahead
     if (tid == 0) {
