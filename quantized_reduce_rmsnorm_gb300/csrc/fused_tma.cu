@@ -11,6 +11,7 @@ namespace {
 // Launch shape of one instantiation: threads per CTA and resident CTAs per SM.
 struct TmaShape {
   int nstage = 0, threads = 0, occ = 0, smem = 0;
+  bool compact = false;  // the compact build (fused_tma_compact.cu)
 };
 
 // Threads per CTA, from the work a thread does per row and barrier (measured
@@ -54,12 +55,30 @@ TmaShape shape_t(const FusedArgs& a, const TmaGeom& g) {
 // two single-stage CTAs (which overlap each other's copies and row
 // barriers) were measured faster; for bf16 rows the two-row ring stays.
 template <int FMT, int PMAX>
-TmaShape choose_shape(const FusedArgs& a, const TmaGeom& g) {
+TmaShape choose_full(const FusedArgs& a, const TmaGeom& g) {
   const TmaShape two = shape_t<FMT, 2, PMAX>(a, g);
   if (FMT == kBF16 && two.occ >= 1) return two;
   const TmaShape one = shape_t<FMT, 1, PMAX>(a, g);
   if (two.occ >= 1 && (two.occ >= 2 || one.occ <= two.occ)) return two;
   return one;
+}
+
+// For the quantized formats the compact build replaces that choice where it
+// holds more CTAs per SM (shared memory, not registers, then bounds the
+// count); bf16 rows measured slower with it.
+template <int FMT, int PMAX>
+TmaShape choose_shape(const FusedArgs& a, const TmaGeom& g) {
+  TmaShape best = choose_full<FMT, PMAX>(a, g);
+  if (FMT == kBF16 || best.threads < 1 || best.threads > 256) return best;
+  for (int ns = 2; ns >= 1; --ns) {
+    const int smem = g.stage_off + ns * g.stage_bytes;
+    const int occ = fused_tma_compact_occupancy(FMT, a.P, ns, best.threads, smem);
+    if (occ > best.occ) {
+      best.nstage = ns, best.occ = occ, best.smem = smem, best.compact = true;
+      break;
+    }
+  }
+  return best;
 }
 
 template <int FMT, int PMAX>
@@ -76,6 +95,8 @@ cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cud
   int64_t grid = static_cast<int64_t>(num_sms()) * sh.occ;
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   if (grid > a.rows) grid = a.rows;
+  if (sh.compact)
+    return launch_fused_tma_compact(FMT, sh.nstage, a, g, sh.threads, sh.smem, grid, st);
   const dim3 gr(static_cast<unsigned>(grid));
   if (sh.nstage == 2)
     k_fused_tma<FMT, 2, PMAX><<<gr, sh.threads, sh.smem, st>>>(a, g);

@@ -24,8 +24,6 @@
 
 namespace fc {
 
-namespace {
-
 constexpr int kTmaThreadsMax = 512;  // threads per CTA at most
 constexpr int kGammaRegChunks = 2;   // gamma chunks a thread keeps in registers
 
@@ -43,6 +41,15 @@ struct TmaGeom {
   int gamma_off;    // byte offset of the h segment buffer in dynamic smem
   int stage_off;    // byte offset of stage 0
 };
+
+// The compact build (fused_tma_compact.cu): resident CTAs per SM of the
+// instantiation for (fmt, P, nstage) at `threads` threads and `smem` bytes
+// (0 when it cannot run), and its launch.
+int fused_tma_compact_occupancy(int fmt, int P, int nstage, int threads, int smem);
+cudaError_t launch_fused_tma_compact(int fmt, int nstage, const FusedArgs& a, const TmaGeom& g,
+                                     int threads, int smem, int64_t grid, cudaStream_t st);
+
+namespace {
 
 template <int FMT>
 __device__ __forceinline__ void issue_row(const FusedArgs& a, const TmaGeom& g, uint8_t* st,
@@ -91,8 +98,12 @@ __device__ __forceinline__ void st_peer_u32(uint32_t addr, uint32_t v) {
 
 // CL: CTAs per row (a cluster of CL CTAs shares each row, CTA r owning
 // chunks [r * cps, (r + 1) * cps); 1: a CTA per row).
-template <int FMT, int NSTAGE, int PMAX, int CL = 1>
-__global__ void __launch_bounds__(kTmaThreadsMax) k_fused_tma(FusedArgs a, TmaGeom g) {
+// COMPACT: built for at most 256 threads and three CTAs per SM (about 80
+// registers, a few values spilled), for shapes where shared memory admits
+// more CTAs than the full register budget does.
+template <int FMT, int NSTAGE, int PMAX, int CL = 1, bool COMPACT = false>
+__global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 1)
+    k_fused_tma(FusedArgs a, TmaGeom g) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float red[2][32];
   __shared__ uint64_t bar[NSTAGE];

@@ -340,6 +340,8 @@ TMA_CASES = [
     # short rows, many per CTA at max_ctas 1 and 3
     ("i4-short-rows", {"P": 2, "T": 37, "H": 4096, "fmt": I4, "group": 32}),
     ("i8-short-rows", {"P": 2, "T": 29, "H": 2048, "fmt": I8, "group": 128}),
+    # single-stage rings of the compact build (shared memory admits 3 CTAs per SM)
+    ("i8-p4-wide", {"P": 4, "T": 9, "H": 8192, "fmt": I8, "group": 128}),
 ]
 
 
