@@ -37,6 +37,55 @@ UNIT = "GB/s"
 L2_BYTES = 129 * 2 ** 20
 
 
+# Before a timed call the stream is held by a spinning kernel for about
+# 100 us (at 2 GHz), so the call's launches are already queued when the
+# start event fires: event intervals are device time, not the host's cost of
+# issuing the call (which is reported on its own).
+HOLD_CYCLES = 200_000
+
+
+def device_timed(fn, reps, warm=2, scrub=None):
+    """(median device us, median host us) of fn() over `reps` repetitions
+    after `warm` untimed ones; `scrub` (a tensor larger than L2) is written
+    before every repetition, outside the events."""
+    import torch
+    dev_us, host_us = [], []
+    for i in range(reps + warm):
+        torch.cuda._sleep(HOLD_CYCLES)
+        if scrub is not None:
+            scrub.add_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        t0 = time.perf_counter()
+        fn()
+        t1 = time.perf_counter()
+        b.record()
+        b.synchronize()
+        if i >= warm:
+            dev_us.append(a.elapsed_time(b) * 1e3)
+            host_us.append((t1 - t0) * 1e6)
+    return statistics.median(dev_us), statistics.median(host_us)
+
+
+def stream_timed(calls, rounds):
+    """Device us per call of `rounds` passes over `calls`, launched back to
+    back between one pair of events (the stream is held while the host
+    queues them)."""
+    import torch
+    n = rounds * len(calls)
+    for c in calls:  # untimed pass
+        c()
+    torch.cuda._sleep(HOLD_CYCLES + 40_000 * n)  # ~20 us of queueing time per call
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(rounds):
+        for c in calls:
+            c()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) * 1e3 / n
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -286,6 +335,7 @@ def run_ours(args):
     sampler = ClockSampler(dev.index)
     with sampler:
         t_wall = time.perf_counter()
+        torch.cuda._sleep(HOLD_CYCLES)  # the host queues ahead of the first timed step
         for i in range(n):
             if flush is not None:
                 flush.add_(1.0)  # scrub L2 between timed steps (outside the events)
@@ -417,7 +467,8 @@ def run_sweep(args):
     Inputs are seeded N(0,1) bf16 generated on the device (a measurement,
     not a parity case); each point is timed with CUDA events, median of
     repetitions, with a 256 MB L2 scrub before every repetition when the
-    point's inputs fit in L2."""
+    point's inputs fit in L2; the calls are bound once (fcomm.Bound) and
+    their host issue time is reported beside the device time."""
     import torch
     from quantized_reduce_rmsnorm_gb300 import fcomm, synth
     from quantized_reduce_rmsnorm_gb300.pipeline import qs_bytes
@@ -439,53 +490,64 @@ def run_sweep(args):
         xs = [torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16) for _ in range(P)]
         res = torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16)
         gam = (1 + 0.1 * torch.randn(H, generator=gen, device=dev)).to(torch.bfloat16)
-        r_out, y = torch.empty_like(res), torch.empty_like(res)
         E = T * H
-        if fmt in (synth.FMT_INT8_SYM, synth.FMT_INT4_ASYM):
-            codes = [fcomm.alloc_qtensor(spec, T, H, dev) for _ in range(P)]
-            payload = fcomm.alloc_qtensor(spec, T, H, dev)
+        quant = fmt in (synth.FMT_INT8_SYM, synth.FMT_INT4_ASYM)
+        if quant:
             qs = qs_bytes(w, E)
             sender_bytes = P * 2 * E + P * qs
             fused_bytes = P * qs + 2 * E + 2 * H + qs + 4 * E
-            send = lambda: fcomm.group_quantize_multi(xs, spec, codes)
-            fuse = lambda: fcomm.allreduce_residual_rmsnorm(codes, spec, T, H, res, r_out, gam,
-                                                            1e-5, y, requant_out=payload)
+            fused_in = P * qs + 2 * E
         else:
             sender_bytes = 0
             fused_bytes = P * 2 * E + 2 * E + 2 * H + 4 * E
-            send = None
-            fuse = lambda: fcomm.allreduce_residual_rmsnorm(xs, spec, T, H, res, r_out, gam,
-                                                            1e-5, y)
+            fused_in = P * 2 * E + 2 * E
+
+        def make_set(xset):
+            """One set of buffers for a sender call and a fused call."""
+            r_out, y = torch.empty_like(res), torch.empty_like(res)
+            if quant:
+                codes = [fcomm.alloc_qtensor(spec, T, H, dev) for _ in range(P)]
+                payload = fcomm.alloc_qtensor(spec, T, H, dev)
+                send = fcomm.bind_group_quantize_multi(xset, spec, codes)
+                send()
+                fuse = fcomm.bind_allreduce_residual_rmsnorm(codes, spec, T, H, res.clone(), r_out,
+                                                             gam, 1e-5, y, requant_out=payload)
+                return send, fuse
+            return None, fcomm.bind_allreduce_residual_rmsnorm(xset, spec, T, H, res.clone(), r_out,
+                                                               gam, 1e-5, y)
+
+        send, fuse = make_set(xs)
         small = (P * 2 + 6) * E < 2 * L2_BYTES
         reps = 15 if E * P * 2 < (64 << 20) else 7
-
-        def timed(fn):
-            out = []
-            for i in range(reps + 2):
-                if small:
-                    flush.add_(1.0)
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                fn()
-                b.record()
-                b.synchronize()
-                if i >= 2:
-                    out.append(a.elapsed_time(b) * 1e3)
-            return statistics.median(out)
-
-        su = timed(send) if send else None
-        fu = timed(fuse)
+        scrub = flush if small else None
+        su, _ = device_timed(send, reps, scrub=scrub) if send else (None, None)
+        fu, fh = device_timed(fuse, reps, scrub=scrub)
         line = {"sweep": True, "message_bytes": msg, "hidden": H, "tokens": T, "P": P,
                 "format": synth.FMT_NAMES[fmt], "fused_us": round(fu, 2),
                 "fused_GBps": round(fused_bytes / fu / 1e3, 1),
                 "fused_frac": round(fused_bytes / fu / 1e3 / peak, 4),
+                "fused_host_us": round(fh, 2),
                 "sender_us": None if su is None else round(su, 2),
                 "sender_GBps": None if su is None else round(sender_bytes / su / 1e3, 1),
                 "l2_scrubbed": small}
+        # Steady state for points whose buffers fit in L2: k buffer sets whose
+        # inputs together exceed twice L2, called back to back in turn, so
+        # every call's inputs are cold and the lines it finds dirty are its
+        # predecessor's outputs (no scrub).
+        k = -(-2 * L2_BYTES // fused_in) + 1
+        if small and k <= 64:
+            sets = [make_set([x.clone() for x in xs] if (quant or j) else xs) for j in range(k)]
+            rounds = max(2, 48 // k)
+            fr = stream_timed([f for _, f in sets], rounds)
+            line.update(rot_sets=k, rot_fused_us=round(fr, 2),
+                        rot_fused_frac=round(fused_bytes / fr / 1e3 / peak, 4))
+            if quant:
+                sr = stream_timed([snd for snd, _ in sets], rounds)
+                line.update(rot_sender_us=round(sr, 2),
+                            rot_sender_frac=round(sender_bytes / sr / 1e3 / peak, 4))
+            del sets
         print(json.dumps(line), flush=True)
-        del xs, res, gam, r_out, y
-        if send:
-            del codes, payload
+        del xs, res, gam, send, fuse
         torch.cuda.empty_cache()
 
 
@@ -516,18 +578,8 @@ def run_gather(args):
         for odt, osz in ((torch.bfloat16, 2), (torch.float32, 4)):
             out = torch.empty(T, H, dtype=odt, device=dev)
             small = qs + osz * E < 2 * L2_BYTES
-            times = []
-            for i in range(max(args.steps, 5) + 3):
-                if small:
-                    flush.add_(1.0)
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                fcomm.allgather_dequant(shards, spec, T, H, out)
-                b.record()
-                b.synchronize()
-                if i >= 3:
-                    times.append(a.elapsed_time(b) * 1e3)
-            us = statistics.median(times)
+            us, _ = device_timed(lambda: fcomm.allgather_dequant(shards, spec, T, H, out),
+                                 max(args.steps, 5), warm=3, scrub=flush if small else None)
             alg = qs + osz * E
             print(json.dumps({"gather": True, "workload": name, "rows": T, "hidden": H, "P": P,
                               "format": synth.FMT_NAMES[spec.fmt], "out": str(odt).split(".")[-1],
@@ -572,16 +624,7 @@ def run_overlap(args):
             torch.matmul(A, B, out=C)
 
     def timed(fn, reps=10):
-        out = []
-        for i in range(reps + 3):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            b.synchronize()
-            if i >= 3:
-                out.append(a.elapsed_time(b) * 1e3)
-        return statistics.median(out)
+        return device_timed(fn, reps, warm=3)[0]
 
     def both(cap):
         cur = torch.cuda.current_stream(dev)

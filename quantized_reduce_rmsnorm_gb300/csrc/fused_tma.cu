@@ -35,18 +35,14 @@ TmaShape shape_t(const FusedArgs& a, const TmaGeom& g) {
   sh.smem = g.stage_off + NSTAGE * g.stage_bytes;
   if (sh.smem > kTmaSmemLimit) return sh;
   auto kern = k_fused_tma<FMT, NSTAGE, PMAX>;
-  static int configured_smem[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  dev = dev < 64 ? dev : 63;
-  if (configured_smem[dev] < sh.smem) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sh.smem) != cudaSuccess)
-      return sh;
-    configured_smem[dev] = sh.smem;
-  }
   sh.threads = tma_threads(FMT, a.P, a.H);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.occ, kern, sh.threads, sh.smem) != cudaSuccess)
-    sh.occ = 0;
+  sh.occ = occupancy_memo(reinterpret_cast<const void*>(kern), sh.threads, sh.smem, 1, [&] {
+    int o = 0;
+    if (raise_smem_limit(reinterpret_cast<const void*>(kern), sh.smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, sh.threads, sh.smem) != cudaSuccess)
+      return 0;
+    return o;
+  });
   return sh;
 }
 

@@ -13,15 +13,6 @@ template <int FMT, int PMAX, int CL>
 cudaError_t launch_cl(const FusedArgs& a, const TmaGeom& g, cudaStream_t st) {
   auto kern = k_fused_tma<FMT, 1, PMAX, CL>;
   const int smem = g.stage_off + g.stage_bytes;
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  dev = dev < 64 ? dev : 63;
-  if (configured[dev] < smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = smem;
-  }
   // one chunk per thread (the segments are short), at least two warps
   int threads = (g.cps + 31) & ~31;
   threads = threads < 64 ? 64 : (threads > kTmaThreadsMax ? kTmaThreadsMax : threads);
@@ -37,9 +28,14 @@ cudaError_t launch_cl(const FusedArgs& a, const TmaGeom& g, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
-    return cudaErrorNotSupported;
+  const int clusters = occupancy_memo(reinterpret_cast<const void*>(kern), threads, smem, CL, [&] {
+    int c = 0;
+    if (raise_smem_limit(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&c, kern, &cfg) != cudaSuccess)
+      return 0;
+    return c;
+  });
+  if (clusters < 1) return cudaErrorNotSupported;
   const int64_t n = a.rows < clusters ? a.rows : clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(n * CL));
   return cudaLaunchKernelEx(&cfg, kern, a, g);

@@ -14,18 +14,13 @@ namespace {
 template <int FMT, int NS, int PMAX>
 int occ_t(int threads, int smem) {
   auto kern = k_fused_tma<FMT, NS, PMAX, 1, true>;
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  dev = dev < 64 ? dev : 63;
-  if (configured[dev] < smem) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  return occupancy_memo(reinterpret_cast<const void*>(kern), threads, smem, 1, [&] {
+    int o = 0;
+    if (raise_smem_limit(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, threads, smem) != cudaSuccess)
       return 0;
-    configured[dev] = smem;
-  }
-  int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem) != cudaSuccess) return 0;
-  return occ;
+    return o;
+  });
 }
 
 template <int FMT, int NS>

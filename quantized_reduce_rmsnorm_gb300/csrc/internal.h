@@ -59,6 +59,33 @@ struct FusedArgs {
 
 int num_sms();
 
+// Host-side memo of occupancy answers (resident CTAs, or clusters, per SM)
+// for one kernel at one launch shape on the current device.  Each answer is
+// queried once and then reused, so a call's host cost is its launch and not
+// the occupancy calculator.  Thread-safe.
+struct OccKey {
+  const void* fn;
+  int dev, threads, smem, cluster;
+};
+bool occ_memo_find(const OccKey& k, int* value);
+void occ_memo_store(const OccKey& k, int value);
+// Raises kernel fn's dynamic shared-memory limit on the current device to at
+// least smem bytes; never lowers it, so every earlier launch shape of the
+// kernel stays valid.
+cudaError_t raise_smem_limit(const void* fn, int smem);
+// query() runs on a miss; it raises the kernel's shared-memory limit where
+// needed, and since the limit never drops, a remembered answer stays valid.
+template <class Q>
+int occupancy_memo(const void* fn, int threads, int smem, int cluster, Q query) {
+  OccKey k{fn, 0, threads, smem, cluster};
+  cudaGetDevice(&k.dev);
+  int v = 0;
+  if (occ_memo_find(k, &v)) return v;
+  v = query();
+  occ_memo_store(k, v);
+  return v;
+}
+
 // Dynamic shared memory a TMA-staged fused CTA may use (GB300: 227 KB per CTA).
 constexpr int kTmaSmemLimit = 224 * 1024;
 

@@ -8,6 +8,8 @@
 // warp touches one contiguous span.  Grids are persistent: a multiple of the
 // SM count, each warp striding over warp tiles, with two tiles in flight per
 // iteration.
+#include <mutex>
+
 #include "device.cuh"
 #include "internal.h"
 
@@ -457,22 +459,69 @@ int num_sms() {
   return sms[dev];
 }
 
+namespace {
+constexpr int kOccMemoMax = 512;
+OccKey g_occ_keys[kOccMemoMax];
+int g_occ_vals[kOccMemoMax];
+int g_occ_n = 0;
+std::mutex g_occ_mu;
+bool same_key(const OccKey& a, const OccKey& b) {
+  return a.fn == b.fn && a.dev == b.dev && a.threads == b.threads && a.smem == b.smem &&
+         a.cluster == b.cluster;
+}
+}  // namespace
+
+bool occ_memo_find(const OccKey& k, int* value) {
+  std::lock_guard<std::mutex> lock(g_occ_mu);
+  for (int i = 0; i < g_occ_n; ++i)
+    if (same_key(g_occ_keys[i], k)) {
+      *value = g_occ_vals[i];
+      return true;
+    }
+  return false;
+}
+
+cudaError_t raise_smem_limit(const void* fn, int smem) {
+  static std::mutex mu;
+  static const void* fns[kOccMemoMax];
+  static int devs[kOccMemoMax], lims[kOccMemoMax];
+  static int n = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  int i = 0;
+  while (i < n && !(fns[i] == fn && devs[i] == dev)) ++i;
+  if (i < n && lims[i] >= smem) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (i == n && n < kOccMemoMax) fns[n] = fn, devs[n] = dev, ++n;
+  if (i < n) lims[i] = smem;
+  return cudaSuccess;
+}
+
+void occ_memo_store(const OccKey& k, int value) {
+  std::lock_guard<std::mutex> lock(g_occ_mu);
+  for (int i = 0; i < g_occ_n; ++i)
+    if (same_key(g_occ_keys[i], k)) return;
+  if (g_occ_n < kOccMemoMax) {  // a full memo only means later misses are re-queried
+    g_occ_keys[g_occ_n] = k;
+    g_occ_vals[g_occ_n] = value;
+    ++g_occ_n;
+  }
+}
+
 template <int FMT, bool TAGGED, int LPG, int TILE>
 cudaError_t launch_quantize_tma_t(const QuantJob& job, cudaStream_t st) {
   constexpr int kWTile = TILE;
   const int smem = kQWarps * kWRingBytes;
   auto kern = k_quantize_tma<FMT, TAGGED, LPG, TILE>;
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  dev = dev < 64 ? dev : 63;
-  if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
-  int occ = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+  const int occ = occupancy_memo(reinterpret_cast<const void*>(kern), kThreads, smem, 1, [&] {
+    int o = 0;
+    if (raise_smem_limit(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kThreads, smem) != cudaSuccess)
+      return 0;
+    return o;
+  });
   if (occ < 1) return cudaErrorInvalidConfiguration;
   const int64_t tps = (job.n + kWTile - 1) / kWTile;
   int64_t grid = static_cast<int64_t>(num_sms()) * occ;

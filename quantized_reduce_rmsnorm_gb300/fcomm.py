@@ -152,6 +152,37 @@ def _qt(q) -> QTensor:
     return QTensor(_ptr(codes), _ptr(scales), _ptr(zeros))
 
 
+class Bound:
+    """One libfcomm call with its arguments marshalled once.
+
+    Calling it launches the entry point again with the same device pointers
+    (the tensors it was bound to must stay alive and in place) on `stream`
+    (default: the current torch stream), with no per-call argument
+    conversion: the host cost of a call is the C entry point itself.  For the
+    calls that carry an epoch (tagged formats), `epoch` may be changed
+    between calls."""
+    __slots__ = ("_fn", "_args", "_si", "_ei", "_keep")
+
+    def __init__(self, fn, args, stream_index, epoch_index=None, keep=()):
+        self._fn, self._args, self._si, self._ei, self._keep = fn, list(args), stream_index, \
+            epoch_index, keep
+
+    @property
+    def epoch(self) -> int:
+        return self._args[self._ei].value
+
+    @epoch.setter
+    def epoch(self, e: int):
+        self._args[self._ei] = ctypes.c_uint32(e & 0xFFFFFFFF)
+
+    def __call__(self, stream=None):
+        a = self._args
+        a[self._si] = _stream(stream)
+        st = self._fn(*a)
+        if st != FC_OK:
+            _check(st)
+
+
 def _rows_hidden(x: torch.Tensor):
     if x.dim() != 2:
         raise ValueError("expected a [rows, hidden] tensor")
@@ -195,11 +226,15 @@ def group_quantize(x: torch.Tensor, spec: QSpec, out, stream=None):
     _check(load().fc_group_quantize(_ptr(x), rows, hidden, spec, _qt(out), _stream(stream)))
 
 
-def group_quantize_multi(xs: Sequence[torch.Tensor], spec: QSpec, outs, stream=None):
+def bind_group_quantize_multi(xs: Sequence[torch.Tensor], spec: QSpec, outs) -> Bound:
     rows, hidden = _rows_hidden(xs[0])
     xp = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
     qo = (QTensor * len(outs))(*[_qt(o) for o in outs])
-    _check(load().fc_group_quantize_multi(xp, len(xs), rows, hidden, spec, qo, _stream(stream)))
+    return Bound(load().fc_group_quantize_multi, [xp, len(xs), rows, hidden, spec, qo, None], 6)
+
+
+def group_quantize_multi(xs: Sequence[torch.Tensor], spec: QSpec, outs, stream=None):
+    bind_group_quantize_multi(xs, spec, outs)(stream)
 
 
 def reduce_dequant_sum(slabs, spec: QSpec, rows: int, hidden: int, out: torch.Tensor,
@@ -257,22 +292,33 @@ def pack_tagged(x: torch.Tensor, epoch: int, blocks: torch.Tensor, stream=None):
     _check(load().fc_pack_tagged(_ptr(x), rows, hidden, epoch, _ptr(blocks), _stream(stream)))
 
 
-def group_quantize_tagged(xs: Sequence[torch.Tensor], spec: QSpec, epoch: int,
-                          blocks: Sequence[torch.Tensor], stream=None):
-    """Quantize P bf16 slabs straight into self-synchronizing blocks."""
+def bind_group_quantize_tagged(xs: Sequence[torch.Tensor], spec: QSpec, epoch: int,
+                               blocks: Sequence[torch.Tensor]) -> Bound:
     rows, hidden = _rows_hidden(xs[0])
     xp = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
     bp = (ctypes.c_void_p * len(blocks))(*[_ptr(b) for b in blocks])
-    _check(load().fc_group_quantize_tagged(xp, len(xs), rows, hidden, spec, epoch, bp,
-                                           _stream(stream)))
+    return Bound(load().fc_group_quantize_tagged,
+                 [xp, len(xs), rows, hidden, spec, ctypes.c_uint32(epoch), bp, None], 7, 5)
+
+
+def group_quantize_tagged(xs: Sequence[torch.Tensor], spec: QSpec, epoch: int,
+                          blocks: Sequence[torch.Tensor], stream=None):
+    """Quantize P bf16 slabs straight into self-synchronizing blocks."""
+    bind_group_quantize_tagged(xs, spec, epoch, blocks)(stream)
+
+
+def bind_pack_tagged_multi(xs: Sequence[torch.Tensor], epoch: int,
+                           blocks: Sequence[torch.Tensor]) -> Bound:
+    rows, hidden = _rows_hidden(xs[0])
+    xp = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+    bp = (ctypes.c_void_p * len(blocks))(*[_ptr(b) for b in blocks])
+    return Bound(load().fc_pack_tagged_multi,
+                 [xp, len(xs), rows, hidden, ctypes.c_uint32(epoch), bp, None], 6, 4)
 
 
 def pack_tagged_multi(xs: Sequence[torch.Tensor], epoch: int, blocks: Sequence[torch.Tensor],
                       stream=None):
-    rows, hidden = _rows_hidden(xs[0])
-    xp = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
-    bp = (ctypes.c_void_p * len(blocks))(*[_ptr(b) for b in blocks])
-    _check(load().fc_pack_tagged_multi(xp, len(xs), rows, hidden, epoch, bp, _stream(stream)))
+    bind_pack_tagged_multi(xs, epoch, blocks)(stream)
 
 
 def allreduce_residual_rmsnorm(slabs, spec: QSpec, rows: int, hidden: int,
@@ -285,13 +331,26 @@ def allreduce_residual_rmsnorm(slabs, spec: QSpec, rows: int, hidden: int,
 
     slabs: list of P (codes, scales, zeros) tuples (INT8/INT4), or of bf16
     tensors / tagged-block tensors (BF16 / BF16_TAGGED)."""
+    bind_allreduce_residual_rmsnorm(slabs, spec, rows, hidden, residual_in, residual_out, gamma,
+                                    eps, y, requant_out, expected_epoch, d_status, max_ctas,
+                                    kernel)(stream)
+
+
+def bind_allreduce_residual_rmsnorm(slabs, spec: QSpec, rows: int, hidden: int,
+                                    residual_in: torch.Tensor, residual_out: torch.Tensor,
+                                    gamma: torch.Tensor, eps: float, y: torch.Tensor,
+                                    requant_out=None, expected_epoch: int = 0,
+                                    d_status: Optional[torch.Tensor] = None, max_ctas: int = 0,
+                                    kernel: int = KERNEL_AUTO) -> Bound:
+    """allreduce_residual_rmsnorm with its arguments marshalled once (Bound)."""
     qs = (QTensor * len(slabs))(*[_qt(s if isinstance(s, (tuple, list)) else (s,))
                                   for s in slabs])
     opts = LaunchOpts(max_ctas, kernel)
-    _check(load().fc_allreduce_residual_rmsnorm_ex(
-        qs, len(slabs), rows, hidden, spec, _ptr(residual_in), _ptr(residual_out), _ptr(gamma),
-        eps, _qt(requant_out), _ptr(y), expected_epoch, _ptr(d_status), ctypes.byref(opts),
-        _stream(stream)))
+    P = ctypes.c_void_p
+    args = [qs, len(slabs), rows, hidden, spec, P(_ptr(residual_in)), P(_ptr(residual_out)),
+            P(_ptr(gamma)), ctypes.c_float(eps), _qt(requant_out), P(_ptr(y)),
+            ctypes.c_uint32(expected_epoch), P(_ptr(d_status)), ctypes.byref(opts), None]
+    return Bound(load().fc_allreduce_residual_rmsnorm_ex, args, 14, 11, keep=(opts,))
 
 
 def token_split(spec: QSpec, P: int, rows: int, hidden: int):

@@ -82,6 +82,37 @@ class Pipeline:
             self.wave_rows = None
             self.bounds = [w.T * i // n for i in range(n + 1)]
         self.launches_per_step = self._launches()
+        self._bind()
+
+    def _bind(self):
+        """Marshal every launch of a step once (fcomm.Bound): a step then
+        spends no host time converting arguments."""
+        w = self.w
+        self._send, self._fuse, self._split = None, None, []
+        if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
+            self._send = fc.bind_group_quantize_multi(self.x, self.spec, self.codes)
+            self._fuse = fc.bind_allreduce_residual_rmsnorm(
+                self.codes, self.spec, w.T, w.H, self.residual, self.residual_out, self.gamma,
+                w.eps, self.y, requant_out=self.payload)
+        elif w.fmt in QTAGGED:
+            self._send = fc.bind_group_quantize_tagged(self.x, self.spec, self.epoch, self.blocks)
+            self._fuse = fc.bind_allreduce_residual_rmsnorm(
+                self.blocks, self.spec, w.T, w.H, self.residual, self.residual_out, self.gamma,
+                w.eps, self.y, requant_out=self.payload, expected_epoch=self.epoch,
+                d_status=self.status[0])
+        elif w.fmt == FMT_BF16:
+            self._fuse = fc.bind_allreduce_residual_rmsnorm(
+                self.x, self.spec, w.T, w.H, self.residual, self.residual_out, self.gamma, w.eps,
+                self.y)
+        else:
+            self._send = fc.bind_pack_tagged_multi(self.x, self.epoch, self.blocks)
+            bpr = fc.tagged_bytes(1, w.H)
+            for i in range(max(1, w.splits)):
+                r0, r1 = self.bounds[i], self.bounds[i + 1]
+                self._split.append(fc.bind_allreduce_residual_rmsnorm(
+                    [b[r0 * bpr:r1 * bpr] for b in self.blocks], self.spec, r1 - r0, w.H,
+                    self.residual[r0:r1], self.residual_out[r0:r1], self.gamma, w.eps,
+                    self.y[r0:r1], expected_epoch=self.epoch, d_status=self.status[i]))
 
     # ------------------------------------------------------------------
     def _launches(self) -> int:
@@ -110,49 +141,28 @@ class Pipeline:
     def sender(self, st):
         """Sender side: group-quantize (INT8/INT4) or pack with a fresh epoch (tagged)."""
         w = self.w
-        if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
-            fc.group_quantize_multi(self.x, self.spec, self.codes, stream=st)
-        elif w.fmt in QTAGGED:
+        if w.fmt in QTAGGED or w.fmt == FMT_BF16_TAGGED:
             self.epoch = (self.epoch + 1) & 0xFFFFFFFF
-            fc.group_quantize_tagged(self.x, self.spec, self.epoch, self.blocks, stream=st)
-        elif w.fmt == FMT_BF16_TAGGED:
-            self.epoch = (self.epoch + 1) & 0xFFFFFFFF
-            fc.pack_tagged_multi(self.x, self.epoch, self.blocks, stream=st)
+            self._send.epoch = self.epoch
+        if self._send is not None:
+            self._send(st)
 
     def consumer(self, st):
         """Receiver side: the fused reduce + residual add + RMSNorm."""
-        w = self.w
-        if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
-            fc.allreduce_residual_rmsnorm(self.codes, self.spec, w.T, w.H, self.residual,
-                                          self.residual_out, self.gamma, w.eps, self.y,
-                                          requant_out=self.payload, stream=st)
-        elif w.fmt in QTAGGED:
-            fc.allreduce_residual_rmsnorm(self.blocks, self.spec, w.T, w.H, self.residual,
-                                          self.residual_out, self.gamma, w.eps, self.y,
-                                          requant_out=self.payload, expected_epoch=self.epoch,
-                                          d_status=self.status[0], stream=st)
-        elif w.fmt == FMT_BF16:
-            fc.allreduce_residual_rmsnorm(self.x, self.spec, w.T, w.H, self.residual,
-                                          self.residual_out, self.gamma, w.eps, self.y,
-                                          stream=st)
+        if self._fuse is not None:
+            self._fuse.epoch = self.epoch
+            self._fuse(st)
         else:
             self._split_consume(st)
 
     def _split_consume(self, st):
-        w = self.w
-        n = max(1, w.splits)
-        bpr = fc.tagged_bytes(1, w.H)
-        bounds = self.bounds
         fork = torch.cuda.Event()
         fork.record(st)
         joins = []
-        for i, s in enumerate(self.streams):
-            r0, r1 = bounds[i], bounds[i + 1]
+        for call, s in zip(self._split, self.streams):
             s.wait_event(fork)
-            fc.allreduce_residual_rmsnorm(
-                [b[r0 * bpr:r1 * bpr] for b in self.blocks], self.spec, r1 - r0, w.H,
-                self.residual[r0:r1], self.residual_out[r0:r1], self.gamma, w.eps,
-                self.y[r0:r1], expected_epoch=self.epoch, d_status=self.status[i], stream=s)
+            call.epoch = self.epoch
+            call(s)
             ev = torch.cuda.Event()
             ev.record(s)
             joins.append(ev)

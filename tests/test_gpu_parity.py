@@ -743,3 +743,48 @@ def test_invalid_arguments_rejected_before_launch():
         fc.group_quantize(x, fc.QSpec(fc.FMT_INT8_SYM, 96), out)   # group not a power of 2
     with pytest.raises(fc.FcommError):
         fc.allreduce_residual_rmsnorm([out], spec, 2, 4096, x, x, x[0], 1e-5, x)  # P = 1
+
+
+def test_bound_call_epoch_and_repeat(orc):
+    """A bound fused call (arguments marshalled once) gives the same bits as
+    the plain call, again on a second launch, and a changed epoch makes
+    every block stale (first index 0) without touching the rest."""
+    w = small("tagged-bound", P=3, T=5, H=1040, fmt=TG, group=0)
+    inp = synth.make_inputs(w, seed=53)
+    xs = [dev_bf16(s) for s in inp["slabs"]]
+    blocks = [torch.empty(fc.tagged_bytes(w.T, w.H), dtype=torch.uint8, device="cuda")
+              for _ in range(w.P)]
+    fc.pack_tagged_multi(xs, 7, blocks)
+    res, gam = dev_bf16(inp["residual"]), dev_bf16(inp["gamma"])
+    h, y = torch.empty_like(res), torch.empty_like(res)
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    call = fc.bind_allreduce_residual_rmsnorm(blocks, fc.BF16_TAGGED, w.T, w.H, res, h, gam,
+                                              w.eps, y, expected_epoch=7, d_status=st)
+    want = oracle_fused(orc, w, inp)
+    for _ in range(2):
+        h.zero_(), y.zero_()
+        call()
+        torch.cuda.synchronize()
+        assert host(st).tolist() == [fc.FC_OK, fc.STATUS_NO_INDEX]
+        check_fused(orc, w, {"h": host_bits(h), "y": host_bits(y)}, want)
+    call.epoch = 8
+    assert call.epoch == 8
+    call()
+    torch.cuda.synchronize()
+    assert host(st).tolist() == [fc.FC_ERR_STALE_BLOCK, 0]
+
+
+def test_launch_shapes_alternate(orc):
+    """Calls whose staged kernels need different shared memory, in the order
+    large, small, large (the second large call reuses remembered launch
+    shapes), all match the oracle."""
+    for H in (16384, 1024, 16384):
+        w = small(f"i8-h{H}", P=4, T=3, H=H, fmt=I8, group=128)
+        inp = synth.make_inputs(w, seed=H)
+        outs = quantize_on_gpu(w, inp)
+        res, gam = dev_bf16(inp["residual"]), dev_bf16(inp["gamma"])
+        h, y = torch.empty_like(res), torch.empty_like(res)
+        fc.allreduce_residual_rmsnorm(outs, fc.INT8_G128, w.T, w.H, res, h, gam, w.eps, y,
+                                      kernel=fc.KERNEL_TMA)
+        torch.cuda.synchronize()
+        check_fused(orc, w, {"h": host_bits(h), "y": host_bits(y)}, oracle_fused(orc, w, inp))
