@@ -143,6 +143,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// --------------------------------------------- programmatic dependent launch --
+// Every kernel here is launched with programmatic stream serialization
+// (launch_pdl): it may be scheduled while the previous kernel in its stream
+// is still finishing.  pdl_begin() is each kernel's first statement: it
+// waits until that previous kernel has completed and its writes are visible
+// (griddepcontrol.wait; a no-op for a launch without the attribute), so no
+// global memory is touched before, and then lets the next kernel in the
+// stream be scheduled as resources free up (griddepcontrol.launch_dependents).
+// The grids here never exceed one wave of resident CTAs, so a dependent CTA
+// only takes a slot the current kernel no longer needs.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- bf16 --
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -38,6 +38,7 @@ __device__ __forceinline__ float block_sum(float v, float (*red)[32], int parity
 // ------------------------------------------------ BF16 / INT8 / INT4 path --
 template <int FMT, int NCH>
 __global__ void __launch_bounds__(kMaxThreads) k_fused(FusedArgs a) {
+  pdl_begin();
   __shared__ float red[2][32];
   const int tid = threadIdx.x, lane = tid & 31;
   const int nthr = blockDim.x;
@@ -239,6 +240,7 @@ __host__ __device__ constexpr int tag_stage_bytes() { return PMAX * 32 * 16 + 38
 
 template <int PMAX>
 __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
+  pdl_begin();
   extern __shared__ __align__(16) uint8_t tsmem[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -408,8 +410,7 @@ cudaError_t launch_rows(K kernel, int threads, const FusedArgs& a, int max_ctas,
   int64_t grid = static_cast<int64_t>(num_sms()) * occupancy(reinterpret_cast<const void*>(kernel), threads);
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   if (grid > a.rows) grid = a.rows;
-  kernel<<<static_cast<int>(grid), threads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), 0, st, a);
 }
 
 int round_warp(int t) { return (t + 31) & ~31; }
@@ -440,8 +441,7 @@ cudaError_t launch_warp_rows(K kernel, const FusedArgs& a, int max_ctas, cudaStr
   const int64_t need = (a.rows + 7) / 8;
   if (grid > need) grid = need;
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
-  kernel<<<static_cast<int>(grid), threads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), 0, st, a);
 }
 
 template <int PMAX>
@@ -464,8 +464,8 @@ cudaError_t launch_tagged_p(const FusedArgs& a, int max_ctas, cudaStream_t st) {
   const int64_t need = (a.rows + kTagWarps - 1) / kTagWarps;
   if (grid > need) grid = need;
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
-  k_fused_tagged<PMAX><<<static_cast<int>(grid), kTagWarps * 32, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_fused_tagged<PMAX>, dim3(static_cast<unsigned>(grid)), dim3(kTagWarps * 32), smem,
+                    st, a);
 }
 
 cudaError_t launch_tagged(const FusedArgs& a, int max_ctas, cudaStream_t st) {

@@ -94,11 +94,8 @@ cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cud
   if (sh.compact)
     return launch_fused_tma_compact(FMT, sh.nstage, a, g, sh.threads, sh.smem, grid, st);
   const dim3 gr(static_cast<unsigned>(grid));
-  if (sh.nstage == 2)
-    k_fused_tma<FMT, 2, PMAX><<<gr, sh.threads, sh.smem, st>>>(a, g);
-  else
-    k_fused_tma<FMT, 1, PMAX><<<gr, sh.threads, sh.smem, st>>>(a, g);
-  return cudaGetLastError();
+  if (sh.nstage == 2) return launch_pdl(k_fused_tma<FMT, 2, PMAX>, gr, dim3(sh.threads), sh.smem, st, a, g);
+  return launch_pdl(k_fused_tma<FMT, 1, PMAX>, gr, dim3(sh.threads), sh.smem, st, a, g);
 }
 
 // The slab loop is unrolled to PMAX (2, 4 or 8) slots, so no instruction is

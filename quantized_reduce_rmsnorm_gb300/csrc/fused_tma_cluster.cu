@@ -38,6 +38,11 @@ cudaError_t launch_cl(const FusedArgs& a, const TmaGeom& g, cudaStream_t st) {
   if (clusters < 1) return cudaErrorNotSupported;
   const int64_t n = a.rows < clusters ? a.rows : clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(n * CL));
+  cudaLaunchAttribute at2[2] = {at[0], {}};  // + programmatic stream serialization (launch_pdl)
+  at2[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at2[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at2;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, a, g);
 }
 

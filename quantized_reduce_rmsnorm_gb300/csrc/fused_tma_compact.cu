@@ -45,13 +45,9 @@ template <int FMT, int NS>
 cudaError_t launch_p(const FusedArgs& a, const TmaGeom& g, int threads, int smem, int64_t grid,
                      cudaStream_t st) {
   const dim3 gr(static_cast<unsigned>(grid));
-  if (a.P <= 2)
-    k_fused_tma<FMT, NS, 2, 1, true><<<gr, threads, smem, st>>>(a, g);
-  else if (a.P <= 4)
-    k_fused_tma<FMT, NS, 4, 1, true><<<gr, threads, smem, st>>>(a, g);
-  else
-    k_fused_tma<FMT, NS, 8, 1, true><<<gr, threads, smem, st>>>(a, g);
-  return cudaGetLastError();
+  if (a.P <= 2) return launch_pdl(k_fused_tma<FMT, NS, 2, 1, true>, gr, dim3(threads), smem, st, a, g);
+  if (a.P <= 4) return launch_pdl(k_fused_tma<FMT, NS, 4, 1, true>, gr, dim3(threads), smem, st, a, g);
+  return launch_pdl(k_fused_tma<FMT, NS, 8, 1, true>, gr, dim3(threads), smem, st, a, g);
 }
 
 template <int NS>

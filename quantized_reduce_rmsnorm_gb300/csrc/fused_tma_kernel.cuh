@@ -104,6 +104,7 @@ __device__ __forceinline__ void st_peer_u32(uint32_t addr, uint32_t v) {
 template <int FMT, int NSTAGE, int PMAX, int CL = 1, bool COMPACT = false>
 __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 1)
     k_fused_tma(FusedArgs a, TmaGeom g) {
+  pdl_begin();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float red[2][32];
   __shared__ uint64_t bar[NSTAGE];

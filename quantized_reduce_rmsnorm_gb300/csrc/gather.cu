@@ -22,6 +22,7 @@ constexpr int kGatherThreads = 256;
 
 template <int FMT, bool OUT_F32>
 __global__ void __launch_bounds__(kGatherThreads) k_allgather(GatherJob j) {
+  pdl_begin();
   constexpr bool TAGGED = FMT == kINT8T || FMT == kINT4T;
   constexpr int BASE = FMT == kINT8T ? kINT8 : FMT == kINT4T ? kINT4 : FMT;
   const int lane = threadIdx.x & 31;
@@ -124,11 +125,9 @@ cudaError_t launch_fmt(bool out_f32, const GatherJob& j, cudaStream_t st) {
   int64_t grid = (j.chunks + kGatherThreads - 1) / kGatherThreads;
   if (grid > 8LL * sms) grid = 8LL * sms;
   if (grid < 1) grid = 1;
-  if (out_f32)
-    k_allgather<FMT, true><<<static_cast<int>(grid), kGatherThreads, 0, st>>>(j);
-  else
-    k_allgather<FMT, false><<<static_cast<int>(grid), kGatherThreads, 0, st>>>(j);
-  return cudaGetLastError();
+  const dim3 gr(static_cast<unsigned>(grid));
+  if (out_f32) return launch_pdl(k_allgather<FMT, true>, gr, dim3(kGatherThreads), 0, st, j);
+  return launch_pdl(k_allgather<FMT, false>, gr, dim3(kGatherThreads), 0, st, j);
 }
 
 }  // namespace

@@ -59,6 +59,26 @@ struct FusedArgs {
 
 int num_sms();
 
+// Launches kern<<<grid, block, smem, st>>>(args...) with programmatic stream
+// serialization: the kernel may be scheduled while the previous kernel in st
+// is finishing (each kernel starts with pdl_begin(), which waits for it), so
+// back-to-back calls lose no launch gap.  Returns the launch status.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       const Args&... args) {
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Host-side memo of occupancy answers (resident CTAs, or clusters, per SM)
 // for one kernel at one launch shape on the current device.  Each answer is
 // queried once and then reused, so a call's host cost is its launch and not

@@ -24,6 +24,7 @@ constexpr int kUnroll = 2;
 template <int FMT, bool IN_F32, int DEQ>
 __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chunks,
                                                        int lpg_shift) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int lpg = 1 << lpg_shift;
   const int64_t tiles = (chunks + 31) >> 5;
@@ -147,6 +148,7 @@ constexpr int kQWarps = kThreads / 32;
 template <int FMT, bool TAGGED = false, int LPG = 0, int TILE = 2048>
 __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int lpg_shift,
                                                            int64_t tiles_per_slab) {
+  pdl_begin();
   constexpr int kWTile = TILE, kWStages = WRing<TILE>::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t bars[kQWarps][WRing<TILE>::kStages];
@@ -300,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int 
 template <int FMT>
 __global__ void __launch_bounds__(kThreads) k_reduce(Slabs s, int P, int lpg_shift, int64_t c0,
                                                      int64_t c1, float* out) {
+  pdl_begin();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
   for (int64_t c = c0 + static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; c < c1;
        c += stride) {
@@ -364,6 +367,7 @@ __device__ __forceinline__ uint32_t ld32_stream(const void* p) {
 
 __global__ void __launch_bounds__(kThreads) k_pack_tagged(PackJob job, int64_t rows, int H, int nb,
                                                           uint32_t epoch) {
+  pdl_begin();
   const uint16_t* __restrict__ x = job.x[blockIdx.y];
   uint4* blocks = job.blocks[blockIdx.y];
   const int lane = threadIdx.x & 31;
@@ -440,8 +444,8 @@ cudaError_t launch_quantize_t(const QuantJob& job, cudaStream_t st) {
   const int64_t tiles = (chunks + 31) / 32;
   const int64_t warps_needed = (tiles * job.P + kUnroll - 1) / kUnroll;
   const int grid = grid_for(warps_needed * 32, kThreads);
-  k_quantize<FMT, IN_F32, DEQ><<<grid, kThreads, 0, st>>>(job, chunks, log2_lanes(job.G));
-  return cudaGetLastError();
+  return launch_pdl(k_quantize<FMT, IN_F32, DEQ>, dim3(grid), dim3(kThreads), 0, st, job, chunks,
+                    log2_lanes(job.G));
 }
 
 }  // namespace
@@ -527,8 +531,8 @@ cudaError_t launch_quantize_tma_t(const QuantJob& job, cudaStream_t st) {
   int64_t grid = static_cast<int64_t>(num_sms()) * occ;
   const int64_t need = (tps * job.P + kQWarps - 1) / kQWarps;
   if (grid > need) grid = need;
-  kern<<<static_cast<int>(grid), kThreads, smem, st>>>(job, log2_lanes(job.G), tps);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, st, job,
+                    log2_lanes(job.G), tps);
 }
 
 // INT8 g128 (8 lanes per group) and INT4 g32 (2 lanes) are specialised
@@ -580,11 +584,8 @@ cudaError_t launch_reduce(int fmt, const Slabs& s, int P, int G, int64_t c0, int
                           float* out, cudaStream_t st) {
   if (c1 <= c0) return cudaSuccess;
   const int grid = grid_for(c1 - c0, kThreads);
-  if (fmt == kINT8)
-    k_reduce<kINT8><<<grid, kThreads, 0, st>>>(s, P, log2_lanes(G), c0, c1, out);
-  else
-    k_reduce<kINT4><<<grid, kThreads, 0, st>>>(s, P, log2_lanes(G), c0, c1, out);
-  return cudaGetLastError();
+  return launch_pdl(fmt == kINT8 ? k_reduce<kINT8> : k_reduce<kINT4>, dim3(grid), dim3(kThreads), 0, st,
+                    s, P, log2_lanes(G), c0, c1, out);
 }
 
 cudaError_t launch_pack_tagged(const void* const* x, void* const* blocks, int P, int64_t rows,
@@ -599,8 +600,7 @@ cudaError_t launch_pack_tagged(const void* const* x, void* const* blocks, int P,
   const int64_t lanes = rows * ((nb + 31) / 32) * 32;
   int grid = grid_for((lanes + kPackUnroll - 1) / kPackUnroll, kThreads);
   grid = (grid + P - 1) / P;  // the P slabs share the resident-CTA budget
-  k_pack_tagged<<<dim3(grid, P), kThreads, 0, st>>>(job, rows, H, nb, epoch);
-  return cudaGetLastError();
+  return launch_pdl(k_pack_tagged, dim3(grid, P), dim3(kThreads), 0, st, job, rows, H, nb, epoch);
 }
 
 }  // namespace fc
