@@ -82,6 +82,7 @@ class Pipeline:
             self.wave_rows = None
             self.bounds = [w.T * i // n for i in range(n + 1)]
         self.launches_per_step = self._launches()
+        self.graph = None
         self._bind()
 
     def _bind(self):
@@ -128,6 +129,36 @@ class Pipeline:
         st = stream or torch.cuda.current_stream(self.device)
         self.sender(st)
         self.consumer(st)
+
+    def capture(self):
+        """Capture one step into a CUDA graph; replay() then issues the whole
+        step with one host call (the launches keep their programmatic
+        dependent launch edges inside the graph).  Untagged formats only: a
+        tagged step packs a fresh epoch every time, which a graph would fix
+        at the captured value."""
+        w = self.w
+        if w.fmt in QTAGGED or w.fmt == FMT_BF16_TAGGED:
+            raise ValueError("graph capture is for untagged formats (the epoch changes per step)")
+        cur = torch.cuda.current_stream(self.device)
+        s = torch.cuda.Stream(self.device)
+        s.wait_stream(cur)
+        self.step(s)  # every launch shape resolved before capture
+        cur.wait_stream(s)
+        torch.cuda.synchronize(self.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            self.step(s)
+        self.graph = g
+        return g
+
+    def replay(self, stream=None):
+        """Launch the captured step (capture() first) on `stream` (default: current)."""
+        st = stream or torch.cuda.current_stream(self.device)
+        if st != torch.cuda.current_stream(self.device):
+            with torch.cuda.stream(st):
+                self.graph.replay()
+        else:
+            self.graph.replay()
 
     def step_marked(self, stream, marks):
         """step() with CUDA events marks[0], marks[1], marks[2] recorded before
