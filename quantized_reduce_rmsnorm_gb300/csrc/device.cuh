@@ -603,6 +603,32 @@ struct RegSettle {
   }
 };
 
+// The exact pass over register arrays, unrolled over the 16 element
+// positions: position i is visited (a warp-uniform branch) when it is
+// flagged in any lane of the warp, every lane computes element i's exact
+// code, and lanes that flagged it keep it.  Registers are indexed at
+// compile time, so a visit costs the exact code alone.  Measured on GB300
+// it pays where flagged elements are dense -- the requantized sum of two
+// INT4 slabs, whose quotients sit on or next to half-integers often (fused
+// kernel, 64 MB messages: 68 -> 60 us) -- and costs time in the larger
+// kernels of more slabs, which keep the index loop (settle_codes).
+template <bool SIGNED>
+__device__ __forceinline__ void settle_codes_regs(uint32_t mask, float s, float r, bool group_ok,
+                                                  const float v[16], uint32_t ub[16]) {
+  const uint32_t any = __reduce_or_sync(kFull, mask);
+  if (!any) return;
+  const float magic = SIGNED ? kMagicI8 : 8388608.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t bit = 1u << (8 * (i & 3) + (i >> 2));  // element 4w + b is mask bit 8b + w
+    if (any & bit) {
+      const float ci = __fsub_rn(__fmaf_rn(v[i], r, magic), magic);  // the fast path's code, recomputed
+      const float res = exact_code<SIGNED>(v[i], s, ci, __fmaf_rn(v[i], r, -ci), group_ok);
+      if (mask & bit) ub[i] = __float_as_uint(__fadd_rn(res, magic));
+    }
+  }
+}
+
 // Without a reload source the exact pass works on the register arrays.  A
 // Reload functor instead returns element i's bf16 bits (low 16 bits) from
 // memory the caller still holds (the sender's staged tile), and the exact
@@ -615,7 +641,9 @@ struct NoReload {
 //   s = max|x| / 127;  q = clamp(rne(x / s), -127, 127);  s == 0 -> q = 0.
 // Writes the codes packed in q[4]; with DEQ also d[i] = q_i * s.  Returns s.
 // With BFW, the lane's max|x| is taken from the packed bf16 inputs bw[8].
-template <bool DEQ, bool BFW = false, class Reload = NoReload>
+// UNROLLED: the exact pass over registers is settle_codes_regs (else the
+// index loop, settle_codes).
+template <bool DEQ, bool BFW = false, class Reload = NoReload, bool UNROLLED = false>
 __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q[4], float d[16],
                                           const uint32_t* bw = nullptr, Reload reload = Reload()) {
   float a = BFW ? bf16_absmax16(bw) : absmax16(v);
@@ -626,7 +654,8 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
   const bool ok = s == 0.0f || (__fmul_rn(a, r) <= 127.25f && s >= kTwoM100);
   const uint32_t mask = round_codes<true>(v, r, ok, ub);
   constexpr bool kReload = !std::is_same<Reload, NoReload>::value;
-  if (!kReload) settle_codes<true>(mask, s, r, ok, RegSettle{v, ub}, RegSettle{v, ub});
+  if (!kReload && UNROLLED) settle_codes_regs<true>(mask, s, r, ok, v, ub);
+  if (!kReload && !UNROLLED) settle_codes<true>(mask, s, r, ok, RegSettle{v, ub}, RegSettle{v, ub});
 #pragma unroll
   for (int j = 0; j < 4; ++j) q[j] = low_bytes4(ub[4 * j], ub[4 * j + 1], ub[4 * j + 2], ub[4 * j + 3]);
   if (kReload)
@@ -650,7 +679,7 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
 // Element 2i in the low nibble of byte i.  Returns s, writes z; with DEQ also
 // d[i] = (q_i * s) + z.  With BFW, the lane's min and max come from the
 // packed bf16 inputs bw[8].
-template <bool DEQ, bool BFW = false, class Reload = NoReload>
+template <bool DEQ, bool BFW = false, class Reload = NoReload, bool UNROLLED = false>
 __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q[2], float& z,
                                           float d[16], const uint32_t* bw = nullptr,
                                           Reload reload = Reload()) {
@@ -682,7 +711,8 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
   const bool ok = s == 0.0f || (__fmul_rn(span, r) <= 15.25f && s >= kTwoM100);
   const uint32_t mask = round_codes<false>(num, r, ok, ub);
   constexpr bool kReload = !std::is_same<Reload, NoReload>::value;
-  if (!kReload) settle_codes<false>(mask, s, r, ok, RegSettle{num, ub}, RegSettle{num, ub});
+  if (!kReload && UNROLLED) settle_codes_regs<false>(mask, s, r, ok, num, ub);
+  if (!kReload && !UNROLLED) settle_codes<false>(mask, s, r, ok, RegSettle{num, ub}, RegSettle{num, ub});
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const uint32_t ev = low_bytes4(ub[8 * j], ub[8 * j + 2], ub[8 * j + 4], ub[8 * j + 6]);

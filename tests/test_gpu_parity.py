@@ -820,3 +820,33 @@ def test_graph_capture_refuses_tagged():
     pipe = Pipeline(w, synth.make_inputs(w, seed=1))
     with pytest.raises(ValueError):
         pipe.capture()
+
+
+@pytest.mark.parametrize("fmt,G", [(I4, 32), (I8, 128)])
+@pytest.mark.parametrize("P", [2, 4])
+@pytest.mark.parametrize("kernel", [fc.KERNEL_AUTO, fc.KERNEL_STREAM], ids=["auto", "stream"])
+def test_fused_dense_exact_ties(orc, fmt, G, P, kernel):
+    """Requantized sums whose quotients are exact half-integers for a large
+    share of elements: every slab holds integers in [0, 15] (INT4) or
+    [-127, 127] (INT8), and every group of every slab holds both extremes at
+    the same positions, so the reduced group spans P times the slab range and
+    its scale is P times the slab scale.  The exact pass then settles dense
+    ties (INT4 with two slabs: every odd sum), in the staged kernel and in the
+    streaming kernel."""
+    T, H = 6, 2048
+    rng = np.random.default_rng(P * 10 + fmt)
+    lo, hi = (0, 15) if fmt == I4 else (-127, 127)
+    slabs = []
+    for _ in range(P):
+        x = rng.integers(lo, hi + 1, size=(T, H)).astype(np.float32)
+        x.reshape(T, H // G, G)[:, :, 0] = lo
+        x.reshape(T, H // G, G)[:, :, 1] = hi
+        slabs.append(orc.f32_to_bf16_array(x.ravel()).reshape(T, H))
+    base = synth.make_inputs(synth.Workload("ties", P=P, T=T, H=H, fmt=fmt, group=G), seed=5)
+    inp = dict(slabs=slabs, residual=base["residual"], gamma=base["gamma"])
+    w = synth.Workload("ties", P=P, T=T, H=H, fmt=fmt, group=G)
+    want = oracle_fused(orc, w, inp)
+    q = want["codes"].view(np.uint8)
+    if fmt == I4 and P == 2:  # a large share of the quotients were exact ties
+        assert np.mean(((q & 0xF) % 2 == 0)) > 0.55
+    check_fused(orc, w, run_fused(w, inp, kernel=kernel), want)
