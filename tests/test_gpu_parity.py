@@ -850,3 +850,33 @@ def test_fused_dense_exact_ties(orc, fmt, G, P, kernel):
     if fmt == I4 and P == 2:  # a large share of the quotients were exact ties
         assert np.mean(((q & 0xF) % 2 == 0)) > 0.55
     check_fused(orc, w, run_fused(w, inp, kernel=kernel), want)
+
+
+SWEEP_PARITY = [(msg, H, P, fmt, G) for msg in (16 << 10, 1 << 20, 16 << 20) for H in (4096, 8192)
+                for P in (2, 4, 8) for fmt, G in ((BF, 0), (I8, 128), (I4, 32))] + \
+               [(256 << 20, 8192, 8, I4, 32)]
+
+
+@pytest.mark.parametrize("msg,H,P,fmt,G", SWEEP_PARITY,
+                         ids=[f"{m >> 10}K-h{h}-p{p}-{synth.FMT_NAMES[f]}" for m, h, p, f, _ in SWEEP_PARITY])
+def test_sweep_point_sampled_rows(orc, msg, H, P, fmt, G):
+    """Message-size sweep shapes (every H, P and format at 16 KB, 1 MB and
+    16 MB messages, and the largest point, a 256 MB message with eight INT4
+    slabs) through the same Pipeline.step() as the benchmark, with seeded
+    N(0,1) inputs; the oracle checks the first, last and random rows."""
+    from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
+    T = msg // (2 * H)
+    w = synth.sweep_workload(H, T, P, fmt, G)
+    pipe = Pipeline(w, synth.make_inputs(w, seed=3))
+    pipe.step()
+    got = pipe.outputs()
+    rows = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(T).integers(0, T, 6)]))
+    sub = synth.Workload(**{**w.__dict__, "T": len(rows)})
+    want = oracle_fused(orc, sub, synth.make_inputs(w, seed=3, rows=rows))
+    assert_bits_equal(got["h"][rows], want["h"], "residual_out")
+    assert_y_close(got["y"][rows], want["y"])
+    if fmt in (I8, I4):
+        assert_bits_equal(got["codes"].reshape(T, -1)[rows], want["codes"], "payload codes")
+        assert_bits_equal(got["scales"].reshape(T, -1)[rows], want["scales"], "payload scales")
+        if fmt == I4:
+            assert_bits_equal(got["zeros"].reshape(T, -1)[rows], want["zeros"], "payload zeros")
