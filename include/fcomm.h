@@ -42,6 +42,16 @@
  *    last failure.  Data-dependent errors (a stale tagged block) are only
  *    reported through the optional device status words, so no call blocks.
  *  - rows == 0 is valid and launches nothing.
+ *  - Launch: every kernel is launched with programmatic stream serialization
+ *    (programmatic dependent launch, sm_90 and later).  It may be scheduled
+ *    while the previous kernel in the stream is finishing, but waits for it
+ *    to complete, and for its writes to become visible, before touching any
+ *    memory, so stream order is kept.  It also lets the next kernel in the
+ *    stream be scheduled early: a kernel the caller launches next with the
+ *    same attribute must execute griddepcontrol.wait
+ *    (cudaGridDependencySynchronize) before it reads this call's outputs.
+ *    A kernel launched without the attribute, and any copy, event or
+ *    host synchronization, is ordered as usual.
  */
 #ifndef FCOMM_H
 #define FCOMM_H

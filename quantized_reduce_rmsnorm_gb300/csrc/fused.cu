@@ -432,18 +432,6 @@ cudaError_t launch_fmt(const FusedArgs& a, int max_ctas, cudaStream_t st) {
   }
 }
 
-// One warp per row: the grid covers the rows with 8-warp CTAs (capped by
-// max_ctas and by the resident limit).
-template <typename K>
-cudaError_t launch_warp_rows(K kernel, const FusedArgs& a, int max_ctas, cudaStream_t st) {
-  const int threads = 256;
-  int64_t grid = static_cast<int64_t>(num_sms()) * occupancy(reinterpret_cast<const void*>(kernel), threads);
-  const int64_t need = (a.rows + 7) / 8;
-  if (grid > need) grid = need;
-  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
-  return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), 0, st, a);
-}
-
 template <int PMAX>
 int tagged_occupancy() {
   constexpr int smem = kTagWarps * kTagStages * tag_stage_bytes<PMAX>();
