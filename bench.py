@@ -435,9 +435,15 @@ def run_ours(args):
 
 def run_e2e(pipe, inputs, step_bytes, args, ws, dev):
     """The same metric through the public API with host buffers: every step
-    copies the inputs from pinned host memory and reads y and residual_out
-    back, all inside the timed region."""
+    copies its inputs from pinned host memory and reads y and residual_out
+    back, all inside the timed region.  Steps are pipelined as a serving loop
+    would run them: two device buffer sets, the uploads on one stream, the
+    step on a second and the downloads on a third, so step i+1's upload
+    overlaps step i's compute and download (measured on GB300: the upload,
+    at ~190 GB/s from pinned memory, bounds the step; a second upload stream
+    gains nothing)."""
     import torch
+    from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
     w = pipe.w
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
         torch.bfloat16).reshape(a.shape).pin_memory()
@@ -445,34 +451,51 @@ def run_e2e(pipe, inputs, step_bytes, args, ws, dev):
     h_res, h_gam = pin(inputs["residual"]), pin(inputs["gamma"])
     h_y = torch.empty(pipe.y.shape, dtype=torch.bfloat16).pin_memory()
     h_h = torch.empty(pipe.y.shape, dtype=torch.bfloat16).pin_memory()
-    st = torch.cuda.current_stream(dev)
     h2d = sum(t.numel() * 2 for t in h_slabs) + h_res.numel() * 2 + h_gam.numel() * 2
     d2h = 2 * h_y.numel() * 2
+    sets = [pipe, Pipeline(w, inputs, device=dev, split=args.split)]
+    s_up, s_cp, s_dn = (torch.cuda.Stream(dev) for _ in range(3))
+    up_done, comp_done, down_done = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+    for ev in comp_done + down_done:
+        ev.record(torch.cuda.current_stream(dev))
 
-    def one():
-        for d, h in zip(pipe.x, h_slabs):
-            d.copy_(h, non_blocking=True)
-        pipe.residual.copy_(h_res, non_blocking=True)
-        pipe.gamma.copy_(h_gam, non_blocking=True)
-        pipe.step(st)
-        h_y.copy_(pipe.y, non_blocking=True)
-        h_h.copy_(pipe.residual_out, non_blocking=True)
+    def one(i):
+        k = i & 1
+        p = sets[k]
+        s_up.wait_event(comp_done[k])  # the set's previous step has read its inputs
+        with torch.cuda.stream(s_up):
+            for d, h in zip(p.x, h_slabs):
+                d.copy_(h, non_blocking=True)
+            p.residual.copy_(h_res, non_blocking=True)
+            p.gamma.copy_(h_gam, non_blocking=True)
+        up_done[k].record(s_up)
+        s_cp.wait_event(up_done[k])
+        s_cp.wait_event(down_done[k])  # the set's previous outputs are read back
+        p.step(s_cp)
+        comp_done[k].record(s_cp)
+        s_dn.wait_event(comp_done[k])
+        with torch.cuda.stream(s_dn):
+            h_y.copy_(p.y, non_blocking=True)
+            h_h.copy_(p.residual_out, non_blocking=True)
+        down_done[k].record(s_dn)
 
     steps = max(3, min(args.steps, 20))
-    for _ in range(min(3, args.warmup)):
-        one()
+    warm = max(2, min(3, args.warmup))
+    for i in range(warm):
+        one(i)
     torch.cuda.synchronize(dev)
     barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(steps):
-        one()
-    e1.record(st)
+    e0.record(s_up)
+    for i in range(steps):
+        one(warm + i)
+    e1.record(s_dn)
     torch.cuda.synchronize(dev)
     ms = allreduce_max(e0.elapsed_time(e1) / steps, ws, dev)
     return {"value": round(whole_job_gbs(step_bytes, ws, ms), 2), "unit": UNIT,
             "ms_per_step": round(ms, 4), "steps": steps, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+            "d2h_bytes_per_step": d2h,
+            "pipelining": "two device buffer sets; upload, step and download on three streams"}
 
 
 def whole_job_gbs(bytes_per_rank_step: int, ws: int, max_step_ms: float) -> float:
