@@ -101,20 +101,27 @@ __device__ __forceinline__ void st_peer_u32(uint32_t addr, uint32_t v) {
 // COMPACT: built for at most 256 threads and three CTAs per SM (about 80
 // registers, a few values spilled), for shapes where shared memory admits
 // more CTAs than the full register budget does.
-template <int FMT, int NSTAGE, int PMAX, int CL = 1, bool COMPACT = false>
+// SUB: sub-stages per stage (CL == 1 only).  With SUB > 1 the geometry g
+// describes one of SUB equal segments of the row, each stage is SUB
+// segment-sized sub-stages on their own mbarriers, and the CTA's threads take
+// one segment per pass-1 iteration (blockDim.x == g.cps): a sub-stage is
+// refilled with the next row as soon as every thread is past it, instead of
+// after the whole row, so the next row's bytes have longer to land.
+template <int FMT, int NSTAGE, int PMAX, int CL = 1, bool COMPACT = false, int SUB = 1>
 __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 1)
     k_fused_tma(FusedArgs a, TmaGeom g) {
   pdl_begin();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float red[2][32];
-  __shared__ uint64_t bar[NSTAGE];
+  static_assert(CL == 1 || SUB == 1, "sub-stages are for a CTA per row");
+  __shared__ uint64_t bar[NSTAGE * SUB];
   __shared__ float cl_tot[2][CL];       // per-CTA sums of squares of the row (cluster)
   __shared__ uint32_t cl_ok[2][CL];     // per-CTA "staged copy arrived" votes
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
   const int nthr = blockDim.x;
   const int H = a.H, cpr = H >> 4, P = a.P;
   const int rank = CL > 1 ? static_cast<int>(cluster_rank()) : 0;
-  const int cps = g.cps, c0 = rank * cps;  // this CTA's chunks of every row
+  const int cps = SUB * g.cps, c0 = rank * cps;  // this CTA's chunks of every row
   const float inv_h = 1.0f / static_cast<float>(H);
   const int lpg = a.G >> 4, sh = a.lpg_shift;
   // h (the bf16 row) lives in its own buffer: each thread reads back only the
@@ -130,11 +137,13 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
   const int64_t seg_blk = rank * (g.cb / 16);  // ... before this CTA's segment
 
   if (tid == 0) {
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(&bar[s], 1);
+    for (int s = 0; s < NSTAGE * SUB; ++s) mbar_init(&bar[s], 1);
     mbar_init_fence();
     for (int s = 0; s < NSTAGE; ++s)
       if (row0 + s * rstride < a.rows)
-        issue_row<FMT>(a, g, stage0 + s * g.stage_bytes, &bar[s], row0 + s * rstride, rank);
+        for (int j = 0; j < SUB; ++j)
+          issue_row<FMT>(a, g, stage0 + (s * SUB + j) * g.stage_bytes, &bar[s * SUB + j], row0 + s * rstride,
+                         SUB > 1 ? j : rank);
   }
   __syncthreads();
   if (CL > 1) cluster_barrier();  // every CTA of the cluster runs before any peer store
@@ -158,12 +167,8 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
   int i = 0;
   for (int64_t row = row0; row < a.rows; row += rstride, ++i) {
     const int s = i % NSTAGE;
-    const uint8_t* st = stage0 + s * g.stage_bytes;
-    const bool ok = mbar_wait_bounded(&bar[s], (i / NSTAGE) & 1);
-    const uint8_t* codes = st;
-    const float* scales = reinterpret_cast<const float*>(st + P * g.cb);
-    const float* zeros = reinterpret_cast<const float*>(st + P * (g.cb + g.sb));
-    const uint4* rrow = reinterpret_cast<const uint4*>(st + P * (g.cb + g.sb + g.zb));
+    const uint32_t par = (i / NSTAGE) & 1;
+    bool ok = SUB > 1 ? true : mbar_wait_bounded(&bar[s], par);
 
     // ---- pass 1: reduce, requantize, dequantize, residual add (h -> hbuf).
     // Every thread runs the same number of iterations so whole warps join
@@ -172,8 +177,16 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
     float2 ss2 = make_float2(0.0f, 0.0f);
     int64_t first_bad = LLONG_MAX;
     for (int cbase = 0; cbase < cps; cbase += nthr) {
-      const int c = cbase + tid;  // chunk of the segment (and of the stage)
+      const int c = cbase + tid;  // chunk of the CTA's part of the row
       const bool act = c < cps;
+      const int j = SUB > 1 ? cbase / nthr : 0;  // its sub-stage
+      if (SUB > 1) ok = mbar_wait_bounded(&bar[s * SUB + j], par) && ok;
+      const int cs = c - j * g.cps;  // chunk within the (sub-)stage
+      const uint8_t* st = stage0 + (s * SUB + j) * g.stage_bytes;
+      const uint8_t* codes = st;
+      const float* scales = reinterpret_cast<const float*>(st + P * g.cb);
+      const float* zeros = reinterpret_cast<const float*>(st + P * (g.cb + g.sb));
+      const uint4* rrow = reinterpret_cast<const uint4*>(st + P * (g.cb + g.sb + g.zb));
       float acc[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
@@ -181,7 +194,7 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
       for (int p = 0; p < PMAX; ++p) {
         if (p < P && act) {
           if (FMT == kBF16) {
-            const uint4* x = reinterpret_cast<const uint4*>(codes + p * g.cb) + 2 * c;
+            const uint4* x = reinterpret_cast<const uint4*>(codes + p * g.cb) + 2 * cs;
             const uint4 x0 = x[0], x1 = x[1];
             const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
@@ -193,7 +206,7 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
           } else if (FMT == kINT8T) {
             // group c>>3, lane k = c&7: code bytes 16k.. = words o.. of blocks b0, b0+1
             const int gl = c >> 3, k = c & 7, b0 = (4 * k) / 3, o = 4 * k - 3 * b0;
-            const uint4* gb = reinterpret_cast<const uint4*>(codes + p * g.cb) + gl * kBlocksPerGroupI8;
+            const uint4* gb = reinterpret_cast<const uint4*>(codes + p * g.cb) + (cs >> 3) * kBlocksPerGroupI8;
             const uint4 B0 = gb[b0], B1 = gb[b0 + 1], BS = gb[kBlocksPerGroupI8 - 1];
             if (B0.w == a.epoch && B1.w == a.epoch && BS.w == a.epoch) {
               const uint32_t W[6] = {B0.x, B0.y, B0.z, B1.x, B1.y, B1.z};
@@ -210,7 +223,7 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
           } else if (FMT == kINT4T) {
             // group c>>1: block 0 = {codes 0-3, 4-7, 8-11}, block 1 = {codes 12-15, scale, zero}
             const int gl = c >> 1, k = c & 1;
-            const uint4* gb = reinterpret_cast<const uint4*>(codes + p * g.cb) + gl * kBlocksPerGroupI4;
+            const uint4* gb = reinterpret_cast<const uint4*>(codes + p * g.cb) + (cs >> 1) * kBlocksPerGroupI4;
             const uint4 B0 = gb[0], B1 = gb[1];
             if (B0.w == a.epoch && B1.w == a.epoch) {
               const uint32_t w[2] = {k ? B0.z : B0.x, k ? B1.x : B0.y};
@@ -221,13 +234,13 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
               first_bad = bad < first_bad ? bad : first_bad;
             }
           } else if (FMT == kINT8) {
-            const uint4 q = reinterpret_cast<const uint4*>(codes + p * g.cb)[c];
+            const uint4 q = reinterpret_cast<const uint4*>(codes + p * g.cb)[cs];
             const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-            dequant_i8_acc(w, scales[p * (g.sb >> 2) + (c >> sh)], acc);
+            dequant_i8_acc(w, scales[p * (g.sb >> 2) + (cs >> sh)], acc);
           } else {
-            const uint2 q = reinterpret_cast<const uint2*>(codes + p * g.cb)[c];
+            const uint2 q = reinterpret_cast<const uint2*>(codes + p * g.cb)[cs];
             const uint32_t w[2] = {q.x, q.y};
-            const int gi = p * (g.sb >> 2) + (c >> sh);
+            const int gi = p * (g.sb >> 2) + (cs >> sh);
             dequant_i4_acc(w, scales[gi], zeros[gi], acc);
           }
         }
@@ -256,7 +269,7 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
       if (act) {
         // h = bf16(fl(o + R)) straight from the packed residual; sum of h^2
         // straight from the packed h
-        const uint4 r0 = rrow[2 * c], r1 = rrow[2 * c + 1];
+        const uint4 r0 = rrow[2 * cs], r1 = rrow[2 * cs + 1];
         const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
         V8 hv;
 #pragma unroll
@@ -270,6 +283,17 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
         for (int k = 0; k < 8; ++k) {
           ss2.x = fma_bf_lo(hv.w[k], hv.w[k], ss2.x);
           ss2.y = fma_bf_hi(hv.w[k], hv.w[k], ss2.y);
+        }
+      }
+      if (SUB > 1 && j < SUB - 1) {
+        // every thread is past sub-stage j: refill it with the next row's segment
+        __syncthreads();
+        if (tid == 0 && ok) {
+          const int64_t nrow = row + NSTAGE * rstride;
+          if (nrow < a.rows) {
+            fence_proxy_async_smem();
+            issue_row<FMT>(a, g, stage0 + (s * SUB + j) * g.stage_bytes, &bar[s * SUB + j], nrow, j);
+          }
         }
       }
     }
@@ -309,12 +333,14 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
     if (!all_ok) break;
     const float inv = inv_rms(tot, inv_h, a.eps);
 
-    // every thread is past its reads of stage s: refill it NSTAGE rows ahead
+    // every thread is past its reads of stage s (its last sub-stage): refill
+    // it NSTAGE rows ahead
     if (tid == 0) {
       const int64_t nrow = row + NSTAGE * rstride;
       if (nrow < a.rows) {
         fence_proxy_async_smem();
-        issue_row<FMT>(a, g, stage0 + s * g.stage_bytes, &bar[s], nrow, rank);
+        issue_row<FMT>(a, g, stage0 + (s * SUB + SUB - 1) * g.stage_bytes, &bar[s * SUB + SUB - 1], nrow,
+                       SUB > 1 ? SUB - 1 : rank);
       }
     }
 
@@ -344,7 +370,7 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
     // a staged copy did not land within the bound: report it and give the
     // copies still in flight one more bounded wait before the CTA exits
     if (a.status) atomicExch(a.status, 2 /* FC_ERR_CUDA */);
-    for (int s = 0; s < NSTAGE; ++s) {
+    for (int s = 0; s < NSTAGE * SUB; ++s) {
       mbar_wait_bounded(&bar[s], 0);
       mbar_wait_bounded(&bar[s], 1);
     }
