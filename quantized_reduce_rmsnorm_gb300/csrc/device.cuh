@@ -713,11 +713,17 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
   constexpr bool kReload = !std::is_same<Reload, NoReload>::value;
   if (!kReload && UNROLLED) settle_codes_regs<false>(mask, s, r, ok, num, ub);
   if (!kReload && !UNROLLED) settle_codes<false>(mask, s, r, ok, RegSettle{num, ub}, RegSettle{num, ub});
+  // Nibble packing by multiply-adds: ub = 0x4B000000 + code with code in
+  // [0, 15] wherever the fast path holds, so sum_i ub[8j+i] * 16^i is the
+  // packed word plus 0x4B000000 * 0x11111111 = 0xFB000000 (mod 2^32).
+  // (Groups outside the fast path have every nibble rewritten by the exact
+  // pass.)
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    const uint32_t ev = low_bytes4(ub[8 * j], ub[8 * j + 2], ub[8 * j + 4], ub[8 * j + 6]);
-    const uint32_t od = low_bytes4(ub[8 * j + 1], ub[8 * j + 3], ub[8 * j + 5], ub[8 * j + 7]);
-    q[j] = ev | (od << 4);
+    uint32_t w = ub[8 * j + 7];
+#pragma unroll
+    for (int i = 6; i >= 1; --i) w = w * 16u + ub[8 * j + i];
+    q[j] = w * 16u + (ub[8 * j] - 0xFB000000u);
   }
   if (kReload)
     settle_codes_lanewise<false>(
