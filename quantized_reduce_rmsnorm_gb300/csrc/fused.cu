@@ -235,6 +235,15 @@ __device__ __forceinline__ void cp_async_wait() {
 
 constexpr int kTagStages = 3;  // block groups in a warp's ring
 constexpr int kTagWarps = 8;
+// A row is shared by kTagRowWarps warps, each streaming a contiguous share of
+// its block groups; their sums of squares meet in shared memory at one CTA
+// barrier per kTagRowsPerCta rows, and persistent CTAs walk the row pairs.
+// Measured on GB300 (token split, two 2048-row subsets of 5120 on two
+// streams, both consumer calls): a warp per row (the last of two waves of
+// CTAs two-thirds full) 122.8 us; two warps per row 123.4 us; four 116.2 us;
+// eight 119.6 us.
+constexpr int kTagRowWarps = 4;
+constexpr int kTagRowsPerCta = kTagWarps / kTagRowWarps;
 template <int PMAX>
 __host__ __device__ constexpr int tag_stage_bytes() { return PMAX * 32 * 16 + 384; }  // 32 blocks per slab + residual
 
@@ -242,9 +251,9 @@ template <int PMAX>
 __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
   pdl_begin();
   extern __shared__ __align__(16) uint8_t tsmem[];
+  __shared__ float red[2][kTagRowsPerCta][kTagRowWarps];  // per-warp sums of squares
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int slot = wid / kTagRowWarps, part = wid % kTagRowWarps;
   const int H = a.H;
   const int nb = (H + 5) / 6;
   const int gpr = (nb + 31) >> 5;
@@ -252,91 +261,99 @@ __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
   const uint32_t epoch = a.epoch;
   constexpr int kStage = tag_stage_bytes<PMAX>();
   uint8_t* ring = tsmem + wid * (kTagStages * kStage);
+  // this warp's block groups of every row: a contiguous share of the row
+  const int g0 = part * gpr / kTagRowWarps, g1 = (part + 1) * gpr / kTagRowWarps;
 
-  for (int64_t row = w0; row < a.rows; row += nw) {
+  int it = 0;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kTagRowsPerCta; base < a.rows;
+       base += static_cast<int64_t>(gridDim.x) * kTagRowsPerCta, ++it) {
+    const int64_t row = base + slot;
+    const bool live = row < a.rows;  // warp-uniform
     const uint16_t* rr = static_cast<const uint16_t*>(a.res_in) + row * H;
     uint16_t* ro = static_cast<uint16_t*>(a.res_out) + row * H;
     float ss = 0.0f;
     int64_t first_bad = LLONG_MAX;
-    // every lane copies its own block of each slab and 16 bytes of the
-    // group's residual chunk (384 bytes = 32 lanes x 6 bf16, 16-byte aligned)
-    auto issue = [&](int gi) {
-      if (gi < gpr) {
-        uint8_t* st = ring + (gi % kTagStages) * kStage;
+    if (live) {
+      // every lane copies its own block of each slab and 16 bytes of the
+      // group's residual chunk (384 bytes = 32 lanes x 6 bf16, 16-byte aligned)
+      auto issue = [&](int gi) {
+        if (gi < g1) {
+          uint8_t* st = ring + ((gi - g0) % kTagStages) * kStage;
+          const int j = gi * 32 + lane;
+          if (j < nb) {
+#pragma unroll
+            for (int p = 0; p < PMAX; ++p)
+              if (p < P)
+                cp_async16(st + (p * 32 + lane) * 16, static_cast<const uint4*>(a.s.codes[p]) + row * nb + j);
+          }
+          const int rbytes = 2 * H - 384 * gi < 384 ? 2 * H - 384 * gi : 384;
+          if (16 * lane < rbytes)
+            cp_async16(st + PMAX * 512 + 16 * lane, reinterpret_cast<const uint8_t*>(rr) + 384 * gi + 16 * lane);
+        }
+        cp_async_commit();  // one commit group per block group (possibly empty)
+      };
+#pragma unroll
+      for (int k = 0; k < kTagStages - 1; ++k) issue(g0 + k);
+      for (int gi = g0; gi < g1; ++gi) {
+        issue(gi + kTagStages - 1);
+        cp_async_wait<kTagStages - 1>();  // this lane's copies of group gi have landed
+        __syncwarp();                     // and every lane's (the residual chunk is shared)
+        const uint8_t* st = ring + ((gi - g0) % kTagStages) * kStage;
         const int j = gi * 32 + lane;
         if (j < nb) {
+          const int e0 = 6 * j;
+          const bool full = e0 + 6 <= H;
+          float acc[6] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-          for (int p = 0; p < PMAX; ++p)
-            if (p < P)
-              cp_async16(st + (p * 32 + lane) * 16, static_cast<const uint4*>(a.s.codes[p]) + row * nb + j);
-        }
-        const int rbytes = 2 * H - 384 * gi < 384 ? 2 * H - 384 * gi : 384;
-        if (16 * lane < rbytes)
-          cp_async16(st + PMAX * 512 + 16 * lane, reinterpret_cast<const uint8_t*>(rr) + 384 * gi + 16 * lane);
-      }
-      cp_async_commit();  // one commit group per block group (possibly empty)
-    };
+          for (int p = 0; p < PMAX; ++p) {
+            if (p < P) {
+              const uint4 bp = *reinterpret_cast<const uint4*>(st + (p * 32 + lane) * 16);
+              if (bp.w == epoch) {
+                const uint32_t w[3] = {bp.x, bp.y, bp.z};
 #pragma unroll
-    for (int gi = 0; gi < kTagStages - 1; ++gi) issue(gi);
-    for (int gi = 0; gi < gpr; ++gi) {
-      issue(gi + kTagStages - 1);
-      cp_async_wait<kTagStages - 1>();  // this lane's copies of group gi have landed
-      __syncwarp();                     // and every lane's (the residual chunk is shared)
-      const uint8_t* st = ring + (gi % kTagStages) * kStage;
-      const int j = gi * 32 + lane;
-      if (j < nb) {
-        const int e0 = 6 * j;
-        const bool full = e0 + 6 <= H;
-        float acc[6] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int p = 0; p < PMAX; ++p) {
-          if (p < P) {
-            const uint4 bp = *reinterpret_cast<const uint4*>(st + (p * 32 + lane) * 16);
-            if (bp.w == epoch) {
-              const uint32_t w[3] = {bp.x, bp.y, bp.z};
-#pragma unroll
-              for (int k = 0; k < 3; ++k) {
-                const float2 t = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
-                                      make_float2(bf_lo(w[k]), bf_hi(w[k])));
-                acc[2 * k] = t.x, acc[2 * k + 1] = t.y;
+                for (int k = 0; k < 3; ++k) {
+                  const float2 t = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
+                                        make_float2(bf_lo(w[k]), bf_hi(w[k])));
+                  acc[2 * k] = t.x, acc[2 * k + 1] = t.y;
+                }
+              } else {
+                const int64_t idx = (static_cast<int64_t>(p) * a.rows + row) * nb + j;
+                first_bad = idx < first_bad ? idx : first_bad;
               }
-            } else {
-              const int64_t idx = (static_cast<int64_t>(p) * a.rows + row) * nb + j;
-              first_bad = idx < first_bad ? idx : first_bad;
             }
           }
-        }
-        const uint8_t* rs = st + PMAX * 512 + 12 * lane;  // this lane's 6 residual values
-        uint32_t rw[3];
-        if (full) {
+          const uint8_t* rs = st + PMAX * 512 + 12 * lane;  // this lane's 6 residual values
+          uint32_t rw[3];
+          if (full) {
 #pragma unroll
-          for (int k = 0; k < 3; ++k) rw[k] = *reinterpret_cast<const uint32_t*>(rs + 4 * k);
-        } else {
+            for (int k = 0; k < 3; ++k) rw[k] = *reinterpret_cast<const uint32_t*>(rs + 4 * k);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+              const int e = e0 + 2 * k;
+              const uint32_t lo = e < H ? *reinterpret_cast<const uint16_t*>(rs + 4 * k) : 0u;
+              const uint32_t hi = e + 1 < H ? *reinterpret_cast<const uint16_t*>(rs + 4 * k + 2) : 0u;
+              rw[k] = lo | (hi << 16);
+            }
+          }
+          uint32_t hw[3];
 #pragma unroll
           for (int k = 0; k < 3; ++k) {
-            const int e = e0 + 2 * k;
-            const uint32_t lo = e < H ? *reinterpret_cast<const uint16_t*>(rs + 4 * k) : 0u;
-            const uint32_t hi = e + 1 < H ? *reinterpret_cast<const uint16_t*>(rs + 4 * k + 2) : 0u;
-            rw[k] = lo | (hi << 16);
+            const float2 h = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
+                                  make_float2(bf_lo(rw[k]), bf_hi(rw[k])));
+            hw[k] = pack_bf2(h.x, h.y);
+            const float h0 = bf_lo(hw[k]), h1 = bf_hi(hw[k]);
+            ss = __fmaf_rn(h0, h0, ss);
+            ss = __fmaf_rn(h1, h1, ss);
           }
+          store6(ro, e0, H, full, hw);
         }
-        uint32_t hw[3];
-#pragma unroll
-        for (int k = 0; k < 3; ++k) {
-          const float2 h = padd(make_float2(acc[2 * k], acc[2 * k + 1]),
-                                make_float2(bf_lo(rw[k]), bf_hi(rw[k])));
-          hw[k] = pack_bf2(h.x, h.y);
-          const float h0 = bf_lo(hw[k]), h1 = bf_hi(hw[k]);
-          ss = __fmaf_rn(h0, h0, ss);
-          ss = __fmaf_rn(h1, h1, ss);
-        }
-        store6(ro, e0, H, full, hw);
+        __syncwarp();  // every lane is done with this slot before it is refilled
       }
-      __syncwarp();  // every lane is done with this slot before it is refilled
+      cp_async_wait<0>();
     }
-    cp_async_wait<0>();
     ss = warp_sum(ss);
-    // first failing block of the row (lanes agree via a min-reduction)
+    // first failing block of this warp's share (lanes agree via a min-reduction)
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) {
       const int64_t o = __shfl_xor_sync(kFull, first_bad, m);
@@ -346,17 +363,24 @@ __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
       atomicCAS(a.status, 0, 3 /* FC_ERR_STALE_BLOCK */);
       atomicMin(a.status + 1, first_bad < INT_MAX ? static_cast<int>(first_bad) : INT_MAX - 1);
     }
-    const float inv = inv_rms(ss, 1.0f / static_cast<float>(H), a.eps);
+    // the row's sum of squares from its warps' shares, in share order
+    if (lane == 0) red[it & 1][slot][part] = ss;
+    __syncthreads();
+    if (!live) continue;
+    float tot = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kTagRowWarps; ++q) tot += red[it & 1][slot][q];
+    const float inv = inv_rms(tot, 1.0f / static_cast<float>(H), a.eps);
     // pass 2 in batches of kOutBatch block groups: all their loads (h, which
     // this lane wrote above and is in L2, and gamma) are issued before any
     // is used, so the L2 latency is paid once per batch
     constexpr int kOutBatch = 4;
-    for (int gb = 0; gb < gpr; gb += kOutBatch) {
+    for (int gb = g0; gb < g1; gb += kOutBatch) {
       uint32_t hw[kOutBatch][3], gw[kOutBatch][3];
 #pragma unroll
       for (int u = 0; u < kOutBatch; ++u) {
         const int j = (gb + u) * 32 + lane;
-        if (gb + u < gpr && j < nb) {
+        if (gb + u < g1 && j < nb) {
           const int e0 = 6 * j;
           load6<false>(ro, e0, H, e0 + 6 <= H, hw[u]);
           load6<true>(static_cast<const uint16_t*>(a.gamma), e0, H, e0 + 6 <= H, gw[u]);
@@ -365,7 +389,7 @@ __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
 #pragma unroll
       for (int u = 0; u < kOutBatch; ++u) {
         const int j = (gb + u) * 32 + lane;
-        if (gb + u < gpr && j < nb) {
+        if (gb + u < g1 && j < nb) {
           const int e0 = 6 * j;
           uint32_t yw[3];
 #pragma unroll
@@ -449,7 +473,7 @@ template <int PMAX>
 cudaError_t launch_tagged_p(const FusedArgs& a, int max_ctas, cudaStream_t st) {
   constexpr int smem = kTagWarps * kTagStages * tag_stage_bytes<PMAX>();
   int64_t grid = static_cast<int64_t>(num_sms()) * tagged_occupancy<PMAX>();
-  const int64_t need = (a.rows + kTagWarps - 1) / kTagWarps;
+  const int64_t need = (a.rows + kTagRowsPerCta - 1) / kTagRowsPerCta;
   if (grid > need) grid = need;
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   return launch_pdl(k_fused_tagged<PMAX>, dim3(static_cast<unsigned>(grid)), dim3(kTagWarps * 32), smem,
@@ -468,7 +492,7 @@ cudaError_t launch_tagged(const FusedArgs& a, int max_ctas, cudaStream_t st) {
 int64_t fused_wave_rows(int fmt, const FusedArgs& a) {
   if (fmt == kTAGGED) {
     const int occ = a.P <= 2 ? tagged_occupancy<2>() : a.P <= 4 ? tagged_occupancy<4>() : tagged_occupancy<8>();
-    return static_cast<int64_t>(num_sms()) * occ * kTagWarps;  // a warp per row
+    return static_cast<int64_t>(num_sms()) * occ * kTagRowsPerCta;  // kTagRowWarps warps per row
   }
   if (fused_tma_eligible(fmt, a)) return fused_tma_wave_rows(fmt, a);
   if (fmt == kINT8T || fmt == kINT4T) return 0;
