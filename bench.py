@@ -175,14 +175,24 @@ def dist_env():
     return ws, rank, local
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments and blank-line or trailing-space
+    differences (string literals in these sources hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(l.rstrip() for l in text.splitlines() if l.strip())
+
+
 def source_hash():
-    """Hash of the CUDA sources: ncu counters are only reported for this build."""
+    """Hash of the CUDA sources' code (comments excluded): ncu counters are
+    reported only for the code they were taken on."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "quantized_reduce_rmsnorm_gb300", "csrc")
     for f in sorted(os.listdir(d)):
         h.update(f.encode())
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

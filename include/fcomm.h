@@ -71,7 +71,7 @@ typedef enum {
   FC_ERR_INVALID = 1,     /* bad argument: null/misaligned pointer, bad size or format */
   FC_ERR_CUDA = 2,        /* a CUDA call or kernel launch failed */
   FC_ERR_STALE_BLOCK = 3, /* device status only: a tagged block carried a wrong epoch */
-  FC_ERR_UNSUPPORTED = 4  /* a valid request this build does not implement */
+  FC_ERR_UNSUPPORTED = 4  /* a valid request the library does not implement */
 } fc_status;
 
 typedef enum {

@@ -151,8 +151,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // (griddepcontrol.wait; a no-op for a launch without the attribute), so no
 // global memory is touched before, and then lets the next kernel in the
 // stream be scheduled as resources free up (griddepcontrol.launch_dependents).
-// The grids here never exceed one wave of resident CTAs, so a dependent CTA
-// only takes a slot the current kernel no longer needs.
+// A dependent grid is scheduled only once every CTA of this grid has issued
+// that instruction (or finished), i.e. has started, so its CTAs never hold a
+// slot that a CTA of this grid still needs in order to start.
 __device__ __forceinline__ void pdl_begin() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
