@@ -78,7 +78,7 @@ TmaShape choose_shape(const FusedArgs& a, const TmaGeom& g) {
 }
 
 // Two half-row sub-stages in place of a one-row stage (k_fused_tma's SUB):
-// for the quantized formats with a one-stage ring whose row is exactly two
+// for the quantized formats (plain or in tagged blocks) with a one-stage ring whose row is exactly two
 // passes of 256 threads (H = 8192), when the half-row pieces are whole groups
 // of 16-byte multiples.  Measured on GB300 against the one-row stage: prefill
 // (INT4, P=4) 132.7 -> 126.9 us, INT8 with two slabs at 64 MB 0.75 -> 0.84 of
@@ -88,7 +88,7 @@ TmaShape choose_shape(const FusedArgs& a, const TmaGeom& g) {
 // for the whole row) and the occupancy of that build, 0 when not applicable.
 template <int FMT, int PMAX, bool COMPACT>
 int sub_shape(const FusedArgs& a, const TmaShape& sh, TmaGeom& g2) {
-  if (FMT != kINT8 && FMT != kINT4) return 0;
+  if (FMT != kINT8 && FMT != kINT4 && FMT != kINT8T && FMT != kINT4T) return 0;
   if (sh.nstage != 1 || sh.threads != 256 || (a.H >> 4) != 2 * sh.threads) return 0;
   if (!geometry(FMT, a, g2, 2)) return 0;
   g2.stage_off = (2 * a.H + 127) & ~127;
