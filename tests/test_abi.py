@@ -174,3 +174,37 @@ def test_allgather_rejects_bad_arguments():
     assert "shards" in lib.fc_last_error().decode()
     # an empty shard may have NULL buffers (checked before any launch: rows = 0)
     assert lib.fc_allgather_dequant(bad, 2, 0, 4096, fc.INT8_G128, 0, 64, 0, None, None) == fc.FC_OK
+
+
+def test_bound_call_reuses_marshalled_arguments():
+    """fcomm.Bound passes the arguments it was built with, substitutes the
+    stream on every call, lets the epoch change between calls and raises on a
+    non-OK status (checked with a stand-in for the C entry point)."""
+    fc.fcomm.load()
+    seen = []
+
+    def entry(*args):
+        seen.append(args)
+        return fc.FC_OK if len(seen) < 3 else fc.FC_ERR_INVALID
+
+    b = fc.fcomm.Bound(entry, ["slabs", 4, ctypes.c_uint32(7), None], 3, 2)
+    b(stream=11)
+    b.epoch = 8
+    b(stream=12)
+    assert seen[0][:2] == ("slabs", 4) and seen[0][2].value == 7 and seen[0][3] == 11
+    assert seen[1][2].value == 8 and seen[1][3] == 12 and b.epoch == 8
+    b.epoch = 2 ** 32 + 5  # epochs are u32
+    assert b.epoch == 5
+    with pytest.raises(fc.FcommError):
+        b(stream=13)
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The hash that ties the committed ncu traffic to the kernel code sees
+    code changes and not comment changes."""
+    import bench
+    src = "int a; // one\n/* two\n three */ int b;  \n\nint c;\n"
+    assert bench.code_only(src) == "int a;\n int b;\nint c;"
+    assert bench.code_only(src) == bench.code_only(src.replace("one", "uno").replace("three", "tres"))
+    assert bench.code_only(src) != bench.code_only(src.replace("int c", "int d"))
+    assert len(bench.source_hash()) == 16
