@@ -78,11 +78,12 @@ TmaShape choose_shape(const FusedArgs& a, const TmaGeom& g) {
 }
 
 // Two half-row sub-stages in place of a one-row stage (k_fused_tma's SUB):
-// for the quantized formats (plain or in tagged blocks) with a one-stage ring whose row is exactly two
-// passes of 256 threads (H = 8192), when the half-row pieces are whole groups
-// of 16-byte multiples.  Measured on GB300 against the one-row stage: prefill
-// (INT4, P=4) 132.7 -> 126.9 us, INT8 with two slabs at 64 MB 0.75 -> 0.84 of
-// the HBM peak, 16 MB messages up to +0.13; rows of 4096 (128 threads,
+// for the quantized formats (plain or in tagged blocks) with a one-stage
+// ring whose row is exactly two passes of 256 threads (H = 8192), when the
+// half-row pieces are whole groups of 16-byte multiples.  Measured on GB300
+// against the one-row stage: prefill (INT4, P=4) 132.7 -> 126.9 us, its
+// tagged form 146.5 -> 137.3 us, INT8 with two slabs at 64 MB 0.75 -> 0.84
+// of the HBM peak, 16 MB messages up to +0.13; rows of 4096 (128 threads,
 // smaller copies) were slower with it (INT4 P=8 0.64 -> 0.56) and keep the
 // one-row stage.  Returns the half-row geometry in g2 (its h buffer sized
 // for the whole row) and the occupancy of that build, 0 when not applicable.
