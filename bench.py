@@ -42,18 +42,34 @@ L2_BYTES = 129 * 2 ** 20
 # start event fires: event intervals are device time, not the host's cost of
 # issuing the call (which is reported on its own).
 HOLD_CYCLES = 200_000
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
+
+
+def scrub_l2(buf):
+    """Evicts the inputs of the next call from L2 by reading `buf` (larger
+    than L2) into one scalar.  Only a read: L2 is left holding clean lines,
+    so the timed call pays no write-back of the scrub's own data."""
+    buf.sum(dtype=buf.dtype)
+
+
+def spread(xs):
+    """(median, p10, p90) of a list of numbers."""
+    a = np.sort(np.asarray(xs, dtype=np.float64))
+    return (float(np.median(a)), float(np.percentile(a, 10)), float(np.percentile(a, 90)))
 
 
 def device_timed(fn, reps, warm=2, scrub=None):
-    """(median device us, median host us) of fn() over `reps` repetitions
-    after `warm` untimed ones; `scrub` (a tensor larger than L2) is written
-    before every repetition, outside the events."""
+    """(median device us, median host us, (p10, p90) device us) of fn() over
+    `reps` repetitions after `warm` untimed ones; `scrub` (a tensor larger
+    than L2) is read before every repetition, outside the events.  One call
+    per event pair: the event clock's tick (about 2 us on GB300) bounds the
+    resolution, so short calls are timed by stream_timed as well."""
     import torch
     dev_us, host_us = [], []
     for i in range(reps + warm):
         torch.cuda._sleep(HOLD_CYCLES)
         if scrub is not None:
-            scrub.add_(1.0)
+            scrub_l2(scrub)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         t0 = time.perf_counter()
@@ -64,26 +80,28 @@ def device_timed(fn, reps, warm=2, scrub=None):
         if i >= warm:
             dev_us.append(a.elapsed_time(b) * 1e3)
             host_us.append((t1 - t0) * 1e6)
-    return statistics.median(dev_us), statistics.median(host_us)
+    med, p10, p90 = spread(dev_us)
+    return med, statistics.median(host_us), (p10, p90)
 
 
-def stream_timed(calls, rounds):
-    """Device us per call of `rounds` passes over `calls`, launched back to
-    back between one pair of events (the stream is held while the host
-    queues them)."""
+def stream_timed(calls, per_rep, reps):
+    """Device us per call: `per_rep` calls launched back to back between one
+    pair of events, cycling through `calls` (one call per buffer set), the
+    stream held while the host queues them; `reps` such repetitions after an
+    untimed one.  Returns (median, p10, p90) over the repetitions."""
     import torch
-    n = rounds * len(calls)
-    for c in calls:  # untimed pass
-        c()
-    torch.cuda._sleep(HOLD_CYCLES + 40_000 * n)  # ~20 us of queueing time per call
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(rounds):
-        for c in calls:
-            c()
-    b.record()
-    b.synchronize()
-    return a.elapsed_time(b) * 1e3 / n
+    out = []
+    for r in range(reps + 1):
+        torch.cuda._sleep(HOLD_CYCLES + 40_000 * per_rep)  # ~20 us of queueing time per call
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(per_rep):
+            calls[i % len(calls)]()
+        b.record()
+        b.synchronize()
+        if r:
+            out.append(a.elapsed_time(b) * 1e3 / per_rep)
+    return spread(out)
 
 
 def parse():
@@ -109,6 +127,14 @@ def parse():
                     help="standalone quantized all-gather (shards -> whole dequantized tensor): one JSON line per case")
     ap.add_argument("--sweep", choices=["quick", "full"], default=None,
                     help="message-size sweep (16 KB..256 MB x P x format): one JSON line per point")
+    ap.add_argument("--sizes", default="",
+                    help="sweep: only these message sizes (e.g. 16M,32M)")
+    ap.add_argument("--only", default="",
+                    help="sweep: only these points, MSG:H:P:FMT[,...] (FMT bf16, int8 or int4)")
+    ap.add_argument("--calls", type=int, default=50,
+                    help="sweep: calls per pair of events in the steady measurement (>= 50)")
+    ap.add_argument("--report-sweep", default="",
+                    help="print the markdown table of a file of sweep JSON lines and exit")
     return ap.parse_args()
 
 
@@ -358,59 +384,58 @@ def run_ours(args):
     alg = pipe.alg_bytes()
     step_bytes = alg["sender"] + alg["fused"]
     in_bytes = w.P * 2 * w.T * w.H  # bf16 slabs read by the first stage
-    flush = None
-    if in_bytes + 2 * w.T * w.H < 2 * L2_BYTES:
-        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    step_in = in_bytes + 2 * w.T * w.H  # + the residual
+    # Workloads whose inputs fit in L2: k pipelines over copies of the inputs,
+    # used in turn, so that every timed step reads cold inputs (together they
+    # exceed twice L2; at most 64 copies, beyond which the inputs stay warm).
+    sets_needed = 1 if step_in >= 2 * L2_BYTES else -(-2 * L2_BYTES // step_in) + 1
+    n_sets = min(sets_needed, 64)
+    pipes = [pipe] + [Pipeline(w, inputs, device=dev, split=args.split) for _ in range(n_sets - 1)]
 
     st = torch.cuda.current_stream(dev)
     if args.graph:
-        pipe.capture()
-    run_step = pipe.replay if args.graph else pipe.step
-    for _ in range(args.warmup):
-        run_step(st)
+        for p in pipes:
+            p.capture()
+    runs = [(p.replay if args.graph else p.step) for p in pipes]
+    for i in range(max(args.warmup, n_sets)):
+        runs[i % n_sets](st)
     torch.cuda.synchronize(dev)
 
-    # timed region 1, the step: with inputs larger than L2, one pair of events
-    # around all K steps (consecutive kernels may overlap their launch with
-    # the previous kernel's tail); with an L2 scrub, a pair per step so that
-    # the scrub stays outside the timing.
+    # timed region 1, the step: one pair of events around all K steps
+    # (consecutive kernels may overlap their launch with the previous
+    # kernel's tail, as in a stream of layers); then one pair per step for
+    # the spread; then, region 2, events around each stage of each step.
     n = args.steps
+    hold = HOLD_CYCLES + 40_000 * min(n, 200)  # covers the host's issue time of the steps
     barrier(ws)
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index)
     with sampler:
         t_wall = time.perf_counter()
-        torch.cuda._sleep(HOLD_CYCLES)  # the host queues ahead of the first timed step
+        torch.cuda._sleep(hold)  # the host queues ahead of the first timed step
         host_s = 0.0  # host time spent issuing the steps
-        if flush is None:
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(st)
-            for i in range(n):
-                t0 = time.perf_counter()
-                run_step(st)
-                host_s += time.perf_counter() - t0
-            e1.record(st)
-            torch.cuda.synchronize(dev)
-            step_ms = e0.elapsed_time(e1) / n
-        else:
-            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-            for i in range(n):
-                flush.add_(1.0)  # scrub L2 between timed steps (outside the events)
-                ev[i][0].record(st)
-                t0 = time.perf_counter()
-                run_step(st)
-                host_s += time.perf_counter() - t0
-                ev[i][1].record(st)
-            torch.cuda.synchronize(dev)
-            step_ms = sum(a.elapsed_time(b) for a, b in ev) / n
-        t_wall = time.perf_counter() - t_wall
-        # timed region 2, the kernels: events around each stage of each step
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
-        torch.cuda._sleep(HOLD_CYCLES)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
         for i in range(n):
-            if flush is not None:
-                flush.add_(1.0)
-            pipe.step_marked(st, ev[i])
+            t0 = time.perf_counter()
+            runs[i % n_sets](st)
+            host_s += time.perf_counter() - t0
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        step_ms = e0.elapsed_time(e1) / n
+        t_wall = time.perf_counter() - t_wall
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        torch.cuda._sleep(hold)
+        for i in range(n):
+            evs[i][0].record(st)
+            runs[i % n_sets](st)
+            evs[i][1].record(st)
+        torch.cuda.synchronize(dev)
+        per_step = [a.elapsed_time(b) for a, b in evs]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        torch.cuda._sleep(hold)
+        for i in range(n):
+            pipes[i % n_sets].step_marked(st, ev[i])
         torch.cuda.synchronize(dev)
     barrier(ws)
     sender_ms = [e[0].elapsed_time(e[1]) for e in ev]
@@ -420,31 +445,37 @@ def run_ours(args):
     value = whole_job_gbs(step_bytes, ws, step_ms)
     peak, peak_kind = peaks()
     kern = [("sender", "k_quantize" if w.fmt in synth.QUANTIZED else "k_pack_tagged", alg["sender"],
-             statistics.mean(sender_ms)),
+             statistics.mean(sender_ms), spread(sender_ms)),
             ("fused", "k_fused_tagged" if w.fmt == 3 else "k_fused", alg["fused"],
-             statistics.mean(fused_ms))]
+             statistics.mean(fused_ms), spread(fused_ms))]
     dom = max(kern, key=lambda k: k[3])
     achieved = dom[2] / (dom[3] * 1e-3) / 1e9
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
         "steps": n, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "step_ms_spread": dict(zip(("median", "p10", "p90"), (round(v, 5) for v in spread(per_step))),
+                               timing="one pair of CUDA events per step, back to back"),
         "us_per_call": round(statistics.mean(fused_ms) * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": {**workload_config(w),
                    **({"split": args.split, "split_rows": pipe.bounds, "wave_rows": pipe.wave_rows}
                       if w.splits > 1 else {}),
-                   "l2": ("L2 scrubbed (256 MB write) before every timed step"
-                          if flush is not None else
-                          f"inputs larger than L2 ({in_bytes / 2**20:.0f} MB of bf16 slabs "
-                          f"read per step vs 129 MB L2)"),
+                   "l2": (f"inputs larger than L2 ({in_bytes / 2**20:.0f} MB of bf16 slabs "
+                          f"read per step vs 129 MB L2)" if n_sets == 1 else
+                          f"{n_sets} copies of the inputs used in turn ({n_sets * step_in / 2**20:.0f} MB"
+                          + (" > twice L2: every step reads cold inputs)" if n_sets == sets_needed else
+                             ", which stay in L2: warm inputs)")),
                    "alg_bytes_per_step": step_bytes},
         "roofline": {"bound": "hbm", "kernel": dom[1], "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "nominal_peak": NOMINAL_HBM_GBS,
                      "traffic": measured_traffic(dom[1], w.name),
                      "alg_bytes_per_launch": dom[2]},
         "stages": {k[0]: {"kernel": k[1], "alg_bytes": k[2], "us": round(k[3] * 1e3, 2),
+                          "us_median_p10_p90": [round(v * 1e3, 2) for v in k[4]],
                           "GB/s": round(k[2] / (k[3] * 1e-3) / 1e9, 1),
                           "frac": round(k[2] / (k[3] * 1e-3) / 1e9 / peak, 4)} for k in kern},
         "host_us_per_step": round(host_s / n * 1e6, 2),
@@ -562,27 +593,61 @@ def allreduce_max(v, ws, dev):
     return float(t.item())
 
 
+def parse_size(t: str) -> int:
+    t = t.strip().upper()
+    mult = {"K": 1 << 10, "M": 1 << 20, "G": 1 << 30}
+    return int(t[:-1]) * mult[t[-1]] if t[-1] in mult else int(t)
+
+
+def sweep_selection(args):
+    """The sweep points to run: every point, the quick subset, or those
+    matching --sizes / --only (MSG:H:P:FMT, FMT one of bf16, int8, int4)."""
+    from quantized_reduce_rmsnorm_gb300 import synth
+    pts = synth.sweep_points()
+    if args.sweep == "quick":
+        pts = [p for p in pts if p[0] in (16 << 10, 1 << 20, 16 << 20, 64 << 20, 256 << 20)]
+    if args.sizes:
+        keep = {parse_size(t) for t in args.sizes.split(",")}
+        pts = [p for p in pts if p[0] in keep]
+    if args.only:
+        names = {"bf16": synth.FMT_BF16, "int8": synth.FMT_INT8_SYM, "int4": synth.FMT_INT4_ASYM}
+        want = set()
+        for item in args.only.split(","):
+            m, h, p, f = item.split(":")
+            want.add((parse_size(m), int(h), int(p), names[f]))
+        pts = [p for p in pts if (p[0], p[1], p[3], p[4]) in want]
+    return pts
+
+
 def run_sweep(args):
     """Message-size sweep of the fused kernel (and the sender quantizer).
 
     Inputs are seeded N(0,1) bf16 generated on the device (a measurement,
-    not a parity case); each point is timed with CUDA events, median of
-    repetitions, with a 256 MB L2 scrub before every repetition when the
-    point's inputs fit in L2; the calls are bound once (fcomm.Bound) and
-    their host issue time is reported beside the device time."""
+    not a parity case); the calls are bound once (fcomm.Bound).  Each point
+    is timed two ways:
+
+    * steady (the reported figure): `--calls` calls (at least 50) back to
+      back between one pair of CUDA events, cycling through k buffer sets
+      whose inputs together exceed twice L2 (so every call reads cold
+      inputs and meets its predecessor's dirty outputs, as in a stream of
+      all-reduce calls); k is capped at 64 for the smallest messages, whose
+      inputs then stay in L2 ("inputs_cold": false).  Median, p10 and p90
+      over the repetitions.
+    * held: one call per event pair after a read-only L2 scrub (cold
+      inputs, clean L2), median of the repetitions; the event clock's tick
+      (about 2 us) bounds its resolution.
+
+    The host's cost of issuing one call is reported beside them."""
     import torch
     from quantized_reduce_rmsnorm_gb300 import fcomm, synth
     from quantized_reduce_rmsnorm_gb300.pipeline import qs_bytes
     fcomm.load()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    peak, _ = peaks()
+    peak, kind = peaks()
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-    pts = synth.sweep_points()
-    if args.sweep == "quick":
-        pts = [p for p in pts if p[0] in (16 << 10, 1 << 20, 16 << 20, 64 << 20, 256 << 20)]
     gen = torch.Generator(device=dev)
-    for msg, H, T, P, fmt, G in pts:
+    for msg, H, T, P, fmt, G in sweep_selection(args):
         if T == 0:
             continue
         gen.manual_seed(msg ^ (H << 8) ^ (P << 4) ^ fmt)
@@ -617,47 +682,81 @@ def run_sweep(args):
             return None, fcomm.bind_allreduce_residual_rmsnorm(xset, spec, T, H, res.clone(), r_out,
                                                                gam, 1e-5, y)
 
-        send, fuse = make_set(xs)
-        small = (P * 2 + 6) * E < 2 * L2_BYTES
-        reps = 15 if E * P * 2 < (64 << 20) else 7
-        scrub = flush if small else None
-        su, _ = device_timed(send, reps, scrub=scrub) if send else (None, None)
-        fu, fh = device_timed(fuse, reps, scrub=scrub)
+        fits = fused_in + 4 * E < 2 * L2_BYTES
+        k = 1 if fused_in >= 2 * L2_BYTES else -(-2 * L2_BYTES // fused_in) + 1
+        cold = k <= 64
+        k = min(k, 64)
+        sets = [make_set(xs)] + [make_set([x.clone() for x in xs]) for _ in range(k - 1)]
+        send, fuse = sets[0]
+        calls = max(args.calls, k)
+        reps = 7
+        fm, fp10, fp90 = stream_timed([f for _, f in sets], calls, reps)
+        hu, fh, hspread = device_timed(fuse, reps, scrub=flush if fits else None)
+        gb = lambda nbytes, us: nbytes / us / 1e3
         line = {"sweep": True, "message_bytes": msg, "hidden": H, "tokens": T, "P": P,
-                "format": synth.FMT_NAMES[fmt], "fused_us": round(fu, 2),
-                "fused_GBps": round(fused_bytes / fu / 1e3, 1),
-                "fused_frac": round(fused_bytes / fu / 1e3 / peak, 4),
+                "format": synth.FMT_NAMES[fmt],
+                "fused_us": round(fm, 3), "fused_us_p10": round(fp10, 3),
+                "fused_us_p90": round(fp90, 3),
+                "fused_GBps": round(gb(fused_bytes, fm), 1),
+                "fused_frac": round(gb(fused_bytes, fm) / peak, 4),
+                "fused_frac_nominal": round(gb(fused_bytes, fm) / NOMINAL_HBM_GBS, 4),
+                "fused_held_us": round(hu, 2),
+                "fused_held_frac": round(gb(fused_bytes, hu) / peak, 4),
                 "fused_host_us": round(fh, 2),
-                "sender_us": None if su is None else round(su, 2),
-                "sender_GBps": None if su is None else round(sender_bytes / su / 1e3, 1),
-                "l2_scrubbed": small}
-        # Steady state for points whose buffers fit in L2: k buffer sets whose
-        # inputs together exceed twice L2, called back to back in turn, so
-        # every call's inputs are cold and the lines it finds dirty are its
-        # predecessor's outputs (no scrub).
-        k = -(-2 * L2_BYTES // fused_in) + 1
-        if small and k <= 64:
-            sets = [make_set([x.clone() for x in xs] if (quant or j) else xs) for j in range(k)]
-            rounds = max(2, 48 // k)
-            fr = stream_timed([f for _, f in sets], rounds)
-            line.update(rot_sets=k, rot_fused_us=round(fr, 2),
-                        rot_fused_frac=round(fused_bytes / fr / 1e3 / peak, 4))
-            if quant:
-                sr = stream_timed([snd for snd, _ in sets], rounds)
-                line.update(rot_sender_us=round(sr, 2),
-                            rot_sender_frac=round(sender_bytes / sr / 1e3 / peak, 4))
-            del sets
+                "sets": k, "calls_per_rep": calls, "reps": reps, "inputs_cold": cold,
+                "held_scrub": "read-only" if fits else "none (inputs larger than L2)",
+                "peak_kind": kind}
+        if quant:
+            sm, sp10, sp90 = stream_timed([s for s, _ in sets], calls, reps)
+            shu, _, _ = device_timed(send, reps, scrub=flush if fits else None)
+            line.update(sender_us=round(sm, 3), sender_us_p10=round(sp10, 3),
+                        sender_us_p90=round(sp90, 3),
+                        sender_GBps=round(gb(sender_bytes, sm), 1),
+                        sender_frac=round(gb(sender_bytes, sm) / peak, 4),
+                        sender_frac_nominal=round(gb(sender_bytes, sm) / NOMINAL_HBM_GBS, 4),
+                        sender_held_us=round(shu, 2))
         print(json.dumps(line), flush=True)
-        del xs, res, gam, send, fuse
+        del xs, res, gam, send, fuse, sets
         torch.cuda.empty_cache()
+
+
+def sweep_report(path):
+    """Markdown table of the sweep's JSON lines (bench.py --sweep ... > path)."""
+    rows = [json.loads(l) for l in open(path) if l.startswith("{") and '"sweep"' in l]
+    peak, kind = peaks()
+    print("| message | H | tokens | P | format | fused us (p10-p90) | fused frac | of 8 TB/s "
+          "| held us | sets | cold | sender us (p10-p90) | sender frac |")
+    print("|---|---|---|---|---|---|---|---|---|---|---|---|---|")
+    for r in rows:
+        snd = (f"{r['sender_us']:.2f} ({r['sender_us_p10']:.2f}-{r['sender_us_p90']:.2f})"
+               if r.get("sender_us") is not None else "-")
+        sf = f"{r['sender_frac']:.3f}" if r.get("sender_frac") is not None else "-"
+        print(f"| {r['message_bytes']} | {r['hidden']} | {r['tokens']} | {r['P']} | {r['format']} "
+              f"| {r['fused_us']:.2f} ({r['fused_us_p10']:.2f}-{r['fused_us_p90']:.2f}) "
+              f"| {r['fused_frac']:.3f} | {r['fused_frac_nominal']:.3f} | {r['fused_held_us']:.2f} "
+              f"| {r['sets']} | {'yes' if r['inputs_cold'] else 'no'} | {snd} | {sf} |")
+    print()
+    for fmt in ("bf16", "int8_sym_g128", "int4_asym_g32"):
+        for lo, label in ((16 << 20, "16 MB and more"), (64 << 20, "64 MB and more")):
+            sel = [r for r in rows if r["format"] == fmt and r["message_bytes"] >= lo]
+            if not sel:
+                continue
+            f = sorted(r["fused_frac"] for r in sel)
+            below = [r for r in sel if r["fused_frac"] < 0.70]
+            print(f"* {fmt}, messages of {label}: fused fraction of the {kind} peak min / median / max "
+                  f"{f[0]:.3f} / {statistics.median(f):.3f} / {f[-1]:.3f}; "
+                  f"{len(below)} of {len(sel)} points below 0.70"
+                  + ("" if not below else " (" + ", ".join(
+                      f"{r['message_bytes'] >> 20} MB H={r['hidden']} P={r['P']}: {r['fused_frac']:.3f}"
+                      for r in below) + ")"))
 
 
 def run_gather(args):
     """The standalone quantized all-gather (fc_allgather_dequant): P shard
     payloads of a prefill-sized and a decode-sized tensor (quantized on the
     device from seeded N(0,1) bf16), gathered and dequantized to bf16 and to
-    fp32; CUDA events, median of the repetitions, a 256 MB L2 scrub before
-    each repetition when the point fits in L2."""
+    fp32; CUDA events, median of the repetitions, a read-only 258 MB L2 scrub
+    before each repetition when the point fits in L2."""
     import torch
     from quantized_reduce_rmsnorm_gb300 import fcomm, synth
     fcomm.load()
@@ -679,8 +778,8 @@ def run_gather(args):
         for odt, osz in ((torch.bfloat16, 2), (torch.float32, 4)):
             out = torch.empty(T, H, dtype=odt, device=dev)
             small = qs + osz * E < 2 * L2_BYTES
-            us, _ = device_timed(lambda: fcomm.allgather_dequant(shards, spec, T, H, out),
-                                 max(args.steps, 5), warm=3, scrub=flush if small else None)
+            us = device_timed(lambda: fcomm.allgather_dequant(shards, spec, T, H, out),
+                              max(args.steps, 5), warm=3, scrub=flush if small else None)[0]
             alg = qs + osz * E
             print(json.dumps({"gather": True, "workload": name, "rows": T, "hidden": H, "P": P,
                               "format": synth.FMT_NAMES[spec.fmt], "out": str(odt).split(".")[-1],
@@ -759,6 +858,9 @@ def run_overlap(args):
 
 def main():
     args = parse()
+    if args.report_sweep:
+        sweep_report(args.report_sweep)
+        return
     if args.gather:
         run_gather(args)
         return

@@ -156,11 +156,12 @@ class Bound:
     """One libfcomm call with its arguments marshalled once.
 
     Calling it launches the entry point again with the same device pointers
-    (the tensors it was bound to must stay alive and in place) on `stream`
-    (default: the current torch stream), with no per-call argument
-    conversion: the host cost of a call is the C entry point itself.  For the
-    calls that carry an epoch (tagged formats), `epoch` may be changed
-    between calls."""
+    on `stream` (default: the current torch stream), with no per-call
+    argument conversion: the host cost of a call is the C entry point
+    itself.  The object holds a reference to every tensor it was bound to,
+    so their memory cannot be freed and handed to another tensor while the
+    bound call exists.  For the calls that carry an epoch (tagged formats),
+    `epoch` may be changed between calls."""
     __slots__ = ("_fn", "_args", "_si", "_ei", "_keep")
 
     def __init__(self, fn, args, stream_index, epoch_index=None, keep=()):
@@ -230,7 +231,8 @@ def bind_group_quantize_multi(xs: Sequence[torch.Tensor], spec: QSpec, outs) -> 
     rows, hidden = _rows_hidden(xs[0])
     xp = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
     qo = (QTensor * len(outs))(*[_qt(o) for o in outs])
-    return Bound(load().fc_group_quantize_multi, [xp, len(xs), rows, hidden, spec, qo, None], 6)
+    return Bound(load().fc_group_quantize_multi, [xp, len(xs), rows, hidden, spec, qo, None], 6,
+                 keep=(tuple(xs), tuple(outs)))
 
 
 def group_quantize_multi(xs: Sequence[torch.Tensor], spec: QSpec, outs, stream=None):
@@ -298,7 +300,8 @@ def bind_group_quantize_tagged(xs: Sequence[torch.Tensor], spec: QSpec, epoch: i
     xp = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
     bp = (ctypes.c_void_p * len(blocks))(*[_ptr(b) for b in blocks])
     return Bound(load().fc_group_quantize_tagged,
-                 [xp, len(xs), rows, hidden, spec, ctypes.c_uint32(epoch), bp, None], 7, 5)
+                 [xp, len(xs), rows, hidden, spec, ctypes.c_uint32(epoch), bp, None], 7, 5,
+                 keep=(tuple(xs), tuple(blocks)))
 
 
 def group_quantize_tagged(xs: Sequence[torch.Tensor], spec: QSpec, epoch: int,
@@ -313,7 +316,8 @@ def bind_pack_tagged_multi(xs: Sequence[torch.Tensor], epoch: int,
     xp = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
     bp = (ctypes.c_void_p * len(blocks))(*[_ptr(b) for b in blocks])
     return Bound(load().fc_pack_tagged_multi,
-                 [xp, len(xs), rows, hidden, ctypes.c_uint32(epoch), bp, None], 6, 4)
+                 [xp, len(xs), rows, hidden, ctypes.c_uint32(epoch), bp, None], 6, 4,
+                 keep=(tuple(xs), tuple(blocks)))
 
 
 def pack_tagged_multi(xs: Sequence[torch.Tensor], epoch: int, blocks: Sequence[torch.Tensor],
@@ -350,7 +354,9 @@ def bind_allreduce_residual_rmsnorm(slabs, spec: QSpec, rows: int, hidden: int,
     args = [qs, len(slabs), rows, hidden, spec, P(_ptr(residual_in)), P(_ptr(residual_out)),
             P(_ptr(gamma)), ctypes.c_float(eps), _qt(requant_out), P(_ptr(y)),
             ctypes.c_uint32(expected_epoch), P(_ptr(d_status)), ctypes.byref(opts), None]
-    return Bound(load().fc_allreduce_residual_rmsnorm_ex, args, 14, 11, keep=(opts,))
+    return Bound(load().fc_allreduce_residual_rmsnorm_ex, args, 14, 11,
+                 keep=(opts, tuple(slabs), residual_in, residual_out, gamma, y, requant_out,
+                       d_status))
 
 
 def token_split(spec: QSpec, P: int, rows: int, hidden: int):

@@ -208,3 +208,32 @@ def test_kernel_hash_ignores_comments_only():
     assert bench.code_only(src) == bench.code_only(src.replace("one", "uno").replace("three", "tres"))
     assert bench.code_only(src) != bench.code_only(src.replace("int c", "int d"))
     assert len(bench.source_hash()) == 16
+
+
+def test_bound_call_keeps_its_tensors_alive(monkeypatch):
+    """A bound call holds every tensor it was bound to: dropping the caller's
+    own references must not free memory the call will touch again (the
+    allocator would hand it to the next tensor).  Binding launches nothing,
+    so host tensors serve here, with the binding's device-memory check
+    relaxed for the test."""
+    import gc
+    import weakref
+
+    import torch
+    monkeypatch.setattr(fc.fcomm, "_ptr", lambda t: None if t is None else t.data_ptr())
+    x = [torch.zeros(2, 128, dtype=torch.bfloat16) for _ in range(2)]
+    outs = [fc.alloc_qtensor(fc.INT8_G128, 2, 128, "cpu") for _ in range(2)]
+    res, gam = torch.zeros(2, 128, dtype=torch.bfloat16), torch.ones(128, dtype=torch.bfloat16)
+    r_out, y = torch.empty_like(res), torch.empty_like(res)
+    pay = fc.alloc_qtensor(fc.INT8_G128, 2, 128, "cpu")
+    send = fc.bind_group_quantize_multi(x, fc.INT8_G128, outs)
+    fuse = fc.bind_allreduce_residual_rmsnorm(outs, fc.INT8_G128, 2, 128, res, r_out, gam, 1e-5, y,
+                                              requant_out=pay)
+    refs = [weakref.ref(t) for t in x + [o[0] for o in outs] + [o[1] for o in outs]
+            + [res, r_out, gam, y, pay[0], pay[1]]]
+    del x, outs, res, gam, r_out, y, pay
+    gc.collect()
+    assert all(r() is not None for r in refs)
+    del send, fuse
+    gc.collect()
+    assert all(r() is None for r in refs)

@@ -697,33 +697,114 @@ def test_allgather_full_size_sampled(orc):
         assert_bits_equal(host_bits(out[r]), orc.f32_to_bf16_array(want), f"row {r}")
 
 
-@pytest.mark.parametrize("name", ["prefill", "token-split", "decode", "prefill-qtagged"])
-def test_full_size_sampled_rows(orc, name):
-    """The full-size workloads through the same Pipeline.step() the
-    benchmark times (token-split: two subsets on two streams); the oracle
-    checks a sample of rows (first, last, random)."""
-    from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
-    w = synth.WORKLOADS[name]
-    pipe = Pipeline(w, synth.make_inputs(w, seed=0))
-    pipe.step()
-    pipe.step()  # a second step: new epoch for tagged blocks, same outputs
+def _row_ranges(T, parts):
+    return [(T * k // parts, T * (k + 1) // parts) for k in range(parts) if T * (k + 1) // parts > T * k // parts]
+
+
+def _host_threads():
+    import os
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_fused_all(orc, w, inp):
+    """The oracle's whole path over every row: the rows are cut into
+    contiguous ranges, each one unmodified oracle call on its own host thread
+    (rows are independent, and tests/test_bench_host.py checks that ranges
+    give the bits of one call).  Returns dict(h, y[, codes, scales, zeros])
+    over all rows, flat in row-major order."""
+    import concurrent.futures as cf
+    fmt = BF if w.fmt == TG else synth.base_format(w.fmt)
+    parts = _row_ranges(w.T, min(w.T, 4 * _host_threads()))
+
+    def one(rr):
+        r0, r1 = rr
+        return orc.allreduce_residual_rmsnorm(fmt, [s[r0:r1] for s in inp["slabs"]],
+                                              inp["residual"][r0:r1], inp["gamma"], r1 - r0, w.H,
+                                              w.group, w.eps)
+    with cf.ThreadPoolExecutor(_host_threads()) as ex:
+        outs = list(ex.map(one, parts))
+    res = {k: np.concatenate([o[k].ravel() for o in outs]) for k in ("h", "y")}
+    for k in ("codes", "scales", "zeros"):
+        if outs[0].get(k) is not None:
+            res[k] = np.concatenate([o[k].ravel() for o in outs])
+    return res
+
+
+def oracle_quant_all(orc, fmt, slab_bits, G, T):
+    """The oracle's quantizer over a whole slab, in contiguous row ranges on
+    host threads (groups never straddle rows).  (codes, scales, zeros)."""
+    import concurrent.futures as cf
+    parts = _row_ranges(T, min(T, 4 * _host_threads()))
+
+    def one(rr):
+        return orc.quantize(fmt, bf16_float(slab_bits[rr[0]:rr[1]]).ravel(), G)
+    with cf.ThreadPoolExecutor(_host_threads()) as ex:
+        outs = list(ex.map(one, parts))
+    cat = lambda i: None if outs[0][i] is None else np.concatenate([o[i] for o in outs])
+    return cat(0), cat(1), cat(2)
+
+
+def check_every_element(orc, w, pipe, inp):
+    """Every output of a Pipeline step against the oracle: residual_out
+    bit-exact, y within one bf16 ulp, the all-gather payload bit-exact, and
+    every slab's sender output (codes, scales, zero-points, or tagged
+    blocks with the step's epoch) bit-exact."""
     got = pipe.outputs()
-    rows = np.unique(np.concatenate([[0, 1, w.T - 1],
-                                     np.random.default_rng(0).integers(0, w.T, 13)]))
-    sub = synth.Workload(**{**w.__dict__, "T": len(rows)})
-    want = oracle_fused(orc, sub, synth.make_inputs(w, seed=0, rows=rows))
-    assert_bits_equal(got["h"][rows], want["h"], "residual_out")
-    assert_y_close(got["y"][rows], want["y"])
+    want = oracle_fused_all(orc, w, inp)
+    assert_bits_equal(got["h"], want["h"], "residual_out")
+    assert_y_close(got["y"], want["y"])
     if w.fmt in (I8, I4, I8T, I4T):
-        codes = got["codes"].reshape(w.T, -1)[rows]
-        assert_bits_equal(codes, want["codes"], "payload codes")
-        assert_bits_equal(got["scales"].reshape(w.T, -1)[rows], want["scales"], "payload scales")
+        assert_bits_equal(got["codes"], want["codes"], "payload codes")
+        assert_bits_equal(got["scales"], want["scales"], "payload scales")
         if w.fmt in (I4, I4T):
-            assert_bits_equal(got["zeros"].reshape(w.T, -1)[rows], want["zeros"], "payload zeros")
+            assert_bits_equal(got["zeros"], want["zeros"], "payload zeros")
+    base = synth.base_format(w.fmt)
+    for p in range(w.P):
+        if w.fmt in (I8, I4, I8T, I4T):
+            q, s_, z = oracle_quant_all(orc, base, inp["slabs"][p], w.group, w.T)
+            if w.fmt in (I8, I4):
+                assert_bits_equal(host(pipe.codes[p][0]), q, f"sender codes, slab {p}")
+                assert_bits_equal(host(pipe.codes[p][1]), s_, f"sender scales, slab {p}")
+                if w.fmt == I4:
+                    assert_bits_equal(host(pipe.codes[p][2]), z, f"sender zeros, slab {p}")
+            else:
+                blk = orc.pack_qtagged(base, q, s_, z, w.group, pipe.epoch)
+                assert_bits_equal(host(pipe.blocks[p]).view(np.uint32), blk, f"sender blocks, slab {p}")
+        elif w.fmt == TG:
+            blk = orc.pack_tagged(inp["slabs"][p], w.T, w.H, pipe.epoch)
+            assert_bits_equal(host(pipe.blocks[p]).view(np.uint32), blk, f"producer blocks, slab {p}")
     if w.fmt in (I8T, I4T):
         assert got["status"].tolist() == [[fc.FC_OK, fc.STATUS_NO_INDEX]]
     if w.fmt == TG:
         assert got["status"].tolist() == [[fc.FC_OK, fc.STATUS_NO_INDEX]] * w.splits
+
+
+FULL_SIZE = ["decode", "prefill", "token-split", "prefill-qtagged", "decode-tiny", "decode-qtagged",
+             "sweep-256M-h8192-p8-int4"]
+
+
+@pytest.mark.parametrize("name", FULL_SIZE)
+def test_full_size_every_element(orc, name):
+    """The full-size workloads through the same Pipeline.step() the
+    benchmark times (token-split: two subsets on two streams; a second step
+    with a new epoch for the tagged formats), every element compared with
+    the oracle; also the largest sweep point (a 256 MB message, eight INT4
+    slabs of 16384 x 8192)."""
+    from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
+    if name.startswith("sweep"):
+        w, seed = synth.sweep_workload(8192, 16384, 8, I4, 32), 3
+    else:
+        w, seed = synth.WORKLOADS[name], 0
+    inp = synth.make_inputs(w, seed=seed)
+    pipe = Pipeline(w, inp)
+    pipe.step()
+    pipe.step()
+    check_every_element(orc, w, pipe, inp)
+    del pipe
+    torch.cuda.empty_cache()
 
 
 def test_rows_zero_launches_nothing():
@@ -855,30 +936,19 @@ def test_fused_dense_exact_ties(orc, fmt, G, P, kernel):
 
 
 SWEEP_PARITY = [(msg, H, P, fmt, G) for msg in (16 << 10, 1 << 20, 16 << 20) for H in (4096, 8192)
-                for P in (2, 4, 8) for fmt, G in ((BF, 0), (I8, 128), (I4, 32))] + \
-               [(256 << 20, 8192, 8, I4, 32)]
+                for P in (2, 4, 8) for fmt, G in ((BF, 0), (I8, 128), (I4, 32))]
 
 
 @pytest.mark.parametrize("msg,H,P,fmt,G", SWEEP_PARITY,
                          ids=[f"{m >> 10}K-h{h}-p{p}-{synth.FMT_NAMES[f]}" for m, h, p, f, _ in SWEEP_PARITY])
-def test_sweep_point_sampled_rows(orc, msg, H, P, fmt, G):
+def test_sweep_point_every_element(orc, msg, H, P, fmt, G):
     """Message-size sweep shapes (every H, P and format at 16 KB, 1 MB and
-    16 MB messages, and the largest point, a 256 MB message with eight INT4
-    slabs) through the same Pipeline.step() as the benchmark, with seeded
-    N(0,1) inputs; the oracle checks the first, last and random rows."""
+    16 MB messages) through the same Pipeline.step() as the benchmark, with
+    seeded N(0,1) inputs; every element against the oracle."""
     from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
     T = msg // (2 * H)
     w = synth.sweep_workload(H, T, P, fmt, G)
-    pipe = Pipeline(w, synth.make_inputs(w, seed=3))
+    inp = synth.make_inputs(w, seed=3)
+    pipe = Pipeline(w, inp)
     pipe.step()
-    got = pipe.outputs()
-    rows = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(T).integers(0, T, 6)]))
-    sub = synth.Workload(**{**w.__dict__, "T": len(rows)})
-    want = oracle_fused(orc, sub, synth.make_inputs(w, seed=3, rows=rows))
-    assert_bits_equal(got["h"][rows], want["h"], "residual_out")
-    assert_y_close(got["y"][rows], want["y"])
-    if fmt in (I8, I4):
-        assert_bits_equal(got["codes"].reshape(T, -1)[rows], want["codes"], "payload codes")
-        assert_bits_equal(got["scales"].reshape(T, -1)[rows], want["scales"], "payload scales")
-        if fmt == I4:
-            assert_bits_equal(got["zeros"].reshape(T, -1)[rows], want["zeros"], "payload zeros")
+    check_every_element(orc, w, pipe, inp)
