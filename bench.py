@@ -131,6 +131,8 @@ def parse():
                     help="sweep: only these message sizes (e.g. 16M,32M)")
     ap.add_argument("--only", default="",
                     help="sweep: only these points, MSG:H:P:FMT[,...] (FMT bf16, int8 or int4)")
+    ap.add_argument("--formats", default="",
+                    help="sweep: only these formats (bf16, int8, int4; comma-separated)")
     ap.add_argument("--calls", type=int, default=50,
                     help="sweep: calls per pair of events in the steady measurement (>= 50)")
     ap.add_argument("--report-sweep", default="",
@@ -609,8 +611,11 @@ def sweep_selection(args):
     if args.sizes:
         keep = {parse_size(t) for t in args.sizes.split(",")}
         pts = [p for p in pts if p[0] in keep]
+    names = {"bf16": synth.FMT_BF16, "int8": synth.FMT_INT8_SYM, "int4": synth.FMT_INT4_ASYM}
+    if args.formats:
+        keep = {names[f] for f in args.formats.split(",")}
+        pts = [p for p in pts if p[4] in keep]
     if args.only:
-        names = {"bf16": synth.FMT_BF16, "int8": synth.FMT_INT8_SYM, "int4": synth.FMT_INT4_ASYM}
         want = set()
         for item in args.only.split(","):
             m, h, p, f = item.split(":")

@@ -241,6 +241,14 @@ __device__ __forceinline__ float2 padd(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return r;
 }
+__device__ __forceinline__ float2 psub(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " sub.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
 __device__ __forceinline__ float2 pmul(float2 a, float2 b) {
   float2 r;
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
@@ -266,6 +274,24 @@ __device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
 constexpr float kTwo23 = 8388608.0f;            // 2^23, bits 0x4B000000
 constexpr float kTwo23p128 = 8388736.0f;        // 2^23 + 128
 constexpr uint32_t kTwo23Bits = 0x4B000000u;
+
+// The same for a byte selector known at compile time, kept opaque to the
+// compiler: measured on GB300 (executed-instruction counts), the INT4
+// dequantizer issues 51 instead of 70 instructions per 16 codes when its
+// byte permutes and nibble masks are written this way, all permutes of a
+// word first and the packed arithmetic after.
+template <int SEL>
+__device__ __forceinline__ float prmt_two23(uint32_t a) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0x4B000000, %2;" : "=r"(r) : "r"(a), "n"(SEL));
+  return __uint_as_float(r);
+}
+// The eight 4-bit codes of w spread one per byte: codes 0, 2, 4, 6 in ev,
+// codes 1, 3, 5, 7 in od.
+__device__ __forceinline__ void spread_nibbles(uint32_t w, uint32_t& ev, uint32_t& od) {
+  asm("{\n .reg .b32 t;\n and.b32 %0, %2, 0x0F0F0F0F;\n shr.u32 t, %2, 4;\n and.b32 %1, t, 0x0F0F0F0F;\n}"
+      : "=r"(ev), "=r"(od) : "r"(w));
+}
 
 // byte k of w as the low byte of 2^23's bit pattern
 __device__ __forceinline__ float byte_in_two23(uint32_t w, int k) {
@@ -316,19 +342,23 @@ __device__ __forceinline__ void dequant_i4_acc_t(const uint32_t w[2], float s, f
   const float2 S = dup2(s), N = dup2(nms), Z = dup2(z);
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    const uint32_t ev = w[j] & 0x0F0F0F0Fu;         // codes 8j + 2k
-    const uint32_t od = (w[j] >> 4) & 0x0F0F0F0Fu;  // codes 8j + 2k + 1
+    uint32_t ev, od;  // codes 8j + 2k, codes 8j + 2k + 1
+    spread_nibbles(w[j], ev, od);
+    float u0[4], u1[4];
+    u0[0] = prmt_two23<0x7540>(ev), u1[0] = prmt_two23<0x7540>(od);
+    u0[1] = prmt_two23<0x7541>(ev), u1[1] = prmt_two23<0x7541>(od);
+    u0[2] = prmt_two23<0x7542>(ev), u1[2] = prmt_two23<0x7542>(od);
+    u0[3] = prmt_two23<0x7543>(ev), u1[3] = prmt_two23<0x7543>(od);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float u0 = byte_in_two23(ev, k), u1 = byte_in_two23(od, k);
       float* a = acc + 8 * j + 2 * k;
       if (FUSED) {
-        const float2 d = padd(pfma(make_float2(u0, u1), S, N), Z);
+        const float2 d = padd(pfma(make_float2(u0[k], u1[k]), S, N), Z);
         const float2 t = padd(make_float2(a[0], a[1]), d);
         a[0] = t.x, a[1] = t.y;
       } else {
-        const float p0 = __fmul_rn(__fadd_rn(u0, -kTwo23), s);
-        const float p1 = __fmul_rn(__fadd_rn(u1, -kTwo23), s);
+        const float p0 = __fmul_rn(__fadd_rn(u0[k], -kTwo23), s);
+        const float p1 = __fmul_rn(__fadd_rn(u1[k], -kTwo23), s);
         a[0] = __fadd_rn(a[0], __fadd_rn(p0, z));
         a[1] = __fadd_rn(a[1], __fadd_rn(p1, z));
       }
@@ -371,31 +401,30 @@ __device__ __forceinline__ float warp_sum(float v) {
 // ------------------------------------------------------------ quantizers --
 // Codes are rne(fl(v / s)), v = x (INT8) or v = fl(x - lo) (INT4): an IEEE
 // division per element by definition.  Computed without one:
-//  1. r ~ 1/s from the hardware reciprocal (relative error <= 2^-23), so the
-//     exact product v * r is within |v/s| * 2^-23 <= 2^-16 of v/s, and fl(v/s)
-//     is within 2^-17 of v/s.  u = fma(v, r, M) with M = 1.5*2^23 (INT8) or
-//     2^23 (INT4) rounds v * r to the nearest integer c and leaves it in the
-//     low mantissa bits of u (which also pack directly into bytes/nibbles);
-//     c = u - M exactly, and n = fma(v, -r, c) = fl(c - v * r).
-//  2. If |n| < 1/2 - 2^-13, v * r is farther than 2^-13 - 2^-25 from every
-//     half-integer, so fl(v/s) is on the same side of each as v * r and
+//  1. r ~ 1/s from the hardware reciprocal (relative error <= 2^-23).  With
+//     r_hi = fl(r (1 + 2^-20)) and r_lo = fl(r (1 - 2^-20)), the exact
+//     products v r_hi and v r_lo bracket fl(v/s) strictly (fl(v/s) is within
+//     2^-24 of v/s relative, and (1 + 2^-20)(1 - 2^-23)(1 - 2^-24) > 1 +
+//     2^-24).  u = fma(v, r_x, M) with M = 1.5*2^23 (INT8) or 2^23 (INT4)
+//     rounds the product to the nearest integer and leaves it in the low
+//     mantissa bits of u (which also pack directly into bytes/nibbles).
+//  2. If both products round to the same integer c, no half-integer lies
+//     strictly between them, hence none between fl(v/s) and them, and
 //     rne(fl(v/s)) = c.
-//  3. Otherwise v/s lies within 2^-12 of the half-integer m next to v * r.
-//     Then D = v - m*s is an integer multiple of 2^(e_s - 25) smaller than
-//     2^(e_s - 11), so it fits in 24 bits and fma(-m, s, v) gives it exactly
-//     (for s >= 2^-100).  fl(v/s) == m exactly when D lies in m's half-ulp
-//     band [-hd, +hu] (hu = 2^(E-24) s for m = +-2^E...; hd = hu/2 only for
-//     |m| = 1/2), ties at the band edges going to m (its significand is
-//     even).  So the code is the even neighbour of m inside the band, and the
-//     neighbour on D's side outside it.
+//  3. Otherwise a half-integer m lies in [v r_lo, v r_hi], so v r is within
+//     2^-20 * 1.1 * 127.25 < 2^-13 of m and v/s within 2^-12 of it; c = the
+//     rounding of v r is m's neighbour on v r's side.  Then D = v - m*s is an
+//     integer multiple of 2^(e_s - 25) smaller than 2^(e_s - 11), so it fits
+//     in 24 bits and fma(-m, s, v) gives it exactly (for s >= 2^-100).
+//     fl(v/s) == m exactly when D lies in m's half-ulp band [-hd, +hu]
+//     (hu = 2^(E-24) s for m = +-2^E...; hd = hu/2 only for |m| = 1/2), ties
+//     at the band edges going to m (its significand is even).  So the code is
+//     the even neighbour of m inside the band, and the neighbour on D's side
+//     outside it.
 //  4. Groups where the bound v * r <= 127.25 (INT8) / 15.25 (INT4) fails or
 //     s < 2^-100 take the IEEE division for every element (never seen on
 //     finite activations; it keeps denormal scales exact).
 constexpr float kMagicI8 = 12582912.0f;         // 1.5 * 2^23, bits 0x4B400000
-// |n| >= 1/2 - 2^-13 (near a half-integer) <=> n*n - kNearSq >= 0; kNearSq =
-// (1/2 - 2^-13)^2 is exact in binary32 and fma(n, n, -kNearSq) has the sign
-// of the exact difference.
-constexpr float kNearSq = 0.24987794458866119384765625f;  // 2^-2 - 2^-13 + 2^-26
 constexpr float kTwoM24 = 5.9604644775390625e-08f;  // 2^-24
 constexpr float kTwoM100 = 7.888609052210118e-31f;  // 2^-100
 
@@ -506,33 +535,41 @@ __device__ __forceinline__ void minmax16(const float v[16], float& lo, float& hi
 // vote per element index.
 // Near-half-integer and division elements are settled after the fast path:
 // round_codes returns a 16-bit mask of the lane's elements that need it (bit
-// 8b + w for element 4w + b: the sign bytes of four values gathered by byte
-// permutes), settle_codes ORs the masks over the warp and one uniform loop
+// 8b + w for element 4w + b, gathered by byte permutes), settle_codes ORs
+// the masks over the warp and one uniform loop
 // visits only the element indices set in some lane, each with a single
 // shared copy of the exact code (steps 3 and 4).  pick(i) supplies the
 // lane's v_i, put(i, u) stores its exact code (u = bits of M + code).
 template <bool SIGNED>
 __device__ __forceinline__ uint32_t round_codes(const float v[16], float r, bool group_ok,
                                                 uint32_t ub[16]) {
+  // Flags from two roundings of every quotient, v * fl(r (1 + 2^-20)) and
+  // v * fl(r (1 - 2^-20)), which bracket fl(v / s) strictly (see the
+  // requantizers below): where both round to the same integer it is
+  // rne(fl(v / s)); where they differ the element lies within 2^-13 of a
+  // half-integer and is flagged.  The difference of the two roundings is 0 or
+  // +-1.0, whose byte 2 is 0x80: byte permutes gather it into the mask.
+  // (Measured on GB300: 6 fewer instructions per 16 values than flags from
+  // the residual c - v r.)
   const float magic = SIGNED ? kMagicI8 : 8388608.0f;
-  const float2 R = dup2(r), NR = dup2(-r), M = dup2(magic), NM = dup2(-magic), NQ = dup2(-kNearSq);
-  uint32_t notnear = 0;  // bit w of byte b: sign of fl(n^2 - kNearSq) for element 4w + b
+  const float2 RH = dup2(__fmul_rn(r, 1.00000095367431640625f)),
+               RL = dup2(__fmul_rn(r, 0.99999904632568359375f)), M = dup2(magic);
+  float2 dd[8];
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const float2 x = make_float2(v[i], v[i + 1]);
+    const float2 a = pfma(x, RH, M), b = pfma(x, RL, M);
+    ub[i] = __float_as_uint(a.x), ub[i + 1] = __float_as_uint(a.y);
+    dd[i / 2] = psub(a, b);
+  }
+  uint32_t flag = 0;  // bit w of byte b: element 4w + b flagged
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    uint32_t sgn[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int i = 4 * w + 2 * h;
-      const float2 x = make_float2(v[i], v[i + 1]);
-      const float2 u = pfma(x, R, M);
-      const float2 n = pfma(x, NR, padd(u, NM));  // fl(code - v * r)
-      const float2 q = pfma(n, n, NQ);
-      ub[i] = __float_as_uint(u.x), ub[i + 1] = __float_as_uint(u.y);
-      sgn[h] = __byte_perm(__float_as_uint(q.x), __float_as_uint(q.y), 0x0073u);
-    }
-    notnear |= (__byte_perm(sgn[0], sgn[1], 0x5410u) >> (7 - w)) & (0x01010101u << w);
+    const uint32_t s0 = __byte_perm(__float_as_uint(dd[2 * w].x), __float_as_uint(dd[2 * w].y), 0x0062u);
+    const uint32_t s1 = __byte_perm(__float_as_uint(dd[2 * w + 1].x), __float_as_uint(dd[2 * w + 1].y), 0x0062u);
+    flag |= (__byte_perm(s0, s1, 0x5410u) >> (7 - w)) & (0x01010101u << w);
   }
-  return group_ok ? (~notnear & 0x0F0F0F0Fu) : 0x0F0F0F0Fu;
+  return group_ok ? flag : 0x0F0F0F0Fu;
 }
 
 template <bool SIGNED>
@@ -669,8 +706,17 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
             if (k == (i >> 2)) q[k] = (q[k] & ~(0xFFu << sh)) | ((rb & 0xFFu) << sh);
         });
   if (DEQ) {
+    if (s < 1.2676506e30f) {  // u - 2^22 = 2^23 + q exactly; fma(2^23 + q, s, -2^23 s) = fl(q s)
+      const float2 C = dup2(-4194304.0f), S = dup2(s), N = dup2(__fmul_rn(-kTwo23, s));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) d[i] = __fmul_rn(__fsub_rn(__uint_as_float(ub[i]), kMagicI8), s);
+      for (int i = 0; i < 16; i += 2) {
+        const float2 t = pfma(padd(make_float2(__uint_as_float(ub[i]), __uint_as_float(ub[i + 1])), C), S, N);
+        d[i] = t.x, d[i + 1] = t.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) d[i] = __fmul_rn(__fsub_rn(__uint_as_float(ub[i]), kMagicI8), s);
+    }
   }
   return s;
 }
@@ -689,10 +735,8 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
     bf16_minmax16(bw, lo, hi);
   else
     minmax16(v, lo, hi);
-  lo = group_min(lo, lpg);
-  hi = group_max(hi, lpg);
-  if (lo == 0.0f) lo = 0.0f;  // -0 -> +0
-  if (hi == 0.0f) hi = 0.0f;
+  lo = __fadd_rn(group_min(lo, lpg), 0.0f);  // -0 + 0 = +0; other values unchanged
+  hi = __fadd_rn(group_max(hi, lpg), 0.0f);
   const float span = __fsub_rn(hi, lo);
   const float s = div15(span);
   z = lo;
@@ -749,6 +793,172 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
       for (int i = 0; i < 16; ++i)
         d[i] = __fadd_rn(__fmul_rn(__fsub_rn(__uint_as_float(ub[i]), kTwo23), s), z);
     }
+  }
+  return s;
+}
+
+// ------------------------------------------------ requantizers (fp32 in) --
+// The requantization of the reduced sums (fp32 values) in kernels that sum
+// eight slabs.  It uses the same two roundings as round_codes (steps
+// 1-3 above) but flags nothing per element: the codes of both roundings are
+// packed side by side and compared word by word, and only a warp in which
+// some word differs builds the per-element mask and settles it.  With four or
+// more slabs an element next to a half-integer is rare (0.05% of the prefill
+// sums, against 0.3% for two slabs, where the mask of round_codes is cheaper),
+// so the common case costs one extra rounding and packing per element (with
+// four slabs the extra live values made the compact build spill).
+// Measured on GB300 (executed instructions per 16 values, quantize and
+// dequantize, random groups): INT4 139 -> 116, INT8 127 -> 96; checked
+// bit-identical to the earlier near-half-integer scheme on 2^20 chunks of
+// random, tie-dense and near-tie groups, and against the oracle by the GPU
+// tests.
+
+// The exact pass over register arrays with a natural-order mask (bit i =
+// element i): position i is visited, unrolled, when any lane of the warp
+// flagged it.
+__device__ __forceinline__ void settle_unrolled(uint32_t mask, float s, float r, bool group_ok,
+                                                const float v[16], bool is_signed, uint32_t ub[16]) {
+  const uint32_t any = __reduce_or_sync(kFull, mask);
+  const float magic = is_signed ? kMagicI8 : kTwo23;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (any & (1u << i)) {
+      const float ci = __fsub_rn(__fmaf_rn(v[i], r, magic), magic);  // the code from r itself
+      const float e = __fmaf_rn(v[i], r, -ci);
+      const float res = is_signed ? exact_code<true>(v[i], s, ci, e, group_ok)
+                                  : exact_code<false>(v[i], s, ci, e, group_ok);
+      if (mask & (1u << i)) ub[i] = __float_as_uint(__fadd_rn(res, magic));
+    }
+  }
+}
+
+// Eight 4-bit codes (ub = bits of 2^23 + code) packed into nibbles by a
+// multiply-add chain (see quant_i4).
+__device__ __forceinline__ uint32_t pack_nibbles8(const uint32_t* ub) {
+  uint32_t w = ub[7];
+#pragma unroll
+  for (int i = 6; i >= 1; --i) w = w * 16u + ub[i];
+  return w * 16u + (ub[0] - 0xFB000000u);
+}
+
+constexpr float kRcpUp = 1.00000095367431640625f;    // 1 + 2^-20
+constexpr float kRcpDown = 0.99999904632568359375f;  // 1 - 2^-20
+
+// INT4 asymmetric requantization of this lane's 16 fp32 values of a group
+// spread over lpg lanes: lo = min, hi = max (a zero extreme taken as +0),
+// s = (hi - lo) / 15, z = lo, q = clamp(rne((v - lo) / s), 0, 15).  Writes the
+// packed codes q[2], z, and d = fl(fl(q s) + z); returns s.  Every lane of the
+// warp must call it.
+__device__ __forceinline__ float requant_i4(const float v[16], int lpg, uint32_t q[2], float& z,
+                                            float d[16]) {
+  float lo, hi;
+  minmax16(v, lo, hi);
+  lo = __fadd_rn(group_min(lo, lpg), 0.0f);  // -0 + 0 = +0; other values unchanged
+  hi = __fadd_rn(group_max(hi, lpg), 0.0f);
+  const float span = __fsub_rn(hi, lo);
+  const float s = div15(span);
+  z = lo;
+  float num[16];  // fl(v - lo)
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const float2 n = padd(make_float2(v[i], v[i + 1]), dup2(-lo));
+    num[i] = n.x, num[i + 1] = n.y;
+  }
+  const float r = s == 0.0f ? 0.0f : rcp_approx(s);
+  const bool ok = s == 0.0f || (__fmul_rn(span, r) <= 15.25f && s >= kTwoM100);
+  const float2 RH = dup2(__fmul_rn(r, kRcpUp)), RL = dup2(__fmul_rn(r, kRcpDown)), M = dup2(kTwo23);
+  uint32_t u1[16];
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const float2 a = pfma(make_float2(num[i], num[i + 1]), RH, M);
+    u1[i] = __float_as_uint(a.x), u1[i + 1] = __float_as_uint(a.y);
+  }
+  q[0] = pack_nibbles8(u1), q[1] = pack_nibbles8(u1 + 8);
+  // the codes from r_lo, folded into packed words as they come (high code
+  // first), so only a pair of them is live at a time
+  uint32_t diff = 0;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int k = 3; k >= 0; --k) {
+      const float2 b = pfma(make_float2(num[8 * j + 2 * k], num[8 * j + 2 * k + 1]), RL, M);
+      w = w * 16u + __float_as_uint(b.y);
+      w = w * 16u + __float_as_uint(b.x);
+    }
+    diff |= q[j] ^ (w - 0xFB000000u);
+  }
+  if (__any_sync(kFull, diff != 0u || !ok)) {  // rare: settle the flagged elements
+    uint32_t mask = 0xFFFFu;
+    if (ok) {
+      mask = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        mask |= (u1[i] != __float_as_uint(__fmaf_rn(num[i], __fmul_rn(r, kRcpDown), kTwo23)) ? 1u : 0u) << i;
+    }
+    settle_unrolled(mask, s, r, ok, num, false, u1);
+    q[0] = pack_nibbles8(u1), q[1] = pack_nibbles8(u1 + 8);
+  }
+  if (s < 1.2676506e30f) {  // fl(q s) = fma(2^23 + q, s, -2^23 s), exact for s < 2^100
+    const float2 S = dup2(s), N = dup2(__fmul_rn(-kTwo23, s)), Z = dup2(z);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const float2 t =
+          padd(pfma(make_float2(__uint_as_float(u1[i]), __uint_as_float(u1[i + 1])), S, N), Z);
+      d[i] = t.x, d[i + 1] = t.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) d[i] = __fadd_rn(__fmul_rn(__fsub_rn(__uint_as_float(u1[i]), kTwo23), s), z);
+  }
+  return s;
+}
+
+// INT8 symmetric requantization of this lane's 16 fp32 values of a group
+// spread over lpg lanes: s = max|v| / 127, q = clamp(rne(v / s), -127, 127);
+// writes q[4] and d = fl(q s); returns s.  Every lane must call it.
+__device__ __forceinline__ float requant_i8(const float v[16], int lpg, uint32_t q[4], float d[16]) {
+  const float a = group_max(absmax16(v), lpg);
+  const float s = div127(a);
+  const float r = s == 0.0f ? 0.0f : rcp_approx(s);
+  const bool ok = s == 0.0f || (__fmul_rn(a, r) <= 127.25f && s >= kTwoM100);
+  const float2 RH = dup2(__fmul_rn(r, kRcpUp)), RL = dup2(__fmul_rn(r, kRcpDown)), M = dup2(kMagicI8);
+  uint32_t u1[16], diff = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {  // four codes at a time: both roundings, packed and compared
+    const float2 a0 = pfma(make_float2(v[4 * j], v[4 * j + 1]), RH, M);
+    const float2 a1 = pfma(make_float2(v[4 * j + 2], v[4 * j + 3]), RH, M);
+    const float2 b0 = pfma(make_float2(v[4 * j], v[4 * j + 1]), RL, M);
+    const float2 b1 = pfma(make_float2(v[4 * j + 2], v[4 * j + 3]), RL, M);
+    u1[4 * j] = __float_as_uint(a0.x), u1[4 * j + 1] = __float_as_uint(a0.y);
+    u1[4 * j + 2] = __float_as_uint(a1.x), u1[4 * j + 3] = __float_as_uint(a1.y);
+    q[j] = low_bytes4(u1[4 * j], u1[4 * j + 1], u1[4 * j + 2], u1[4 * j + 3]);
+    diff |= q[j] ^ low_bytes4(__float_as_uint(b0.x), __float_as_uint(b0.y), __float_as_uint(b1.x),
+                              __float_as_uint(b1.y));
+  }
+  if (__any_sync(kFull, diff != 0u || !ok)) {  // rare: settle the flagged elements
+    uint32_t mask = 0xFFFFu;
+    if (ok) {
+      mask = 0;
+      const float rl = __fmul_rn(r, kRcpDown);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        mask |= (u1[i] != __float_as_uint(__fmaf_rn(v[i], rl, kMagicI8)) ? 1u : 0u) << i;
+    }
+    settle_unrolled(mask, s, r, ok, v, true, u1);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = low_bytes4(u1[4 * j], u1[4 * j + 1], u1[4 * j + 2], u1[4 * j + 3]);
+  }
+  if (s < 1.2676506e30f) {  // u - 2^22 = 2^23 + q exactly; fma(2^23 + q, s, -2^23 s) = fl(q s)
+    const float2 C = dup2(-4194304.0f), S = dup2(s), N = dup2(__fmul_rn(-kTwo23, s));
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const float2 t = pfma(padd(make_float2(__uint_as_float(u1[i]), __uint_as_float(u1[i + 1])), C), S, N);
+      d[i] = t.x, d[i + 1] = t.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) d[i] = __fmul_rn(__fsub_rn(__uint_as_float(u1[i]), kMagicI8), s);
   }
   return s;
 }
