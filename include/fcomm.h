@@ -127,9 +127,13 @@ fc_status fc_shard_range(fc_qspec spec, int64_t rows, int64_t hidden, int P, int
  * Per group (fp32, IEEE division, round-to-nearest-even codes, no FMA):
  *  INT8: s = max|x|/127; q = clamp(rne(x/s), -127, 127); s == 0 -> codes 0.
  *  INT4: lo = min, hi = max (a zero extreme is +0); s = (hi-lo)/15; z = lo;
- *        q = clamp(rne((x-lo)/s), 0, 15); s == 0 -> codes 0. */
+ *        q = clamp(rne((x-lo)/s), 0, 15); s == 0 -> codes 0.
+ * d_status (optional, two int32 words of device memory, 4-byte aligned) is
+ * set by this call to {FC_OK, 0x7F7F7F7F}; word 0 becomes FC_ERR_CUDA if a
+ * shared-memory staging copy of the input fails to land within its bounded
+ * wait (about a second), in which case the outputs are incomplete. */
 fc_status fc_group_quantize(const void* x_bf16, int64_t rows, int64_t hidden, fc_qspec spec,
-                            fc_qtensor out, fc_stream_t stream);
+                            fc_qtensor out, int32_t* d_status, fc_stream_t stream);
 
 /* Self-synchronizing quantized payloads (flash-comm, abstract: every block
  * carries evidence of its readiness; applied to Flash Communication's
@@ -146,17 +150,17 @@ fc_status fc_group_quantize(const void* x_bf16, int64_t rows, int64_t hidden, fc
  * every block checked against expected_epoch, stale blocks reported through
  * d_status like FC_FMT_BF16_TAGGED (block index counted over the blocks of
  * slab 0's rows, then slab 1's, ...); its requant_out (optional) is the plain
- * INT8/INT4 payload. */
+ * INT8/INT4 payload.  d_status: optional, as for fc_group_quantize. */
 fc_status fc_group_quantize_tagged(const void* const* x_bf16, int P, int64_t rows,
                                    int64_t hidden, fc_qspec spec, uint32_t epoch,
-                                   void* const* blocks, fc_stream_t stream);
+                                   void* const* blocks, int32_t* d_status, fc_stream_t stream);
 
 /* Quantize P bf16 slabs in one launch; slab p reads x_bf16[p] and writes
  * out[p] (host arrays of P entries, 1 <= P <= 8).  Same result as P calls of
- * fc_group_quantize. */
+ * fc_group_quantize.  d_status: optional, as for fc_group_quantize. */
 fc_status fc_group_quantize_multi(const void* const* x_bf16, int P, int64_t rows,
                                   int64_t hidden, fc_qspec spec, const fc_qtensor* out,
-                                  fc_stream_t stream);
+                                  int32_t* d_status, fc_stream_t stream);
 
 /* Reduce-scatter stage math of the two-step All-Reduce (Flash Communication,
  * "Main contributions" 2; flash-comm abstract for the fixed order):
@@ -168,11 +172,15 @@ fc_status fc_group_quantize_multi(const void* const* x_bf16, int P, int64_t rows
 fc_status fc_reduce_dequant_sum(const fc_qtensor* slabs, int P, int64_t rows, int64_t hidden,
                                 fc_qspec spec, int shard, float* out_f32, fc_stream_t stream);
 
-/* Requantize a reduced fp32 tensor (same quantizer as fc_group_quantize,
- * applied to the fp32 values) into requant_out (the all-gather payload), and
- * write its dequantization to `out` as out_dtype FC_FMT_BF16 (round to
- * nearest even) or FC_FMT_F32.  requant_out.codes may be NULL (payload not
- * stored); out may be NULL (no dequantized output). */
+/* All-gather half of the two-step All-Reduce (Flash Communication, "Core
+ * ideas": every reduced shard is requantized and sent to every rank, which
+ * dequantizes it).  Requantize a reduced fp32 tensor (same quantizer as
+ * fc_group_quantize, applied to the fp32 values) into requant_out (the
+ * all-gather payload), and write its dequantization to `out` as out_dtype
+ * FC_FMT_BF16 (round to nearest even) or FC_FMT_F32.  requant_out.codes may
+ * be NULL (payload not stored); out may be NULL (no dequantized output).
+ * The kernel reads its input with plain loads (no staging copy, no wait),
+ * so it has no status word. */
 fc_status fc_requant_gather(const float* reduced_f32, int64_t rows, int64_t hidden, fc_qspec spec,
                             fc_qtensor requant_out, void* out, int32_t out_dtype,
                             fc_stream_t stream);

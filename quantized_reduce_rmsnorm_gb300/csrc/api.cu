@@ -153,8 +153,19 @@ fc_status fc_shard_range(fc_qspec spec, int64_t rows, int64_t hidden, int P, int
   return ok();
 }
 
+// {FC_OK, 0x7F7F7F7F} into an optional two-word device status, ordered before
+// the call's kernel on its stream.
+fc_status reset_status(int32_t* d_status, cudaStream_t st) {
+  if (!d_status) return ok();
+  if (!aligned(d_status, 4)) return fail(FC_ERR_INVALID, "d_status must be 4-byte aligned");
+  cudaError_t e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(d_status + 1, 0x7F, sizeof(int32_t), st);
+  return e == cudaSuccess ? ok() : cuda_status(e, "d_status reset");
+}
+
 fc_status fc_group_quantize_multi(const void* const* x_bf16, int P, int64_t rows, int64_t hidden,
-                                  fc_qspec spec, const fc_qtensor* out, fc_stream_t stream) {
+                                  fc_qspec spec, const fc_qtensor* out, int32_t* d_status,
+                                  fc_stream_t stream) {
   if (fc_status s = check_shape(spec, rows, hidden, true)) return s;
   if (P < 1 || P > 8) return fail(FC_ERR_INVALID, "P must be in [1, 8] (got %d)", P);
   if (rows == 0) return ok();
@@ -171,13 +182,15 @@ fc_status fc_group_quantize_multi(const void* const* x_bf16, int P, int64_t rows
   job.n = rows * hidden;
   job.P = P;
   job.G = spec.group;
+  job.status = d_status;
+  if (fc_status s = reset_status(d_status, (cudaStream_t)stream)) return s;
   return cuda_status(fc::launch_quantize(spec.fmt, false, fc::kDeqNone, job, (cudaStream_t)stream),
                      "fc_group_quantize launch");
 }
 
 fc_status fc_group_quantize_tagged(const void* const* x_bf16, int P, int64_t rows,
                                    int64_t hidden, fc_qspec spec, uint32_t epoch,
-                                   void* const* blocks, fc_stream_t stream) {
+                                   void* const* blocks, int32_t* d_status, fc_stream_t stream) {
   if (!qtagged(spec.fmt))
     return fail(FC_ERR_INVALID, "format %d is not a tagged quantized format", spec.fmt);
   if (fc_status s = check_shape(spec, rows, hidden, false)) return s;
@@ -195,13 +208,15 @@ fc_status fc_group_quantize_tagged(const void* const* x_bf16, int P, int64_t row
   job.P = P;
   job.G = spec.group;
   job.epoch = epoch;
+  job.status = d_status;
+  if (fc_status s = reset_status(d_status, (cudaStream_t)stream)) return s;
   return cuda_status(fc::launch_quantize_tagged(spec.fmt, job, (cudaStream_t)stream),
                      "fc_group_quantize_tagged launch");
 }
 
 fc_status fc_group_quantize(const void* x_bf16, int64_t rows, int64_t hidden, fc_qspec spec,
-                            fc_qtensor out, fc_stream_t stream) {
-  return fc_group_quantize_multi(&x_bf16, 1, rows, hidden, spec, &out, stream);
+                            fc_qtensor out, int32_t* d_status, fc_stream_t stream) {
+  return fc_group_quantize_multi(&x_bf16, 1, rows, hidden, spec, &out, d_status, stream);
 }
 
 fc_status fc_reduce_dequant_sum(const fc_qtensor* slabs, int P, int64_t rows, int64_t hidden,

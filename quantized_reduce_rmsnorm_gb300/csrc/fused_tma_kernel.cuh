@@ -136,14 +136,27 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
   const int64_t bpr = g.row_cb / 16;           // tagged blocks per row and slab
   const int64_t seg_blk = rank * (g.cb / 16);  // ... before this CTA's segment
 
+  // tid 0's last copy into each (sub-)stage x: bit x of `used`, its phase
+  // parity in `ppar`.  On a timeout tid 0 waits once for each of these: a
+  // wait on the parity of the last phase returns at once if that copy has
+  // landed (no later copy was issued into the stage) and otherwise waits for
+  // it, bounded.  Kept in shared memory (only tid 0 touches them).
+  __shared__ uint32_t used, ppar;
+  auto note_issue = [&](int x, int iter) {
+    used |= 1u << x;
+    ppar = (ppar & ~(1u << x)) | (static_cast<uint32_t>((iter / NSTAGE) & 1) << x);
+  };
+  if (tid == 0) used = 0, ppar = 0;
   if (tid == 0) {
     for (int s = 0; s < NSTAGE * SUB; ++s) mbar_init(&bar[s], 1);
     mbar_init_fence();
     for (int s = 0; s < NSTAGE; ++s)
       if (row0 + s * rstride < a.rows)
-        for (int j = 0; j < SUB; ++j)
+        for (int j = 0; j < SUB; ++j) {
           issue_row<FMT>(a, g, stage0 + (s * SUB + j) * g.stage_bytes, &bar[s * SUB + j], row0 + s * rstride,
                          SUB > 1 ? j : rank);
+          note_issue(s * SUB + j, s);
+        }
   }
   __syncthreads();
   if (CL > 1) cluster_barrier();  // every CTA of the cluster runs before any peer store
@@ -298,6 +311,7 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
           if (nrow < a.rows) {
             fence_proxy_async_smem();
             issue_row<FMT>(a, g, stage0 + (s * SUB + j) * g.stage_bytes, &bar[s * SUB + j], nrow, j);
+            note_issue(s * SUB + j, i + NSTAGE);
           }
         }
       }
@@ -346,8 +360,10 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
         fence_proxy_async_smem();
         issue_row<FMT>(a, g, stage0 + (s * SUB + SUB - 1) * g.stage_bytes, &bar[s * SUB + SUB - 1], nrow,
                        SUB > 1 ? SUB - 1 : rank);
+        note_issue(s * SUB + SUB - 1, i + NSTAGE);
       }
     }
+
 
     // ---- pass 2: y = bf16(fl(h * gamma) * inv); h * gamma is exact in binary32
     auto out_chunk = [&](int c, const uint32_t gw[8]) {
@@ -372,13 +388,12 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
     }
   }
   if (!all_ok && tid == 0) {
-    // a staged copy did not land within the bound: report it and give the
-    // copies still in flight one more bounded wait before the CTA exits
+    // a staged copy did not land within the bound: report it and give each
+    // copy still in flight one bounded wait, with its own phase parity,
+    // before the CTA exits
     if (a.status) atomicExch(a.status, 2 /* FC_ERR_CUDA */);
-    for (int s = 0; s < NSTAGE * SUB; ++s) {
-      mbar_wait_bounded(&bar[s], 0);
-      mbar_wait_bounded(&bar[s], 1);
-    }
+    for (int x = 0; x < NSTAGE * SUB; ++x)
+      if ((used >> x) & 1u) mbar_wait_bounded(&bar[x], (ppar >> x) & 1u);
   }
 }
 

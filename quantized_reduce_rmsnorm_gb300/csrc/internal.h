@@ -32,6 +32,7 @@ struct QuantJob {
   float* scales[8];
   float* zeros[8];
   void* deq;  // NULL, bf16 or fp32 [n] (P == 1 only)
+  int32_t* status;  // NULL, or word 0 set to FC_ERR_CUDA if a staged copy never lands
   uint32_t epoch;  // tagged quantized output only
   int64_t n;  // elements per tensor (multiple of G)
   int P;

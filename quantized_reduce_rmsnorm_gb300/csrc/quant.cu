@@ -130,13 +130,14 @@ __global__ void __launch_bounds__(kThreads) k_quantize(QuantJob job, int64_t chu
 // cursor steps; calls with fewer 2048-element tiles than resident warps
 // (decode) keep the smaller tiles, which spread over more warps.  Both use
 // 8 KB of ring per warp.
-template <int TILE>
+template <int TILE, int STAGES>
 struct WRing {
-  static constexpr int kStages = TILE == 1024 ? 4 : 2;
+  static constexpr int kStages = STAGES;
   static constexpr int kBytes = kStages * TILE * 2;
 };
-constexpr int kWRingBytes = WRing<2048>::kBytes;
-static_assert(WRing<1024>::kBytes == WRing<2048>::kBytes, "one shared-memory size for both tilings");
+template <int TILE>
+constexpr int default_stages() { return TILE == 1024 ? 4 : 2; }
+static_assert(WRing<1024, 4>::kBytes == WRing<2048, 2>::kBytes, "one shared-memory size for both tilings");
 constexpr int kQWarps = kThreads / 32;
 
 // TAGGED: the codes and scales go out as self-synchronizing blocks carrying
@@ -145,13 +146,14 @@ constexpr int kQWarps = kThreads / 32;
 // words 0..2 of a 16-byte block, the epoch in word 3.
 // LPG: lanes per group when known at compile time (the two standard group
 // sizes), 0 to take it from lpg_shift.
-template <int FMT, bool TAGGED = false, int LPG = 0, int TILE = 2048>
-__global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int lpg_shift,
-                                                           int64_t tiles_per_slab) {
+template <int FMT, bool TAGGED = false, int LPG = 0, int TILE = 2048, int STAGES = default_stages<TILE>()>
+__global__ void __launch_bounds__(kThreads, STAGES == 1 ? 4 : 3)
+    k_quantize_tma(QuantJob job, int lpg_shift, int64_t tiles_per_slab) {
   pdl_begin();
-  constexpr int kWTile = TILE, kWStages = WRing<TILE>::kStages;
+  constexpr int kWTile = TILE, kWStages = STAGES;
+  constexpr int kRingBytes = WRing<TILE, STAGES>::kBytes;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint64_t bars[kQWarps][WRing<TILE>::kStages];
+  __shared__ uint64_t bars[kQWarps][STAGES];
   // INT8 tagged: a warp assembles its 4 groups' payloads (33 words each) here
   __shared__ uint32_t qstage[TAGGED && FMT == kINT8 ? kQWarps : 1][4][33];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int 
   const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kQWarps + wid;
   const int64_t wstride = static_cast<int64_t>(gridDim.x) * kQWarps;
   if (w0 >= total) return;  // whole warp
-  uint8_t* ring = smem + wid * kWRingBytes;
+  uint8_t* ring = smem + wid * kRingBytes;
   uint64_t* bar = bars[wid];
 
   // A cursor over the flattened (slab, tile) space that only moves forward by
@@ -210,6 +212,14 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int 
     }
     if (!__all_sync(kFull, mbar_wait_bounded(&bar[st], (k / kWStages) & 1))) {
       ok = false;  // a tile never landed (about a second): stop, outputs incomplete
+      if (lane == 0) {
+        if (job.status) atomicExch(job.status, 2 /* FC_ERR_CUDA */);
+        // the copies still in flight: this iteration's and the ones issued
+        // ahead of it, each waited for once with its own phase parity
+        for (int j = 0; j < kWStages; ++j)
+          if (t + j * wstride < total)
+            mbar_wait_bounded(&bar[(k + j) % kWStages], ((k + j) / kWStages) & 1);
+      }
       break;
     }
     const int p = cur.p;
@@ -293,8 +303,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_tma(QuantJob job, int 
     }
     __syncwarp();  // every lane is done with stage st before lane 0 refills it
   }
-  if (!ok && lane == 0)  // give copies still in flight a bounded wait before exiting
-    for (int s = 0; s < kWStages; ++s) mbar_wait_bounded(&bar[s], 0), mbar_wait_bounded(&bar[s], 1);
+  (void)ok;
 }
 
 // --------------------------------------------------------- reduce kernel --
@@ -514,11 +523,11 @@ void occ_memo_store(const OccKey& k, int value) {
   }
 }
 
-template <int FMT, bool TAGGED, int LPG, int TILE>
+template <int FMT, bool TAGGED, int LPG, int TILE, int STAGES = default_stages<TILE>()>
 cudaError_t launch_quantize_tma_t(const QuantJob& job, cudaStream_t st) {
   constexpr int kWTile = TILE;
-  const int smem = kQWarps * kWRingBytes;
-  auto kern = k_quantize_tma<FMT, TAGGED, LPG, TILE>;
+  const int smem = kQWarps * WRing<TILE, STAGES>::kBytes;
+  auto kern = k_quantize_tma<FMT, TAGGED, LPG, TILE, STAGES>;
   const int occ = occupancy_memo(reinterpret_cast<const void*>(kern), kThreads, smem, 1, [&] {
     int o = 0;
     if (raise_smem_limit(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||

@@ -94,14 +94,14 @@ def load(path: Optional[str] = None):
         "fc_tagged_bytes": (ctypes.c_size_t, [i64, i64]),
         "fc_shard_range": (i32, [QS, i64, i64, i32, i32, ctypes.POINTER(i64),
                                  ctypes.POINTER(i64)]),
-        "fc_group_quantize": (i32, [P, i64, i64, QS, QT, P]),
-        "fc_group_quantize_multi": (i32, [P, i32, i64, i64, QS, P, P]),
+        "fc_group_quantize": (i32, [P, i64, i64, QS, QT, P, P]),
+        "fc_group_quantize_multi": (i32, [P, i32, i64, i64, QS, P, P, P]),
         "fc_reduce_dequant_sum": (i32, [P, i32, i64, i64, QS, i32, P, P]),
         "fc_requant_gather": (i32, [P, i64, i64, QS, QT, P, i32, P]),
         "fc_allgather_dequant": (i32, [ctypes.POINTER(QT), i32, i64, i64, QS, i32, P, u32, P, P]),
         "fc_pack_tagged": (i32, [P, i64, i64, u32, P, P]),
         "fc_pack_tagged_multi": (i32, [P, i32, i64, i64, u32, P, P]),
-        "fc_group_quantize_tagged": (i32, [P, i32, i64, i64, QS, u32, P, P]),
+        "fc_group_quantize_tagged": (i32, [P, i32, i64, i64, QS, u32, P, P, P]),
         "fc_allreduce_residual_rmsnorm": (
             i32, [P, i32, i64, i64, QS, P, P, P, f32, QT, P, u32, P, P]),
         "fc_allreduce_residual_rmsnorm_ex": (
@@ -221,22 +221,28 @@ def alloc_qtensor(spec: QSpec, rows: int, hidden: int, device="cuda"):
 
 
 # --------------------------------------------------------------- compute ---
-def group_quantize(x: torch.Tensor, spec: QSpec, out, stream=None):
-    """Quantize one [rows, hidden] bf16 slab into out = (codes, scales[, zeros])."""
+def group_quantize(x: torch.Tensor, spec: QSpec, out, stream=None,
+                   d_status: Optional[torch.Tensor] = None):
+    """Quantize one [rows, hidden] bf16 slab into out = (codes, scales[, zeros]);
+    d_status: optional int32[2] device status words (see fcomm.h)."""
     rows, hidden = _rows_hidden(x)
-    _check(load().fc_group_quantize(_ptr(x), rows, hidden, spec, _qt(out), _stream(stream)))
+    _check(load().fc_group_quantize(_ptr(x), rows, hidden, spec, _qt(out), _ptr(d_status),
+                                    _stream(stream)))
 
 
-def bind_group_quantize_multi(xs: Sequence[torch.Tensor], spec: QSpec, outs) -> Bound:
+def bind_group_quantize_multi(xs: Sequence[torch.Tensor], spec: QSpec, outs,
+                              d_status: Optional[torch.Tensor] = None) -> Bound:
     rows, hidden = _rows_hidden(xs[0])
     xp = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
     qo = (QTensor * len(outs))(*[_qt(o) for o in outs])
-    return Bound(load().fc_group_quantize_multi, [xp, len(xs), rows, hidden, spec, qo, None], 6,
-                 keep=(tuple(xs), tuple(outs)))
+    return Bound(load().fc_group_quantize_multi,
+                 [xp, len(xs), rows, hidden, spec, qo, ctypes.c_void_p(_ptr(d_status)), None], 7,
+                 keep=(tuple(xs), tuple(outs), d_status))
 
 
-def group_quantize_multi(xs: Sequence[torch.Tensor], spec: QSpec, outs, stream=None):
-    bind_group_quantize_multi(xs, spec, outs)(stream)
+def group_quantize_multi(xs: Sequence[torch.Tensor], spec: QSpec, outs, stream=None,
+                         d_status: Optional[torch.Tensor] = None):
+    bind_group_quantize_multi(xs, spec, outs, d_status)(stream)
 
 
 def reduce_dequant_sum(slabs, spec: QSpec, rows: int, hidden: int, out: torch.Tensor,
@@ -295,19 +301,22 @@ def pack_tagged(x: torch.Tensor, epoch: int, blocks: torch.Tensor, stream=None):
 
 
 def bind_group_quantize_tagged(xs: Sequence[torch.Tensor], spec: QSpec, epoch: int,
-                               blocks: Sequence[torch.Tensor]) -> Bound:
+                               blocks: Sequence[torch.Tensor],
+                               d_status: Optional[torch.Tensor] = None) -> Bound:
     rows, hidden = _rows_hidden(xs[0])
     xp = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
     bp = (ctypes.c_void_p * len(blocks))(*[_ptr(b) for b in blocks])
     return Bound(load().fc_group_quantize_tagged,
-                 [xp, len(xs), rows, hidden, spec, ctypes.c_uint32(epoch), bp, None], 7, 5,
-                 keep=(tuple(xs), tuple(blocks)))
+                 [xp, len(xs), rows, hidden, spec, ctypes.c_uint32(epoch), bp,
+                  ctypes.c_void_p(_ptr(d_status)), None], 8, 5,
+                 keep=(tuple(xs), tuple(blocks), d_status))
 
 
 def group_quantize_tagged(xs: Sequence[torch.Tensor], spec: QSpec, epoch: int,
-                          blocks: Sequence[torch.Tensor], stream=None):
+                          blocks: Sequence[torch.Tensor], stream=None,
+                          d_status: Optional[torch.Tensor] = None):
     """Quantize P bf16 slabs straight into self-synchronizing blocks."""
-    bind_group_quantize_tagged(xs, spec, epoch, blocks)(stream)
+    bind_group_quantize_tagged(xs, spec, epoch, blocks, d_status)(stream)
 
 
 def bind_pack_tagged_multi(xs: Sequence[torch.Tensor], epoch: int,

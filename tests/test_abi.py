@@ -70,21 +70,21 @@ def _status(call):
 ])
 def test_quantize_rejects_bad_specs(hidden, group, fmt):
     st, msg = _status(lambda L: L.fc_group_quantize(None, 4, hidden, fc.QSpec(fmt, group),
-                                                    fc.QTensor(), None))
+                                                    fc.QTensor(), None, None))
     assert st == fc.FC_ERR_INVALID and msg
 
 
 def test_pointer_checks_precede_any_launch():
     q = fc.QTensor(64, 128, None)
-    st, msg = _status(lambda L: L.fc_group_quantize(None, 4, 4096, fc.INT8_G128, q, None))
+    st, msg = _status(lambda L: L.fc_group_quantize(None, 4, 4096, fc.INT8_G128, q, None, None))
     assert st == fc.FC_ERR_INVALID and "NULL" in msg
-    st, msg = _status(lambda L: L.fc_group_quantize(48, 4, 4096, fc.INT8_G128, q, None))
+    st, msg = _status(lambda L: L.fc_group_quantize(48, 4, 4096, fc.INT8_G128, q, None, None))
     assert st == fc.FC_ERR_INVALID and "aligned" in msg
     bad = fc.QTensor(64, 130, None)   # scales not 4-byte aligned
-    st, msg = _status(lambda L: L.fc_group_quantize(64, 4, 4096, fc.INT8_G128, bad, None))
+    st, msg = _status(lambda L: L.fc_group_quantize(64, 4, 4096, fc.INT8_G128, bad, None, None))
     assert st == fc.FC_ERR_INVALID and "scales" in msg
     nozeros = fc.QTensor(64, 128, None)
-    st, msg = _status(lambda L: L.fc_group_quantize(64, 4, 4096, fc.INT4_G32, nozeros, None))
+    st, msg = _status(lambda L: L.fc_group_quantize(64, 4, 4096, fc.INT4_G32, nozeros, None, None))
     assert st == fc.FC_ERR_INVALID and "zeros" in msg
 
 
@@ -115,7 +115,7 @@ def test_reduce_rejects_bad_shard():
 
 def test_rows_zero_is_a_no_op():
     lib = fc.fcomm.load()
-    st = lib.fc_group_quantize(None, 0, 4096, fc.INT8_G128, fc.QTensor(), None)
+    st = lib.fc_group_quantize(None, 0, 4096, fc.INT8_G128, fc.QTensor(), None, None)
     assert st == fc.FC_OK
 
 
@@ -237,3 +237,32 @@ def test_bound_call_keeps_its_tensors_alive(monkeypatch):
     del send, fuse
     gc.collect()
     assert all(r() is None for r in refs)
+
+
+def test_bound_sender_passes_its_status_word(monkeypatch):
+    """The sender calls marshal their optional status word into the C call
+    (checked with a stand-in for the entry point, binding host tensors): a
+    staged copy that never lands is then reported in it, not lost."""
+    import torch
+    monkeypatch.setattr(fc.fcomm, "_ptr", lambda t: None if t is None else t.data_ptr())
+    seen = []
+
+    class FakeLib:
+        def fc_group_quantize_multi(self, *args):
+            seen.append(("multi", args))
+            return fc.FC_OK
+
+        def fc_group_quantize_tagged(self, *args):
+            seen.append(("tagged", args))
+            return fc.FC_OK
+
+    out = [fc.alloc_qtensor(fc.INT8_G128, 2, 128, "cpu")]
+    monkeypatch.setattr(fc.fcomm, "load", lambda path=None: FakeLib())
+    x = [torch.zeros(2, 128, dtype=torch.bfloat16)]
+    st = torch.zeros(2, dtype=torch.int32)
+    fc.bind_group_quantize_multi(x, fc.INT8_G128, out, d_status=st)(stream=5)
+    fc.bind_group_quantize_tagged(x, fc.INT8_G128_TAGGED, 3, [torch.zeros(64, dtype=torch.uint8)],
+                                  d_status=st)(stream=6)
+    (k1, a1), (k2, a2) = seen
+    assert k1 == "multi" and a1[6].value == st.data_ptr() and a1[7] == 5
+    assert k2 == "tagged" and a2[7].value == st.data_ptr() and a2[8] == 6 and a2[5].value == 3

@@ -952,3 +952,34 @@ def test_sweep_point_every_element(orc, msg, H, P, fmt, G):
     pipe = Pipeline(w, inp)
     pipe.step()
     check_every_element(orc, w, pipe, inp)
+
+
+@pytest.mark.parametrize("fmt,G,tagged", [(I8, 128, False), (I4, 32, False), (I8T, 128, True)])
+def test_sender_status_word_reset_to_ok(orc, fmt, G, tagged):
+    """The sender calls set their optional status word to {FC_OK, 0x7F7F7F7F}
+    (a staged copy that never lands would turn word 0 into FC_ERR_CUDA; that
+    path needs a fault to trigger and is not run), and the codes are still
+    the oracle's."""
+    w = small("status", P=3, T=5, H=2048, fmt=fmt, group=G)
+    inp = synth.make_inputs(w, seed=71)
+    xs = [dev_bf16(s) for s in inp["slabs"]]
+    st = torch.full((2,), -5, dtype=torch.int32, device="cuda")
+    spec = spec_of(fmt, G)
+    if tagged:
+        blocks = [torch.empty(fc.codes_bytes(spec, w.T, w.H), dtype=torch.uint8, device="cuda")
+                  for _ in range(w.P)]
+        fc.group_quantize_tagged(xs, spec, 4, blocks, d_status=st)
+    else:
+        outs = [fc.alloc_qtensor(spec, w.T, w.H) for _ in range(w.P)]
+        fc.group_quantize_multi(xs, spec, outs, d_status=st)
+    torch.cuda.synchronize()
+    assert host(st).tolist() == [fc.FC_OK, fc.STATUS_NO_INDEX]
+    base = synth.base_format(fmt)
+    for p in range(w.P):
+        q, s_, z = orc.quantize(base, bf16_float(inp["slabs"][p]).ravel(), G)
+        if tagged:
+            assert_bits_equal(host(blocks[p]).view(np.uint32), orc.pack_qtagged(base, q, s_, z, G, 4),
+                              f"blocks slab {p}")
+        else:
+            assert_bits_equal(host(outs[p][0]), q, f"codes slab {p}")
+            assert_bits_equal(host(outs[p][1]), s_, f"scales slab {p}")
