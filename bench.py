@@ -132,9 +132,14 @@ def parse():
     ap.add_argument("--only", default="",
                     help="sweep: only these points, MSG:H:P:FMT[,...] (FMT bf16, int8 or int4)")
     ap.add_argument("--formats", default="",
-                    help="sweep: only these formats (bf16, int8, int4; comma-separated)")
+                    help="sweep: these formats (bf16, int8, int4 and the tagged bf16t, int8t, int4t; "
+                         "comma-separated; default the untagged three)")
     ap.add_argument("--calls", type=int, default=50,
                     help="sweep: calls per pair of events in the steady measurement (>= 50)")
+    ap.add_argument("--split-table", action="store_true",
+                    help="even vs wave-aware token split on row counts around wave multiples")
+    ap.add_argument("--selector", action="store_true",
+                    help="the protocol selector's estimates and picks against measured steps")
     ap.add_argument("--report-sweep", default="",
                     help="print the markdown table of a file of sweep JSON lines and exit")
     return ap.parse_args()
@@ -216,11 +221,12 @@ def source_hash():
     """Hash of the kernel and launch code (comments excluded): ncu counters
     are reported only for the code they were taken on.  api.cu is left out:
     it holds the C entry points' argument checks and the host-only queries,
-    and defines no kernel and no launch shape."""
+    and defines no kernel and no launch shape; so is rates.inc, the measured
+    table the host-only protocol selector reads."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "quantized_reduce_rmsnorm_gb300", "csrc")
     for f in sorted(os.listdir(d)):
-        if f == "api.cu":
+        if f in ("api.cu", "rates.inc"):
             continue
         h.update(f.encode())
         with open(os.path.join(d, f), encoding="utf-8") as fh:
@@ -605,16 +611,17 @@ def sweep_selection(args):
     """The sweep points to run: every point, the quick subset, or those
     matching --sizes / --only (MSG:H:P:FMT, FMT one of bf16, int8, int4)."""
     from quantized_reduce_rmsnorm_gb300 import synth
-    pts = synth.sweep_points()
+    pts = synth.sweep_points(synth.SWEEP_FORMATS + synth.SWEEP_TAGGED_FORMATS)
     if args.sweep == "quick":
         pts = [p for p in pts if p[0] in (16 << 10, 1 << 20, 16 << 20, 64 << 20, 256 << 20)]
     if args.sizes:
         keep = {parse_size(t) for t in args.sizes.split(",")}
         pts = [p for p in pts if p[0] in keep]
-    names = {"bf16": synth.FMT_BF16, "int8": synth.FMT_INT8_SYM, "int4": synth.FMT_INT4_ASYM}
-    if args.formats:
-        keep = {names[f] for f in args.formats.split(",")}
-        pts = [p for p in pts if p[4] in keep]
+    names = {"bf16": synth.FMT_BF16, "int8": synth.FMT_INT8_SYM, "int4": synth.FMT_INT4_ASYM,
+             "bf16t": synth.FMT_BF16_TAGGED, "int8t": synth.FMT_INT8_TAGGED,
+             "int4t": synth.FMT_INT4_TAGGED}
+    keep = {names[f] for f in (args.formats or "bf16,int8,int4").split(",")}
+    pts = [p for p in pts if p[4] in keep]
     if args.only:
         want = set()
         for item in args.only.split(","):
@@ -624,8 +631,109 @@ def sweep_selection(args):
     return pts
 
 
+def measure_point(msg, H, T, P, fmt, G, calls=50, reps=7, flush=None, gen=None, held=True):
+    """Steady (and held) device time of the fused call and the sender call of
+    one sweep shape on seeded N(0,1) inputs generated on the device: see
+    run_sweep.  Returns a dict of the sweep's JSON fields."""
+    import torch
+    from quantized_reduce_rmsnorm_gb300 import fcomm, synth
+    from quantized_reduce_rmsnorm_gb300.pipeline import qs_bytes
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peak, kind = peaks()
+    if gen is None:
+        gen = torch.Generator(device=dev)
+    gen.manual_seed(msg ^ (H << 8) ^ (P << 4) ^ fmt)
+    w = synth.sweep_workload(H, T, P, fmt, G)
+    spec = fcomm.QSpec(fmt, G)
+    xs = [torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16) for _ in range(P)]
+    res = torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16)
+    gam = (1 + 0.1 * torch.randn(H, generator=gen, device=dev)).to(torch.bfloat16)
+    E = T * H
+    quant = fmt in (synth.FMT_INT8_SYM, synth.FMT_INT4_ASYM)
+    qtag = fmt in synth.QTAGGED
+    btag = fmt == synth.FMT_BF16_TAGGED
+    if quant or qtag:
+        qs = qs_bytes(w, E)
+        wire = fcomm.codes_bytes(spec, T, H) if qtag else qs  # one slab's payload
+        sender_bytes = P * 2 * E + P * wire
+        fused_bytes = P * wire + 2 * E + 2 * H + qs + 4 * E
+        fused_in = P * wire + 2 * E
+    elif btag:
+        wire = fcomm.tagged_bytes(T, H)
+        sender_bytes = P * 2 * E + P * wire
+        fused_bytes = P * wire + 2 * E + 2 * H + 4 * E
+        fused_in = P * wire + 2 * E
+    else:
+        sender_bytes = 0
+        fused_bytes = P * 2 * E + 2 * E + 2 * H + 4 * E
+        fused_in = P * 2 * E + 2 * E
+    epoch = 1  # every call packs and expects the same epoch (timing only)
+
+    def make_set(xset):
+        """One set of buffers for a sender call and a fused call."""
+        r_out, y = torch.empty_like(res), torch.empty_like(res)
+        if quant:
+            codes = [fcomm.alloc_qtensor(spec, T, H, dev) for _ in range(P)]
+            payload = fcomm.alloc_qtensor(spec, T, H, dev)
+            send = fcomm.bind_group_quantize_multi(xset, spec, codes)
+            send()
+            fuse = fcomm.bind_allreduce_residual_rmsnorm(codes, spec, T, H, res.clone(), r_out,
+                                                         gam, 1e-5, y, requant_out=payload)
+            return send, fuse
+        if qtag or btag:
+            nb = fcomm.codes_bytes(spec, T, H) if qtag else fcomm.tagged_bytes(T, H)
+            blocks = [torch.empty(nb, dtype=torch.uint8, device=dev) for _ in range(P)]
+            st = torch.zeros(2, dtype=torch.int32, device=dev)
+            send = (fcomm.bind_group_quantize_tagged(xset, spec, epoch, blocks) if qtag
+                    else fcomm.bind_pack_tagged_multi(xset, epoch, blocks))
+            send()
+            payload = fcomm.alloc_qtensor(fcomm.QSpec(synth.base_format(fmt), G), T, H, dev) \
+                if qtag else None
+            fuse = fcomm.bind_allreduce_residual_rmsnorm(blocks, spec, T, H, res.clone(), r_out,
+                                                         gam, 1e-5, y, requant_out=payload,
+                                                         expected_epoch=epoch, d_status=st)
+            return send, fuse
+        return None, fcomm.bind_allreduce_residual_rmsnorm(xset, spec, T, H, res.clone(), r_out,
+                                                           gam, 1e-5, y)
+
+    fits = fused_in + 4 * E < 2 * L2_BYTES
+    k = 1 if fused_in >= 2 * L2_BYTES else -(-2 * L2_BYTES // fused_in) + 1
+    cold = k <= 64
+    k = min(k, 64)
+    sets = [make_set(xs)] + [make_set([x.clone() for x in xs]) for _ in range(k - 1)]
+    send, fuse = sets[0]
+    calls = max(calls, k)
+    fm, fp10, fp90 = stream_timed([f for _, f in sets], calls, reps)
+    gb = lambda nbytes, us: nbytes / us / 1e3
+    line = {"sweep": True, "message_bytes": msg, "hidden": H, "tokens": T, "P": P,
+            "format": synth.FMT_NAMES[fmt],
+            "fused_us": round(fm, 3), "fused_us_p10": round(fp10, 3), "fused_us_p90": round(fp90, 3),
+            "fused_GBps": round(gb(fused_bytes, fm), 1),
+            "fused_frac": round(gb(fused_bytes, fm) / peak, 4),
+            "fused_frac_nominal": round(gb(fused_bytes, fm) / NOMINAL_HBM_GBS, 4),
+            "sets": k, "calls_per_rep": calls, "reps": reps, "inputs_cold": cold,
+            "peak_kind": kind}
+    if held:
+        hu, fh, _ = device_timed(fuse, reps, scrub=flush if fits else None)
+        line.update(fused_held_us=round(hu, 2), fused_held_frac=round(gb(fused_bytes, hu) / peak, 4),
+                    fused_host_us=round(fh, 2),
+                    held_scrub="read-only" if fits else "none (inputs larger than L2)")
+    if sender_bytes:
+        sm, sp10, sp90 = stream_timed([s for s, _ in sets], calls, reps)
+        line.update(sender_us=round(sm, 3), sender_us_p10=round(sp10, 3),
+                    sender_us_p90=round(sp90, 3),
+                    sender_GBps=round(gb(sender_bytes, sm), 1),
+                    sender_frac=round(gb(sender_bytes, sm) / peak, 4),
+                    sender_frac_nominal=round(gb(sender_bytes, sm) / NOMINAL_HBM_GBS, 4))
+        if held:
+            line.update(sender_held_us=round(device_timed(send, reps, scrub=flush if fits else None)[0], 2))
+    del xs, res, gam, send, fuse, sets
+    torch.cuda.empty_cache()
+    return line
+
+
 def run_sweep(args):
-    """Message-size sweep of the fused kernel (and the sender quantizer).
+    """Message-size sweep of the fused kernel (and the sender).
 
     Inputs are seeded N(0,1) bf16 generated on the device (a measurement,
     not a parity case); the calls are bound once (fcomm.Bound).  Each point
@@ -644,85 +752,102 @@ def run_sweep(args):
 
     The host's cost of issuing one call is reported beside them."""
     import torch
-    from quantized_reduce_rmsnorm_gb300 import fcomm, synth
-    from quantized_reduce_rmsnorm_gb300.pipeline import qs_bytes
+    from quantized_reduce_rmsnorm_gb300 import fcomm
     fcomm.load()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    peak, kind = peaks()
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     gen = torch.Generator(device=dev)
     for msg, H, T, P, fmt, G in sweep_selection(args):
         if T == 0:
             continue
-        gen.manual_seed(msg ^ (H << 8) ^ (P << 4) ^ fmt)
-        w = synth.sweep_workload(H, T, P, fmt, G)
-        spec = fcomm.QSpec(fmt, G)
-        xs = [torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16) for _ in range(P)]
-        res = torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16)
-        gam = (1 + 0.1 * torch.randn(H, generator=gen, device=dev)).to(torch.bfloat16)
-        E = T * H
-        quant = fmt in (synth.FMT_INT8_SYM, synth.FMT_INT4_ASYM)
-        if quant:
-            qs = qs_bytes(w, E)
-            sender_bytes = P * 2 * E + P * qs
-            fused_bytes = P * qs + 2 * E + 2 * H + qs + 4 * E
-            fused_in = P * qs + 2 * E
-        else:
-            sender_bytes = 0
-            fused_bytes = P * 2 * E + 2 * E + 2 * H + 4 * E
-            fused_in = P * 2 * E + 2 * E
-
-        def make_set(xset):
-            """One set of buffers for a sender call and a fused call."""
-            r_out, y = torch.empty_like(res), torch.empty_like(res)
-            if quant:
-                codes = [fcomm.alloc_qtensor(spec, T, H, dev) for _ in range(P)]
-                payload = fcomm.alloc_qtensor(spec, T, H, dev)
-                send = fcomm.bind_group_quantize_multi(xset, spec, codes)
-                send()
-                fuse = fcomm.bind_allreduce_residual_rmsnorm(codes, spec, T, H, res.clone(), r_out,
-                                                             gam, 1e-5, y, requant_out=payload)
-                return send, fuse
-            return None, fcomm.bind_allreduce_residual_rmsnorm(xset, spec, T, H, res.clone(), r_out,
-                                                               gam, 1e-5, y)
-
-        fits = fused_in + 4 * E < 2 * L2_BYTES
-        k = 1 if fused_in >= 2 * L2_BYTES else -(-2 * L2_BYTES // fused_in) + 1
-        cold = k <= 64
-        k = min(k, 64)
-        sets = [make_set(xs)] + [make_set([x.clone() for x in xs]) for _ in range(k - 1)]
-        send, fuse = sets[0]
-        calls = max(args.calls, k)
-        reps = 7
-        fm, fp10, fp90 = stream_timed([f for _, f in sets], calls, reps)
-        hu, fh, hspread = device_timed(fuse, reps, scrub=flush if fits else None)
-        gb = lambda nbytes, us: nbytes / us / 1e3
-        line = {"sweep": True, "message_bytes": msg, "hidden": H, "tokens": T, "P": P,
-                "format": synth.FMT_NAMES[fmt],
-                "fused_us": round(fm, 3), "fused_us_p10": round(fp10, 3),
-                "fused_us_p90": round(fp90, 3),
-                "fused_GBps": round(gb(fused_bytes, fm), 1),
-                "fused_frac": round(gb(fused_bytes, fm) / peak, 4),
-                "fused_frac_nominal": round(gb(fused_bytes, fm) / NOMINAL_HBM_GBS, 4),
-                "fused_held_us": round(hu, 2),
-                "fused_held_frac": round(gb(fused_bytes, hu) / peak, 4),
-                "fused_host_us": round(fh, 2),
-                "sets": k, "calls_per_rep": calls, "reps": reps, "inputs_cold": cold,
-                "held_scrub": "read-only" if fits else "none (inputs larger than L2)",
-                "peak_kind": kind}
-        if quant:
-            sm, sp10, sp90 = stream_timed([s for s, _ in sets], calls, reps)
-            shu, _, _ = device_timed(send, reps, scrub=flush if fits else None)
-            line.update(sender_us=round(sm, 3), sender_us_p10=round(sp10, 3),
-                        sender_us_p90=round(sp90, 3),
-                        sender_GBps=round(gb(sender_bytes, sm), 1),
-                        sender_frac=round(gb(sender_bytes, sm) / peak, 4),
-                        sender_frac_nominal=round(gb(sender_bytes, sm) / NOMINAL_HBM_GBS, 4),
-                        sender_held_us=round(shu, 2))
+        line = measure_point(msg, H, T, P, fmt, G, calls=args.calls, flush=flush, gen=gen)
         print(json.dumps(line), flush=True)
-        del xs, res, gam, send, fuse, sets
-        torch.cuda.empty_cache()
+
+
+SELECTOR_POINTS = [  # (rows, hidden, P): on and off the measured grid of sizes, P and hidden
+    (64, 8192, 4), (192, 8192, 4), (1024, 8192, 4), (3072, 8192, 4), (6144, 8192, 4),
+    (64, 8192, 8), (768, 8192, 8), (4096, 8192, 8), (256, 4096, 2), (2048, 4096, 2),
+    (512, 8192, 3), (2048, 8192, 6), (1024, 5120, 8), (8192, 5120, 4), (16384, 8192, 2),
+]
+
+
+def selector_check(points, calls=50, reps=5):
+    """For each (rows, hidden, P): every encoding's measured step (sender +
+    fused steady device time, as in the sweep) beside the protocol
+    selector's estimate for one GPU, the selector's pick and the measured
+    fastest.  Returns one dict per point."""
+    import torch
+    from quantized_reduce_rmsnorm_gb300 import fcomm, synth
+    fcomm.load()
+    gen = torch.Generator(device=torch.device("cuda", torch.cuda.current_device()))
+    encs = synth.SWEEP_FORMATS + synth.SWEEP_TAGGED_FORMATS
+    out = []
+    for rows, H, P in points:
+        meas, est = {}, {}
+        for fmt, G in encs:
+            r = measure_point(2 * rows * H, H, rows, P, fmt, G, calls=calls, reps=reps, gen=gen,
+                              held=False)
+            name = synth.FMT_NAMES[fmt]
+            meas[name] = r["fused_us"] + (r.get("sender_us") or 0.0)
+            est[name] = fcomm.protocol_estimate(rows, H, P, fcomm.QSpec(fmt, G))
+        pick, pick_est = fcomm.select_protocol(rows, H, P, 4)
+        pick_name = synth.FMT_NAMES[pick.fmt]
+        fastest = min(meas, key=meas.get)
+        out.append({"selector": True, "rows": rows, "hidden": H, "P": P,
+                    "message_bytes": 2 * rows * H,
+                    "measured_us": {k: round(v, 2) for k, v in meas.items()},
+                    "estimate_us": {k: round(v, 2) for k, v in est.items()},
+                    "est_error": {k: round(est[k] / meas[k] - 1, 3) for k in meas},
+                    "pick": pick_name, "fastest": fastest,
+                    "pick_over_fastest": round(meas[pick_name] / meas[fastest], 4)})
+    return out
+
+
+def run_split_table(args):
+    """bench.py --split-table: two token subsets on two streams at the even
+    boundary and at the wave-aware one (fc_token_split), on row counts around
+    multiples of the fused kernel's wave, for a tagged and two quantized
+    workloads; steady device time per step (each subset's fused call on its
+    own stream, the sender before them), 20 steps per pair of events."""
+    import torch
+    from quantized_reduce_rmsnorm_gb300 import fcomm, synth
+    from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
+    fcomm.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cases = [synth.Workload("split-bf16-tagged", P=8, T=0, H=5120, fmt=synth.FMT_BF16_TAGGED, group=0,
+                            splits=2),
+             synth.Workload("split-int8", P=8, T=0, H=8192, fmt=synth.FMT_INT8_SYM, group=128, splits=2),
+             synth.Workload("split-int4", P=4, T=0, H=8192, fmt=synth.FMT_INT4_ASYM, group=32, splits=2)]
+    for base in cases:
+        _, wave = fcomm.token_split(fcomm.QSpec(base.fmt, base.group), base.P, 4096, base.H)
+        for T in (2 * wave - wave // 4, 2 * wave + 16, 2 * wave + wave // 4, 2 * wave + wave // 2,
+                  3 * wave + wave // 3):
+            w = synth.Workload(**{**base.__dict__, "T": int(T)})
+            inp = synth.make_inputs(w, seed=5)
+            res = {}
+            for mode in ("even", "wave"):
+                pipe = Pipeline(w, inp, device=dev, split=mode)
+                m, p10, p90 = stream_timed([pipe.step], 20, 5)
+                res[mode] = (m, p10, p90, pipe.bounds)
+                del pipe
+            print(json.dumps({"split_table": True, "workload": w.name, "P": w.P, "tokens": w.T,
+                              "hidden": w.H, "wave_rows": wave,
+                              "even_us": round(res["even"][0], 2), "even_bounds": res["even"][3],
+                              "wave_us": round(res["wave"][0], 2), "wave_bounds": res["wave"][3],
+                              "wave_over_even": round(res["wave"][0] / res["even"][0], 4),
+                              "p10_p90_even": [round(v, 2) for v in res["even"][1:3]],
+                              "p10_p90_wave": [round(v, 2) for v in res["wave"][1:3]]}), flush=True)
+            torch.cuda.empty_cache()
+
+
+def run_selector(args):
+    """bench.py --selector: the protocol selector against measurements (one GPU)."""
+    import torch
+    torch.cuda.set_device(0)
+    for line in selector_check(SELECTOR_POINTS, calls=args.calls):
+        print(json.dumps(line), flush=True)
 
 
 def sweep_report(path):
@@ -741,7 +866,8 @@ def sweep_report(path):
               f"| {r['fused_frac']:.3f} | {r['fused_frac_nominal']:.3f} | {r['fused_held_us']:.2f} "
               f"| {r['sets']} | {'yes' if r['inputs_cold'] else 'no'} | {snd} | {sf} |")
     print()
-    for fmt in ("bf16", "int8_sym_g128", "int4_asym_g32"):
+    for fmt in ("bf16", "int8_sym_g128", "int4_asym_g32", "bf16_tagged", "int8_sym_g128_tagged",
+                "int4_asym_g32_tagged"):
         for lo, label in ((16 << 20, "16 MB and more"), (64 << 20, "64 MB and more")):
             sel = [r for r in rows if r["format"] == fmt and r["message_bytes"] >= lo]
             if not sel:
@@ -865,6 +991,12 @@ def main():
     args = parse()
     if args.report_sweep:
         sweep_report(args.report_sweep)
+        return
+    if args.selector:
+        run_selector(args)
+        return
+    if args.split_table:
+        run_split_table(args)
         return
     if args.gather:
         run_gather(args)

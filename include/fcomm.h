@@ -287,19 +287,20 @@ fc_status fc_token_split(int P, int64_t rows, int64_t hidden, fc_qspec spec, int
  * readiness encoding to the message size and the number of GPUs, balancing
  * synchronization overhead against additional data-transfer cost).  One-GPU
  * analogue: for P ranks reducing rows x hidden bf16 partial sums, estimate
- * for every format whose bit width is >= min_bits (16: bf16 only; 8: + INT8;
- * 4: + INT4) and its tagged variant
- *   t = t_fixed + fused_bytes(format) / rate(format)          (this GPU)
- *     + [t_fixed + sender_bytes(format) / sender_rate(format)] (quantize/pack)
- *     + 2 (P-1)/P * payload(format) / link_gbps               (wire, optional)
- *     + (untagged ? 2 * barrier_us : 0)                        (readiness)
- * where rate(format) is the fused kernel's measured algorithmic rate on
- * GB300 (message-size sweep, 64-256 MB points) and t_fixed its measured
- * per-call floor; tagged formats pay 16/12 of the payload and need no
- * barrier.  link == NULL models one GPU (no wire, no barrier): then plain
- * bf16 wins, since quantizing only pays off when the wire is the bottleneck.
- * *choice receives the fastest format (group 128 for INT8, 32 for
- * INT4), *est_us its estimate.  Host-only; no GPU needed. */
+ * one all-reduce step for every encoding whose bit width is >= min_bits (16:
+ * bf16 only; 8: + INT8 g128; 4: + INT4 g32), plain and tagged:
+ *   t = fused(format) + sender(format)                      (this GPU)
+ *     + 2 (P-1)/P * payload(format) / link_gbps              (wire, optional)
+ *     + (untagged ? 2 * barrier_us : 0)                      (readiness)
+ * where fused and sender are the steady-state device times of one call
+ * measured on GB300 by the message-size sweep (every encoding, P in {2, 4,
+ * 8}, hidden 4096 and 8192, messages 16 KB .. 256 MB, compiled into the
+ * library), interpolated log-linearly in the message size (proportional to
+ * it above 256 MB), linearly in P, at the nearest measured hidden size;
+ * tagged encodings carry 16/12 of the payload and need no barrier.  link ==
+ * NULL models one GPU (no wire, no barrier).  *choice receives the fastest
+ * encoding (group 128 for INT8, 32 for INT4), *est_us its estimate.
+ * Host-only; no GPU needed; hidden must be a multiple of 128. */
 typedef struct {
   double link_gbps;  /* per-GPU interconnect bandwidth, GB/s (> 0) */
   double barrier_us; /* cost of one all-rank readiness barrier, us (>= 0) */
@@ -307,6 +308,13 @@ typedef struct {
 
 fc_status fc_select_protocol(int64_t rows, int64_t hidden, int P, int min_bits,
                              const fc_link_model* link, fc_qspec* choice, double* est_us);
+
+/* The estimate fc_select_protocol makes for one encoding `spec` (BF16,
+ * BF16_TAGGED, INT8_SYM or INT8_TAGGED with group 128, INT4_ASYM or
+ * INT4_TAGGED with group 32; other specs return FC_ERR_UNSUPPORTED), in
+ * *est_us.  Host-only. */
+fc_status fc_protocol_estimate(int64_t rows, int64_t hidden, int P, fc_qspec spec,
+                               const fc_link_model* link, double* est_us);
 
 /* --------------------------------------------------------------- misc --- */
 const char* fc_status_string(fc_status s);

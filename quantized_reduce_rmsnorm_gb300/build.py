@@ -37,7 +37,8 @@ def sources():
 
 def _inputs():
     return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(
-        os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
+        os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.inc")) + glob.glob(
+        os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

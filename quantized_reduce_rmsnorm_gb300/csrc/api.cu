@@ -2,6 +2,7 @@
 // Every entry point validates all arguments before it launches anything,
 // never allocates, frees or synchronizes, and launches on the caller's
 // stream.
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -92,6 +93,66 @@ fc_status check_qtensor(const fc_qtensor& t, int fmt, const char* name) {
     return fail(FC_ERR_INVALID, "%s.codes (bf16 data) must be 32-byte aligned", name);
   }
   return FC_OK;
+}
+
+}  // namespace
+
+namespace {
+
+#include "rates.inc"
+
+// One call's device time from a measured table (rates.inc): encoding f
+// (table order), P slabs, rows x hidden bf16 partial sums.  The table's
+// hidden (4096 or 8192) nearest to `hidden`; message bytes interpolated
+// log-linearly between the measured sizes 16 KB .. 256 MB (the 16 KB time
+// below them, proportional to bytes above); P linearly between 2, 4 and 8.
+// 0 where the table holds 0 (bf16 has no sender).
+double table_us(const double (&t)[6][3][2][15], int f, int P, int64_t rows, int64_t hidden) {
+  const int h = hidden > 6144 ? 1 : 0;
+  const double M = 2.0 * static_cast<double>(rows) * static_cast<double>(hidden);
+  auto at = [&](int pi) {
+    const double* v = t[f][pi][h];
+    const double m0 = 16384.0;
+    if (v[0] <= 0.0) return 0.0;
+    if (M <= m0) return v[0];
+    const double x = std::log2(M / m0);
+    if (x >= 14.0) return v[14] * M / (m0 * 16384.0);
+    const int i = static_cast<int>(x);
+    const double fr = x - i;
+    return std::exp2((1.0 - fr) * std::log2(v[i]) + fr * std::log2(v[i + 1]));
+  };
+  if (P <= 2) return at(0);
+  if (P <= 4) return at(0) + (at(1) - at(0)) * (P - 2) / 2.0;
+  return at(1) + (at(2) - at(1)) * (P - 4) / 4.0;
+}
+
+// The encodings, in the order of the measured table.
+struct Cand {
+  int fmt, group, bits;
+  bool tagged;
+};
+const Cand kCands[6] = {
+    {FC_FMT_BF16, 0, 16, false},       {FC_FMT_BF16_TAGGED, 0, 16, true},
+    {FC_FMT_INT8_SYM, 128, 8, false},  {FC_FMT_INT8_TAGGED, 128, 8, true},
+    {FC_FMT_INT4_ASYM, 32, 4, false},  {FC_FMT_INT4_TAGGED, 32, 4, true},
+};
+
+// Estimated us of one all-reduce step in encoding f: this GPU's measured
+// fused call and sender call (interpolated), plus, with a link model, the
+// wire time of the two-step reduce (2 (P-1)/P of a slab's payload per rank)
+// and two readiness barriers for the untagged encodings.  Payload per slab:
+// bf16 2E; INT8 g128 E + 4E/128; INT4 g32 E/2 + 8E/32; the tagged encodings
+// carry 12 payload bytes in every 16.
+double estimate_us(int f, int64_t rows, int64_t hidden, int P, const fc_link_model* link) {
+  double t = table_us(kFusedUs, f, P, rows, hidden) + table_us(kSenderUs, f, P, rows, hidden);
+  if (link) {
+    const double E = static_cast<double>(rows) * static_cast<double>(hidden);
+    const double base = f < 2 ? 2 * E : f < 4 ? E + 4 * E / 128 : E / 2 + 8 * E / 32;
+    const double payload = kCands[f].tagged ? base * 16 / 12 : base;
+    t += 2.0 * (P - 1) / P * payload / (link->link_gbps * 1e3);
+    if (!kCands[f].tagged) t += 2.0 * link->barrier_us;
+  }
+  return t;
 }
 
 }  // namespace
@@ -456,6 +517,29 @@ fc_status fc_token_split(int P, int64_t rows, int64_t hidden, fc_qspec spec, int
   return ok();
 }
 
+fc_status fc_protocol_estimate(int64_t rows, int64_t hidden, int P, fc_qspec spec,
+                               const fc_link_model* link, double* est_us) {
+  if (rows <= 0 || hidden <= 0 || hidden % 128 != 0)
+    return fail(FC_ERR_INVALID, "need rows > 0 and hidden a positive multiple of 128");
+  if (P < 2 || P > 8) return fail(FC_ERR_INVALID, "P must be in [2, 8] (got %d)", P);
+  if (!est_us) return fail(FC_ERR_INVALID, "est_us must not be NULL");
+  if (link && (!(link->link_gbps > 0.0) || !(link->barrier_us >= 0.0)))
+    return fail(FC_ERR_INVALID, "link_gbps must be > 0 and barrier_us >= 0");
+  int f = -1;
+  switch (spec.fmt) {
+    case FC_FMT_BF16: f = 0; break;
+    case FC_FMT_BF16_TAGGED: f = 1; break;
+    case FC_FMT_INT8_SYM: f = spec.group == 128 ? 2 : -1; break;
+    case FC_FMT_INT8_TAGGED: f = spec.group == 128 ? 3 : -1; break;
+    case FC_FMT_INT4_ASYM: f = spec.group == 32 ? 4 : -1; break;
+    case FC_FMT_INT4_TAGGED: f = spec.group == 32 ? 5 : -1; break;
+    default: break;
+  }
+  if (f < 0) return fail(FC_ERR_UNSUPPORTED, "no measured rates for format %d group %d", spec.fmt, spec.group);
+  *est_us = estimate_us(f, rows, hidden, P, link);
+  return ok();
+}
+
 fc_status fc_select_protocol(int64_t rows, int64_t hidden, int P, int min_bits,
                              const fc_link_model* link, fc_qspec* choice, double* est_us) {
   if (rows <= 0 || hidden <= 0 || hidden % 128 != 0)
@@ -466,49 +550,15 @@ fc_status fc_select_protocol(int64_t rows, int64_t hidden, int P, int min_bits,
   if (!choice) return fail(FC_ERR_INVALID, "choice must not be NULL");
   if (link && (!(link->link_gbps > 0.0) || !(link->barrier_us >= 0.0)))
     return fail(FC_ERR_INVALID, "link_gbps must be > 0 and barrier_us >= 0");
-  const double E = static_cast<double>(rows) * static_cast<double>(hidden);
-  struct Cand {
-    int fmt, group, bits;
-    double payload;  // bytes one rank sends for its whole slab
-    double rate;     // fused kernel, algorithmic GB/s on GB300 (measured)
-    double srate;    // sender (quantize / pack) kernel, GB/s (measured); 0: none
-    bool tagged;
-  };
-  // payload per slab: bf16 2E; INT8 g128 E + 4E/128; INT4 g32 E/2 + 8E/32;
-  // the tagged encodings carry 12 payload bytes in every 16.
-  // Rates (GB/s of algorithmic bytes, GB300): bf16 and INT8 from the median
-  // of the message-size sweep at 64-256 MB; INT4, INT4 tagged and bf16 tagged
-  // from the 8192 x 8192 (P=4) and 4096 x 5120 (P=8) steps; INT8 tagged is
-  // not measured at these sizes and takes INT8's rates scaled by the INT4
-  // tagged / untagged ratios.
-  const Cand cands[] = {
-      {FC_FMT_BF16, 0, 16, 2 * E, 6360.0, 0.0, false},
-      {FC_FMT_BF16_TAGGED, 0, 16, 2 * E * 16 / 12, 4960.0, 5780.0, true},
-      {FC_FMT_INT8_SYM, 128, 8, E + 4 * E / 128, 5680.0, 5410.0, false},
-      {FC_FMT_INT8_TAGGED, 128, 8, (E + 4 * E / 128) * 16 / 12, 5440.0, 6070.0, true},
-      {FC_FMT_INT4_ASYM, 32, 4, E / 2 + 8 * E / 32, 5140.0, 5110.0, false},
-      {FC_FMT_INT4_TAGGED, 32, 4, (E / 2 + 8 * E / 32) * 16 / 12, 4920.0, 5770.0, true},
-  };
-  const double t_fixed = 9.0;  // us: measured per-call floor of the fused kernel
   double best = 1e300;
-  const Cand* pick = nullptr;
-  for (const Cand& c : cands) {
-    if (c.bits < min_bits) continue;
-    // requant payload (quantized only) + residual in, residual_out + y out
-    const double requant = c.bits < 16 ? (c.fmt == FC_FMT_INT8_SYM || c.fmt == FC_FMT_INT8_TAGGED
-                                              ? E + 4 * E / 128 : E / 2 + 8 * E / 32)
-                                        : 0.0;
-    const double fused_bytes = P * c.payload + 2 * E + requant + 4 * E;
-    double t = t_fixed + fused_bytes / (c.rate * 1e3);
-    if (c.srate > 0.0) t += t_fixed + P * (2 * E + c.payload) / (c.srate * 1e3);  // sender
-    if (link) {
-      t += 2.0 * (P - 1) / P * c.payload / (link->link_gbps * 1e3);
-      if (!c.tagged) t += 2.0 * link->barrier_us;
-    }
-    if (t < best) best = t, pick = &c;
+  int pick = -1;
+  for (int i = 0; i < 6; ++i) {
+    if (kCands[i].bits < min_bits) continue;
+    const double t = estimate_us(i, rows, hidden, P, link);
+    if (t < best) best = t, pick = i;
   }
-  choice->fmt = pick->fmt;
-  choice->group = pick->group;
+  choice->fmt = kCands[pick].fmt;
+  choice->group = kCands[pick].group;
   if (est_us) *est_us = best;
   return ok();
 }

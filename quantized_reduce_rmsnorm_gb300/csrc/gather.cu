@@ -114,16 +114,11 @@ __global__ void __launch_bounds__(kGatherThreads) k_allgather(GatherJob j) {
 
 template <int FMT>
 cudaError_t launch_fmt(bool out_f32, const GatherJob& j, cudaStream_t st) {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms < 1) sms = 1;
-  }
-  // persistent: 8 CTAs of 8 warps per SM at most, fewer when the tensor is small
+  // persistent: 8 CTAs of 8 warps per SM of the current device at most, fewer
+  // when the tensor is small
+  const int64_t sms = num_sms();
   int64_t grid = (j.chunks + kGatherThreads - 1) / kGatherThreads;
-  if (grid > 8LL * sms) grid = 8LL * sms;
+  if (grid > 8 * sms) grid = 8 * sms;
   if (grid < 1) grid = 1;
   const dim3 gr(static_cast<unsigned>(grid));
   if (out_f32) return launch_pdl(k_allgather<FMT, true>, gr, dim3(kGatherThreads), 0, st, j);

@@ -8,6 +8,7 @@
 // warp touches one contiguous span.  Grids are persistent: a multiple of the
 // SM count, each warp striding over warp tiles, with two tiles in flight per
 // iteration.
+#include <atomic>
 #include <mutex>
 
 #include "device.cuh"
@@ -459,17 +460,20 @@ cudaError_t launch_quantize_t(const QuantJob& job, cudaStream_t st) {
 
 }  // namespace
 
+// SM count of the current device, queried once per device (thread-safe: a
+// racing first query stores the same value).
 int num_sms() {
-  static int sms[64] = {0};
+  static std::atomic<int> sms[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (sms[dev] == 0) {
-    int v = 0;
+  int v = sms[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    sms[dev] = v > 0 ? v : 1;
+    if (v < 1) v = 1;
+    sms[dev].store(v, std::memory_order_relaxed);
   }
-  return sms[dev];
+  return v;
 }
 
 namespace {

@@ -28,6 +28,7 @@ EXPORTS = (
     "fc_pack_tagged_multi", "fc_group_quantize_tagged",
     "fc_allreduce_residual_rmsnorm", "fc_allreduce_residual_rmsnorm_ex", "fc_status_string",
     "fc_last_error", "fc_version", "fc_token_split", "fc_select_protocol", "fc_allgather_dequant",
+    "fc_protocol_estimate",
 )
 
 
@@ -112,6 +113,7 @@ def load(path: Optional[str] = None):
         "fc_token_split": (i32, [i32, i64, i64, QS, ctypes.POINTER(i64), ctypes.POINTER(i64)]),
         "fc_select_protocol": (i32, [i64, i64, i32, i32, P, ctypes.POINTER(QSpec),
                                      ctypes.POINTER(ctypes.c_double)]),
+        "fc_protocol_estimate": (i32, [i64, i64, i32, QS, P, ctypes.POINTER(ctypes.c_double)]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -388,3 +390,14 @@ def select_protocol(rows: int, hidden: int, P: int, min_bits: int,
 
 def version() -> str:
     return load().fc_version().decode()
+
+
+def protocol_estimate(rows: int, hidden: int, P: int, spec: QSpec,
+                      link_gbps: Optional[float] = None, barrier_us: float = 0.0) -> float:
+    """The selector's estimated us of one step in encoding `spec`."""
+    link = LinkModel(link_gbps, barrier_us) if link_gbps is not None else None
+    est = ctypes.c_double()
+    _check(load().fc_protocol_estimate(rows, hidden, P, spec,
+                                       ctypes.byref(link) if link is not None else None,
+                                       ctypes.byref(est)))
+    return est.value

@@ -9,8 +9,11 @@ standing in as P slabs in one GPU's HBM:
 * BF16: the fused reduce + residual add + RMSNorm on the bf16 slabs;
 * BF16_TAGGED: the producers pack every slab into epoch-tagged blocks with a
   fresh epoch (one launch for all slabs), then the consumer validates and reduces
-  them; with ``splits`` > 1 the token rows are split into that many subsets
-  that run on their own streams (TokenWeave's token splitting).
+  them.
+
+With ``splits`` > 1 (BF16_TAGGED, INT8, INT4) the token rows are split into
+that many subsets whose fused calls run on their own streams (TokenWeave's
+token splitting), at even or wave-aware boundaries.
 
 All device memory is allocated here by torch at construction; ``step()``
 only launches libfcomm kernels.  ``alg_bytes()`` gives the bytes the method
@@ -71,7 +74,8 @@ class Pipeline:
             self.blocks = [torch.empty(fc.tagged_bytes(T, H), dtype=torch.uint8, device=device)
                            for _ in range(w.P)]
             self.status = torch.zeros(max(1, w.splits), 2, dtype=torch.int32, device=device)
-            self.streams = [torch.cuda.Stream(device=device) for _ in range(max(1, w.splits))]
+        if max(1, w.splits) > 1:
+            self.streams = [torch.cuda.Stream(device=device) for _ in range(w.splits)]
         # token-subset boundaries: even, or wave-aware (the first subset is
         # whole waves of the fused kernel on this GPU)
         n = max(1, w.splits)
@@ -92,9 +96,20 @@ class Pipeline:
         self._send, self._fuse, self._split = None, None, []
         if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
             self._send = fc.bind_group_quantize_multi(self.x, self.spec, self.codes)
-            self._fuse = fc.bind_allreduce_residual_rmsnorm(
-                self.codes, self.spec, w.T, w.H, self.residual, self.residual_out, self.gamma,
-                w.eps, self.y, requant_out=self.payload)
+            if max(1, w.splits) == 1:
+                self._fuse = fc.bind_allreduce_residual_rmsnorm(
+                    self.codes, self.spec, w.T, w.H, self.residual, self.residual_out, self.gamma,
+                    w.eps, self.y, requant_out=self.payload)
+            else:  # token subsets: each a fused call over its rows' codes, scales, zeros
+                for i in range(w.splits):
+                    r0, r1 = self.bounds[i], self.bounds[i + 1]
+                    rows = lambda q: None if q is None else q[self._qoff(q, r0):self._qoff(q, r1)]
+                    sub = lambda qt: tuple(rows(q) for q in qt)
+                    self._split.append(fc.bind_allreduce_residual_rmsnorm(
+                        [sub(c) for c in self.codes], self.spec, r1 - r0, w.H,
+                        self.residual[r0:r1], self.residual_out[r0:r1], self.gamma, w.eps,
+                        self.y[r0:r1],
+                        requant_out=None if self.payload is None else sub(self.payload)))
         elif w.fmt in QTAGGED:
             self._send = fc.bind_group_quantize_tagged(self.x, self.spec, self.epoch, self.blocks)
             self._fuse = fc.bind_allreduce_residual_rmsnorm(
@@ -115,10 +130,16 @@ class Pipeline:
                     self.residual[r0:r1], self.residual_out[r0:r1], self.gamma, w.eps,
                     self.y[r0:r1], expected_epoch=self.epoch, d_status=self.status[i]))
 
+    def _qoff(self, q, r: int) -> int:
+        """Index of row r's first entry in a flat codes, scales or zeros tensor."""
+        return r * (q.numel() // self.w.T)
+
     # ------------------------------------------------------------------
     def _launches(self) -> int:
         w = self.w
-        if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM) or w.fmt in QTAGGED:
+        if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
+            return 1 + max(1, w.splits)
+        if w.fmt in QTAGGED:
             return 2
         if w.fmt == FMT_BF16:
             return 1
@@ -192,7 +213,8 @@ class Pipeline:
         joins = []
         for call, s in zip(self._split, self.streams):
             s.wait_event(fork)
-            call.epoch = self.epoch
+            if self.w.fmt == FMT_BF16_TAGGED:
+                call.epoch = self.epoch
             call(s)
             ev = torch.cuda.Event()
             ev.record(s)
@@ -208,8 +230,8 @@ class Pipeline:
         if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
             qs = qs_bytes(w, E)
             return {"sender": P * 2 * E + P * qs,
-                    "fused": P * qs + 2 * E + 2 * H + (qs if self.payload is not None else 0)
-                    + 4 * E}
+                    "fused": P * qs + 2 * E + max(1, w.splits) * 2 * H
+                    + (qs if self.payload is not None else 0) + 4 * E}
         if w.fmt in QTAGGED:
             tb = fc.codes_bytes(self.spec, w.T, w.H)
             qs = qs_bytes(w, E)

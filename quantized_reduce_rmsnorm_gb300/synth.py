@@ -92,7 +92,13 @@ WORKLOADS = {
 }
 
 
-def sweep_points():
+SWEEP_FORMATS = ((FMT_BF16, 0), (FMT_INT8_SYM, 128), (FMT_INT4_ASYM, 32))
+# the self-synchronizing encodings of the same payloads (rates for the
+# protocol selector; the sweep's figure of merit is the untagged three)
+SWEEP_TAGGED_FORMATS = ((FMT_BF16_TAGGED, 0), (FMT_INT8_TAGGED, 128), (FMT_INT4_TAGGED, 32))
+
+
+def sweep_points(formats=SWEEP_FORMATS):
     """(message bytes, H, T, P, fmt, group) of the message-size sweep."""
     pts = []
     for i in range(15):
@@ -100,7 +106,7 @@ def sweep_points():
         for H in (4096, 8192):
             T = msg // (2 * H)
             for P in (2, 4, 8):
-                for fmt, G in ((FMT_BF16, 0), (FMT_INT8_SYM, 128), (FMT_INT4_ASYM, 32)):
+                for fmt, G in formats:
                     pts.append((msg, H, T, P, fmt, G))
     return pts
 

@@ -266,3 +266,45 @@ def test_bound_sender_passes_its_status_word(monkeypatch):
     (k1, a1), (k2, a2) = seen
     assert k1 == "multi" and a1[6].value == st.data_ptr() and a1[7] == 5
     assert k2 == "tagged" and a2[7].value == st.data_ptr() and a2[8] == 6 and a2[5].value == 3
+
+
+def _rates_table():
+    """kFusedUs and kSenderUs parsed from the committed rates.inc."""
+    import numpy as np
+    path = os.path.join(os.path.dirname(fc.fcomm.__file__), "csrc", "rates.inc")
+    text = open(path).read()
+    tabs = {}
+    for name in ("kFusedUs", "kSenderUs"):
+        body = text.split(name + "[6][3][2][15] = {", 1)[1].split("};", 1)[0]
+        vals = [float(v) for v in re.findall(r"[-+]?\d+\.\d+", body)]
+        tabs[name] = np.array(vals).reshape(6, 3, 2, 15)
+    return tabs
+
+
+def test_protocol_estimate_reads_the_measured_table():
+    """At measured points the estimate is the table's fused + sender time;
+    between sizes it lies between its neighbours; above 256 MB it grows in
+    proportion to the bytes; P between 4 and 8 interpolates linearly."""
+    t = _rates_table()
+    specs = [fc.BF16, fc.BF16_TAGGED, fc.INT8_G128, fc.INT8_G128_TAGGED, fc.INT4_G32,
+             fc.INT4_G32_TAGGED]
+    for f, spec in enumerate(specs):
+        for pi, P in enumerate((2, 4, 8)):
+            for hi, H in enumerate((4096, 8192)):
+                for m in (0, 6, 14):
+                    rows = ((16 << 10) << m) // (2 * H)
+                    if rows == 0:
+                        continue
+                    want = t["kFusedUs"][f, pi, hi, m] + t["kSenderUs"][f, pi, hi, m]
+                    assert abs(fc.protocol_estimate(rows, H, P, spec) - want) < 1e-6 * want + 1e-9
+        # between 1 MB and 2 MB (H = 8192: 64 and 128 rows)
+        lo = fc.protocol_estimate(64, 8192, 4, spec)
+        hi_ = fc.protocol_estimate(128, 8192, 4, spec)
+        mid = fc.protocol_estimate(96, 8192, 4, spec)
+        assert min(lo, hi_) - 1e-9 <= mid <= max(lo, hi_) + 1e-9
+        big = fc.protocol_estimate(16384, 8192, 8, spec)
+        assert abs(fc.protocol_estimate(32768, 8192, 8, spec) - 2 * big) < 1e-6 * big
+        e4, e8 = fc.protocol_estimate(1024, 8192, 4, spec), fc.protocol_estimate(1024, 8192, 8, spec)
+        assert abs(fc.protocol_estimate(1024, 8192, 6, spec) - (e4 + e8) / 2) < 1e-6 * e8
+    with pytest.raises(fc.FcommError):
+        fc.protocol_estimate(64, 8192, 4, fc.QSpec(fc.FMT_INT8_SYM, 64))

@@ -516,6 +516,24 @@ def test_wave_aware_token_split(orc):
     assert_bits_equal(outs[1]["h"], want["h"], "residual_out")
 
 
+@pytest.mark.parametrize("fmt,G,P,H", [(I8, 128, 8, 8192), (I4, 32, 4, 8192), (I4, 32, 3, 4096)])
+@pytest.mark.parametrize("mode", ["even", "wave"])
+def test_quantized_token_split_every_element(orc, fmt, G, P, H, mode):
+    """Two token subsets of a quantized workload, each a fused call on its own
+    stream over its rows' codes, scales and zero-points: every element
+    against the oracle, at the even and the wave-aware boundary (a row count
+    past one wave, so the two differ)."""
+    from quantized_reduce_rmsnorm_gb300.pipeline import Pipeline
+    _, wave = fc.token_split(spec_of(fmt, G), P, 4096, H)
+    w = synth.Workload("qsplit", P=P, T=wave + wave // 3 + 7, H=H, fmt=fmt, group=G, splits=2)
+    inp = synth.make_inputs(w, seed=41)
+    pipe = Pipeline(w, inp, split=mode)
+    assert 0 < pipe.bounds[1] < w.T
+    pipe.step()
+    pipe.step()
+    check_every_element(orc, w, pipe, inp)
+
+
 # ---------------------------------------- self-synchronizing quantized payloads --
 QT_CASES = [("decode-qtagged", {"T": 12}), ("prefill-qtagged", {"T": 10}),
             ("i8t-p3", {"P": 3, "T": 5, "H": 1152, "fmt": I8T, "group": 128}),
@@ -983,3 +1001,15 @@ def test_sender_status_word_reset_to_ok(orc, fmt, G, tagged):
         else:
             assert_bits_equal(host(outs[p][0]), q, f"codes slab {p}")
             assert_bits_equal(host(outs[p][1]), s_, f"scales slab {p}")
+
+
+def test_protocol_selector_pick_within_5pct_of_measured_fastest():
+    """One GPU (no link model): the selector's pick, from the measured rates
+    compiled into the library, is within 5% of the encoding measured fastest
+    here (sender + fused steady device time), at shapes on and off the
+    measured grid; the estimate errors are reported."""
+    import bench
+    for r in bench.selector_check([(192, 8192, 4), (768, 8192, 8), (512, 8192, 3)], calls=50, reps=3):
+        print(r["rows"], r["hidden"], r["P"], "pick", r["pick"], "fastest", r["fastest"],
+              "errors", r["est_error"])
+        assert r["pick_over_fastest"] <= 1.05, r
