@@ -886,8 +886,11 @@ def run_gather(args):
     """The standalone quantized all-gather (fc_allgather_dequant): P shard
     payloads of a prefill-sized and a decode-sized tensor (quantized on the
     device from seeded N(0,1) bf16), gathered and dequantized to bf16 and to
-    fp32; CUDA events, median of the repetitions, a read-only 258 MB L2 scrub
-    before each repetition when the point fits in L2."""
+    fp32.  Timed as the sweep times the fused call: `--calls` bound calls
+    back to back per pair of CUDA events, cycling through buffer sets whose
+    payloads and outputs together exceed twice L2 (at most 64 sets), median
+    and p10/p90 over 7 repetitions; plus one held call after a read-only L2
+    scrub."""
     import torch
     from quantized_reduce_rmsnorm_gb300 import fcomm, synth
     fcomm.load()
@@ -899,26 +902,35 @@ def run_gather(args):
     for name, T, H, P, spec in (("prefill", 8192, 8192, 4, fcomm.INT4_G32),
                                 ("prefill", 8192, 8192, 4, fcomm.INT8_G128),
                                 ("decode", 64, 8192, 8, fcomm.INT8_G128)):
-        gen.manual_seed(T ^ P)
-        x = torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16)
-        whole = fcomm.alloc_qtensor(spec, T, H, dev)
-        fcomm.group_quantize(x, spec, whole)
-        shards = fcomm.shard_views(whole, spec, T, H, P)
         E = T * H
         qs = fcomm.codes_bytes(spec, T, H) + fcomm.groups(spec, T, H) * (8 if spec.fmt == fcomm.FMT_INT4_ASYM else 4)
         for odt, osz in ((torch.bfloat16, 2), (torch.float32, 4)):
-            out = torch.empty(T, H, dtype=odt, device=dev)
-            small = qs + osz * E < 2 * L2_BYTES
-            us = device_timed(lambda: fcomm.allgather_dequant(shards, spec, T, H, out),
-                              max(args.steps, 5), warm=3, scrub=flush if small else None)[0]
             alg = qs + osz * E
+            n_sets = max(1, min(64, -(-2 * L2_BYTES // alg) + 1))
+            calls, keep = [], []
+            for k in range(n_sets):
+                gen.manual_seed((T ^ P) + 7919 * k)
+                x = torch.randn(T, H, generator=gen, device=dev).to(torch.bfloat16)
+                whole = fcomm.alloc_qtensor(spec, T, H, dev)
+                fcomm.group_quantize(x, spec, whole)
+                del x
+                out = torch.empty(T, H, dtype=odt, device=dev)
+                calls.append(fcomm.bind_allgather_dequant(fcomm.shard_views(whole, spec, T, H, P),
+                                                          spec, T, H, out))
+                keep.append(whole)
+            med, p10, p90 = stream_timed(calls, max(args.calls, 50), 7)
+            held = device_timed(calls[0], 7, warm=2, scrub=flush)[0]
             print(json.dumps({"gather": True, "workload": name, "rows": T, "hidden": H, "P": P,
                               "format": synth.FMT_NAMES[spec.fmt], "out": str(odt).split(".")[-1],
-                              "us": round(us, 2), "alg_bytes": alg, "GB/s": round(alg / us / 1e3, 1),
-                              "frac": round(alg / us / 1e3 / peak, 4), "peak_kind": kind,
-                              "l2_scrubbed": small}), flush=True)
-        del x, whole, shards, out
-        torch.cuda.empty_cache()
+                              "us": round(med, 2), "us_p10": round(p10, 2), "us_p90": round(p90, 2),
+                              "held_us": round(held, 2), "sets": n_sets,
+                              "inputs_cold": n_sets * alg > 2 * L2_BYTES,
+                              "alg_bytes": alg, "GB/s": round(alg / med / 1e3, 1),
+                              "frac": round(alg / med / 1e3 / peak, 4),
+                              "frac_nominal": round(alg / med / 1e3 / NOMINAL_HBM_GBS, 4),
+                              "peak_kind": kind}), flush=True)
+            del calls, keep
+            torch.cuda.empty_cache()
 
 
 def run_overlap(args):

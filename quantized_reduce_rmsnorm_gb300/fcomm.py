@@ -276,6 +276,19 @@ def allgather_dequant(shards, spec: QSpec, rows: int, hidden: int, out: torch.Te
                                        expected_epoch, _ptr(d_status), _stream(stream)))
 
 
+def bind_allgather_dequant(shards, spec: QSpec, rows: int, hidden: int, out: torch.Tensor,
+                           expected_epoch: int = 0, d_status: Optional[torch.Tensor] = None) -> Bound:
+    """allgather_dequant with its arguments marshalled once (fcomm.Bound)."""
+    qs = (QTensor * len(shards))(*[_qt(s if isinstance(s, (tuple, list)) else (s,))
+                                   for s in shards])
+    od = FMT_F32 if out.dtype == torch.float32 else FMT_BF16
+    return Bound(load().fc_allgather_dequant,
+                 [qs, len(shards), rows, hidden, spec, od, ctypes.c_void_p(_ptr(out)),
+                  ctypes.c_uint32(expected_epoch & 0xFFFFFFFF), ctypes.c_void_p(_ptr(d_status)),
+                  None], 9,
+                 epoch_index=7, keep=(shards, out, d_status, qs))
+
+
 def shard_views(q, spec: QSpec, rows: int, hidden: int, P: int):
     """The P shard payloads (views, no copy) of a whole payload q = (codes,
     scales, zeros) or tagged blocks, in the partition fc_allgather_dequant reads."""

@@ -268,6 +268,36 @@ def test_bound_sender_passes_its_status_word(monkeypatch):
     assert k2 == "tagged" and a2[7].value == st.data_ptr() and a2[8] == 6 and a2[5].value == 3
 
 
+def test_bound_allgather_marshals_once(monkeypatch):
+    """The bound all-gather passes the shards, the output, the epoch, the
+    status word and the stream of each call (stand-in entry point, host
+    tensors), and holds the tensors it was bound to."""
+    import torch
+    monkeypatch.setattr(fc.fcomm, "_ptr", lambda t: None if t is None else t.data_ptr())
+    seen = []
+
+    class FakeLib:
+        def fc_allgather_dequant(self, *args):
+            seen.append(args)
+            return fc.FC_OK
+
+    whole = fc.alloc_qtensor(fc.INT8_G128, 4, 256, "cpu")
+    shards = fc.shard_views(whole, fc.INT8_G128, 4, 256, 3)
+    monkeypatch.setattr(fc.fcomm, "load", lambda path=None: FakeLib())
+    out = torch.zeros(4, 256, dtype=torch.float32)
+    st = torch.zeros(2, dtype=torch.int32)
+    call = fc.bind_allgather_dequant(shards, fc.INT8_G128, 4, 256, out, expected_epoch=9, d_status=st)
+    call(stream=4)
+    call.epoch = 10
+    call(stream=5)
+    (a1, a2) = seen
+    assert a1[1] == 3 and a1[2] == 4 and a1[3] == 256 and a1[5] == fc.FMT_F32
+    assert a1[6].value == out.data_ptr() and a1[8].value == st.data_ptr()
+    assert a1[7].value == 9 and a1[9] == 4 and a2[7].value == 10 and a2[9] == 5
+    assert a1[0][0].codes == shards[0][0].data_ptr() and a1[0][2].scales == shards[2][1].data_ptr()
+    assert any(t is out for t in call._keep)
+
+
 def _rates_table():
     """kFusedUs and kSenderUs parsed from the committed rates.inc."""
     import numpy as np
