@@ -146,17 +146,32 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // --------------------------------------------- programmatic dependent launch --
 // Every kernel here is launched with programmatic stream serialization
 // (launch_pdl): it may be scheduled while the previous kernel in its stream
-// is still finishing.  pdl_begin() is each kernel's first statement: it
-// waits until that previous kernel has completed and its writes are visible
-// (griddepcontrol.wait; a no-op for a launch without the attribute), so no
-// global memory is touched before, and then lets the next kernel in the
-// stream be scheduled as resources free up (griddepcontrol.launch_dependents).
+// is still finishing.  pdl_begin() waits until that previous kernel has
+// completed and its writes are visible (griddepcontrol.wait; a no-op for a
+// launch without the attribute).  No global memory is read or written
+// before it; the only thing a kernel may issue earlier is prefetch_l2 of its
+// first tiles (below), which returns no data.  pdl_begin() then lets the next
+// kernel in the stream be scheduled as resources free up
+// (griddepcontrol.launch_dependents).
 // A dependent grid is scheduled only once every CTA of this grid has issued
 // that instruction (or finished), i.e. has started, so its CTAs never hold a
 // slot that a CTA of this grid still needs in order to start.
 __device__ __forceinline__ void pdl_begin() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Asks the TMA engine to bring [p, p + bytes) into L2 (cp.async.bulk.prefetch;
+// p and bytes multiples of 16).  Nothing comes back to the SM.  The staged
+// kernels issue it for their first tiles before pdl_begin(), so those tiles'
+// DRAM latency overlaps the tail of the previous kernel in the stream (whose
+// last CTAs are still running when this kernel's first CTAs become resident).
+// It cannot make a later load see stale data: the loads that use the data
+// are issued after pdl_begin(), when the previous kernel's writes are visible,
+// and L2, which serves them, is this GPU's point of coherence for global
+// memory -- a line prefetched before a write is updated by that write.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // ----------------------------------------------------------------- bf16 --

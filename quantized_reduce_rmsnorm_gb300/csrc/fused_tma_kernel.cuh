@@ -72,6 +72,21 @@ __device__ __forceinline__ void issue_row(const FusedArgs& a, const TmaGeom& g, 
             32 * g.cps, bar);
 }
 
+// L2 prefetch of the bytes issue_row copies (issued before pdl_begin()).
+template <int FMT>
+__device__ __forceinline__ void prefetch_row(const FusedArgs& a, const TmaGeom& g, int64_t row, int rank) {
+  const int P = a.P;
+  const int64_t co = row * g.row_cb + static_cast<int64_t>(rank) * g.cb;
+  const int64_t so = row * g.row_sb + static_cast<int64_t>(rank) * g.sb;
+  for (int p = 0; p < P; ++p) {
+    prefetch_l2(static_cast<const uint8_t*>(a.s.codes[p]) + co, g.cb);
+    if (FMT == kINT8 || FMT == kINT4) prefetch_l2(reinterpret_cast<const uint8_t*>(a.s.scales[p]) + so, g.sb);
+    if (FMT == kINT4) prefetch_l2(reinterpret_cast<const uint8_t*>(a.s.zeros[p]) + so, g.zb);
+  }
+  prefetch_l2(static_cast<const uint8_t*>(a.res_in) + row * 2 * a.H + static_cast<int64_t>(rank) * 32 * g.cps,
+              32 * g.cps);
+}
+
 // Thread-block clusters: the CTA's rank, a barrier over the whole cluster
 // (release/acquire: shared-memory writes before it are visible to every CTA
 // after it), and stores into a peer CTA's shared memory.
@@ -110,7 +125,6 @@ __device__ __forceinline__ void st_peer_u32(uint32_t addr, uint32_t v) {
 template <int FMT, int NSTAGE, int PMAX, int CL = 1, bool COMPACT = false, int SUB = 1>
 __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 1)
     k_fused_tma(FusedArgs a, TmaGeom g) {
-  pdl_begin();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float red[2][32];
   static_assert(CL == 1 || SUB == 1, "sub-stages are for a CTA per row");
@@ -150,6 +164,13 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
   if (tid == 0) {
     for (int s = 0; s < NSTAGE * SUB; ++s) mbar_init(&bar[s], 1);
     mbar_init_fence();
+    for (int s = 0; s < NSTAGE; ++s)
+      if (row0 + s * rstride < a.rows)
+        for (int j = 0; j < SUB; ++j) prefetch_row<FMT>(a, g, row0 + s * rstride, SUB > 1 ? j : rank);
+  }
+  if (blockIdx.x == 0 && tid == 32) prefetch_l2(a.gamma, static_cast<uint32_t>(2 * H));  // every CTA reads it
+  pdl_begin();
+  if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s)
       if (row0 + s * rstride < a.rows)
         for (int j = 0; j < SUB; ++j) {

@@ -150,7 +150,6 @@ constexpr int kQWarps = kThreads / 32;
 template <int FMT, bool TAGGED = false, int LPG = 0, int TILE = 2048, int STAGES = default_stages<TILE>()>
 __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 4 : 3)
     k_quantize_tma(QuantJob job, int lpg_shift, int64_t tiles_per_slab) {
-  pdl_begin();
   constexpr int kWTile = TILE, kWStages = STAGES;
   constexpr int kRingBytes = WRing<TILE, STAGES>::kBytes;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -191,6 +190,16 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 4 : 3)
   if (lane == 0) {
     for (int s = 0; s < kWStages; ++s) mbar_init(&bar[s], 1);
     mbar_init_fence();
+    // the first tiles into L2 while the previous kernel finishes
+    Cursor pf = first;
+    for (int s = 0; s < kWStages - 1 && w0 + s * wstride < total; ++s, pf = advance(pf, wstride)) {
+      const int64_t e0 = pf.tt * kWTile, rem = job.n - e0;
+      prefetch_l2(static_cast<const uint16_t*>(job.x[pf.p]) + e0,
+                  static_cast<uint32_t>((rem < kWTile ? rem : kWTile) * 2));
+    }
+  }
+  pdl_begin();
+  if (lane == 0) {
     for (int s = 0; s < kWStages - 1; ++s) {
       if (w0 + s * wstride < total) issue(ahead, s);
       ahead = advance(ahead, wstride);

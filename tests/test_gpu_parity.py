@@ -342,6 +342,8 @@ TMA_CASES = [
     ("i8-short-rows", {"P": 2, "T": 29, "H": 2048, "fmt": I8, "group": 128}),
     # single-stage rings of the compact build (shared memory admits 3 CTAs per SM)
     ("i8-p4-wide", {"P": 4, "T": 9, "H": 8192, "fmt": I8, "group": 128}),
+    # eight INT4 slabs at H = 8192: the build without the h buffer (capped grids)
+    ("i4-p8-h8192", {"P": 8, "T": 9, "H": 8192, "fmt": I4, "group": 32}),
 ]
 
 
@@ -537,7 +539,9 @@ def test_quantized_token_split_every_element(orc, fmt, G, P, H, mode):
 # ---------------------------------------- self-synchronizing quantized payloads --
 QT_CASES = [("decode-qtagged", {"T": 12}), ("prefill-qtagged", {"T": 10}),
             ("i8t-p3", {"P": 3, "T": 5, "H": 1152, "fmt": I8T, "group": 128}),
-            ("i4t-p5", {"P": 5, "T": 7, "H": 4128, "fmt": I4T, "group": 32})]
+            ("i4t-p5", {"P": 5, "T": 7, "H": 4128, "fmt": I4T, "group": 32}),
+            # enough rows for a CTA per row: the build without the h buffer
+            ("i8t-p8-h8192-rows", {"P": 8, "T": 160, "H": 8192, "fmt": I8T, "group": 128})]
 
 
 @pytest.mark.parametrize("name,kw", QT_CASES, ids=[c[0] for c in QT_CASES])
