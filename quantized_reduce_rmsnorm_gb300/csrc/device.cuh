@@ -46,6 +46,18 @@ __device__ __forceinline__ V8 ld256_keep(const void* p) {
   return r;
 }
 
+// Streamed load on the coherent path (for a tensor the kernel may also
+// write, e.g. a residual that aliases residual_out), without L1 allocation.
+__device__ __forceinline__ V8 ld256_coherent(const void* p) {
+  V8 r;
+  asm volatile("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]),
+                 "=r"(r.w[6]), "=r"(r.w[7])
+               : "l"(p)
+               : "memory");
+  return r;
+}
+
 __device__ __forceinline__ uint4 ld128_stream(const void* p) {
   uint4 r;
   asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

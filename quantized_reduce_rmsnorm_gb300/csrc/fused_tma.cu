@@ -105,6 +105,34 @@ int sub_shape(const FusedArgs& a, const TmaShape& sh, TmaGeom& g2) {
   });
 }
 
+// The half-row sub-stages without the residual in them (k_fused_tma's RG),
+// for eight slabs of tagged INT8 at H = 8192, whose 104 KB row of tagged
+// blocks plus the residual and h leaves room for one CTA per SM (which then
+// takes a two-row ring); without the residual, two CTAs of half-row
+// sub-stages fit.  Returns that occupancy (0 when not applicable) and the
+// geometry in g3.
+template <int FMT, int PMAX>
+int rg_shape(const FusedArgs& a, const TmaShape& sh, TmaGeom& g3) {
+  if constexpr (PMAX != 8 || FMT != kINT8T) {
+    return 0;
+  } else {
+    if (sh.threads != 256 || (a.H >> 4) != 2 * sh.threads) return 0;  // (any ring depth)
+    if (!geometry(FMT, a, g3, 2)) return 0;
+    g3.stage_bytes -= 32 * g3.cps;  // no residual in the stage
+    g3.stage_off = (2 * a.H + 127) & ~127;
+    const int smem = g3.stage_off + 2 * g3.stage_bytes;
+    if (smem > kTmaSmemLimit) return 0;
+    auto kern = k_fused_tma<FMT, 1, PMAX, 1, false, 2, true>;
+    return occupancy_memo(reinterpret_cast<const void*>(kern), sh.threads, smem, 1, [&] {
+      int o = 0;
+      if (raise_smem_limit(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, sh.threads, smem) != cudaSuccess)
+        return 0;
+      return o;
+    });
+  }
+}
+
 template <int FMT, int PMAX>
 cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cudaStream_t st) {
   const TmaShape sh = choose_shape<FMT, PMAX>(a, g);
@@ -119,6 +147,17 @@ cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cud
   int64_t grid = static_cast<int64_t>(num_sms()) * sh.occ;
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   if (grid > a.rows) grid = a.rows;
+  if constexpr (PMAX == 8 && FMT == kINT8T) {
+    TmaGeom g3;
+    const int occ3 = rg_shape<FMT, PMAX>(a, sh, g3);
+    if (occ3 > sh.occ) {
+      int64_t grid3 = static_cast<int64_t>(num_sms()) * occ3;
+      if (max_ctas > 0 && grid3 > max_ctas) grid3 = max_ctas;
+      if (grid3 > a.rows) grid3 = a.rows;
+      return launch_pdl(k_fused_tma<FMT, 1, PMAX, 1, false, 2, true>, dim3(static_cast<unsigned>(grid3)),
+                        dim3(sh.threads), g3.stage_off + 2 * g3.stage_bytes, st, a, g3);
+    }
+  }
   {
     TmaGeom g2;
     const int occ2 = sh.compact ? sub_shape<FMT, PMAX, true>(a, sh, g2) : sub_shape<FMT, PMAX, false>(a, sh, g2);
@@ -167,7 +206,13 @@ int64_t wave_fmt(const FusedArgs& a, const TmaGeom& g) {
   const TmaShape sh = a.P <= 2 ? choose_shape<FMT, 2>(a, g)
                       : a.P <= 4 ? choose_shape<FMT, 4>(a, g)
                                  : choose_shape<FMT, 8>(a, g);
-  return static_cast<int64_t>(num_sms()) * (sh.occ > 0 ? sh.occ : 1);  // a CTA per row
+  int occ = sh.occ;
+  if (a.P > 4) {
+    TmaGeom g3;
+    const int occ3 = rg_shape<FMT, 8>(a, sh, g3);
+    occ = occ3 > occ ? occ3 : occ;
+  }
+  return static_cast<int64_t>(num_sms()) * (occ > 0 ? occ : 1);  // a CTA per row
 }
 
 int64_t fused_tma_wave_rows(int fmt, const FusedArgs& a) {

@@ -51,7 +51,7 @@ cudaError_t launch_fused_tma_compact(int fmt, int nstage, const FusedArgs& a, co
 
 namespace {
 
-template <int FMT>
+template <int FMT, bool RG = false>
 __device__ __forceinline__ void issue_row(const FusedArgs& a, const TmaGeom& g, uint8_t* st,
                                           uint64_t* bar, int64_t row, int rank) {
   mbar_expect_tx(bar, static_cast<uint32_t>(g.stage_bytes));
@@ -67,9 +67,10 @@ __device__ __forceinline__ void issue_row(const FusedArgs& a, const TmaGeom& g, 
       bulk_load(st + P * (g.cb + g.sb) + p * g.zb, reinterpret_cast<const uint8_t*>(a.s.zeros[p]) + so,
                 g.zb, bar);
   }
-  bulk_load(st + P * (g.cb + g.sb + g.zb),
-            static_cast<const uint8_t*>(a.res_in) + row * 2 * a.H + static_cast<int64_t>(rank) * 32 * g.cps,
-            32 * g.cps, bar);
+  if (!RG)
+    bulk_load(st + P * (g.cb + g.sb + g.zb),
+              static_cast<const uint8_t*>(a.res_in) + row * 2 * a.H + static_cast<int64_t>(rank) * 32 * g.cps,
+              32 * g.cps, bar);
 }
 
 // L2 prefetch of the bytes issue_row copies (issued before pdl_begin()).
@@ -122,7 +123,11 @@ __device__ __forceinline__ void st_peer_u32(uint32_t addr, uint32_t v) {
 // one segment per pass-1 iteration (blockDim.x == g.cps): a sub-stage is
 // refilled with the next row as soon as every thread is past it, instead of
 // after the whole row, so the next row's bytes have longer to land.
-template <int FMT, int NSTAGE, int PMAX, int CL = 1, bool COMPACT = false, int SUB = 1>
+// RG: the residual is not staged; each thread loads its chunk of it straight
+// from global memory before the chunk's slab loop, whose work hides the
+// load.  Its stage is 2 * H bytes smaller, which is what lets a second CTA
+// per SM fit for eight tagged INT8 slabs at H = 8192.
+template <int FMT, int NSTAGE, int PMAX, int CL = 1, bool COMPACT = false, int SUB = 1, bool RG = false>
 __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 1)
     k_fused_tma(FusedArgs a, TmaGeom g) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
     for (int s = 0; s < NSTAGE; ++s)
       if (row0 + s * rstride < a.rows)
         for (int j = 0; j < SUB; ++j) {
-          issue_row<FMT>(a, g, stage0 + (s * SUB + j) * g.stage_bytes, &bar[s * SUB + j], row0 + s * rstride,
+          issue_row<FMT, RG>(a, g, stage0 + (s * SUB + j) * g.stage_bytes, &bar[s * SUB + j], row0 + s * rstride,
                          SUB > 1 ? j : rank);
           note_issue(s * SUB + j, s);
         }
@@ -221,6 +226,8 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
       const float* scales = reinterpret_cast<const float*>(st + P * g.cb);
       const float* zeros = reinterpret_cast<const float*>(st + P * (g.cb + g.sb));
       const uint4* rrow = reinterpret_cast<const uint4*>(st + P * (g.cb + g.sb + g.zb));
+      V8 rv;  // RG: this chunk's residual, loaded while the slabs are summed
+      if (RG && act) rv = ld256_coherent(static_cast<const uint16_t*>(a.res_in) + (row * cpr + c0 + c) * 16);
       float acc[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
@@ -308,8 +315,15 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
       if (act) {
         // h = bf16(fl(o + R)) straight from the packed residual; sum of h^2
         // straight from the packed h
-        const uint4 r0 = rrow[2 * cs], r1 = rrow[2 * cs + 1];
-        const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        uint32_t rw[8];
+        if (RG) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) rw[k] = rv.w[k];
+        } else {
+          const uint4 r0 = rrow[2 * cs], r1 = rrow[2 * cs + 1];
+          rw[0] = r0.x, rw[1] = r0.y, rw[2] = r0.z, rw[3] = r0.w;
+          rw[4] = r1.x, rw[5] = r1.y, rw[6] = r1.z, rw[7] = r1.w;
+        }
         V8 hv;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
@@ -331,7 +345,7 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
           const int64_t nrow = row + NSTAGE * rstride;
           if (nrow < a.rows) {
             fence_proxy_async_smem();
-            issue_row<FMT>(a, g, stage0 + (s * SUB + j) * g.stage_bytes, &bar[s * SUB + j], nrow, j);
+            issue_row<FMT, RG>(a, g, stage0 + (s * SUB + j) * g.stage_bytes, &bar[s * SUB + j], nrow, j);
             note_issue(s * SUB + j, i + NSTAGE);
           }
         }
@@ -379,7 +393,7 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
       const int64_t nrow = row + NSTAGE * rstride;
       if (nrow < a.rows) {
         fence_proxy_async_smem();
-        issue_row<FMT>(a, g, stage0 + (s * SUB + SUB - 1) * g.stage_bytes, &bar[s * SUB + SUB - 1], nrow,
+        issue_row<FMT, RG>(a, g, stage0 + (s * SUB + SUB - 1) * g.stage_bytes, &bar[s * SUB + SUB - 1], nrow,
                        SUB > 1 ? SUB - 1 : rank);
         note_issue(s * SUB + SUB - 1, i + NSTAGE);
       }

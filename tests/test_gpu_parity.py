@@ -566,13 +566,15 @@ def test_quantized_tagged_producer_and_consumer(orc, name, kw):
 @pytest.mark.parametrize("H", [1024, 8192])
 @pytest.mark.parametrize("T", [4, 8], ids=["cta-per-row", "cluster-per-row"])
 @pytest.mark.parametrize("fmt,G,nbg", [(I8T, 128, 11), (I4T, 32, 2)])
-def test_quantized_tagged_stale_blocks(orc, fmt, G, nbg, T, H):
+@pytest.mark.parametrize("P", [3, 8])
+def test_quantized_tagged_stale_blocks(orc, fmt, G, nbg, T, H, P):
     """Blocks built on the host by the oracle, one tag corrupted before upload
     (4 rows: a CTA per row, whose 8192-element rows are staged as two half-row
     sub-stages; 8 rows: each row shared by a cluster of CTAs, whose segments
-    offset the block index)."""
+    offset the block index; eight INT8 slabs at H = 8192 take the build whose
+    stage holds no residual)."""
     base = synth.base_format(fmt)
-    w = synth.Workload("qtstale", P=3, T=T, H=H, fmt=fmt, group=G)
+    w = synth.Workload("qtstale", P=P, T=T, H=H, fmt=fmt, group=G)
     inp = synth.make_inputs(w, seed=42)
     ep = 5
     blocks = []
