@@ -438,21 +438,17 @@ __device__ __forceinline__ float warp_sum(float v) {
 //  2. If both products round to the same integer c, no half-integer lies
 //     strictly between them, hence none between fl(v/s) and them, and
 //     rne(fl(v/s)) = c.
-//  3. Otherwise a half-integer m lies in [v r_lo, v r_hi], so v r is within
-//     2^-20 * 1.1 * 127.25 < 2^-13 of m and v/s within 2^-12 of it; c = the
-//     rounding of v r is m's neighbour on v r's side.  Then D = v - m*s is an
-//     integer multiple of 2^(e_s - 25) smaller than 2^(e_s - 11), so it fits
-//     in 24 bits and fma(-m, s, v) gives it exactly (for s >= 2^-100).
-//     fl(v/s) == m exactly when D lies in m's half-ulp band [-hd, +hu]
-//     (hu = 2^(E-24) s for m = +-2^E...; hd = hu/2 only for |m| = 1/2), ties
-//     at the band edges going to m (its significand is even).  So the code is
-//     the even neighbour of m inside the band, and the neighbour on D's side
-//     outside it.
+//  3. Otherwise (a half-integer lies between the two products: the element
+//     sits next to one; bf16 inputs put about 0.2% of the elements there)
+//     the element is flagged, and the exact pass gives it its code by the
+//     definition, the IEEE quotient rounded to the nearest even integer.
+//     (An exact resolution next to the half-integer m through D = v - m*s,
+//     which fma gives exactly, took more instructions per flagged element.)
 //  4. Groups where the bound v * r <= 127.25 (INT8) / 15.25 (INT4) fails or
-//     s < 2^-100 take the IEEE division for every element (never seen on
-//     finite activations; it keeps denormal scales exact).
+//     s < 2^-100 flag every element, i.e. take the IEEE division for all of
+//     them (never seen on finite activations; it keeps denormal scales
+//     exact).
 constexpr float kMagicI8 = 12582912.0f;         // 1.5 * 2^23, bits 0x4B400000
-constexpr float kTwoM24 = 5.9604644775390625e-08f;  // 2^-24
 constexpr float kTwoM100 = 7.888609052210118e-31f;  // 2^-100
 
 // fl(x / 15) and fl(x / 127) for the scales, without a division: with
@@ -481,28 +477,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
 
 __device__ __forceinline__ uint32_t low_bytes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
-}
-
-// Exact code for an element whose fast-path value sits next to a half-integer
-// (step 3 above).  c: the fast-path integer, e = v * r - c (up to rounding),
-// v the numerator.
-__device__ __forceinline__ float resolve_near_half(float v, float s, float c, float e) {
-  const uint32_t sm = 0x80000000u;
-  // the half-integer next to v * r, on e's side of c (exact)
-  const float m = __fadd_rn(c, __uint_as_float(0x3F000000u | (__float_as_uint(e) & sm)));
-  const float am = fabsf(m);
-  const float d = __fmaf_rn(-m, s, v);  // v - m*s, exact
-  const float hu = __fmul_rn(__fmul_rn(__uint_as_float(__float_as_uint(am) & 0x7F800000u), kTwoM24), s);
-  const float hd = am == 0.5f ? __fmul_rn(hu, 0.5f) : hu;
-  // > 0: |v/s| lies beyond |m| (d with the sign of m folded in)
-  const float dp = __uint_as_float(__float_as_uint(d) ^ (__float_as_uint(m) & sm));
-  const float half_m = __uint_as_float(0x3F000000u | (__float_as_uint(m) & sm));
-  const float away = __fadd_rn(m, half_m);
-  const float toward = __fsub_rn(m, half_m);
-  // fl(v/s) == m inside the band: ties to the even integer
-  const bool away_even = (__float_as_uint(__fadd_rn(away, kMagicI8)) & 1u) == 0u;
-  const float tie = away_even ? away : toward;
-  return dp > hu ? away : (dp < -hd ? toward : tie);
 }
 
 // Lane-local group statistics on the 16 bf16 inputs packed in w[8] with
@@ -557,15 +531,14 @@ __device__ __forceinline__ void minmax16(const float v[16], float& lo, float& hi
 // code in its low byte or nibble; the code itself is M + code - M).  group_ok:
 // fl(vmax * r) is within the code range and s >= 2^-100 (else every element
 // takes the division); s == 0 is passed as r == 0 with group_ok set, which
-// yields codes 0.  Every lane of the warp must call this: the
-// near-half-integer pass is entered by warp vote and runs converged, one
-// vote per element index.
-// Near-half-integer and division elements are settled after the fast path:
+// yields codes 0.  Every lane of the warp must call this.
+// Flagged elements (next to a half-integer, or in a group outside the fast
+// path's bounds) are settled after the fast path:
 // round_codes returns a 16-bit mask of the lane's elements that need it (bit
 // 8b + w for element 4w + b, gathered by byte permutes), settle_codes ORs
 // the masks over the warp and one uniform loop
-// visits only the element indices set in some lane, each with a single
-// shared copy of the exact code (steps 3 and 4).  pick(i) supplies the
+// visits only the element indices set in some lane, each lane computing
+// that element's code by division (steps 3 and 4).  pick(i) supplies the
 // lane's v_i, put(i, u) stores its exact code (u = bits of M + code).
 template <bool SIGNED>
 __device__ __forceinline__ uint32_t round_codes(const float v[16], float r, bool group_ok,
@@ -599,25 +572,23 @@ __device__ __forceinline__ uint32_t round_codes(const float v[16], float r, bool
   return group_ok ? flag : 0x0F0F0F0Fu;
 }
 
+// The code by its definition: the IEEE quotient, rounded to the nearest
+// even integer, clamped to the code range.
 template <bool SIGNED>
-__device__ __forceinline__ float exact_code(float v, float s, float c, float e, bool group_ok) {
-  if (group_ok) return resolve_near_half(v, s, c, e);
-  const float q = rintf(__fdiv_rn(v, s));  // the definition, for groups outside the fast path's bounds
+__device__ __forceinline__ float code_by_division(float v, float s) {
+  const float q = rintf(__fdiv_rn(v, s));
   return SIGNED ? fminf(127.0f, fmaxf(-127.0f, q)) : fminf(15.0f, fmaxf(0.0f, q));
 }
 
 template <bool SIGNED, class Pick, class Put>
-__device__ __forceinline__ void settle_codes(uint32_t mask, float s, float r, bool group_ok,
-                                             Pick pick, Put put) {
+__device__ __forceinline__ void settle_codes(uint32_t mask, float s, Pick pick, Put put) {
   const float magic = SIGNED ? kMagicI8 : 8388608.0f;
   uint32_t todo = __reduce_or_sync(kFull, mask);
   while (todo) {  // warp-uniform
     const int pos = __ffs(todo) - 1;
     todo &= todo - 1;
     const int i = 4 * (pos & 7) + (pos >> 3);
-    const float vi = pick(i);
-    const float ci = __fsub_rn(__fmaf_rn(vi, r, magic), magic);  // the fast path's code, recomputed
-    const float res = exact_code<SIGNED>(vi, s, ci, __fmaf_rn(vi, r, -ci), group_ok);
+    const float res = code_by_division<SIGNED>(pick(i), s);
     if ((mask >> pos) & 1u) put(i, __float_as_uint(__fadd_rn(res, magic)));
   }
 }
@@ -631,18 +602,14 @@ __device__ __forceinline__ void settle_codes(uint32_t mask, float s, float r, bo
 // to its half-integer (measured on GB300 with the sender: prefill 133.4 ->
 // 127.9 us; without any exact pass it would take 114.1 us).
 template <bool SIGNED, class Pick, class Put>
-__device__ __forceinline__ void settle_codes_lanewise(uint32_t mask, float s, float r, bool group_ok,
-                                                      Pick pick, Put put) {
-  (void)r, (void)group_ok;
+__device__ __forceinline__ void settle_codes_lanewise(uint32_t mask, float s, Pick pick, Put put) {
   const float magic = SIGNED ? kMagicI8 : 8388608.0f;
   while (__any_sync(kFull, mask != 0u)) {
     if (mask) {
       const int pos = __ffs(mask) - 1;
       mask &= mask - 1;
       const int i = 4 * (pos & 7) + (pos >> 3);
-      const float q = rintf(__fdiv_rn(pick(i), s));
-      const float res = SIGNED ? fminf(127.0f, fmaxf(-127.0f, q)) : fminf(15.0f, fmaxf(0.0f, q));
-      put(i, __float_as_uint(__fadd_rn(res, magic)));
+      put(i, __float_as_uint(__fadd_rn(code_by_division<SIGNED>(pick(i), s), magic)));
     }
   }
 }
@@ -677,13 +644,13 @@ struct RegSettle {
 // flagged in any lane of the warp, every lane computes element i's exact
 // code, and lanes that flagged it keep it.  Registers are indexed at
 // compile time, so a visit costs the exact code alone.  Measured on GB300
-// it pays where flagged elements are dense -- the requantized sum of two
-// INT4 slabs, whose quotients sit on or next to half-integers often (fused
-// kernel, 64 MB messages: 68 -> 60 us) -- and costs time in the larger
-// kernels of more slabs, which keep the index loop (settle_codes).
+// (with the earlier exact resolution next to the half-integer) it pays
+// where flagged elements are dense -- the requantized sum of two INT4 slabs,
+// whose quotients sit on or next to half-integers often (fused kernel, 64 MB
+// messages: 68 -> 60 us) -- and costs time in the larger kernels of more
+// slabs, which keep the index loop (settle_codes).
 template <bool SIGNED>
-__device__ __forceinline__ void settle_codes_regs(uint32_t mask, float s, float r, bool group_ok,
-                                                  const float v[16], uint32_t ub[16]) {
+__device__ __forceinline__ void settle_codes_regs(uint32_t mask, float s, const float v[16], uint32_t ub[16]) {
   const uint32_t any = __reduce_or_sync(kFull, mask);
   if (!any) return;
   const float magic = SIGNED ? kMagicI8 : 8388608.0f;
@@ -691,8 +658,7 @@ __device__ __forceinline__ void settle_codes_regs(uint32_t mask, float s, float 
   for (int i = 0; i < 16; ++i) {
     const uint32_t bit = 1u << (8 * (i & 3) + (i >> 2));  // element 4w + b is mask bit 8b + w
     if (any & bit) {
-      const float ci = __fsub_rn(__fmaf_rn(v[i], r, magic), magic);  // the fast path's code, recomputed
-      const float res = exact_code<SIGNED>(v[i], s, ci, __fmaf_rn(v[i], r, -ci), group_ok);
+      const float res = code_by_division<SIGNED>(v[i], s);
       if (mask & bit) ub[i] = __float_as_uint(__fadd_rn(res, magic));
     }
   }
@@ -723,13 +689,13 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
   const bool ok = s == 0.0f || (__fmul_rn(a, r) <= 127.25f && s >= kTwoM100);
   const uint32_t mask = round_codes<true>(v, r, ok, ub);
   constexpr bool kReload = !std::is_same<Reload, NoReload>::value;
-  if (!kReload && UNROLLED) settle_codes_regs<true>(mask, s, r, ok, v, ub);
-  if (!kReload && !UNROLLED) settle_codes<true>(mask, s, r, ok, RegSettle{v, ub}, RegSettle{v, ub});
+  if (!kReload && UNROLLED) settle_codes_regs<true>(mask, s, v, ub);
+  if (!kReload && !UNROLLED) settle_codes<true>(mask, s, RegSettle{v, ub}, RegSettle{v, ub});
 #pragma unroll
   for (int j = 0; j < 4; ++j) q[j] = low_bytes4(ub[4 * j], ub[4 * j + 1], ub[4 * j + 2], ub[4 * j + 3]);
   if (kReload)
     settle_codes_lanewise<true>(
-        mask, s, r, ok, [&](int i) { return __uint_as_float(reload(i) << 16); },
+        mask, s, [&](int i) { return __uint_as_float(reload(i) << 16); },
         [&](int i, uint32_t rb) {
           const int sh = 8 * (i & 3);
 #pragma unroll
@@ -787,8 +753,8 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
   const bool ok = s == 0.0f || (__fmul_rn(span, r) <= 15.25f && s >= kTwoM100);
   const uint32_t mask = round_codes<false>(num, r, ok, ub);
   constexpr bool kReload = !std::is_same<Reload, NoReload>::value;
-  if (!kReload && UNROLLED) settle_codes_regs<false>(mask, s, r, ok, num, ub);
-  if (!kReload && !UNROLLED) settle_codes<false>(mask, s, r, ok, RegSettle{num, ub}, RegSettle{num, ub});
+  if (!kReload && UNROLLED) settle_codes_regs<false>(mask, s, num, ub);
+  if (!kReload && !UNROLLED) settle_codes<false>(mask, s, RegSettle{num, ub}, RegSettle{num, ub});
   // Nibble packing by multiply-adds: ub = 0x4B000000 + code with code in
   // [0, 15] wherever the fast path holds, so sum_i ub[8j+i] * 16^i is the
   // packed word plus 0x4B000000 * 0x11111111 = 0xFB000000 (mod 2^32).
@@ -803,7 +769,7 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
   }
   if (kReload)
     settle_codes_lanewise<false>(
-        mask, s, r, ok, [&](int i) { return add_bf_lo(reload(i), -lo); },
+        mask, s, [&](int i) { return add_bf_lo(reload(i), -lo); },
         [&](int i, uint32_t rb) {
           const int sh = 4 * (i & 7);
 #pragma unroll
@@ -847,17 +813,14 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
 // The exact pass over register arrays with a natural-order mask (bit i =
 // element i): position i is visited, unrolled, when any lane of the warp
 // flagged it.
-__device__ __forceinline__ void settle_unrolled(uint32_t mask, float s, float r, bool group_ok,
-                                                const float v[16], bool is_signed, uint32_t ub[16]) {
+__device__ __forceinline__ void settle_unrolled(uint32_t mask, float s, const float v[16], bool is_signed,
+                                                uint32_t ub[16]) {
   const uint32_t any = __reduce_or_sync(kFull, mask);
   const float magic = is_signed ? kMagicI8 : kTwo23;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     if (any & (1u << i)) {
-      const float ci = __fsub_rn(__fmaf_rn(v[i], r, magic), magic);  // the code from r itself
-      const float e = __fmaf_rn(v[i], r, -ci);
-      const float res = is_signed ? exact_code<true>(v[i], s, ci, e, group_ok)
-                                  : exact_code<false>(v[i], s, ci, e, group_ok);
+      const float res = is_signed ? code_by_division<true>(v[i], s) : code_by_division<false>(v[i], s);
       if (mask & (1u << i)) ub[i] = __float_as_uint(__fadd_rn(res, magic));
     }
   }
@@ -927,7 +890,7 @@ __device__ __forceinline__ float requant_i4(const float v[16], int lpg, uint32_t
       for (int i = 0; i < 16; ++i)
         mask |= (u1[i] != __float_as_uint(__fmaf_rn(num[i], __fmul_rn(r, kRcpDown), kTwo23)) ? 1u : 0u) << i;
     }
-    settle_unrolled(mask, s, r, ok, num, false, u1);
+    settle_unrolled(mask, s, num, false, u1);
     q[0] = pack_nibbles8(u1), q[1] = pack_nibbles8(u1 + 8);
   }
   if (s < 1.2676506e30f) {  // fl(q s) = fma(2^23 + q, s, -2^23 s), exact for s < 2^100
@@ -976,7 +939,7 @@ __device__ __forceinline__ float requant_i8(const float v[16], int lpg, uint32_t
       for (int i = 0; i < 16; ++i)
         mask |= (u1[i] != __float_as_uint(__fmaf_rn(v[i], rl, kMagicI8)) ? 1u : 0u) << i;
     }
-    settle_unrolled(mask, s, r, ok, v, true, u1);
+    settle_unrolled(mask, s, v, true, u1);
 #pragma unroll
     for (int j = 0; j < 4; ++j) q[j] = low_bytes4(u1[4 * j], u1[4 * j + 1], u1[4 * j + 2], u1[4 * j + 3]);
   }

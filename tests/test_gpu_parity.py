@@ -86,9 +86,11 @@ def test_group_quantize_single_matches_multi():
 
 @pytest.mark.parametrize("fmt,G", [(I8, 128), (I4, 32)])
 def test_quantize_degenerate_groups(orc, fmt, G):
-    """All-zero groups, constant groups, signed zeros, one huge outlier, ties."""
+    """All-zero groups, constant groups, signed zeros, one huge outlier, ties,
+    and groups whose scale is below 2^-100 or subnormal (every element of
+    those takes the division)."""
     H = 512
-    x = np.zeros((4, H), np.float32)
+    x = np.zeros((6, H), np.float32)
     x[1, :] = 2.5                                  # constant row
     x[2, :G] = -0.0
     x[2, G:2 * G:2] = -0.0
@@ -96,9 +98,12 @@ def test_quantize_degenerate_groups(orc, fmt, G):
     x[2, 2 * G:] = np.arange(H - 2 * G) * 0.5      # exact ties after scaling
     x[3, :] = np.linspace(-3, 3, H)
     x[3, 7] = 3.0e30                               # one huge outlier
+    x[4, :] = np.linspace(-1, 1, H) * 1e-33        # scales below 2^-100
+    x[5, :] = np.linspace(-1, 1, H) * 3e-39        # bf16 subnormals
+    x[5, ::3] = np.float32(2.0 ** -126) * 1.5
     bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     spec = spec_of(fmt, G)
-    out = fc.alloc_qtensor(spec, 4, H)
+    out = fc.alloc_qtensor(spec, 6, H)
     fc.group_quantize(dev_bf16(bits), spec, out)
     torch.cuda.synchronize()
     q, s, z = orc.quantize(fmt, bf16_float(bits).ravel(), G)
@@ -316,6 +321,21 @@ FUSED_CASES = [
     ("tagged-h16", {"P": 4, "T": 3, "H": 16, "fmt": TG, "group": 0}),
     ("i8-h16", {"P": 2, "T": 5, "H": 16, "fmt": I8, "group": 16}),
 ]
+
+
+@pytest.mark.parametrize("fmt,G", [(I4, 32), (I8, 128)])
+@pytest.mark.parametrize("P", [2, 4, 8])
+@pytest.mark.parametrize("kernel", [fc.KERNEL_STREAM, fc.KERNEL_AUTO], ids=["stream", "auto"])
+def test_fused_tiny_sums(orc, fmt, G, P, kernel):
+    """Slabs near 1e-33 (and their sums): every requantization scale is below
+    2^-100, so every element of the payload takes the division, in each
+    build's exact pass (two, four and eight slabs)."""
+    w = synth.Workload("tiny", P=P, T=6, H=8192, fmt=fmt, group=G, outlier_frac=1.0,
+                       outlier_scale=1.0e-33)
+    inp = synth.make_inputs(w, seed=29)
+    want = oracle_fused(orc, w, inp)
+    assert float(np.max(want["scales"])) < 2.0 ** -100
+    check_fused(orc, w, run_fused(w, inp, kernel=kernel), want)
 
 
 @pytest.mark.parametrize("kernel", [fc.KERNEL_STREAM, fc.KERNEL_AUTO], ids=["stream", "auto"])
