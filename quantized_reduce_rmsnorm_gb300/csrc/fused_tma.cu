@@ -106,14 +106,19 @@ int sub_shape(const FusedArgs& a, const TmaShape& sh, TmaGeom& g2) {
 }
 
 // The half-row sub-stages without the residual in them (k_fused_tma's RG),
-// for eight slabs of tagged INT8 at H = 8192, whose 104 KB row of tagged
-// blocks plus the residual and h leaves room for one CTA per SM (which then
-// takes a two-row ring); without the residual, two CTAs of half-row
-// sub-stages fit.  Returns that occupancy (0 when not applicable) and the
-// geometry in g3.
+// for eight slabs at H = 8192 where it raises the CTAs per SM:
+// * tagged INT8: its 104 KB row of tagged blocks plus the residual and h left
+//   room for one CTA per SM (which then took a two-row ring); without the
+//   residual two fit (64 MB 0.51 -> 0.67 of the measured HBM peak);
+// * INT4: 64 KB with the residual and h held two CTAs per SM; without the
+//   residual, the compact build (gamma read per row from L1, no spills) runs
+//   three (64 MB 0.65 -> 0.71, 256 MB 0.68 -> 0.74).
+// Returns that occupancy (0 when not applicable), the geometry in g3 and the
+// build in compact.
 template <int FMT, int PMAX>
-int rg_shape(const FusedArgs& a, const TmaShape& sh, TmaGeom& g3) {
-  if constexpr (PMAX != 8 || FMT != kINT8T) {
+int rg_shape(const FusedArgs& a, const TmaShape& sh, TmaGeom& g3, bool& compact) {
+  compact = false;
+  if constexpr (PMAX != 8 || (FMT != kINT8T && FMT != kINT4)) {
     return 0;
   } else {
     if (sh.threads != 256 || (a.H >> 4) != 2 * sh.threads) return 0;  // (any ring depth)
@@ -122,14 +127,19 @@ int rg_shape(const FusedArgs& a, const TmaShape& sh, TmaGeom& g3) {
     g3.stage_off = (2 * a.H + 127) & ~127;
     const int smem = g3.stage_off + 2 * g3.stage_bytes;
     if (smem > kTmaSmemLimit) return 0;
-    auto kern = k_fused_tma<FMT, 1, PMAX, 1, false, 2, true>;
-    return occupancy_memo(reinterpret_cast<const void*>(kern), sh.threads, smem, 1, [&] {
-      int o = 0;
-      if (raise_smem_limit(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, sh.threads, smem) != cudaSuccess)
-        return 0;
-      return o;
-    });
+    auto occ_of = [&](auto kern) {
+      return occupancy_memo(reinterpret_cast<const void*>(kern), sh.threads, smem, 1, [&] {
+        int o = 0;
+        if (raise_smem_limit(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, sh.threads, smem) != cudaSuccess)
+          return 0;
+        return o;
+      });
+    };
+    const int of = occ_of(k_fused_tma<FMT, 1, PMAX, 1, false, 2, true>);
+    const int oc = FMT == kINT4 ? occ_of(k_fused_tma<FMT, 1, PMAX, 1, true, 2, true>) : 0;
+    compact = oc > of;
+    return compact ? oc : of;
   }
 }
 
@@ -147,15 +157,18 @@ cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cud
   int64_t grid = static_cast<int64_t>(num_sms()) * sh.occ;
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   if (grid > a.rows) grid = a.rows;
-  if constexpr (PMAX == 8 && FMT == kINT8T) {
+  if constexpr (PMAX == 8 && (FMT == kINT8T || FMT == kINT4)) {
     TmaGeom g3;
-    const int occ3 = rg_shape<FMT, PMAX>(a, sh, g3);
+    bool compact = false;
+    const int occ3 = rg_shape<FMT, PMAX>(a, sh, g3, compact);
     if (occ3 > sh.occ) {
       int64_t grid3 = static_cast<int64_t>(num_sms()) * occ3;
       if (max_ctas > 0 && grid3 > max_ctas) grid3 = max_ctas;
       if (grid3 > a.rows) grid3 = a.rows;
-      return launch_pdl(k_fused_tma<FMT, 1, PMAX, 1, false, 2, true>, dim3(static_cast<unsigned>(grid3)),
-                        dim3(sh.threads), g3.stage_off + 2 * g3.stage_bytes, st, a, g3);
+      const dim3 gr3(static_cast<unsigned>(grid3));
+      const int smem3 = g3.stage_off + 2 * g3.stage_bytes;
+      if (compact) return launch_pdl(k_fused_tma<FMT, 1, PMAX, 1, true, 2, true>, gr3, dim3(sh.threads), smem3, st, a, g3);
+      return launch_pdl(k_fused_tma<FMT, 1, PMAX, 1, false, 2, true>, gr3, dim3(sh.threads), smem3, st, a, g3);
     }
   }
   {
@@ -209,7 +222,8 @@ int64_t wave_fmt(const FusedArgs& a, const TmaGeom& g) {
   int occ = sh.occ;
   if (a.P > 4) {
     TmaGeom g3;
-    const int occ3 = rg_shape<FMT, 8>(a, sh, g3);
+    bool compact = false;
+    const int occ3 = rg_shape<FMT, 8>(a, sh, g3, compact);
     occ = occ3 > occ ? occ3 : occ;
   }
   return static_cast<int64_t>(num_sms()) * (occ > 0 ? occ : 1);  // a CTA per row

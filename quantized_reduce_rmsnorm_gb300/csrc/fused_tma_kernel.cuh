@@ -188,9 +188,12 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
   if (CL > 1) cluster_barrier();  // every CTA of the cluster runs before any peer store
 
   // gamma of this thread's first chunks, read once: every row uses the same chunks
-  uint32_t greg[kGammaRegChunks][8];
+  // (the compact build without a staged residual reads gamma per row from
+  // L1 instead: registers are what bounds its CTAs per SM)
+  constexpr int GRC = RG && COMPACT ? 0 : kGammaRegChunks;
+  uint32_t greg[GRC > 0 ? GRC : 1][8];
 #pragma unroll
-  for (int j = 0; j < kGammaRegChunks; ++j) {
+  for (int j = 0; j < GRC; ++j) {
     const int c = tid + j * nthr;
     if (c < cps) {
       const V8 gv = ld256_keep(static_cast<const uint16_t*>(a.gamma) + (c0 + c) * 16);
@@ -415,9 +418,9 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
       st256(static_cast<uint16_t*>(a.y) + (row * cpr + c0 + c) * 16, yv);
     };
 #pragma unroll
-    for (int j = 0; j < kGammaRegChunks; ++j)
+    for (int j = 0; j < GRC; ++j)
       if (tid + j * nthr < cps) out_chunk(tid + j * nthr, greg[j]);
-    for (int c = tid + kGammaRegChunks * nthr; c < cps; c += nthr) {
+    for (int c = tid + GRC * nthr; c < cps; c += nthr) {
       const V8 gv = ld256_keep(static_cast<const uint16_t*>(a.gamma) + (c0 + c) * 16);
       out_chunk(c, gv.w);
     }
