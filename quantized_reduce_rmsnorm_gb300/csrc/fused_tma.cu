@@ -148,9 +148,16 @@ cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cud
   const TmaShape sh = choose_shape<FMT, PMAX>(a, g);
   if (sh.occ < 1) return cudaErrorInvalidConfiguration;
   // a batch too small to give every SM a CTA (decode): share each row among
-  // a cluster of CTAs instead (measured ~0.5 us faster on 64 x 8192 rows; a
-  // single row gains nothing), not under a CTA budget, which caps CTAs
-  if (max_ctas == 0 && a.rows >= 8 && 2 * a.rows <= static_cast<int64_t>(num_sms()) * sh.occ) {
+  // a cluster of CTAs instead, not under a CTA budget, which caps CTAs.
+  // Measured on GB300 (back-to-back calls, a CTA per row -> clusters): rows
+  // of 8192, 8..128 of them, 0.4-2.2 us faster (eight INT8 slabs, 64 rows:
+  // 7.8 -> 6.4 us); 192 rows 6.5 -> 10.6 us slower (more clusters than fit
+  // at once); plain rows of 4096 slower at every count (64 rows, eight INT8
+  // slabs: 5.2 -> 6.5 us), tagged ones faster (INT4, two slabs, 32 rows:
+  // 10.8 -> 9.4 us); a single row gains nothing.
+  constexpr bool kTagged = FMT == kINT8T || FMT == kINT4T;
+  if (max_ctas == 0 && a.rows >= 8 && a.rows <= 128 && (a.H >= 8192 || kTagged) &&
+      2 * a.rows <= static_cast<int64_t>(num_sms()) * sh.occ) {
     const cudaError_t e = launch_fused_tma_cluster(FMT, a, st);
     if (e != cudaErrorNotSupported) return e;
   }
@@ -161,7 +168,10 @@ cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cud
     TmaGeom g3;
     bool compact = false;
     const int occ3 = rg_shape<FMT, PMAX>(a, sh, g3, compact);
-    if (occ3 > sh.occ) {
+    // only for more rows than one wave of the staged build: a lone row per
+    // CTA ran slower there (a row of gamma from L2, not registers; 256 rows
+    // of eight INT4 slabs 9.8 -> 12.3 us)
+    if (occ3 > sh.occ && a.rows > static_cast<int64_t>(num_sms()) * sh.occ) {
       int64_t grid3 = static_cast<int64_t>(num_sms()) * occ3;
       if (max_ctas > 0 && grid3 > max_ctas) grid3 = max_ctas;
       if (grid3 > a.rows) grid3 = a.rows;
@@ -224,7 +234,7 @@ int64_t wave_fmt(const FusedArgs& a, const TmaGeom& g) {
     TmaGeom g3;
     bool compact = false;
     const int occ3 = rg_shape<FMT, 8>(a, sh, g3, compact);
-    occ = occ3 > occ ? occ3 : occ;
+    if (a.rows > static_cast<int64_t>(num_sms()) * occ) occ = occ3 > occ ? occ3 : occ;
   }
   return static_cast<int64_t>(num_sms()) * (occ > 0 ? occ : 1);  // a CTA per row
 }

@@ -590,9 +590,10 @@ def test_quantized_tagged_producer_and_consumer(orc, name, kw):
 def test_quantized_tagged_stale_blocks(orc, fmt, G, nbg, T, H, P):
     """Blocks built on the host by the oracle, one tag corrupted before upload
     (4 rows: a CTA per row, whose 8192-element rows are staged as two half-row
-    sub-stages; 8 rows: each row shared by a cluster of CTAs, whose segments
-    offset the block index; eight INT8 slabs at H = 8192 take the build whose
-    stage holds no residual)."""
+    sub-stages; 8 rows of 8192: each row shared by a cluster of CTAs, whose
+    segments offset the block index, while 8 rows of 1024 take a CTA per row;
+    eight INT8 slabs at H = 8192 take the build whose stage holds no
+    residual)."""
     base = synth.base_format(fmt)
     w = synth.Workload("qtstale", P=P, T=T, H=H, fmt=fmt, group=G)
     inp = synth.make_inputs(w, seed=42)
