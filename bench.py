@@ -18,6 +18,7 @@ Prints one JSON line on rank 0.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import ctypes
 import hashlib
 import json
@@ -43,6 +44,18 @@ L2_BYTES = 129 * 2 ** 20
 # issuing the call (which is reported on its own).
 HOLD_CYCLES = 200_000
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
+
+
+@contextlib.contextmanager
+def nvtx(name):
+    """An NVTX range around a timed region (visible in nsys/ncu timelines;
+    a host-side marker only, nothing is added to the device work)."""
+    import torch
+    torch.cuda.nvtx.range_push(name)
+    try:
+        yield
+    finally:
+        torch.cuda.nvtx.range_pop()
 
 
 def scrub_l2(buf):
@@ -423,28 +436,31 @@ def run_ours(args):
         torch.cuda._sleep(hold)  # the host queues ahead of the first timed step
         host_s = 0.0  # host time spent issuing the steps
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(st)
-        for i in range(n):
-            t0 = time.perf_counter()
-            runs[i % n_sets](st)
-            host_s += time.perf_counter() - t0
-        e1.record(st)
-        torch.cuda.synchronize(dev)
+        with nvtx(f"{w.name}: {n} timed steps"):
+            e0.record(st)
+            for i in range(n):
+                t0 = time.perf_counter()
+                runs[i % n_sets](st)
+                host_s += time.perf_counter() - t0
+            e1.record(st)
+            torch.cuda.synchronize(dev)
         step_ms = e0.elapsed_time(e1) / n
         t_wall = time.perf_counter() - t_wall
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
         torch.cuda._sleep(hold)
-        for i in range(n):
-            evs[i][0].record(st)
-            runs[i % n_sets](st)
-            evs[i][1].record(st)
-        torch.cuda.synchronize(dev)
+        with nvtx(f"{w.name}: per-step events"):
+            for i in range(n):
+                evs[i][0].record(st)
+                runs[i % n_sets](st)
+                evs[i][1].record(st)
+            torch.cuda.synchronize(dev)
         per_step = [a.elapsed_time(b) for a, b in evs]
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
         torch.cuda._sleep(hold)
-        for i in range(n):
-            pipes[i % n_sets].step_marked(st, ev[i])
-        torch.cuda.synchronize(dev)
+        with nvtx(f"{w.name}: stage pass"):
+            for i in range(n):
+                pipes[i % n_sets].step_marked(st, ev[i])
+            torch.cuda.synchronize(dev)
     barrier(ws)
     sender_ms = [e[0].elapsed_time(e[1]) for e in ev]
     fused_ms = [e[1].elapsed_time(e[2]) for e in ev]
@@ -567,11 +583,12 @@ def run_e2e(pipe, inputs, step_bytes, args, ws, dev):
     torch.cuda.synchronize(dev)
     barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_up)
-    for i in range(steps):
-        one(warm + i)
-    e1.record(s_dn)
-    torch.cuda.synchronize(dev)
+    with nvtx("e2e: timed steps with host copies"):
+        e0.record(s_up)
+        for i in range(steps):
+            one(warm + i)
+        e1.record(s_dn)
+        torch.cuda.synchronize(dev)
     ms = allreduce_max(e0.elapsed_time(e1) / steps, ws, dev)
     return {"value": round(whole_job_gbs(step_bytes, ws, ms), 2), "unit": UNIT,
             "ms_per_step": round(ms, 4), "steps": steps, "h2d_bytes_per_step": h2d,
