@@ -99,6 +99,21 @@ __device__ __forceinline__ void st64(void* p, uint2 v) {
   asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
+// Single words and bytes on the coherent path: a thread patching what it
+// stored earlier in the same kernel (program order keeps the read after the
+// store it follows).
+__device__ __forceinline__ uint32_t ld_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_u8(uint8_t* p, uint32_t v) {
+  asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void stf(float* p, float v) {
   asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
@@ -671,6 +686,13 @@ __device__ __forceinline__ void settle_codes_regs(uint32_t mask, float s, const 
 struct NoReload {
   __device__ __forceinline__ uint32_t operator()(int) const { return 0u; }
 };
+// DeferSettle: no exact pass here; the flag mask (bit 8b + w for element
+// 4w + b) goes to *mask and the caller settles the flagged elements later
+// (the sender, once per staged tile for all its chunks).
+struct DeferSettle {
+  uint32_t* mask;
+  __device__ __forceinline__ uint32_t operator()(int) const { return 0u; }
+};
 
 // INT8 symmetric on this lane's 16 values of a group spread over lpg lanes:
 //   s = max|x| / 127;  q = clamp(rne(x / s), -127, 127);  s == 0 -> q = 0.
@@ -688,9 +710,11 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
   const float r = s == 0.0f ? 0.0f : rcp_approx(s);
   const bool ok = s == 0.0f || (__fmul_rn(a, r) <= 127.25f && s >= kTwoM100);
   const uint32_t mask = round_codes<true>(v, r, ok, ub);
-  constexpr bool kReload = !std::is_same<Reload, NoReload>::value;
-  if (!kReload && UNROLLED) settle_codes_regs<true>(mask, s, v, ub);
-  if (!kReload && !UNROLLED) settle_codes<true>(mask, s, RegSettle{v, ub}, RegSettle{v, ub});
+  constexpr bool kDefer = std::is_same<Reload, DeferSettle>::value;
+  constexpr bool kReload = !std::is_same<Reload, NoReload>::value && !kDefer;
+  if constexpr (kDefer) *reload.mask = mask;
+  if (!kReload && !kDefer && UNROLLED) settle_codes_regs<true>(mask, s, v, ub);
+  if (!kReload && !kDefer && !UNROLLED) settle_codes<true>(mask, s, RegSettle{v, ub}, RegSettle{v, ub});
 #pragma unroll
   for (int j = 0; j < 4; ++j) q[j] = low_bytes4(ub[4 * j], ub[4 * j + 1], ub[4 * j + 2], ub[4 * j + 3]);
   if (kReload)
@@ -752,9 +776,11 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
   const float r = s == 0.0f ? 0.0f : rcp_approx(s);
   const bool ok = s == 0.0f || (__fmul_rn(span, r) <= 15.25f && s >= kTwoM100);
   const uint32_t mask = round_codes<false>(num, r, ok, ub);
-  constexpr bool kReload = !std::is_same<Reload, NoReload>::value;
-  if (!kReload && UNROLLED) settle_codes_regs<false>(mask, s, num, ub);
-  if (!kReload && !UNROLLED) settle_codes<false>(mask, s, RegSettle{num, ub}, RegSettle{num, ub});
+  constexpr bool kDefer = std::is_same<Reload, DeferSettle>::value;
+  constexpr bool kReload = !std::is_same<Reload, NoReload>::value && !kDefer;
+  if constexpr (kDefer) *reload.mask = mask;
+  if (!kReload && !kDefer && UNROLLED) settle_codes_regs<false>(mask, s, num, ub);
+  if (!kReload && !kDefer && !UNROLLED) settle_codes<false>(mask, s, RegSettle{num, ub}, RegSettle{num, ub});
   // Nibble packing by multiply-adds: ub = 0x4B000000 + code with code in
   // [0, 15] wherever the fast path holds, so sum_i ub[8j+i] * 16^i is the
   // packed word plus 0x4B000000 * 0x11111111 = 0xFB000000 (mod 2^32).

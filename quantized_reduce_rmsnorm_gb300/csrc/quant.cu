@@ -238,8 +238,15 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 4 : 3)
     const int ne = static_cast<int>(rem < kWTile ? rem : kWTile);
     const uint4* tile = reinterpret_cast<const uint4*>(ring + st * (kWTile * 2));
     const int nch = ne >> 4;
+    // untagged: each chunk's flag mask, scale and minimum, settled once for
+    // the whole tile below
+    constexpr int kNJ = kWTile / 16 / 32;
+    uint32_t mk[kNJ];
+    float sj[kNJ], zj[kNJ];
 #pragma unroll
-    for (int j = 0; j < kWTile / 16 / 32; ++j) {
+    for (int j = 0; j < kNJ; ++j) mk[j] = 0u, sj[j] = 0.0f, zj[j] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kNJ; ++j) {
       const int cl = j * 32 + lane;
       const bool act = cl < nch;
       uint32_t bw[8];
@@ -261,7 +268,13 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 4 : 3)
       auto reload = [xs](int i) { return static_cast<uint32_t>(xs[i]); };
       if (FMT == kINT8) {
         uint32_t q[4];
-        const float s = quant_i8<false, true>(v, lpg, q, d, bw, reload);
+        float s;
+        if constexpr (TAGGED) {
+          s = quant_i8<false, true>(v, lpg, q, d, bw, reload);
+        } else {
+          s = quant_i8<false, true>(v, lpg, q, d, bw, DeferSettle{&mk[j]});
+          sj[j] = s;
+        }
         if (TAGGED) {
           // lpg == 8: lane = (group in warp) * 8 + k; stage the payload, then
           // one lane per block writes it (11 blocks per group, 44 per warp)
@@ -289,8 +302,13 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 4 : 3)
         }
       } else {
         uint32_t q[2];
-        float z;
-        const float s = quant_i4<false, true>(v, lpg, q, z, d, bw, reload);
+        float z, s;
+        if constexpr (TAGGED) {
+          s = quant_i4<false, true>(v, lpg, q, z, d, bw, reload);
+        } else {
+          s = quant_i4<false, true>(v, lpg, q, z, d, bw, DeferSettle{&mk[j]});
+          sj[j] = s, zj[j] = z;
+        }
         if (TAGGED) {
           // lpg == 2: the even lane writes block 0 {its two code words, the odd
           // lane's first}, the odd lane block 1 {its second, scale, zero}
@@ -307,6 +325,47 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 4 : 3)
           if ((lane & (lpg - 1)) == 0) {
             stf(job.scales[p] + (c >> lpg_shift), s);
             stf(job.zeros[p] + (c >> lpg_shift), z);
+          }
+        }
+      }
+    }
+    if constexpr (!TAGGED) {
+      // The exact pass for the whole tile: each lane settles its flagged
+      // elements of all its chunks in turn (re-read from the staged tile,
+      // which lane 0 refills only after this), and patches the stored codes.
+      // Once per tile instead of once per chunk, the warp loops about half as
+      // often (flags are sparse: most lanes hold at most one per tile).
+      const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile);
+      auto pending = [&]() {
+        uint32_t m = 0u;
+#pragma unroll
+        for (int j = 0; j < kNJ; ++j) m |= mk[j];
+        return m;
+      };
+      while (__any_sync(kFull, pending() != 0u)) {
+        if (pending() != 0u) {
+          int js = 0;
+#pragma unroll
+          for (int j = kNJ - 1; j >= 0; --j)
+            if (mk[j]) js = j;
+          uint32_t m = 0u;
+          float s = 0.0f, z = 0.0f;
+#pragma unroll
+          for (int j = 0; j < kNJ; ++j)
+            if (j == js) m = mk[j], s = sj[j], z = zj[j], mk[j] &= mk[j] - 1u;
+          const int pos = __ffs(m) - 1;
+          const int i = 4 * (pos & 7) + (pos >> 3);  // mask bit 8b + w is element 4w + b
+          const int cl = js * 32 + lane;
+          const uint32_t xb = t16[16 * cl + i];
+          const int64_t c = (e0 >> 4) + cl;
+          if (FMT == kINT8) {
+            const int code = __float2int_rn(code_by_division<true>(__uint_as_float(xb << 16), s));
+            st_u8(static_cast<uint8_t*>(job.codes[p]) + c * 16 + i, static_cast<uint32_t>(code) & 0xFFu);
+          } else {
+            const int code = __float2int_rn(code_by_division<false>(add_bf_lo(xb, -z), s));
+            uint32_t* wp = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(job.codes[p]) + c * 8) + (i >> 3);
+            const int sh = 4 * (i & 7);
+            st_u32(wp, (ld_u32(wp) & ~(0xFu << sh)) | (static_cast<uint32_t>(code) << sh));
           }
         }
       }
