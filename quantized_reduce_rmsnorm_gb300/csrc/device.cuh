@@ -99,12 +99,18 @@ __device__ __forceinline__ void st64(void* p, uint2 v) {
   asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
-// Single words and bytes on the coherent path: a thread patching what it
-// stored earlier in the same kernel (program order keeps the read after the
-// store it follows).
+// Single words and bytes on the coherent path, for a warp patching codes it
+// stored earlier in the same kernel: ld_u32 for a word the thread stored
+// itself (program order), ld_u32_l2 for one another lane of the warp stored
+// (read from L2, after a warp barrier).
 __device__ __forceinline__ uint32_t ld_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_u32_l2(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 __device__ __forceinline__ void st_u32(uint32_t* p, uint32_t v) {

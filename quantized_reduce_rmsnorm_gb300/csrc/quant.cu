@@ -238,8 +238,8 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 4 : 3)
     const int ne = static_cast<int>(rem < kWTile ? rem : kWTile);
     const uint4* tile = reinterpret_cast<const uint4*>(ring + st * (kWTile * 2));
     const int nch = ne >> 4;
-    // untagged: each chunk's flag mask, scale and minimum, settled once for
-    // the whole tile below
+    // each chunk's flag mask, scale and minimum, settled once for the whole
+    // tile below
     constexpr int kNJ = kWTile / 16 / 32;
     uint32_t mk[kNJ];
     float sj[kNJ], zj[kNJ];
@@ -263,18 +263,11 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 4 : 3)
       for (int i = 0; i < 8; ++i) v[2 * i] = bf_lo(bw[i]), v[2 * i + 1] = bf_hi(bw[i]);
       const int64_t c = (e0 >> 4) + cl;  // global chunk of slab p
       float d[16];
-      // the exact pass re-reads an element's bf16 from the staged tile
-      const uint16_t* xs = reinterpret_cast<const uint16_t*>(tile) + 16 * cl;
-      auto reload = [xs](int i) { return static_cast<uint32_t>(xs[i]); };
       if (FMT == kINT8) {
         uint32_t q[4];
         float s;
-        if constexpr (TAGGED) {
-          s = quant_i8<false, true>(v, lpg, q, d, bw, reload);
-        } else {
-          s = quant_i8<false, true>(v, lpg, q, d, bw, DeferSettle{&mk[j]});
-          sj[j] = s;
-        }
+        s = quant_i8<false, true>(v, lpg, q, d, bw, DeferSettle{&mk[j]});
+        sj[j] = s;
         if (TAGGED) {
           // lpg == 8: lane = (group in warp) * 8 + k; stage the payload, then
           // one lane per block writes it (11 blocks per group, 44 per warp)
@@ -303,12 +296,8 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 4 : 3)
       } else {
         uint32_t q[2];
         float z, s;
-        if constexpr (TAGGED) {
-          s = quant_i4<false, true>(v, lpg, q, z, d, bw, reload);
-        } else {
-          s = quant_i4<false, true>(v, lpg, q, z, d, bw, DeferSettle{&mk[j]});
-          sj[j] = s, zj[j] = z;
-        }
+        s = quant_i4<false, true>(v, lpg, q, z, d, bw, DeferSettle{&mk[j]});
+        sj[j] = s, zj[j] = z;
         if (TAGGED) {
           // lpg == 2: the even lane writes block 0 {its two code words, the odd
           // lane's first}, the odd lane block 1 {its second, scale, zero}
@@ -329,12 +318,16 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 4 : 3)
         }
       }
     }
-    if constexpr (!TAGGED) {
+    {
       // The exact pass for the whole tile: each lane settles its flagged
       // elements of all its chunks in turn (re-read from the staged tile,
       // which lane 0 refills only after this), and patches the stored codes.
       // Once per tile instead of once per chunk, the warp loops about half as
       // often (flags are sparse: most lanes hold at most one per tile).
+      // Tagged INT4 blocks hold an odd lane's first code word in its even
+      // neighbour's block; the warp barrier orders that store before the
+      // patch.
+      if (TAGGED) __syncwarp();
       const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile);
       auto pending = [&]() {
         uint32_t m = 0u;
@@ -358,14 +351,26 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 4 : 3)
           const int cl = js * 32 + lane;
           const uint32_t xb = t16[16 * cl + i];
           const int64_t c = (e0 >> 4) + cl;
+          uint8_t* out = static_cast<uint8_t*>(job.codes[p]);
           if (FMT == kINT8) {
             const int code = __float2int_rn(code_by_division<true>(__uint_as_float(xb << 16), s));
-            st_u8(static_cast<uint8_t*>(job.codes[p]) + c * 16 + i, static_cast<uint32_t>(code) & 0xFFu);
+            // plain: 16 code bytes per chunk; tagged: payload word 4k + i/4 of
+            // the group (k = chunk within the group), three words per block
+            const int pw = 4 * (cl & 7) + (i >> 2);
+            uint8_t* bp = TAGGED ? out + ((c >> 3) * kBlocksPerGroupI8 + pw / 3) * 16 + (pw % 3) * 4 + (i & 3)
+                                 : out + c * 16 + i;
+            st_u8(bp, static_cast<uint32_t>(code) & 0xFFu);
           } else {
             const int code = __float2int_rn(code_by_division<false>(add_bf_lo(xb, -z), s));
-            uint32_t* wp = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(job.codes[p]) + c * 8) + (i >> 3);
+            // plain: two code words per chunk; tagged: block 0 = {even lane's
+            // words, odd lane's first}, block 1 = {odd lane's second, ...}
+            const int k = i >> 3;
+            const int wi = !TAGGED ? 0 : (cl & 1) == 0 ? k : (k == 0 ? 2 : 4);
+            uint32_t* wp = TAGGED ? reinterpret_cast<uint32_t*>(out + (c >> 1) * kBlocksPerGroupI4 * 16) + wi
+                                  : reinterpret_cast<uint32_t*>(out + c * 8) + k;
             const int sh = 4 * (i & 7);
-            st_u32(wp, (ld_u32(wp) & ~(0xFu << sh)) | (static_cast<uint32_t>(code) << sh));
+            const uint32_t old = TAGGED ? ld_u32_l2(wp) : ld_u32(wp);
+            st_u32(wp, (old & ~(0xFu << sh)) | (static_cast<uint32_t>(code) << sh));
           }
         }
       }
