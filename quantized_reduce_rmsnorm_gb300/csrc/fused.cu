@@ -233,7 +233,18 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-constexpr int kTagStages = 3;  // block groups in a warp's ring
+// Block groups in a warp's ring, and the CTAs per SM its registers are
+// bounded for: two slabs, three groups and four CTAs (62 registers); four
+// slabs, three and three; eight slabs, two groups and three CTAs (70
+// registers; three groups would leave room for two).  Measured on GB300
+// against three groups and unbounded registers everywhere (back-to-back
+// calls, same box): eight slabs 91.1 -> 86.7 us (H = 4096), 94.3 -> 90.6 us
+// (H = 8192), 63.2 -> 59.8 us (the 2048-row token-split subset); two slabs
+// 72.0 -> 70.6 us.
+template <int PMAX>
+__host__ __device__ constexpr int tag_stages() { return PMAX <= 4 ? 3 : 2; }
+template <int PMAX>
+constexpr int tag_min_ctas() { return PMAX <= 2 ? 4 : 3; }  // CTAs per SM the registers are bounded for
 constexpr int kTagWarps = 8;
 // A row is shared by kTagRowWarps warps, each streaming a contiguous share of
 // its block groups; their sums of squares meet in shared memory at one CTA
@@ -248,7 +259,7 @@ template <int PMAX>
 __host__ __device__ constexpr int tag_stage_bytes() { return PMAX * 32 * 16 + 384; }  // 32 blocks per slab + residual
 
 template <int PMAX>
-__global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
+__global__ void __launch_bounds__(256, tag_min_ctas<PMAX>()) k_fused_tagged(FusedArgs a) {
   pdl_begin();
   extern __shared__ __align__(16) uint8_t tsmem[];
   __shared__ float red[2][kTagRowsPerCta][kTagRowWarps];  // per-warp sums of squares
@@ -260,6 +271,7 @@ __global__ void __launch_bounds__(256) k_fused_tagged(FusedArgs a) {
   const int P = a.P;
   const uint32_t epoch = a.epoch;
   constexpr int kStage = tag_stage_bytes<PMAX>();
+  constexpr int kTagStages = tag_stages<PMAX>();
   uint8_t* ring = tsmem + wid * (kTagStages * kStage);
   // this warp's block groups of every row: a contiguous share of the row
   const int g0 = part * gpr / kTagRowWarps, g1 = (part + 1) * gpr / kTagRowWarps;
@@ -458,7 +470,7 @@ cudaError_t launch_fmt(const FusedArgs& a, int max_ctas, cudaStream_t st) {
 
 template <int PMAX>
 int tagged_occupancy() {
-  constexpr int smem = kTagWarps * kTagStages * tag_stage_bytes<PMAX>();
+  constexpr int smem = kTagWarps * tag_stages<PMAX>() * tag_stage_bytes<PMAX>();
   static int occ = 0;
   if (!occ) {
     cudaFuncSetAttribute(k_fused_tagged<PMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -471,7 +483,7 @@ int tagged_occupancy() {
 
 template <int PMAX>
 cudaError_t launch_tagged_p(const FusedArgs& a, int max_ctas, cudaStream_t st) {
-  constexpr int smem = kTagWarps * kTagStages * tag_stage_bytes<PMAX>();
+  constexpr int smem = kTagWarps * tag_stages<PMAX>() * tag_stage_bytes<PMAX>();
   int64_t grid = static_cast<int64_t>(num_sms()) * tagged_occupancy<PMAX>();
   const int64_t need = (a.rows + kTagRowsPerCta - 1) / kTagRowsPerCta;
   if (grid > need) grid = need;
