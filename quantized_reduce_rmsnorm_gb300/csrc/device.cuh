@@ -614,27 +614,6 @@ __device__ __forceinline__ void settle_codes(uint32_t mask, float s, Pick pick, 
   }
 }
 
-// The same with each lane settling its own flagged elements in turn (the
-// index differs between lanes), for callers that can fetch any element by a
-// lane-varying index: the warp loops max-over-lanes times, not once per
-// distinct index.  Each visit computes the definition itself, the IEEE
-// quotient rounded to the nearest even integer: that takes fewer
-// instructions than recomputing the fast path's code and resolving it next
-// to its half-integer (measured on GB300 with the sender: prefill 133.4 ->
-// 127.9 us; without any exact pass it would take 114.1 us).
-template <bool SIGNED, class Pick, class Put>
-__device__ __forceinline__ void settle_codes_lanewise(uint32_t mask, float s, Pick pick, Put put) {
-  const float magic = SIGNED ? kMagicI8 : 8388608.0f;
-  while (__any_sync(kFull, mask != 0u)) {
-    if (mask) {
-      const int pos = __ffs(mask) - 1;
-      mask &= mask - 1;
-      const int i = 4 * (pos & 7) + (pos >> 3);
-      put(i, __float_as_uint(__fadd_rn(code_by_division<SIGNED>(pick(i), s), magic)));
-    }
-  }
-}
-
 // pick / put over the register arrays (a switch on the warp-uniform index)
 struct RegSettle {
   const float* v;
@@ -685,19 +664,14 @@ __device__ __forceinline__ void settle_codes_regs(uint32_t mask, float s, const 
   }
 }
 
-// Without a reload source the exact pass works on the register arrays.  A
-// Reload functor instead returns element i's bf16 bits (low 16 bits) from
-// memory the caller still holds (the sender's staged tile), and the exact
-// codes are patched into the packed words.
-struct NoReload {
-  __device__ __forceinline__ uint32_t operator()(int) const { return 0u; }
-};
-// DeferSettle: no exact pass here; the flag mask (bit 8b + w for element
-// 4w + b) goes to *mask and the caller settles the flagged elements later
+// Where the quantizers settle the flagged elements: SettleHere, in this call,
+// over the register arrays (the fused kernels' requantization); DeferSettle,
+// not at all: the flag mask (bit 8b + w for element 4w + b) goes to *mask
+// and the caller settles those elements later and patches the stored codes
 // (the sender, once per staged tile for all its chunks).
+struct SettleHere {};
 struct DeferSettle {
   uint32_t* mask;
-  __device__ __forceinline__ uint32_t operator()(int) const { return 0u; }
 };
 
 // INT8 symmetric on this lane's 16 values of a group spread over lpg lanes:
@@ -706,9 +680,9 @@ struct DeferSettle {
 // With BFW, the lane's max|x| is taken from the packed bf16 inputs bw[8].
 // UNROLLED: the exact pass over registers is settle_codes_regs (else the
 // index loop, settle_codes).
-template <bool DEQ, bool BFW = false, class Reload = NoReload, bool UNROLLED = false>
+template <bool DEQ, bool BFW = false, class Settle = SettleHere, bool UNROLLED = false>
 __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q[4], float d[16],
-                                          const uint32_t* bw = nullptr, Reload reload = Reload()) {
+                                          const uint32_t* bw = nullptr, Settle settle = Settle()) {
   float a = BFW ? bf16_absmax16(bw) : absmax16(v);
   a = group_max(a, lpg);
   const float s = div127(a);
@@ -716,22 +690,16 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
   const float r = s == 0.0f ? 0.0f : rcp_approx(s);
   const bool ok = s == 0.0f || (__fmul_rn(a, r) <= 127.25f && s >= kTwoM100);
   const uint32_t mask = round_codes<true>(v, r, ok, ub);
-  constexpr bool kDefer = std::is_same<Reload, DeferSettle>::value;
-  constexpr bool kReload = !std::is_same<Reload, NoReload>::value && !kDefer;
-  if constexpr (kDefer) *reload.mask = mask;
-  if (!kReload && !kDefer && UNROLLED) settle_codes_regs<true>(mask, s, v, ub);
-  if (!kReload && !kDefer && !UNROLLED) settle_codes<true>(mask, s, RegSettle{v, ub}, RegSettle{v, ub});
+  if constexpr (std::is_same<Settle, DeferSettle>::value) {
+    *settle.mask = mask;
+  } else {
+    if (UNROLLED)
+      settle_codes_regs<true>(mask, s, v, ub);
+    else
+      settle_codes<true>(mask, s, RegSettle{v, ub}, RegSettle{v, ub});
+  }
 #pragma unroll
   for (int j = 0; j < 4; ++j) q[j] = low_bytes4(ub[4 * j], ub[4 * j + 1], ub[4 * j + 2], ub[4 * j + 3]);
-  if (kReload)
-    settle_codes_lanewise<true>(
-        mask, s, [&](int i) { return __uint_as_float(reload(i) << 16); },
-        [&](int i, uint32_t rb) {
-          const int sh = 8 * (i & 3);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (k == (i >> 2)) q[k] = (q[k] & ~(0xFFu << sh)) | ((rb & 0xFFu) << sh);
-        });
   if (DEQ) {
     if (s < 1.2676506e30f) {  // u - 2^22 = 2^23 + q exactly; fma(2^23 + q, s, -2^23 s) = fl(q s)
       const float2 C = dup2(-4194304.0f), S = dup2(s), N = dup2(__fmul_rn(-kTwo23, s));
@@ -753,10 +721,10 @@ __device__ __forceinline__ float quant_i8(const float v[16], int lpg, uint32_t q
 // Element 2i in the low nibble of byte i.  Returns s, writes z; with DEQ also
 // d[i] = (q_i * s) + z.  With BFW, the lane's min and max come from the
 // packed bf16 inputs bw[8].
-template <bool DEQ, bool BFW = false, class Reload = NoReload, bool UNROLLED = false>
+template <bool DEQ, bool BFW = false, class Settle = SettleHere, bool UNROLLED = false>
 __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q[2], float& z,
                                           float d[16], const uint32_t* bw = nullptr,
-                                          Reload reload = Reload()) {
+                                          Settle settle = Settle()) {
   float lo, hi;
   if (BFW)
     bf16_minmax16(bw, lo, hi);
@@ -782,11 +750,14 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
   const float r = s == 0.0f ? 0.0f : rcp_approx(s);
   const bool ok = s == 0.0f || (__fmul_rn(span, r) <= 15.25f && s >= kTwoM100);
   const uint32_t mask = round_codes<false>(num, r, ok, ub);
-  constexpr bool kDefer = std::is_same<Reload, DeferSettle>::value;
-  constexpr bool kReload = !std::is_same<Reload, NoReload>::value && !kDefer;
-  if constexpr (kDefer) *reload.mask = mask;
-  if (!kReload && !kDefer && UNROLLED) settle_codes_regs<false>(mask, s, num, ub);
-  if (!kReload && !kDefer && !UNROLLED) settle_codes<false>(mask, s, RegSettle{num, ub}, RegSettle{num, ub});
+  if constexpr (std::is_same<Settle, DeferSettle>::value) {
+    *settle.mask = mask;
+  } else {
+    if (UNROLLED)
+      settle_codes_regs<false>(mask, s, num, ub);
+    else
+      settle_codes<false>(mask, s, RegSettle{num, ub}, RegSettle{num, ub});
+  }
   // Nibble packing by multiply-adds: ub = 0x4B000000 + code with code in
   // [0, 15] wherever the fast path holds, so sum_i ub[8j+i] * 16^i is the
   // packed word plus 0x4B000000 * 0x11111111 = 0xFB000000 (mod 2^32).
@@ -799,15 +770,6 @@ __device__ __forceinline__ float quant_i4(const float v[16], int lpg, uint32_t q
     for (int i = 6; i >= 1; --i) w = w * 16u + ub[8 * j + i];
     q[j] = w * 16u + (ub[8 * j] - 0xFB000000u);
   }
-  if (kReload)
-    settle_codes_lanewise<false>(
-        mask, s, [&](int i) { return add_bf_lo(reload(i), -lo); },
-        [&](int i, uint32_t rb) {
-          const int sh = 4 * (i & 7);
-#pragma unroll
-          for (int k = 0; k < 2; ++k)
-            if (k == (i >> 3)) q[k] = (q[k] & ~(0xFu << sh)) | ((rb & 0xFu) << sh);
-        });
   if (DEQ) {  // d = fl(fl(q * s) + z); fl(q * s) = fma(2^23 + q, s, -2^23 * s) for s < 2^100
     if (s < 1.2676506e30f) {
       const float2 S = dup2(s), N = dup2(__fmul_rn(-kTwo23, s)), Z = dup2(z);

@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
         // flags as a mask pay (and the compact builds have no registers for the
         // alternative); eight: flags by comparing packed words
         const float s8 = PMAX >= 8 ? requant_i8(acc, lpg, q, acc)
-                                   : quant_i8<true, false, NoReload, (PMAX <= 2)>(acc, lpg, q, acc);
+                                   : quant_i8<true, false, SettleHere, (PMAX <= 2)>(acc, lpg, q, acc);
         if (act && a.rq_codes) {
           st128(static_cast<int8_t*>(a.rq_codes) + gc * 16, make_uint4(q[0], q[1], q[2], q[3]));
           if ((lane & (lpg - 1)) == 0) stf(a.rq_scales + gg, s8);
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
         uint32_t q[2];
         float z;
         const float s4 = PMAX >= 8 ? requant_i4(acc, lpg, q, z, acc)
-                                   : quant_i4<true, false, NoReload, (PMAX <= 2)>(acc, lpg, q, z, acc);
+                                   : quant_i4<true, false, SettleHere, (PMAX <= 2)>(acc, lpg, q, z, acc);
         if (act && a.rq_codes) {
           st64(static_cast<uint8_t*>(a.rq_codes) + gc * 8, make_uint2(q[0], q[1]));
           if ((lane & (lpg - 1)) == 0) {
