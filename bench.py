@@ -286,7 +286,10 @@ def oracle_sample(w, inputs, target_s: float, threads: int = 1):
     ranges, each run by the unmodified oracle on its own host thread (rows
     are independent; the C calls release the interpreter lock).
 
-    Returns (GB/s of algorithmic bytes, seconds, rows)."""
+    When every row of the inputs takes less than target_s, the whole
+    workload is run repeatedly (passes) until about target_s has elapsed.
+
+    Returns (GB/s of algorithmic bytes, seconds, rows, passes)."""
     import concurrent.futures as cf
     import oracle
     from quantized_reduce_rmsnorm_gb300.pipeline import qs_bytes
@@ -317,6 +320,13 @@ def oracle_sample(w, inputs, target_s: float, threads: int = 1):
     dt = run(probe)
     rows = int(min(avail, max(probe, probe * target_s / max(dt, 1e-6))))
     dt = run(rows)
+    passes = 1
+    if rows == avail and dt < target_s:
+        passes = max(1, int(round(target_s / max(dt, 1e-6))))
+        t0 = time.perf_counter()
+        for _ in range(passes):
+            run(rows)
+        dt = time.perf_counter() - t0
     if pool is not None:
         pool.shutdown()
     sub = Workload(**{**w.__dict__, "T": rows})
@@ -326,7 +336,7 @@ def oracle_sample(w, inputs, target_s: float, threads: int = 1):
         alg = (w.P * 2 * E + w.P * qs) + (w.P * qs + 2 * E + 2 * w.H + qs + 4 * E)
     else:
         alg = w.P * 2 * E + 2 * E + 2 * w.H + 4 * E
-    return alg / dt / 1e9, dt, rows
+    return passes * alg / dt / 1e9, dt, rows, passes
 
 
 def run_reference(args):
@@ -343,20 +353,21 @@ def run_reference(args):
     n = host_cores()
     vals = []
     for i in range(args.warmup + args.steps):
-        gbs, dt, r = oracle_sample(w, inputs, per_step, threads=n)
+        gbs, dt, r, passes = oracle_sample(w, inputs, per_step, threads=n)
         if i >= args.warmup:
-            vals.append((gbs, dt, r))
+            vals.append((gbs, dt, r, passes))
     v = statistics.median(x[0] for x in vals)
     ms = statistics.median(x[1] for x in vals) * 1e3
-    r = vals[-1][2]
+    r, passes = vals[-1][2], vals[-1][3]
+    reps = f" ({passes} passes over them)" if passes > 1 else ""
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(w, note=f"oracle on {r} of {w.T} rows per step, {n} host threads"),
+        "config": workload_config(w, note=f"oracle on {r} of {w.T} rows per step{reps}, {n} host threads"),
         "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": n, "kind": "oracle",
-                         "sample": f"{r} of {w.T} rows of the {w.name} workload per step, in {n} "
+                         "sample": f"{r} of {w.T} rows of the {w.name} workload per step{reps}, in {n} "
                                    f"contiguous row ranges on {n} host threads"},
         "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -515,14 +526,18 @@ def run_ours(args):
         out["e2e"] = run_e2e(pipe, inputs, step_bytes, args, ws, dev)
     if ws == 1 and rank == 0 and not args.no_cpu_baseline:
         n = host_cores()
-        gbs, dt, rows = oracle_sample(w, inputs, args.cpu_seconds / 2, threads=n)
-        gbs1, dt1, rows1 = oracle_sample(w, inputs, args.cpu_seconds / 2)
+        gbs, dt, rows, passes = oracle_sample(w, inputs, args.cpu_seconds / 2, threads=n)
+        gbs1, dt1, rows1, passes1 = oracle_sample(w, inputs, args.cpu_seconds / 2)
         out["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": n,
                                "kind": "oracle",
-                               "sample": f"first {rows} of {w.T} rows of the same inputs in {n} "
-                                         f"contiguous row ranges on {n} host threads, {dt:.1f} s",
+                               "sample": f"first {rows} of {w.T} rows of the same inputs"
+                                         + (f" ({passes} passes over them)" if passes > 1 else "")
+                                         + f" in {n} contiguous row ranges on {n} host threads, "
+                                           f"{dt:.1f} s",
                                "single_core": {"value": round(gbs1, 4), "cores": 1,
-                                               "sample": f"first {rows1} rows, {dt1:.1f} s"}}
+                                               "sample": f"first {rows1} rows"
+                                                         + (f", {passes1} passes" if passes1 > 1 else "")
+                                                         + f", {dt1:.1f} s"}}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:

@@ -28,8 +28,8 @@ def test_oracle_sample_on_threads():
     w = synth.Workload("rows", P=2, T=24, H=1024, fmt=synth.FMT_INT8_SYM, group=128)
     inp = synth.make_inputs(w, seed=2)
     for threads in (1, 3):
-        gbs, dt, rows = bench.oracle_sample(w, inp, 0.01, threads=threads)
-        assert gbs > 0 and dt > 0 and 1 <= rows <= w.T
+        gbs, dt, rows, passes = bench.oracle_sample(w, inp, 0.01, threads=threads)
+        assert gbs > 0 and dt > 0 and 1 <= rows <= w.T and passes >= 1
     assert bench.host_cores() >= 1
 
 
