@@ -143,6 +143,55 @@ int rg_shape(const FusedArgs& a, const TmaShape& sh, TmaGeom& g3, bool& compact)
   }
 }
 
+// The residual-free compact build for the tagged quantized formats
+// (fused_tma_rg.cu).  Tagged slab rows are 16/12 the bytes of the plain
+// payload, so with the residual in the stage shared memory bounds the CTAs
+// per SM below what the compact build's registers allow, or leaves room only
+// for a one-row stage where the plain format takes a two-row ring.  Among the
+// builds of fused_tma_rg.cu (a two-row ring; a one-row stage; two half-row
+// sub-stages) the plan with the most CTAs per SM, then the deepest ring, is
+// returned when it beats the current plan (occ_now CTAs per SM, a ring of
+// depth_now half rows: 4 two-row ring, 3 half-row sub-stages, 2 one row):
+// more CTAs per SM, or as many with a two-row ring in place of a one-row
+// stage.  Measured on GB300 against the staged residual (64 MB messages,
+// fraction of the measured HBM peak): four tagged INT8 slabs 0.75 -> 0.82 at
+// H = 4096 (five -> six CTAs) and H = 8192 (two -> three); two tagged INT4
+// slabs at H = 4096 0.65 -> 0.67 (five -> six); eight tagged INT4 slabs at
+// H = 4096 0.66 -> 0.68 (four -> five); two tagged INT8 slabs at H = 4096
+// 0.77 -> 0.80 (a two-row ring).  A two-row ring in place of half-row
+// sub-stages at the same count (two slabs, H = 8192) was slower at 16 MB
+// (+4-6%), and an L2 prefetch of each row's residual, slower everywhere
+// (eight INT4 slabs at 64 MB: 88 -> 109 us).
+struct RgPlan {
+  int occ = 0, nstage = 0, sub = 0, smem = 0;
+  TmaGeom g{};
+};
+template <int FMT>
+RgPlan rg_tagged_plan(const FusedArgs& a, int threads, int occ_now, int depth_now) {
+  RgPlan best;
+  int best_depth = 0;
+  if (FMT != kINT8T && FMT != kINT4T) return best;
+  const int cands[3][2] = {{2, 1}, {1, 2}, {1, 1}};
+  for (const auto& c : cands) {
+    const int ns = c[0], sub = c[1];
+    if (sub == 2 && (threads != 256 || (a.H >> 4) != 2 * threads)) continue;
+    TmaGeom g;
+    if (!geometry(FMT, a, g, sub)) continue;
+    g.stage_bytes -= 32 * g.cps;  // no residual in the stage
+    g.stage_off = (2 * a.H + 127) & ~127;
+    const int smem = g.stage_off + ns * sub * g.stage_bytes;
+    if (smem > kTmaSmemLimit) continue;
+    const int occ = fused_tma_rg_occupancy(FMT, a.P, ns, sub, threads, smem);
+    const int depth = ns == 2 ? 4 : sub == 2 ? 3 : 2;
+    if (occ > best.occ || (occ == best.occ && occ > 0 && depth > best_depth)) {
+      best.occ = occ, best.nstage = ns, best.sub = sub, best.smem = smem, best.g = g;
+      best_depth = depth;
+    }
+  }
+  if (!(best.occ > occ_now || (best.occ == occ_now && best_depth >= depth_now + 2))) best.occ = 0;
+  return best;
+}
+
 template <int FMT, int PMAX>
 cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cudaStream_t st) {
   const TmaShape sh = choose_shape<FMT, PMAX>(a, g);
@@ -184,7 +233,21 @@ cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cud
   {
     TmaGeom g2;
     const int occ2 = sh.compact ? sub_shape<FMT, PMAX, true>(a, sh, g2) : sub_shape<FMT, PMAX, false>(a, sh, g2);
-    if (occ2 >= sh.occ && occ2 > 0) {
+    const bool sub2 = occ2 >= sh.occ && occ2 > 0;
+    if constexpr (kTagged) {
+      // only for more rows than one wave of the current plan (as above)
+      if (a.rows > static_cast<int64_t>(num_sms()) * sh.occ) {
+        const RgPlan rp = rg_tagged_plan<FMT>(a, sh.threads, sub2 ? occ2 : sh.occ,
+                                              sub2 ? 3 : 2 * sh.nstage);
+        if (rp.occ > 0) {
+          int64_t grid4 = static_cast<int64_t>(num_sms()) * rp.occ;
+          if (max_ctas > 0 && grid4 > max_ctas) grid4 = max_ctas;
+          if (grid4 > a.rows) grid4 = a.rows;
+          return launch_fused_tma_rg(FMT, rp.nstage, rp.sub, a, rp.g, sh.threads, rp.smem, grid4, st);
+        }
+      }
+    }
+    if (sub2) {
       const int smem2 = g2.stage_off + 2 * g2.stage_bytes;
       if (sh.compact)
         return launch_pdl(k_fused_tma<FMT, 1, PMAX, 1, true, 2>, dim3(static_cast<unsigned>(grid)),
@@ -224,19 +287,35 @@ bool fused_tma_eligible(int fmt, const FusedArgs& a) {
   return aligned16(a.res_in) && aligned16(a.gamma);
 }
 
-template <int FMT>
-int64_t wave_fmt(const FusedArgs& a, const TmaGeom& g) {
-  const TmaShape sh = a.P <= 2 ? choose_shape<FMT, 2>(a, g)
-                      : a.P <= 4 ? choose_shape<FMT, 4>(a, g)
-                                 : choose_shape<FMT, 8>(a, g);
-  int occ = sh.occ;
-  if (a.P > 4) {
+// CTAs per SM of the plan launch_tma_p takes for a call of a.rows rows
+// (the cluster launch aside): the same choices in the same order.
+template <int FMT, int PMAX>
+int plan_occ(const FusedArgs& a, const TmaGeom& g) {
+  const TmaShape sh = choose_shape<FMT, PMAX>(a, g);
+  if (sh.occ < 1) return 1;
+  const bool more = a.rows > static_cast<int64_t>(num_sms()) * sh.occ;
+  if constexpr (PMAX == 8 && (FMT == kINT8T || FMT == kINT4)) {
     TmaGeom g3;
     bool compact = false;
-    const int occ3 = rg_shape<FMT, 8>(a, sh, g3, compact);
-    if (a.rows > static_cast<int64_t>(num_sms()) * occ) occ = occ3 > occ ? occ3 : occ;
+    const int occ3 = rg_shape<FMT, PMAX>(a, sh, g3, compact);
+    if (occ3 > sh.occ && more) return occ3;
   }
-  return static_cast<int64_t>(num_sms()) * (occ > 0 ? occ : 1);  // a CTA per row
+  if constexpr (FMT == kINT8T || FMT == kINT4T) {
+    if (more) {
+      TmaGeom g2;
+      const int occ2 = sh.compact ? sub_shape<FMT, PMAX, true>(a, sh, g2) : sub_shape<FMT, PMAX, false>(a, sh, g2);
+      const bool sub2 = occ2 >= sh.occ && occ2 > 0;
+      const RgPlan rp = rg_tagged_plan<FMT>(a, sh.threads, sub2 ? occ2 : sh.occ, sub2 ? 3 : 2 * sh.nstage);
+      if (rp.occ > 0) return rp.occ;
+    }
+  }
+  return sh.occ;
+}
+
+template <int FMT>
+int64_t wave_fmt(const FusedArgs& a, const TmaGeom& g) {
+  const int occ = a.P <= 2 ? plan_occ<FMT, 2>(a, g) : a.P <= 4 ? plan_occ<FMT, 4>(a, g) : plan_occ<FMT, 8>(a, g);
+  return static_cast<int64_t>(num_sms()) * occ;  // a CTA per row
 }
 
 int64_t fused_tma_wave_rows(int fmt, const FusedArgs& a) {

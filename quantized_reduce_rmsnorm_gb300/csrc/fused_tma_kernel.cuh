@@ -49,6 +49,14 @@ int fused_tma_compact_occupancy(int fmt, int P, int nstage, int threads, int sme
 cudaError_t launch_fused_tma_compact(int fmt, int nstage, const FusedArgs& a, const TmaGeom& g,
                                      int threads, int smem, int64_t grid, cudaStream_t st);
 
+// The compact build with the residual left out of the stage, for the tagged
+// quantized formats (fused_tma_rg.cu): resident CTAs per SM of the
+// instantiation for (fmt, P, nstage, sub) at `threads` threads and `smem`
+// bytes (0 when that combination is not built), and its launch.
+int fused_tma_rg_occupancy(int fmt, int P, int nstage, int sub, int threads, int smem);
+cudaError_t launch_fused_tma_rg(int fmt, int nstage, int sub, const FusedArgs& a, const TmaGeom& g,
+                                int threads, int smem, int64_t grid, cudaStream_t st);
+
 namespace {
 
 template <int FMT, bool RG = false>
@@ -126,7 +134,8 @@ __device__ __forceinline__ void st_peer_u32(uint32_t addr, uint32_t v) {
 // RG: the residual is not staged; each thread loads its chunk of it straight
 // from global memory before the chunk's slab loop, whose work hides the
 // load.  Its stage is 2 * H bytes smaller, which is what lets a second CTA
-// per SM fit for eight tagged INT8 slabs at H = 8192.
+// per SM fit for eight tagged INT8 slabs at H = 8192, and a sixth for two
+// tagged INT4 slabs at H = 4096.
 template <int FMT, int NSTAGE, int PMAX, int CL = 1, bool COMPACT = false, int SUB = 1, bool RG = false>
 __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 1)
     k_fused_tma(FusedArgs a, TmaGeom g) {
@@ -188,9 +197,9 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
   if (CL > 1) cluster_barrier();  // every CTA of the cluster runs before any peer store
 
   // gamma of this thread's first chunks, read once: every row uses the same chunks
-  // (the compact build without a staged residual reads gamma per row from
-  // L1 instead: registers are what bounds its CTAs per SM)
-  constexpr int GRC = RG && COMPACT ? 0 : kGammaRegChunks;
+  // (the compact eight-slab build without a staged residual reads gamma per
+  // row from L1 instead: registers are what bounds its CTAs per SM)
+  constexpr int GRC = RG && COMPACT && PMAX == 8 ? 0 : kGammaRegChunks;
   uint32_t greg[GRC > 0 ? GRC : 1][8];
 #pragma unroll
   for (int j = 0; j < GRC; ++j) {

@@ -1,0 +1,97 @@
+// fused_tma_rg.cu -- the compact build of the TMA-staged fused kernel
+// (fused_tma_kernel.cuh) with the residual left out of the stage (RG), for
+// the tagged quantized formats.  A tagged slab row is 16/12 the bytes of the
+// plain payload, so with the residual in it the stage is what bounds CTAs per
+// SM; without it, the compact build's registers do, as for the plain formats.
+// Built for the shapes where that raises the CTAs per SM or admits a deeper
+// ring (fused_tma.cu chooses):
+//   two tagged slabs (INT4 g32 or INT8 g128): a two-row ring;
+//   four tagged INT8 slabs: a one-row stage, whole or as two half-row sub-stages;
+//   eight tagged INT4 slabs: a one-row stage.
+#include "fused_tma_kernel.cuh"
+
+namespace fc {
+
+namespace {
+
+template <int FMT, int NS, int PMAX, int SUB>
+constexpr bool rg_built() {
+  if (FMT == kINT4T) return (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 8 && NS == 1 && SUB == 1);
+  if (FMT == kINT8T) return (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 4 && NS == 1);
+  return false;
+}
+
+template <int FMT, int NS, int PMAX, int SUB>
+int occ_t(int threads, int smem) {
+  if constexpr (!rg_built<FMT, NS, PMAX, SUB>()) {
+    return 0;
+  } else {
+    auto kern = k_fused_tma<FMT, NS, PMAX, 1, true, SUB, true>;
+    return occupancy_memo(reinterpret_cast<const void*>(kern), threads, smem, 1, [&] {
+      int o = 0;
+      if (raise_smem_limit(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, threads, smem) != cudaSuccess)
+        return 0;
+      return o;
+    });
+  }
+}
+
+template <int FMT, int NS, int SUB>
+int occ_p(int P, int threads, int smem) {
+  if (P <= 2) return occ_t<FMT, NS, 2, SUB>(threads, smem);
+  if (P <= 4) return occ_t<FMT, NS, 4, SUB>(threads, smem);
+  return occ_t<FMT, NS, 8, SUB>(threads, smem);
+}
+
+template <int FMT>
+int occ_fmt(int P, int nstage, int sub, int threads, int smem) {
+  if (nstage == 2) return sub == 1 ? occ_p<FMT, 2, 1>(P, threads, smem) : 0;
+  return sub == 1 ? occ_p<FMT, 1, 1>(P, threads, smem) : occ_p<FMT, 1, 2>(P, threads, smem);
+}
+
+template <int FMT, int NS, int PMAX, int SUB>
+cudaError_t launch_t(const FusedArgs& a, const TmaGeom& g, int threads, int smem, int64_t grid,
+                     cudaStream_t st) {
+  if constexpr (!rg_built<FMT, NS, PMAX, SUB>()) {
+    return cudaErrorInvalidConfiguration;
+  } else {
+    return launch_pdl(k_fused_tma<FMT, NS, PMAX, 1, true, SUB, true>, dim3(static_cast<unsigned>(grid)),
+                      dim3(threads), smem, st, a, g);
+  }
+}
+
+template <int FMT, int NS, int SUB>
+cudaError_t launch_p(const FusedArgs& a, const TmaGeom& g, int threads, int smem, int64_t grid,
+                     cudaStream_t st) {
+  if (a.P <= 2) return launch_t<FMT, NS, 2, SUB>(a, g, threads, smem, grid, st);
+  if (a.P <= 4) return launch_t<FMT, NS, 4, SUB>(a, g, threads, smem, grid, st);
+  return launch_t<FMT, NS, 8, SUB>(a, g, threads, smem, grid, st);
+}
+
+template <int FMT>
+cudaError_t launch_fmt(int nstage, int sub, const FusedArgs& a, const TmaGeom& g, int threads, int smem,
+                       int64_t grid, cudaStream_t st) {
+  if (nstage == 2)
+    return sub == 1 ? launch_p<FMT, 2, 1>(a, g, threads, smem, grid, st) : cudaErrorInvalidConfiguration;
+  return sub == 1 ? launch_p<FMT, 1, 1>(a, g, threads, smem, grid, st)
+                  : launch_p<FMT, 1, 2>(a, g, threads, smem, grid, st);
+}
+
+}  // namespace
+
+int fused_tma_rg_occupancy(int fmt, int P, int nstage, int sub, int threads, int smem) {
+  if (threads > 256 || smem > kTmaSmemLimit) return 0;
+  if (fmt == kINT4T) return occ_fmt<kINT4T>(P, nstage, sub, threads, smem);
+  if (fmt == kINT8T) return occ_fmt<kINT8T>(P, nstage, sub, threads, smem);
+  return 0;
+}
+
+cudaError_t launch_fused_tma_rg(int fmt, int nstage, int sub, const FusedArgs& a, const TmaGeom& g,
+                                int threads, int smem, int64_t grid, cudaStream_t st) {
+  if (fmt == kINT4T) return launch_fmt<kINT4T>(nstage, sub, a, g, threads, smem, grid, st);
+  if (fmt == kINT8T) return launch_fmt<kINT8T>(nstage, sub, a, g, threads, smem, grid, st);
+  return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace fc

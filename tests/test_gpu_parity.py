@@ -576,7 +576,17 @@ QT_CASES = [("decode-qtagged", {"T": 12}), ("prefill-qtagged", {"T": 10}),
             ("i8t-p3", {"P": 3, "T": 5, "H": 1152, "fmt": I8T, "group": 128}),
             ("i4t-p5", {"P": 5, "T": 7, "H": 4128, "fmt": I4T, "group": 32}),
             # enough rows for a CTA per row: the build without the h buffer
-            ("i8t-p8-h8192-rows", {"P": 8, "T": 160, "H": 8192, "fmt": I8T, "group": 128})]
+            ("i8t-p8-h8192-rows", {"P": 8, "T": 160, "H": 8192, "fmt": I8T, "group": 128}),
+            # more rows than one wave: the residual-free stages of the tagged
+            # formats (two-row rings for two slabs; one-row stages for eight
+            # INT4 and four INT8 slabs, as two half-row sub-stages at H = 8192)
+            ("i4t-p2-h4096-rows", {"P": 2, "T": 1000, "H": 4096, "fmt": I4T, "group": 32}),
+            ("i4t-p2-h8192-rows", {"P": 2, "T": 480, "H": 8192, "fmt": I4T, "group": 32}),
+            ("i4t-p8-h4096-rows", {"P": 8, "T": 640, "H": 4096, "fmt": I4T, "group": 32}),
+            ("i8t-p2-h4096-rows", {"P": 2, "T": 1000, "H": 4096, "fmt": I8T, "group": 128}),
+            ("i8t-p2-h8192-rows", {"P": 2, "T": 480, "H": 8192, "fmt": I8T, "group": 128}),
+            ("i8t-p4-h4096-rows", {"P": 4, "T": 800, "H": 4096, "fmt": I8T, "group": 128}),
+            ("i8t-p4-h8192-rows", {"P": 4, "T": 320, "H": 8192, "fmt": I8T, "group": 128})]
 
 
 @pytest.mark.parametrize("name,kw", QT_CASES, ids=[c[0] for c in QT_CASES])
@@ -609,6 +619,21 @@ def test_quantized_tagged_stale_blocks(orc, fmt, G, nbg, T, H, P):
     segments offset the block index, while 8 rows of 1024 take a CTA per row;
     eight INT8 slabs at H = 8192 take the build whose stage holds no
     residual)."""
+    check_stale_blocks(orc, fmt, G, nbg, T, H, P, ((1, 2, 5), (2, 3, None), (0, 0, nbg - 1)))
+
+
+@pytest.mark.parametrize("fmt,G,nbg,T,H,P", [(I4T, 32, 2, 1000, 4096, 2), (I8T, 128, 11, 320, 8192, 4)],
+                         ids=["i4t-p2-two-row-ring", "i8t-p4-half-rows"])
+def test_quantized_tagged_stale_blocks_residual_free(orc, fmt, G, nbg, T, H, P):
+    """The residual-free stages of the tagged formats (more rows than one
+    wave) report the first stale block too: in the first row, a middle row
+    and the last row."""
+    check_stale_blocks(orc, fmt, G, nbg, T, H, P, ((1, T - 1, 3), (0, T // 2, None), (P - 1, 0, 0)))
+
+
+def check_stale_blocks(orc, fmt, G, nbg, T, H, P, sites):
+    """sites: (slab, row, block) to corrupt one at a time (block None: the
+    row's last block); each call must report that block's flat index."""
     base = synth.base_format(fmt)
     w = synth.Workload("qtstale", P=P, T=T, H=H, fmt=fmt, group=G)
     inp = synth.make_inputs(w, seed=42)
@@ -632,7 +657,8 @@ def test_quantized_tagged_stale_blocks(orc, fmt, G, nbg, T, H, P):
     want = oracle_fused(orc, w, inp)
     assert_bits_equal(host_bits(r_out), want["h"], "residual_out")
     bpr = (w.H // G) * nbg
-    for slab, row, blk in ((1, 2, 5), (2, 3, bpr - 1), (0, 0, nbg - 1)):
+    for slab, row, blk in sites:
+        blk = bpr - 1 if blk is None else blk
         bad = [b.copy() for b in blocks]
         bad[slab][4 * (row * bpr + blk) + 3] = ep + 1
         assert call(bad) == [fc.FC_ERR_STALE_BLOCK, (slab * w.T + row) * bpr + blk]
