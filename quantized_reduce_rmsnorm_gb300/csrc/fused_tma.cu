@@ -143,34 +143,36 @@ int rg_shape(const FusedArgs& a, const TmaShape& sh, TmaGeom& g3, bool& compact)
   }
 }
 
-// The residual-free compact build for the tagged quantized formats
-// (fused_tma_rg.cu).  Tagged slab rows are 16/12 the bytes of the plain
-// payload, so with the residual in the stage shared memory bounds the CTAs
+// The residual-free compact build (fused_tma_rg.cu) for shapes of the
+// quantized formats whose staged residual makes shared memory bound the CTAs
 // per SM below what the compact build's registers allow, or leaves room only
-// for a one-row stage where the plain format takes a two-row ring.  Among the
+// for a one-row stage (most of them tagged: a tagged slab row is 16/12 the
+// bytes of the plain payload).  Among the
 // builds of fused_tma_rg.cu (a two-row ring; a one-row stage; two half-row
 // sub-stages) the plan with the most CTAs per SM, then the deepest ring, is
 // returned when it beats the current plan (occ_now CTAs per SM, a ring of
 // depth_now half rows: 4 two-row ring, 3 half-row sub-stages, 2 one row):
 // more CTAs per SM, or as many with a two-row ring in place of a one-row
 // stage.  Measured on GB300 against the staged residual (64 MB messages,
-// fraction of the measured HBM peak): four tagged INT8 slabs 0.75 -> 0.82 at
-// H = 4096 (five -> six CTAs) and H = 8192 (two -> three); two tagged INT4
-// slabs at H = 4096 0.65 -> 0.67 (five -> six); eight tagged INT4 slabs at
-// H = 4096 0.66 -> 0.68 (four -> five); two tagged INT8 slabs at H = 4096
-// 0.77 -> 0.80 (a two-row ring).  A two-row ring in place of half-row
-// sub-stages at the same count (two slabs, H = 8192) was slower at 16 MB
-// (+4-6%), and an L2 prefetch of each row's residual, slower everywhere
-// (eight INT4 slabs at 64 MB: 88 -> 109 us).
+// fraction of the measured HBM peak): eight INT4 slabs at H = 4096
+// 0.71 -> 0.79 (five -> six CTAs; 32 MB 0.64 -> 0.71); four tagged INT8 slabs
+// 0.75 -> 0.82 at H = 4096 (five -> six) and H = 8192 (two -> three); two
+// tagged INT4 slabs at H = 4096 0.65 -> 0.67 (five -> six); eight tagged INT4
+// slabs at H = 4096 0.66 -> 0.68 (four -> five); two tagged INT8 slabs at
+// H = 4096 0.77 -> 0.80 (a two-row ring).  Slower, and not taken: a two-row
+// ring in place of half-row sub-stages at the same count (two slabs,
+// H = 8192; +4-6% at 16 MB) or of a one-row stage for four plain INT4 slabs
+// (+2-7%), and an L2 prefetch of each row's residual (eight INT4 slabs at
+// H = 8192, 64 MB: 88 -> 109 us).
 struct RgPlan {
   int occ = 0, nstage = 0, sub = 0, smem = 0;
   TmaGeom g{};
 };
 template <int FMT>
-RgPlan rg_tagged_plan(const FusedArgs& a, int threads, int occ_now, int depth_now) {
+RgPlan rg_plan(const FusedArgs& a, int threads, int occ_now, int depth_now) {
   RgPlan best;
   int best_depth = 0;
-  if (FMT != kINT8T && FMT != kINT4T) return best;
+  if (FMT == kBF16) return best;
   const int cands[3][2] = {{2, 1}, {1, 2}, {1, 1}};
   for (const auto& c : cands) {
     const int ns = c[0], sub = c[1];
@@ -189,6 +191,11 @@ RgPlan rg_tagged_plan(const FusedArgs& a, int threads, int occ_now, int depth_no
     }
   }
   if (!(best.occ > occ_now || (best.occ == occ_now && best_depth >= depth_now + 2))) best.occ = 0;
+  // two plain INT8 slabs carry the least work per chunk to hide the threads'
+  // residual loads behind: at H = 4096 the build measured faster from 64 MB
+  // (0.80 -> 0.92 of the measured HBM peak) and slower at 16 and 32 MB
+  // (0.74 -> 0.65, 0.87 -> 0.83), so it is taken for calls of eight waves or more
+  if (FMT == kINT8 && a.P <= 2 && a.rows < 8 * static_cast<int64_t>(num_sms()) * best.occ) best.occ = 0;
   return best;
 }
 
@@ -234,10 +241,10 @@ cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cud
     TmaGeom g2;
     const int occ2 = sh.compact ? sub_shape<FMT, PMAX, true>(a, sh, g2) : sub_shape<FMT, PMAX, false>(a, sh, g2);
     const bool sub2 = occ2 >= sh.occ && occ2 > 0;
-    if constexpr (kTagged) {
+    if constexpr (FMT != kBF16) {
       // only for more rows than one wave of the current plan (as above)
       if (a.rows > static_cast<int64_t>(num_sms()) * sh.occ) {
-        const RgPlan rp = rg_tagged_plan<FMT>(a, sh.threads, sub2 ? occ2 : sh.occ,
+        const RgPlan rp = rg_plan<FMT>(a, sh.threads, sub2 ? occ2 : sh.occ,
                                               sub2 ? 3 : 2 * sh.nstage);
         if (rp.occ > 0) {
           int64_t grid4 = static_cast<int64_t>(num_sms()) * rp.occ;
@@ -300,12 +307,12 @@ int plan_occ(const FusedArgs& a, const TmaGeom& g) {
     const int occ3 = rg_shape<FMT, PMAX>(a, sh, g3, compact);
     if (occ3 > sh.occ && more) return occ3;
   }
-  if constexpr (FMT == kINT8T || FMT == kINT4T) {
+  if constexpr (FMT != kBF16) {
     if (more) {
       TmaGeom g2;
       const int occ2 = sh.compact ? sub_shape<FMT, PMAX, true>(a, sh, g2) : sub_shape<FMT, PMAX, false>(a, sh, g2);
       const bool sub2 = occ2 >= sh.occ && occ2 > 0;
-      const RgPlan rp = rg_tagged_plan<FMT>(a, sh.threads, sub2 ? occ2 : sh.occ, sub2 ? 3 : 2 * sh.nstage);
+      const RgPlan rp = rg_plan<FMT>(a, sh.threads, sub2 ? occ2 : sh.occ, sub2 ? 3 : 2 * sh.nstage);
       if (rp.occ > 0) return rp.occ;
     }
   }

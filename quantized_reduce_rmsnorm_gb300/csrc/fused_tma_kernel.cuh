@@ -49,8 +49,8 @@ int fused_tma_compact_occupancy(int fmt, int P, int nstage, int threads, int sme
 cudaError_t launch_fused_tma_compact(int fmt, int nstage, const FusedArgs& a, const TmaGeom& g,
                                      int threads, int smem, int64_t grid, cudaStream_t st);
 
-// The compact build with the residual left out of the stage, for the tagged
-// quantized formats (fused_tma_rg.cu): resident CTAs per SM of the
+// The compact build with the residual left out of the stage, for shapes of
+// the quantized formats (fused_tma_rg.cu): resident CTAs per SM of the
 // instantiation for (fmt, P, nstage, sub) at `threads` threads and `smem`
 // bytes (0 when that combination is not built), and its launch.
 int fused_tma_rg_occupancy(int fmt, int P, int nstage, int sub, int threads, int smem);

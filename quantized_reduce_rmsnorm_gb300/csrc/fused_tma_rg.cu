@@ -1,13 +1,13 @@
 // fused_tma_rg.cu -- the compact build of the TMA-staged fused kernel
 // (fused_tma_kernel.cuh) with the residual left out of the stage (RG), for
-// the tagged quantized formats.  A tagged slab row is 16/12 the bytes of the
-// plain payload, so with the residual in it the stage is what bounds CTAs per
-// SM; without it, the compact build's registers do, as for the plain formats.
-// Built for the shapes where that raises the CTAs per SM or admits a deeper
-// ring (fused_tma.cu chooses):
-//   two tagged slabs (INT4 g32 or INT8 g128): a two-row ring;
-//   four tagged INT8 slabs: a one-row stage, whole or as two half-row sub-stages;
-//   eight tagged INT4 slabs: a one-row stage.
+// the shapes whose staged residual makes shared memory, not the compact
+// build's registers, bound the CTAs per SM (or leaves room only for a
+// one-row stage).  A tagged slab row is 16/12 the bytes of the plain payload,
+// so most of them are tagged.  Built for (fused_tma.cu chooses):
+//   two slabs (INT8 g128, tagged INT4 g32 or INT8 g128): a two-row ring;
+//   four tagged INT8 slabs: a one-row stage, whole or as two half-row
+//     sub-stages;
+//   eight INT4 slabs (plain or tagged): a one-row stage.
 #include "fused_tma_kernel.cuh"
 
 namespace fc {
@@ -18,6 +18,8 @@ template <int FMT, int NS, int PMAX, int SUB>
 constexpr bool rg_built() {
   if (FMT == kINT4T) return (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 8 && NS == 1 && SUB == 1);
   if (FMT == kINT8T) return (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 4 && NS == 1);
+  if (FMT == kINT4) return PMAX == 8 && NS == 1 && SUB == 1;
+  if (FMT == kINT8) return PMAX == 2 && NS == 2 && SUB == 1;
   return false;
 }
 
@@ -84,6 +86,8 @@ int fused_tma_rg_occupancy(int fmt, int P, int nstage, int sub, int threads, int
   if (threads > 256 || smem > kTmaSmemLimit) return 0;
   if (fmt == kINT4T) return occ_fmt<kINT4T>(P, nstage, sub, threads, smem);
   if (fmt == kINT8T) return occ_fmt<kINT8T>(P, nstage, sub, threads, smem);
+  if (fmt == kINT4) return occ_fmt<kINT4>(P, nstage, sub, threads, smem);
+  if (fmt == kINT8) return occ_fmt<kINT8>(P, nstage, sub, threads, smem);
   return 0;
 }
 
@@ -91,6 +95,8 @@ cudaError_t launch_fused_tma_rg(int fmt, int nstage, int sub, const FusedArgs& a
                                 int threads, int smem, int64_t grid, cudaStream_t st) {
   if (fmt == kINT4T) return launch_fmt<kINT4T>(nstage, sub, a, g, threads, smem, grid, st);
   if (fmt == kINT8T) return launch_fmt<kINT8T>(nstage, sub, a, g, threads, smem, grid, st);
+  if (fmt == kINT4) return launch_fmt<kINT4>(nstage, sub, a, g, threads, smem, grid, st);
+  if (fmt == kINT8) return launch_fmt<kINT8>(nstage, sub, a, g, threads, smem, grid, st);
   return cudaErrorInvalidConfiguration;
 }
 

@@ -398,12 +398,19 @@ def test_fused_in_place_residual_and_capped_grid(orc):
             check_fused(orc, w, run_fused(w, inp, max_ctas=cap, kernel=kernel), want)
 
 
-def test_fused_in_place_residual_free_stage(orc):
-    """Eight INT4 slabs at H = 8192 with more rows than one wave of the staged
-    build take the stage without the residual (each thread loads its residual
-    chunk from global memory): residual_out aliasing the residual, and
-    capped grids, still give the oracle's bits."""
-    w = synth.Workload("i4p8-rows", P=8, T=320, H=8192, fmt=I4, group=32)
+RG_PLAIN = [(I4, 32, 8, 320, 8192), (I4, 32, 8, 800, 4096), (I8, 128, 2, 7300, 4096)]
+
+
+@pytest.mark.parametrize("fmt,G,P,T,H", RG_PLAIN,
+                         ids=[f"{synth.FMT_NAMES[f]}-p{p}-h{h}" for f, _, p, _, h in RG_PLAIN])
+def test_fused_in_place_residual_free_stage(orc, fmt, G, P, T, H):
+    """Shapes with more rows than one wave of the staged build whose stage
+    leaves the residual out (each thread loads its residual chunk from global
+    memory): eight INT4 slabs at H = 8192 (half-row sub-stages) and at
+    H = 4096 (one-row stage), two INT8 slabs at H = 4096 (a two-row ring,
+    taken from eight waves of rows).  residual_out aliasing the residual, and capped grids,
+    still give the oracle's bits."""
+    w = synth.Workload("rg-rows", P=P, T=T, H=H, fmt=fmt, group=G)
     inp = synth.make_inputs(w, seed=31)
     want = oracle_fused(orc, w, inp)
     check_fused(orc, w, run_fused(w, inp, alias=True), want)
