@@ -215,13 +215,12 @@ fc_status fc_shard_range(fc_qspec spec, int64_t rows, int64_t hidden, int P, int
 }
 
 // {FC_OK, 0x7F7F7F7F} into an optional two-word device status, ordered before
-// the call's kernel on its stream.
+// the call's kernel on its stream (a one-thread kernel, so the launches of a
+// stream still overlap one another's prologue and tail).
 fc_status reset_status(int32_t* d_status, cudaStream_t st) {
   if (!d_status) return ok();
   if (!aligned(d_status, 4)) return fail(FC_ERR_INVALID, "d_status must be 4-byte aligned");
-  cudaError_t e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(d_status + 1, 0x7F, sizeof(int32_t), st);
-  return e == cudaSuccess ? ok() : cuda_status(e, "d_status reset");
+  return cuda_status(fc::launch_reset_status(d_status, st), "d_status reset");
 }
 
 fc_status fc_group_quantize_multi(const void* const* x_bf16, int P, int64_t rows, int64_t hidden,
@@ -382,12 +381,8 @@ fc_status fc_allgather_dequant(const fc_qtensor* shards, int P, int64_t rows, in
   j.out = out;
   j.epoch = expected_epoch;
   cudaStream_t st = (cudaStream_t)stream;
-  if (d_status) {
-    j.status = d_status;
-    cudaError_t e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(d_status + 1, 0x7F, sizeof(int32_t), st);
-    if (e != cudaSuccess) return cuda_status(e, "d_status reset");
-  }
+  j.status = d_status;
+  if (fc_status s = reset_status(d_status, st)) return s;
   return cuda_status(fc::launch_allgather(spec.fmt, out_dtype == FC_FMT_F32, j, st),
                      "fc_allgather_dequant launch");
 }
@@ -459,12 +454,8 @@ fc_status fc_allreduce_residual_rmsnorm_ex(const fc_qtensor* slabs, int P, int64
   a.eps = eps;
   a.epoch = expected_epoch;
   cudaStream_t st = (cudaStream_t)stream;
-  if (d_status) {
-    a.status = d_status;
-    cudaError_t e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(d_status + 1, 0x7F, sizeof(int32_t), st);
-    if (e != cudaSuccess) return cuda_status(e, "d_status reset");
-  }
+  a.status = d_status;
+  if (fc_status s = reset_status(d_status, st)) return s;
   const int path = opts ? opts->kernel : 0;
   const cudaError_t e = fc::launch_fused(spec.fmt, a, opts ? opts->max_ctas : 0, path, st);
   if (e == cudaErrorNotSupported)

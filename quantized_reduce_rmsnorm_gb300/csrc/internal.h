@@ -128,6 +128,9 @@ cudaError_t launch_quantize(int fmt, bool in_f32, int deq_kind, const QuantJob& 
 // Sender quantization of P bf16 slabs straight into epoch-tagged blocks
 // (fmt kINT8T / kINT4T; job.codes[p] are the block arrays).
 cudaError_t launch_quantize_tagged(int fmt, const QuantJob& job, cudaStream_t st);
+// {FC_OK, no index} into a call's two status words, ordered after the previous
+// kernel in the stream and before the call's kernel (quant.cu).
+cudaError_t launch_reset_status(int32_t* d_status, cudaStream_t st);
 // Sum of dequantized slabs over the 16-element chunks [c0, c1).
 // Standalone all-gather: shard p holds chunks [first[p], first[p+1]) of the
 // whole tensor (16-element chunks), indexed from its own chunk 0; for the

@@ -689,4 +689,24 @@ cudaError_t launch_pack_tagged(const void* const* x, void* const* blocks, int P,
   return launch_pdl(k_pack_tagged, dim3(grid, P), dim3(kThreads), 0, st, job, rows, H, nb, epoch);
 }
 
+// The two status words of a call, {FC_OK, no index}, written after the
+// previous kernel in the stream has finished (it may write them too) and
+// before the call's own kernel reads or writes them.  A one-thread kernel
+// launched with programmatic dependent launch, like the kernels it precedes:
+// the next kernel may be scheduled as soon as this one starts, so its
+// prologue (barrier set-up, L2 prefetch of its first tiles) still overlaps
+// the previous kernel's tail, and its griddepcontrol.wait returns only after
+// this kernel, and therefore the one before it, has completed.  Two memset
+// nodes in its place break that chain.
+__global__ void k_reset_status(int32_t* s) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  s[0] = 0;           // FC_OK
+  s[1] = 0x7F7F7F7F;  // no block index
+}
+
+cudaError_t launch_reset_status(int32_t* d_status, cudaStream_t st) {
+  return launch_pdl(k_reset_status, dim3(1), dim3(1), 0, st, d_status);
+}
+
 }  // namespace fc
