@@ -136,14 +136,17 @@ class Pipeline:
 
     # ------------------------------------------------------------------
     def _launches(self) -> int:
+        """Kernels launched per step: the sender, the consumer call(s), and for
+        each consumer call that takes a status word the one-thread kernel
+        that resets it."""
         w = self.w
         if w.fmt in (FMT_INT8_SYM, FMT_INT4_ASYM):
             return 1 + max(1, w.splits)
         if w.fmt in QTAGGED:
-            return 2
+            return 1 + 2
         if w.fmt == FMT_BF16:
             return 1
-        return 1 + max(1, w.splits)
+        return 1 + 2 * max(1, w.splits)
 
     def step(self, stream=None):
         """Launch one pass of the hot path on `stream` (default: current)."""
