@@ -163,9 +163,13 @@ int rg_shape(const FusedArgs& a, const TmaShape& sh, TmaGeom& g3, bool& compact)
 // ring in place of half-row sub-stages at the same count (two slabs,
 // H = 8192; +4-6% at 16 MB) or of a one-row stage for four plain INT4 slabs
 // (+2-7%), and an L2 prefetch of each row's residual (eight INT4 slabs at
-// H = 8192, 64 MB: 88 -> 109 us).
+// H = 8192, 64 MB: 88 -> 109 us).  Eight tagged INT4 slabs also drop the h
+// row buffer (pass 2 reads h back from residual_out through L2), for a
+// third CTA per SM at H = 8192 and a sixth at 4096: 64 MB 0.70 -> 0.72 and
+// 0.70 -> 0.75, 256 MB 0.73 -> 0.76 and 0.76 -> 0.80.
 struct RgPlan {
   int occ = 0, nstage = 0, sub = 0, smem = 0;
+  bool hb = true;  // h in the shared-memory row buffer (else read back from residual_out)
   TmaGeom g{};
 };
 template <int FMT>
@@ -173,20 +177,23 @@ RgPlan rg_plan(const FusedArgs& a, int threads, int occ_now, int depth_now) {
   RgPlan best;
   int best_depth = 0;
   if (FMT == kBF16) return best;
-  const int cands[3][2] = {{2, 1}, {1, 2}, {1, 1}};
+  // (stages, sub-stages, h row buffer): with the buffer first, so that at
+  // equal CTAs per SM the build that keeps h on chip is taken
+  const int cands[6][3] = {{2, 1, 1}, {1, 2, 1}, {1, 1, 1}, {2, 1, 0}, {1, 2, 0}, {1, 1, 0}};
   for (const auto& c : cands) {
     const int ns = c[0], sub = c[1];
+    const bool hb = c[2] != 0;
     if (sub == 2 && (threads != 256 || (a.H >> 4) != 2 * threads)) continue;
     TmaGeom g;
     if (!geometry(FMT, a, g, sub)) continue;
     g.stage_bytes -= 32 * g.cps;  // no residual in the stage
-    g.stage_off = (2 * a.H + 127) & ~127;
+    g.stage_off = hb ? (2 * a.H + 127) & ~127 : 0;
     const int smem = g.stage_off + ns * sub * g.stage_bytes;
     if (smem > kTmaSmemLimit) continue;
-    const int occ = fused_tma_rg_occupancy(FMT, a.P, ns, sub, threads, smem);
+    const int occ = fused_tma_rg_occupancy(FMT, a.P, ns, sub, hb, threads, smem);
     const int depth = ns == 2 ? 4 : sub == 2 ? 3 : 2;
     if (occ > best.occ || (occ == best.occ && occ > 0 && depth > best_depth)) {
-      best.occ = occ, best.nstage = ns, best.sub = sub, best.smem = smem, best.g = g;
+      best.occ = occ, best.nstage = ns, best.sub = sub, best.smem = smem, best.g = g, best.hb = hb;
       best_depth = depth;
     }
   }
@@ -250,7 +257,7 @@ cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cud
           int64_t grid4 = static_cast<int64_t>(num_sms()) * rp.occ;
           if (max_ctas > 0 && grid4 > max_ctas) grid4 = max_ctas;
           if (grid4 > a.rows) grid4 = a.rows;
-          return launch_fused_tma_rg(FMT, rp.nstage, rp.sub, a, rp.g, sh.threads, rp.smem, grid4, st);
+          return launch_fused_tma_rg(FMT, rp.nstage, rp.sub, rp.hb, a, rp.g, sh.threads, rp.smem, grid4, st);
         }
       }
     }

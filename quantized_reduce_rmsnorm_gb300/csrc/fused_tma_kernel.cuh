@@ -51,10 +51,11 @@ cudaError_t launch_fused_tma_compact(int fmt, int nstage, const FusedArgs& a, co
 
 // The compact build with the residual left out of the stage, for shapes of
 // the quantized formats (fused_tma_rg.cu): resident CTAs per SM of the
-// instantiation for (fmt, P, nstage, sub) at `threads` threads and `smem`
-// bytes (0 when that combination is not built), and its launch.
-int fused_tma_rg_occupancy(int fmt, int P, int nstage, int sub, int threads, int smem);
-cudaError_t launch_fused_tma_rg(int fmt, int nstage, int sub, const FusedArgs& a, const TmaGeom& g,
+// instantiation for (fmt, P, nstage, sub, with or without the h row buffer)
+// at `threads` threads and `smem` bytes (0 when that combination is not
+// built), and its launch.
+int fused_tma_rg_occupancy(int fmt, int P, int nstage, int sub, bool hb, int threads, int smem);
+cudaError_t launch_fused_tma_rg(int fmt, int nstage, int sub, bool hb, const FusedArgs& a, const TmaGeom& g,
                                 int threads, int smem, int64_t grid, cudaStream_t st);
 
 namespace {
@@ -136,7 +137,12 @@ __device__ __forceinline__ void st_peer_u32(uint32_t addr, uint32_t v) {
 // load.  Its stage is 2 * H bytes smaller, which is what lets a second CTA
 // per SM fit for eight tagged INT8 slabs at H = 8192, and a sixth for two
 // tagged INT4 slabs at H = 4096.
-template <int FMT, int NSTAGE, int PMAX, int CL = 1, bool COMPACT = false, int SUB = 1, bool RG = false>
+// HB: h is kept in the shared-memory row buffer (else pass 2 reads each
+// chunk back from residual_out, which this thread has just written and L2
+// still holds: 2 * H bytes less shared memory per CTA, for one more CTA per
+// SM where that buffer is what keeps it out).
+template <int FMT, int NSTAGE, int PMAX, int CL = 1, bool COMPACT = false, int SUB = 1, bool RG = false,
+          bool HB = true>
 __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 1)
     k_fused_tma(FusedArgs a, TmaGeom g) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -340,9 +346,11 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           hv.w[k] = pack_bf2(add_bf_lo(rw[k], acc[2 * k]), add_bf_hi(rw[k], acc[2 * k + 1]));
-        uint4* hp = reinterpret_cast<uint4*>(hbuf) + 2 * c;
-        hp[0] = make_uint4(hv.w[0], hv.w[1], hv.w[2], hv.w[3]);
-        hp[1] = make_uint4(hv.w[4], hv.w[5], hv.w[6], hv.w[7]);
+        if (HB) {
+          uint4* hp = reinterpret_cast<uint4*>(hbuf) + 2 * c;
+          hp[0] = make_uint4(hv.w[0], hv.w[1], hv.w[2], hv.w[3]);
+          hp[1] = make_uint4(hv.w[4], hv.w[5], hv.w[6], hv.w[7]);
+        }
         st256(static_cast<uint16_t*>(a.res_out) + gc * 16, hv);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -414,9 +422,17 @@ __global__ void __launch_bounds__(COMPACT ? 256 : kTmaThreadsMax, COMPACT ? 3 : 
 
     // ---- pass 2: y = bf16(fl(h * gamma) * inv); h * gamma is exact in binary32
     auto out_chunk = [&](int c, const uint32_t gw[8]) {
-      const uint4* hp = reinterpret_cast<const uint4*>(hbuf) + 2 * c;
-      const uint4 h0 = hp[0], h1 = hp[1];
-      const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+      uint32_t hw[8];
+      if (HB) {
+        const uint4* hp = reinterpret_cast<const uint4*>(hbuf) + 2 * c;
+        const uint4 h0 = hp[0], h1 = hp[1];
+        hw[0] = h0.x, hw[1] = h0.y, hw[2] = h0.z, hw[3] = h0.w;
+        hw[4] = h1.x, hw[5] = h1.y, hw[6] = h1.z, hw[7] = h1.w;
+      } else {  // this thread's own store of the chunk, read back through L2
+        const V8 hv = ld256_coherent(static_cast<const uint16_t*>(a.res_out) + (row * cpr + c0 + c) * 16);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) hw[k] = hv.w[k];
+      }
       V8 yv;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {

@@ -586,10 +586,14 @@ QT_CASES = [("decode-qtagged", {"T": 12}), ("prefill-qtagged", {"T": 10}),
             ("i8t-p8-h8192-rows", {"P": 8, "T": 160, "H": 8192, "fmt": I8T, "group": 128}),
             # more rows than one wave: the residual-free stages of the tagged
             # formats (two-row rings for two slabs; one-row stages for eight
-            # INT4 and four INT8 slabs, as two half-row sub-stages at H = 8192)
+            # INT4 and four INT8 slabs, as two half-row sub-stages at H = 8192;
+            # eight INT4 slabs without the h row buffer)
             ("i4t-p2-h4096-rows", {"P": 2, "T": 1000, "H": 4096, "fmt": I4T, "group": 32}),
             ("i4t-p2-h8192-rows", {"P": 2, "T": 480, "H": 8192, "fmt": I4T, "group": 32}),
             ("i4t-p8-h4096-rows", {"P": 8, "T": 640, "H": 4096, "fmt": I4T, "group": 32}),
+            # eight tagged INT4 slabs at H = 8192: half-row sub-stages without the
+            # h row buffer (pass 2 reads h back from residual_out)
+            ("i4t-p8-h8192-rows", {"P": 8, "T": 320, "H": 8192, "fmt": I4T, "group": 32}),
             ("i8t-p2-h4096-rows", {"P": 2, "T": 1000, "H": 4096, "fmt": I8T, "group": 128}),
             ("i8t-p2-h8192-rows", {"P": 2, "T": 480, "H": 8192, "fmt": I8T, "group": 128}),
             ("i8t-p4-h4096-rows", {"P": 4, "T": 800, "H": 4096, "fmt": I8T, "group": 128}),
@@ -629,8 +633,9 @@ def test_quantized_tagged_stale_blocks(orc, fmt, G, nbg, T, H, P):
     check_stale_blocks(orc, fmt, G, nbg, T, H, P, ((1, 2, 5), (2, 3, None), (0, 0, nbg - 1)))
 
 
-@pytest.mark.parametrize("fmt,G,nbg,T,H,P", [(I4T, 32, 2, 1000, 4096, 2), (I8T, 128, 11, 320, 8192, 4)],
-                         ids=["i4t-p2-two-row-ring", "i8t-p4-half-rows"])
+@pytest.mark.parametrize("fmt,G,nbg,T,H,P", [(I4T, 32, 2, 1000, 4096, 2), (I8T, 128, 11, 320, 8192, 4),
+                                              (I4T, 32, 2, 320, 8192, 8)],
+                         ids=["i4t-p2-two-row-ring", "i8t-p4-half-rows", "i4t-p8-no-h-buffer"])
 def test_quantized_tagged_stale_blocks_residual_free(orc, fmt, G, nbg, T, H, P):
     """The residual-free stages of the tagged formats (more rows than one
     wave) report the first stale block too: in the first row, a middle row
@@ -663,6 +668,15 @@ def check_stale_blocks(orc, fmt, G, nbg, T, H, P, sites):
     assert call(blocks) == [fc.FC_OK, fc.STATUS_NO_INDEX]
     want = oracle_fused(orc, w, inp)
     assert_bits_equal(host_bits(r_out), want["h"], "residual_out")
+    # residual_out aliasing the residual (builds without the h row buffer
+    # read h back from it)
+    r_al = r_in.clone()
+    fc.allreduce_residual_rmsnorm([dev(b.view(np.int32)) for b in blocks], spec, w.T, w.H, r_al, r_al, gam,
+                                  w.eps, y, expected_epoch=ep, d_status=st)
+    torch.cuda.synchronize()
+    assert list(host(st)) == [fc.FC_OK, fc.STATUS_NO_INDEX]
+    assert_bits_equal(host_bits(r_al), want["h"], "residual_out in place")
+    assert_y_close(host_bits(y), want["y"])
     bpr = (w.H // G) * nbg
     for slab, row, blk in sites:
         blk = bpr - 1 if blk is None else blk
