@@ -166,7 +166,9 @@ int rg_shape(const FusedArgs& a, const TmaShape& sh, TmaGeom& g3, bool& compact)
 // H = 8192, 64 MB: 88 -> 109 us).  Eight tagged INT4 slabs also drop the h
 // row buffer (pass 2 reads h back from residual_out through L2), for a
 // third CTA per SM at H = 8192 and a sixth at 4096: 64 MB 0.70 -> 0.72 and
-// 0.70 -> 0.75, 256 MB 0.73 -> 0.76 and 0.76 -> 0.80.
+// 0.70 -> 0.75, 256 MB 0.73 -> 0.76 and 0.76 -> 0.80; so do eight plain INT8
+// slabs at H = 8192 (two -> three CTAs): 16 MB 0.67 -> 0.70, 64 MB
+// 0.84 -> 0.94, 256 MB 0.90 -> 0.98.
 struct RgPlan {
   int occ = 0, nstage = 0, sub = 0, smem = 0;
   bool hb = true;  // h in the shared-memory row buffer (else read back from residual_out)

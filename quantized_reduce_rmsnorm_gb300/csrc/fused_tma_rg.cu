@@ -9,7 +9,8 @@
 //     sub-stages;
 //   eight INT4 slabs (plain or tagged): a one-row stage; for eight tagged
 //     INT4 slabs also without the h row buffer (pass 2 reads h back from
-//     residual_out), as a one-row stage or two half-row sub-stages.
+//     residual_out), as a one-row stage or two half-row sub-stages;
+//   eight INT8 slabs: two half-row sub-stages without the h row buffer.
 #include "fused_tma_kernel.cuh"
 
 namespace fc {
@@ -23,7 +24,7 @@ constexpr bool rg_built() {
   if (FMT == kINT4T)
     return HB ? (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 8 && NS == 1 && SUB == 1)
               : PMAX == 8 && NS == 1;
-  if (!HB) return false;
+  if (!HB) return FMT == kINT8 && PMAX == 8 && NS == 1 && SUB == 2;
   if (FMT == kINT8T) return (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 4 && NS == 1);
   if (FMT == kINT4) return PMAX == 8 && NS == 1 && SUB == 1;
   if (FMT == kINT8) return PMAX == 2 && NS == 2 && SUB == 1;

@@ -398,7 +398,7 @@ def test_fused_in_place_residual_and_capped_grid(orc):
             check_fused(orc, w, run_fused(w, inp, max_ctas=cap, kernel=kernel), want)
 
 
-RG_PLAIN = [(I4, 32, 8, 320, 8192), (I4, 32, 8, 800, 4096), (I8, 128, 2, 7300, 4096)]
+RG_PLAIN = [(I4, 32, 8, 320, 8192), (I4, 32, 8, 800, 4096), (I8, 128, 2, 7300, 4096), (I8, 128, 8, 320, 8192)]
 
 
 @pytest.mark.parametrize("fmt,G,P,T,H", RG_PLAIN,
@@ -408,7 +408,9 @@ def test_fused_in_place_residual_free_stage(orc, fmt, G, P, T, H):
     leaves the residual out (each thread loads its residual chunk from global
     memory): eight INT4 slabs at H = 8192 (half-row sub-stages) and at
     H = 4096 (one-row stage), two INT8 slabs at H = 4096 (a two-row ring,
-    taken from eight waves of rows).  residual_out aliasing the residual, and capped grids,
+    taken from eight waves of rows), eight INT8 slabs at H = 8192 (half-row
+    sub-stages without the h row buffer: pass 2 reads h back from
+    residual_out).  residual_out aliasing the residual, and capped grids,
     still give the oracle's bits."""
     w = synth.Workload("rg-rows", P=P, T=T, H=H, fmt=fmt, group=G)
     inp = synth.make_inputs(w, seed=31)
