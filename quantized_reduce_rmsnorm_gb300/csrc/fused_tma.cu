@@ -168,9 +168,13 @@ int rg_shape(const FusedArgs& a, const TmaShape& sh, TmaGeom& g3, bool& compact)
 // third CTA per SM at H = 8192 and a sixth at 4096: 64 MB 0.70 -> 0.72 and
 // 0.70 -> 0.75, 256 MB 0.73 -> 0.76 and 0.76 -> 0.80; so do eight plain INT8
 // slabs at H = 8192 (two -> three CTAs): 16 MB 0.67 -> 0.70, 64 MB
-// 0.84 -> 0.94, 256 MB 0.90 -> 0.98.
+// 0.84 -> 0.94, 256 MB 0.90 -> 0.98.  At equal resident warps the smaller
+// CTA is taken: eight INT8 slabs at H = 4096 as six 128-thread CTAs (two
+// chunks a thread, no h row buffer) in place of three of 256: 64 MB
+// 0.76 -> 0.93, 256 MB 0.82 -> 0.97, 16 MB 0.61 -> 0.67 (a CTA barrier waits
+// on four warps, not eight).
 struct RgPlan {
-  int occ = 0, nstage = 0, sub = 0, smem = 0;
+  int occ = 0, nstage = 0, sub = 0, smem = 0, threads = 0;
   bool hb = true;  // h in the shared-memory row buffer (else read back from residual_out)
   TmaGeom g{};
 };
@@ -181,25 +185,36 @@ RgPlan rg_plan(const FusedArgs& a, int threads, int occ_now, int depth_now) {
   if (FMT == kBF16) return best;
   // (stages, sub-stages, h row buffer): with the buffer first, so that at
   // equal CTAs per SM the build that keeps h on chip is taken
-  const int cands[6][3] = {{2, 1, 1}, {1, 2, 1}, {1, 1, 1}, {2, 1, 0}, {1, 2, 0}, {1, 1, 0}};
+  // (stages, sub-stages, h row buffer, threads halved): half the threads
+  // (two chunks each) for rows of 256 chunks whose build takes one chunk per
+  // thread, as six four-warp CTAs in place of three eight-warp ones
+  const int cands[8][4] = {{2, 1, 1, 0}, {1, 2, 1, 0}, {1, 1, 1, 0}, {2, 1, 0, 0}, {1, 2, 0, 0}, {1, 1, 0, 0},
+                           {1, 1, 1, 1}, {1, 1, 0, 1}};
   for (const auto& c : cands) {
     const int ns = c[0], sub = c[1];
     const bool hb = c[2] != 0;
-    if (sub == 2 && (threads != 256 || (a.H >> 4) != 2 * threads)) continue;
+    const int thr = c[3] ? threads / 2 : threads;
+    if (c[3] && (threads != 256 || (a.H >> 4) != 256)) continue;
+    if (sub == 2 && (thr != 256 || (a.H >> 4) != 2 * thr)) continue;
     TmaGeom g;
     if (!geometry(FMT, a, g, sub)) continue;
     g.stage_bytes -= 32 * g.cps;  // no residual in the stage
     g.stage_off = hb ? (2 * a.H + 127) & ~127 : 0;
     const int smem = g.stage_off + ns * sub * g.stage_bytes;
     if (smem > kTmaSmemLimit) continue;
-    const int occ = fused_tma_rg_occupancy(FMT, a.P, ns, sub, hb, threads, smem);
+    const int occ = fused_tma_rg_occupancy(FMT, a.P, ns, sub, hb, thr, smem);
     const int depth = ns == 2 ? 4 : sub == 2 ? 3 : 2;
-    if (occ > best.occ || (occ == best.occ && occ > 0 && depth > best_depth)) {
+    // compared by resident warps, then ring depth, then the smaller CTA
+    const int w = occ * thr, bw = best.occ * best.threads;
+    if (w > bw || (w == bw && occ > 0 && (depth > best_depth || (depth == best_depth && thr < best.threads)))) {
       best.occ = occ, best.nstage = ns, best.sub = sub, best.smem = smem, best.g = g, best.hb = hb;
+      best.threads = thr;
       best_depth = depth;
     }
   }
-  if (!(best.occ > occ_now || (best.occ == occ_now && best_depth >= depth_now + 2))) best.occ = 0;
+  const int64_t warps_now = static_cast<int64_t>(occ_now) * threads, warps = static_cast<int64_t>(best.occ) * best.threads;
+  if (!(warps > warps_now || (warps == warps_now && (best_depth >= depth_now + 2 || best.threads < threads))))
+    best.occ = 0;
   // two plain INT8 slabs carry the least work per chunk to hide the threads'
   // residual loads behind: at H = 4096 the build measured faster from 64 MB
   // (0.80 -> 0.92 of the measured HBM peak) and slower at 16 and 32 MB
@@ -259,7 +274,7 @@ cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cud
           int64_t grid4 = static_cast<int64_t>(num_sms()) * rp.occ;
           if (max_ctas > 0 && grid4 > max_ctas) grid4 = max_ctas;
           if (grid4 > a.rows) grid4 = a.rows;
-          return launch_fused_tma_rg(FMT, rp.nstage, rp.sub, rp.hb, a, rp.g, sh.threads, rp.smem, grid4, st);
+          return launch_fused_tma_rg(FMT, rp.nstage, rp.sub, rp.hb, a, rp.g, rp.threads, rp.smem, grid4, st);
         }
       }
     }

@@ -24,7 +24,7 @@ constexpr bool rg_built() {
   if (FMT == kINT4T)
     return HB ? (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 8 && NS == 1 && SUB == 1)
               : PMAX == 8 && NS == 1;
-  if (!HB) return FMT == kINT8 && PMAX == 8 && NS == 1 && SUB == 2;
+  if (!HB) return FMT == kINT8 && PMAX == 8 && NS == 1;
   if (FMT == kINT8T) return (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 4 && NS == 1);
   if (FMT == kINT4) return PMAX == 8 && NS == 1 && SUB == 1;
   if (FMT == kINT8) return PMAX == 2 && NS == 2 && SUB == 1;

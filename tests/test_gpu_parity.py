@@ -398,7 +398,8 @@ def test_fused_in_place_residual_and_capped_grid(orc):
             check_fused(orc, w, run_fused(w, inp, max_ctas=cap, kernel=kernel), want)
 
 
-RG_PLAIN = [(I4, 32, 8, 320, 8192), (I4, 32, 8, 800, 4096), (I8, 128, 2, 7300, 4096), (I8, 128, 8, 320, 8192)]
+RG_PLAIN = [(I4, 32, 8, 320, 8192), (I4, 32, 8, 800, 4096), (I8, 128, 2, 7300, 4096), (I8, 128, 8, 320, 8192),
+            (I8, 128, 8, 480, 4096)]
 
 
 @pytest.mark.parametrize("fmt,G,P,T,H", RG_PLAIN,
@@ -410,7 +411,8 @@ def test_fused_in_place_residual_free_stage(orc, fmt, G, P, T, H):
     H = 4096 (one-row stage), two INT8 slabs at H = 4096 (a two-row ring,
     taken from eight waves of rows), eight INT8 slabs at H = 8192 (half-row
     sub-stages without the h row buffer: pass 2 reads h back from
-    residual_out).  residual_out aliasing the residual, and capped grids,
+    residual_out) and at H = 4096 (one-row stage without the h row buffer,
+    128-thread CTAs).  residual_out aliasing the residual, and capped grids,
     still give the oracle's bits."""
     w = synth.Workload("rg-rows", P=P, T=T, H=H, fmt=fmt, group=G)
     inp = synth.make_inputs(w, seed=31)
