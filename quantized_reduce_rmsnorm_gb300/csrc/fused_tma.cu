@@ -185,16 +185,19 @@ RgPlan rg_plan(const FusedArgs& a, int threads, int occ_now, int depth_now) {
   if (FMT == kBF16) return best;
   // (stages, sub-stages, h row buffer): with the buffer first, so that at
   // equal CTAs per SM the build that keeps h on chip is taken
-  // (stages, sub-stages, h row buffer, threads halved): half the threads
-  // (two chunks each) for rows of 256 chunks whose build takes one chunk per
-  // thread, as six four-warp CTAs in place of three eight-warp ones
-  const int cands[8][4] = {{2, 1, 1, 0}, {1, 2, 1, 0}, {1, 1, 1, 0}, {2, 1, 0, 0}, {1, 2, 0, 0}, {1, 1, 0, 0},
-                           {1, 1, 1, 1}, {1, 1, 0, 1}};
+  // (stages, sub-stages, h row buffer, threads halved): 256-thread builds
+  // of the plain formats are also tried at 128 threads (twice the chunks a
+  // thread), as six four-warp CTAs per SM in place of three eight-warp ones.
+  // Not the tagged formats: four tagged INT4 slabs at H = 8192 so built ran
+  // as fast alone, but the prefill-qtagged step, back to back, went
+  // 245 -> 303 us (its per-stage times unchanged).
+  const int cands[10][4] = {{2, 1, 1, 0}, {1, 2, 1, 0}, {1, 1, 1, 0}, {2, 1, 0, 0}, {1, 2, 0, 0}, {1, 1, 0, 0},
+                            {2, 1, 1, 1}, {1, 1, 1, 1}, {2, 1, 0, 1}, {1, 1, 0, 1}};
   for (const auto& c : cands) {
     const int ns = c[0], sub = c[1];
     const bool hb = c[2] != 0;
     const int thr = c[3] ? threads / 2 : threads;
-    if (c[3] && (threads != 256 || (a.H >> 4) != 256)) continue;
+    if (c[3] && (threads != 256 || FMT == kINT4T || FMT == kINT8T)) continue;
     if (sub == 2 && (thr != 256 || (a.H >> 4) != 2 * thr)) continue;
     TmaGeom g;
     if (!geometry(FMT, a, g, sub)) continue;
@@ -215,11 +218,17 @@ RgPlan rg_plan(const FusedArgs& a, int threads, int occ_now, int depth_now) {
   const int64_t warps_now = static_cast<int64_t>(occ_now) * threads, warps = static_cast<int64_t>(best.occ) * best.threads;
   if (!(warps > warps_now || (warps == warps_now && (best_depth >= depth_now + 2 || best.threads < threads))))
     best.occ = 0;
-  // two plain INT8 slabs carry the least work per chunk to hide the threads'
-  // residual loads behind: at H = 4096 the build measured faster from 64 MB
-  // (0.80 -> 0.92 of the measured HBM peak) and slower at 16 and 32 MB
-  // (0.74 -> 0.65, 0.87 -> 0.83), so it is taken for calls of eight waves or more
-  if (FMT == kINT8 && a.P <= 2 && a.rows < 8 * static_cast<int64_t>(num_sms()) * best.occ) best.occ = 0;
+  // Taken for calls of eight waves or more only:
+  // * two plain INT8 slabs carry the least work per chunk to hide the threads'
+  //   residual loads behind: at H = 4096 the build measured faster from 64 MB
+  //   (0.80 -> 0.92 of the measured HBM peak), slower at 16 and 32 MB
+  //   (0.74 -> 0.65, 0.87 -> 0.83);
+  // * 128-thread CTAs with four chunks a thread (rows of 8192) take twice as
+  //   long per row: faster on long calls (256 MB, two or four INT4 or INT8
+  //   slabs, 4-9%; prefill fused 119 -> 112 us), slower at 16 and 64 MB
+  //   (2-26%).
+  const bool long_only = (FMT == kINT8 && a.P <= 2) || (best.threads < threads && (a.H >> 4) > 2 * best.threads);
+  if (long_only && a.rows < 8 * static_cast<int64_t>(num_sms()) * best.occ) best.occ = 0;
   return best;
 }
 

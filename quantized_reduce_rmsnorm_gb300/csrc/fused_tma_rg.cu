@@ -10,7 +10,11 @@
 //   eight INT4 slabs (plain or tagged): a one-row stage; for eight tagged
 //     INT4 slabs also without the h row buffer (pass 2 reads h back from
 //     residual_out), as a one-row stage or two half-row sub-stages;
-//   eight INT8 slabs: two half-row sub-stages without the h row buffer.
+//   eight INT8 slabs: two half-row sub-stages without the h row buffer, or
+//     at H = 4096 a one-row stage as 128-thread CTAs;
+//   rows of 8192 of two or four plain slabs in calls of eight waves or more:
+//     128-thread CTAs without the h row buffer (a two-row ring for two
+//     slabs, a one-row stage for four).
 #include "fused_tma_kernel.cuh"
 
 namespace fc {
@@ -21,13 +25,20 @@ namespace {
 // residual_out through L2).
 template <int FMT, int NS, int PMAX, int SUB, bool HB>
 constexpr bool rg_built() {
-  if (FMT == kINT4T)
-    return HB ? (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 8 && NS == 1 && SUB == 1)
-              : PMAX == 8 && NS == 1;
-  if (!HB) return FMT == kINT8 && PMAX == 8 && NS == 1;
-  if (FMT == kINT8T) return (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 4 && NS == 1);
-  if (FMT == kINT4) return PMAX == 8 && NS == 1 && SUB == 1;
-  if (FMT == kINT8) return PMAX == 2 && NS == 2 && SUB == 1;
+  if (HB) {
+    if (FMT == kINT4T) return (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 8 && NS == 1 && SUB == 1);
+    if (FMT == kINT8T) return (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 4 && NS == 1);
+    if (FMT == kINT4) return PMAX == 8 && NS == 1 && SUB == 1;
+    if (FMT == kINT8) return PMAX == 2 && NS == 2 && SUB == 1;
+    return false;
+  }
+  // without the h row buffer: eight slabs (one-row stage or half-row
+  // sub-stages), and the 128-thread CTAs of plain rows of 8192 (two-row
+  // rings for two slabs, one-row stages for four)
+  if (FMT == kINT4T) return PMAX == 8 && NS == 1;
+  if (FMT == kINT8)
+    return (PMAX == 8 && NS == 1) || (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 4 && NS == 1 && SUB == 1);
+  if (FMT == kINT4) return (PMAX == 2 && NS == 2 && SUB == 1) || (PMAX == 4 && NS == 1 && SUB == 1);
   return false;
 }
 

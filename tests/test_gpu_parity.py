@@ -399,7 +399,8 @@ def test_fused_in_place_residual_and_capped_grid(orc):
 
 
 RG_PLAIN = [(I4, 32, 8, 320, 8192), (I4, 32, 8, 800, 4096), (I8, 128, 2, 7300, 4096), (I8, 128, 8, 320, 8192),
-            (I8, 128, 8, 480, 4096)]
+            (I8, 128, 8, 480, 4096), (I4, 32, 2, 7300, 8192), (I4, 32, 4, 7300, 8192), (I8, 128, 4, 7300, 8192),
+            (I8, 128, 2, 7300, 8192)]
 
 
 @pytest.mark.parametrize("fmt,G,P,T,H", RG_PLAIN,
@@ -412,7 +413,10 @@ def test_fused_in_place_residual_free_stage(orc, fmt, G, P, T, H):
     taken from eight waves of rows), eight INT8 slabs at H = 8192 (half-row
     sub-stages without the h row buffer: pass 2 reads h back from
     residual_out) and at H = 4096 (one-row stage without the h row buffer,
-    128-thread CTAs).  residual_out aliasing the residual, and capped grids,
+    128-thread CTAs), and the 128-thread CTAs without the h row buffer for
+    rows of 8192 in calls of eight waves or more (two INT4 or INT8 slabs:
+    two-row rings; four: one-row stages).  residual_out aliasing the
+    residual, and capped grids,
     still give the oracle's bits."""
     w = synth.Workload("rg-rows", P=P, T=T, H=H, fmt=fmt, group=G)
     inp = synth.make_inputs(w, seed=31)
@@ -598,6 +602,8 @@ QT_CASES = [("decode-qtagged", {"T": 12}), ("prefill-qtagged", {"T": 10}),
             # eight tagged INT4 slabs at H = 8192: half-row sub-stages without the
             # h row buffer (pass 2 reads h back from residual_out)
             ("i4t-p8-h8192-rows", {"P": 8, "T": 320, "H": 8192, "fmt": I4T, "group": 32}),
+            # four tagged INT4 slabs at H = 8192 (the prefill-qtagged rows)
+            ("i4t-p4-h8192-rows", {"P": 4, "T": 480, "H": 8192, "fmt": I4T, "group": 32}),
             ("i8t-p2-h4096-rows", {"P": 2, "T": 1000, "H": 4096, "fmt": I8T, "group": 128}),
             ("i8t-p2-h8192-rows", {"P": 2, "T": 480, "H": 8192, "fmt": I8T, "group": 128}),
             ("i8t-p4-h4096-rows", {"P": 4, "T": 800, "H": 4096, "fmt": I8T, "group": 128}),
