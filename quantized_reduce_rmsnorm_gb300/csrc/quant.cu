@@ -139,6 +139,7 @@ struct WRing {
 template <int TILE>
 constexpr int default_stages() { return TILE == 1024 ? 4 : 2; }
 static_assert(WRing<1024, 4>::kBytes == WRing<2048, 2>::kBytes, "one shared-memory size for both tilings");
+static_assert(WRing<1536, 2>::kBytes <= WRing<2048, 2>::kBytes, "1536-element tiles fit the same budget");
 constexpr int kQWarps = kThreads / 32;
 
 // TAGGED: the codes and scales go out as self-synchronizing blocks carrying
@@ -622,11 +623,21 @@ cudaError_t launch_quantize_tma_t(const QuantJob& job, cudaStream_t st) {
 }
 
 // INT8 g128 (8 lanes per group) and INT4 g32 (2 lanes) are specialised
+// Tile size: the elements the busiest warp streams, ceil(tiles / resident
+// warps) * tile, bound a call too small to fill the GPU several times over.
+// 1536-element tiles (three chunks a lane, two deep) are taken where they
+// make that strictly smaller than both other sizes: a decode step's eight
+// 64 x 8192 slabs are 4096 tiles of 1024 for 3648 resident warps (2048
+// elements on the busiest), or 2731 of 1536 (1536).
 template <int FMT, bool TAGGED, int LPG>
 cudaError_t launch_quantize_tma_tile(const QuantJob& job, cudaStream_t st) {
   // resident warps: three CTAs of kQWarps per SM
+  const int64_t warps = static_cast<int64_t>(num_sms()) * 3 * kQWarps;
+  auto busiest = [&](int64_t tile) { return ((job.n + tile - 1) / tile * job.P + warps - 1) / warps * tile; };
+  const int64_t b1 = busiest(1024), b15 = busiest(1536), b2 = busiest(2048);
+  if (b15 < b1 && b15 < b2) return launch_quantize_tma_t<FMT, TAGGED, LPG, 1536>(job, st);
   const int64_t big_tiles = (job.n + 2047) / 2048 * job.P;
-  if (big_tiles < static_cast<int64_t>(num_sms()) * 3 * kQWarps)
+  if (big_tiles < warps)
     return launch_quantize_tma_t<FMT, TAGGED, LPG, 1024>(job, st);
   return launch_quantize_tma_t<FMT, TAGGED, LPG, 2048>(job, st);
 }
