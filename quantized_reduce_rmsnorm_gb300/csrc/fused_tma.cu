@@ -183,14 +183,14 @@ RgPlan rg_plan(const FusedArgs& a, int threads, int occ_now, int depth_now) {
   RgPlan best;
   int best_depth = 0;
   if (FMT == kBF16) return best;
-  // (stages, sub-stages, h row buffer): with the buffer first, so that at
-  // equal CTAs per SM the build that keeps h on chip is taken
-  // (stages, sub-stages, h row buffer, threads halved): 256-thread builds
-  // of the plain formats are also tried at 128 threads (twice the chunks a
-  // thread), as six four-warp CTAs per SM in place of three eight-warp ones.
-  // Not the tagged formats: four tagged INT4 slabs at H = 8192 so built ran
-  // as fast alone, but the prefill-qtagged step, back to back, went
-  // 245 -> 303 us (its per-stage times unchanged).
+  // Candidates (stages, sub-stages, h row buffer, threads halved), those
+  // with the h row buffer first, so that where two tie the build that keeps
+  // h on chip is taken.  256-thread builds of the plain formats are also
+  // tried at 128 threads (twice the chunks a thread), as six four-warp CTAs
+  // per SM in place of three eight-warp ones; not those of the tagged
+  // formats: four tagged INT4 slabs at H = 8192 so built ran as fast alone,
+  // but the prefill-qtagged step, back to back, went 245 -> 303 us with
+  // unchanged per-stage times.
   const int cands[10][4] = {{2, 1, 1, 0}, {1, 2, 1, 0}, {1, 1, 1, 0}, {2, 1, 0, 0}, {1, 2, 0, 0}, {1, 1, 0, 0},
                             {2, 1, 1, 1}, {1, 1, 1, 1}, {2, 1, 0, 1}, {1, 1, 0, 1}};
   for (const auto& c : cands) {
