@@ -275,8 +275,11 @@ cudaError_t launch_tma_p(const FusedArgs& a, const TmaGeom& g, int max_ctas, cud
     const int occ2 = sh.compact ? sub_shape<FMT, PMAX, true>(a, sh, g2) : sub_shape<FMT, PMAX, false>(a, sh, g2);
     const bool sub2 = occ2 >= sh.occ && occ2 > 0;
     if constexpr (FMT != kBF16) {
-      // only for more rows than one wave of the current plan (as above)
-      if (a.rows > static_cast<int64_t>(num_sms()) * sh.occ) {
+      // only for more rows than one wave of the current plan (as above), and
+      // not under a CTA cap below that wave: there the CTAs per SM these
+      // plans add do not count, and the 128-thread ones make each CTA slower
+      const int64_t wave = static_cast<int64_t>(num_sms()) * sh.occ;
+      if (a.rows > wave && (max_ctas == 0 || max_ctas >= wave)) {
         const RgPlan rp = rg_plan<FMT>(a, sh.threads, sub2 ? occ2 : sh.occ,
                                               sub2 ? 3 : 2 * sh.nstage);
         if (rp.occ > 0) {
