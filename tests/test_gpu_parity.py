@@ -400,7 +400,9 @@ def test_fused_in_place_residual_and_capped_grid(orc):
 
 RG_PLAIN = [(I4, 32, 8, 320, 8192), (I4, 32, 8, 800, 4096), (I8, 128, 2, 7300, 4096), (I8, 128, 8, 320, 8192),
             (I8, 128, 8, 480, 4096), (I4, 32, 2, 7300, 8192), (I4, 32, 4, 7300, 8192), (I8, 128, 4, 7300, 8192),
-            (I8, 128, 2, 7300, 8192)]
+            (I8, 128, 2, 7300, 8192),
+            # slab counts between the built ones take the build for the next one up
+            (I4, 32, 6, 800, 4096), (I8, 128, 5, 480, 4096), (I4, 32, 3, 7300, 8192), (I8, 128, 7, 320, 8192)]
 
 
 @pytest.mark.parametrize("fmt,G,P,T,H", RG_PLAIN,
@@ -604,6 +606,8 @@ QT_CASES = [("decode-qtagged", {"T": 12}), ("prefill-qtagged", {"T": 10}),
             ("i4t-p8-h8192-rows", {"P": 8, "T": 320, "H": 8192, "fmt": I4T, "group": 32}),
             # four tagged INT4 slabs at H = 8192 (the prefill-qtagged rows)
             ("i4t-p4-h8192-rows", {"P": 4, "T": 480, "H": 8192, "fmt": I4T, "group": 32}),
+            ("i4t-p6-h8192-rows", {"P": 6, "T": 320, "H": 8192, "fmt": I4T, "group": 32}),
+            ("i8t-p3-h4096-rows", {"P": 3, "T": 800, "H": 4096, "fmt": I8T, "group": 128}),
             ("i8t-p2-h4096-rows", {"P": 2, "T": 1000, "H": 4096, "fmt": I8T, "group": 128}),
             ("i8t-p2-h8192-rows", {"P": 2, "T": 480, "H": 8192, "fmt": I8T, "group": 128}),
             ("i8t-p4-h4096-rows", {"P": 4, "T": 800, "H": 4096, "fmt": I8T, "group": 128}),
